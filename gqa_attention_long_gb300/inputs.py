@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs of the expert-attention workloads.
+
+This module only draws random numbers and fills buffers; it holds none of the method's
+arithmetic, so both the CUDA path and the CPU oracle can consume what it produces.
+
+Shapes and distributions follow the pages' statement of the workload
+(alpamayo_tt/EXPERT_NOTES.md, sections "Layouts" and "Attention over the VLM cache: masking
+approach"): raw q [16, 64, 128], k and v [8, 64, 128], per-channel q_norm / k_norm gains [128],
+and a per-layer VLM KV cache [8, Smax, 128] whose rows [0, S) are valid. The pages' real cache
+comes from the VLM prefill of a driving prompt (about 4.6K prompt tokens plus up to 256
+generated ones) and is not available, so a standard-normal bf16 cache stands in for it.
+Hidden rows [S, Smax-64) are filled with a constant (the pages' tests use 7.0) or with
+arbitrary garbage to check that they are never read.
+
+Everything is drawn on the CPU with ``torch.Generator`` so that a given seed yields the same
+bytes on every machine.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+HQ, HKV, D, T = 16, 8, 128, 64
+
+
+@dataclass
+class LayerInputs:
+    q_raw: torch.Tensor    # bf16 [16, 64, 128]
+    k_raw: torch.Tensor    # bf16 [8, 64, 128]
+    v_raw: torch.Tensor    # bf16 [8, 64, 128]
+    q_gamma: torch.Tensor  # bf16 [128]
+    k_gamma: torch.Tensor  # bf16 [128]
+    k_cache: torch.Tensor  # bf16 [8, Smax, 128]
+    v_cache: torch.Tensor  # bf16 [8, Smax, 128]
+    S: int
+    Smax: int
+
+
+def layer_inputs(seed: int, S: int, Smax: int, hidden_fill: float | str = 7.0,
+                 tail_fill: float | None = None) -> LayerInputs:
+    """One layer's inputs, all bf16 on the CPU.
+
+    raw q/k/v and cache K/V ~ N(0, 1); gains 1 + 0.1 N(0, 1). ``hidden_fill`` sets rows
+    [S, Smax-64): a number, ``"garbage"`` (N(0, 1e4) values), ``"nan"`` or ``"inf"``.
+    ``tail_fill`` optionally overwrites rows [Smax-64, Smax) before the call (they are
+    rewritten by the path anyway).
+    """
+    assert 0 <= S <= Smax - T and Smax % T == 0
+    g = torch.Generator().manual_seed(int(seed))
+    bf = torch.bfloat16
+    q_raw = torch.randn(HQ, T, D, generator=g).to(bf)
+    k_raw = torch.randn(HKV, T, D, generator=g).to(bf)
+    v_raw = torch.randn(HKV, T, D, generator=g).to(bf)
+    q_gamma = (1.0 + 0.1 * torch.randn(D, generator=g)).to(bf)
+    k_gamma = (1.0 + 0.1 * torch.randn(D, generator=g)).to(bf)
+    k_cache = torch.randn(HKV, Smax, D, generator=g).to(bf)
+    v_cache = torch.randn(HKV, Smax, D, generator=g).to(bf)
+    fill_hidden(k_cache, v_cache, S, Smax, hidden_fill, seed)
+    if tail_fill is not None:
+        k_cache[:, Smax - T:] = tail_fill
+        v_cache[:, Smax - T:] = tail_fill
+    return LayerInputs(q_raw, k_raw, v_raw, q_gamma, k_gamma, k_cache, v_cache, int(S), int(Smax))
+
+
+def fill_hidden(k_cache: torch.Tensor, v_cache: torch.Tensor, S: int, Smax: int,
+                hidden_fill: float | str, seed: int = 0) -> None:
+    """Overwrite rows [S, Smax-64) of both caches in place."""
+    lo, hi = S, Smax - T
+    if hi <= lo:
+        return
+    if isinstance(hidden_fill, str):
+        if hidden_fill == "garbage":
+            g = torch.Generator().manual_seed(int(seed) + 7919)
+            for c in (k_cache, v_cache):
+                c[:, lo:hi] = (1e4 * torch.randn(c.shape[0], hi - lo, c.shape[2], generator=g)).to(c.dtype)
+        elif hidden_fill == "nan":
+            k_cache[:, lo:hi] = float("nan")
+            v_cache[:, lo:hi] = float("nan")
+        elif hidden_fill == "inf":
+            k_cache[:, lo:hi] = float("inf")
+            v_cache[:, lo:hi] = float("-inf")
+        else:
+            raise ValueError(hidden_fill)
+    else:
+        k_cache[:, lo:hi] = float(hidden_fill)
+        v_cache[:, lo:hi] = float(hidden_fill)
+
+
+def zero_inputs_like(x: LayerInputs, **zeroed: bool) -> LayerInputs:
+    """A copy of x with the named tensors (e.g. ``q_raw=True``) set to zero."""
+    d = dict(x.__dict__)
+    for name, on in zeroed.items():
+        if on:
+            d[name] = torch.zeros_like(d[name])
+    return LayerInputs(**d)
+
+
+# Workloads of the benchmark and the parity tests. Seeds: 1000 * config + layer (config 0: 0).
+CONFIGS = {
+    0: dict(name="tiny single layer", layers=1, S=256, Smax=512, hidden_fill=7.0, kv="bf16"),
+    1: dict(name="main shape, one layer", layers=1, S=4700, Smax=8192, hidden_fill=7.0, kv="bf16"),
+    2: dict(name="tighter cache, one layer", layers=1, S=4700, Smax=5120, hidden_fill=7.0, kv="bf16"),
+    3: dict(name="fp8 e4m3 cache, one layer", layers=1, S=4700, Smax=8192, hidden_fill=7.0, kv="fp8"),
+    4: dict(name="64-layer Euler step", layers=64, S_sweep=(1024, 2048, 4700, 8128), Smax=8192,
+            hidden_fill=7.0, kv="bf16"),
+}
+
+
+def config_seed(config: int, layer: int) -> int:
+    return 0 if config == 0 else 1000 * config + layer

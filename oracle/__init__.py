@@ -1,0 +1,27 @@
+"""Test infrastructure: a plain, slow, float64 CPU oracle of the expert attention path.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference arm may import this package. The product library never links, imports or
+calls it, and it shares no code, tables or constants with the CUDA path.
+
+Modules
+-------
+expert_attention : the per-layer attention of the flow-matching action expert
+                   (q/k RMSNorm, HF rotate_half RoPE, tail placement, masked
+                   non-causal GQA softmax attention), written out in fp64.
+fp8_e4m3         : the OCP E4M3 ("e4m3fn") code table, a round-to-nearest-even
+                   saturating encoder, and the per-(kv head, 128-row block)
+                   cache quantiser used by the FP8 cache variant.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against closed forms,
+invariants, brute force on tiny inputs and independent library routines.
+"""
+from .expert_attention import (  # noqa: F401
+    D, EPS, HQ, HKV, MASK_MIN, REP, T, THETA,
+    attention_concat, attention_tail_masked, bf16_round, expert_attention_layer,
+    expert_attention_layer_fp8, inv_freq, prologue, rms_norm, rope_angles, rope_rotate_half,
+)
+from .fp8_e4m3 import (  # noqa: F401
+    E4M3_MAX, decode_e4m3, dequantize_cache, e4m3_magnitudes, encode_e4m3_rne_sat,
+    quantize_cache_blocks, quantize_tail_rows,
+)

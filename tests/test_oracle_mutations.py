@@ -1,0 +1,80 @@
+"""Plants plausible mistakes in the oracle (CPU only) and checks that its pins catch each one.
+
+The mistakes are patched into the oracle module for the duration of one test; nothing on the
+CUDA path is involved.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.expert_attention as ea
+from tests import test_oracle_pins as pins
+
+
+def _rope_wrong_sign(x, pos, theta=ea.THETA):
+    x = np.asarray(x, dtype=np.float64)
+    a = ea.rope_angles(pos, theta, x.shape[-1])
+    cos = np.concatenate([np.cos(a), np.cos(a)], -1)
+    sin = np.concatenate([np.sin(a), np.sin(a)], -1)
+    rot = np.concatenate([x[..., 64:], -x[..., :64]], -1)   # planted: signs swapped
+    return x * cos + rot * sin
+
+
+def _rms_eps_outside(x, gamma, eps=ea.EPS):
+    x = np.asarray(x, dtype=np.float64)
+    return np.asarray(gamma) * x / (np.sqrt(np.mean(x * x, -1, keepdims=True)) + eps)  # planted
+
+
+def _attend_wrong_scale(q, keys, vals, bias=None):
+    s = (q @ keys.T) / ea.D                                  # planted: 1/D instead of 1/sqrt(D)
+    if bias is not None:
+        s = s + bias
+    p = np.exp(s - s.max(-1, keepdims=True))
+    return (p @ vals) / p.sum(-1, keepdims=True)
+
+
+def _concat_wrong_group(q, k_cache, v_cache, S, k_own, v_own):
+    out = np.empty((16, 64, 128))
+    for h in range(16):
+        g = h % 8                                            # planted: wrong GQA map
+        keys = np.concatenate([np.asarray(k_cache[g, :S], np.float64), k_own[g]], 0)
+        vals = np.concatenate([np.asarray(v_cache[g, :S], np.float64), v_own[g]], 0)
+        out[h] = ea._softmax_attend(q[h], keys, vals)
+    return out
+
+
+def _inv_freq_wrong(theta=ea.THETA, dim=ea.D):
+    return theta ** (-np.arange(dim // 2, dtype=np.float64) / dim)   # planted: missing factor 2
+
+
+def _prologue_wrong_pos(q_raw, k_raw, v_raw, q_gamma, k_gamma, S, rope_delta):
+    pos = np.arange(64) + int(rope_delta)                    # planted: S dropped from positions
+    return (ea.rope_rotate_half(ea.rms_norm(q_raw, q_gamma), pos),
+            ea.rope_rotate_half(ea.rms_norm(k_raw, k_gamma), pos), np.asarray(v_raw, np.float64))
+
+
+MUTATIONS = [
+    ("rope_rotate_half", _rope_wrong_sign, pins.test_rope_matches_complex_rotation),
+    ("rms_norm", _rms_eps_outside, pins.test_rms_norm_eps_inside_the_root),
+    ("_softmax_attend", _attend_wrong_scale, pins.test_matches_torch_sdpa_fp64),
+    ("attention_concat", _concat_wrong_group, pins.test_gqa_group_mapping),
+    ("inv_freq", _inv_freq_wrong, pins.test_inv_freq_closed_forms),
+    ("prologue", _prologue_wrong_pos, pins.test_prologue_positions_are_t_plus_delta_plus_S),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pin_catches_planted_mistake(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(ea, name, bad)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_unpatched_pins_pass():
+    for _, _, pin in MUTATIONS:
+        pin()
+    assert math.isfinite(1.0)
