@@ -1,0 +1,322 @@
+"""Benchmark of the expert-attention hot path on GB300.
+
+Default workload: one 64-layer Euler step of the action expert's attention (64 independent
+layers, S = 4700 valid cache rows, Smax = 8192, bf16 KV caches of [8, 8192, 128] per layer,
+2.15 GB in total), run as one ``expert_attn_layers`` call per step. Prints ONE JSON line with
+the metric in microseconds per layer, the achieved HBM bandwidth and roofline fraction of the
+dominant (attention) kernel, an end-to-end number through the C ABI with host buffers, and the
+fp64 CPU oracle timed on the host cores as a reported baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    torchrun --nproc-per-node N bench.py --gpus N ...   (N independent replicas, weak scaling)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_attention_long_gb300.inputs import config_seed, layer_inputs, layer_inputs_on_device  # noqa: E402
+
+METRIC = "µs/layer & achieved HBM GB/s (% roofline), expert attention, S=4700 Smax=8192"
+HQ, HKV, D, T = 16, 8, 128, 64
+
+
+def algo_bytes_per_layer(S: int, b: int = 2) -> int:
+    """Algorithmic HBM bytes of one layer: live cache K/V rows, own K/V rows written and read
+    back, raw q/k/v read, output written."""
+    return 2 * HKV * S * D * b + 2 * (2 * HKV * T * D * b) + (HQ + 2 * HKV) * T * D * 2 + HQ * T * D * 2
+
+
+def attn_kernel_bytes_per_layer(S: int, b: int = 2) -> int:
+    """Algorithmic bytes of the attention kernel alone: live cache K/V rows, own K/V rows, output."""
+    return 2 * HKV * S * D * b + 2 * HKV * T * D * b + HQ * T * D * 2
+
+
+def flops_per_layer(S: int) -> int:
+    return 4 * (2 * T) * D * (S + T) * HKV
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(S: int, Smax: int, n_layers: int, min_seconds: float) -> dict:
+    """The fp64 CPU oracle, as it stands, on n_layers distinct layers of the workload, repeated
+    until min_seconds of oracle time; returns microseconds per layer."""
+    import oracle
+    f = lambda t: t.double().numpy()  # noqa: E731
+    arrays = []
+    for l in range(n_layers):
+        x = layer_inputs(config_seed(4, l), S, Smax)
+        arrays.append([f(v) for v in (x.q_raw, x.k_raw, x.v_raw, x.q_gamma, x.k_gamma, x.k_cache, x.v_cache)])
+    done, spent = 0, 0.0
+    while spent < min_seconds or done == 0:
+        for a in arrays:
+            t0 = time.perf_counter()
+            oracle.expert_attention_layer(*a, S, Smax, 0)
+            spent += time.perf_counter() - t0
+            done += 1
+    return {"us_per_layer": spent / done * 1e6, "layers": done, "seconds": spent}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    """Reference arm: the fp64 CPU oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    S, Smax = args.S, args.Smax
+    for _ in range(args.warmup):
+        oracle_sample(S, Smax, 1, 0.0)
+    times = []
+    for _ in range(args.steps):
+        times.append(oracle_sample(S, Smax, 1, 0.0)["us_per_layer"])
+    us = statistics.mean(times)
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/layer", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us * 1e-3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args),
+            "cpu_baseline": {"value": us, "unit": "us/layer", "cores": cores, "kind": "oracle",
+                             "sample": "one layer of the workload per step (fp64 numpy oracle, BLAS threads = all cores)"},
+            "e2e": {"value": us, "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args) -> dict:
+    return {"workload": f"{args.layers}-layer Euler step of expert attention, S={args.S}, Smax={args.Smax}, bf16 KV cache",
+            "layers": args.layers, "S": args.S, "Smax": args.Smax, "q_heads": HQ, "kv_heads": HKV,
+            "head_dim": D, "tokens": T, "global_batch": 1,
+            "l2": "inputs larger than L2 (distinct caches of all layers, no flush)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--S", type=int, default=4700)
+    ap.add_argument("--Smax", type=int, default=8192)
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import gqa_attention_long_gb300 as ea
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    S, Smax, n = args.S, args.Smax, args.layers
+    xs = [layer_inputs_on_device(config_seed(4, l) + 100000 * rank, S, Smax, dev) for l in range(n)]
+    Ls = [ea.LayerBuffers(q_raw=x.q_raw, k_raw=x.k_raw, v_raw=x.v_raw, q_gamma=x.q_gamma, k_gamma=x.k_gamma,
+                          k_cache=x.k_cache, v_cache=x.v_cache,
+                          out=torch.empty(HQ, T, D, dtype=torch.bfloat16, device=dev)) for x in xs]
+    ws = ea.alloc_workspace(n, Smax)
+    arr = ea.make_args(Ls, Smax, ea.EA_KV_BF16)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ea.expert_attn_layers(Ls, S, Smax, 0, ea.EA_KV_BF16, ws, stream, _arr=arr)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device time with CUDA events on the launching stream
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
+    st, bits = ea.expert_attn_read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"kernel status bits {bits:#x}")
+    ms_step = ms_total / args.steps
+    us_layer = ms_step * 1e3 / (n * world)
+
+    # ---- dominant kernel (attention) timed on its own with events between the kernels
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e in evs:  # torch creates the CUDA event on first record
+        for x in e:
+            x.record(stream)
+    for i in range(args.steps):
+        ea.expert_attn_layers_profiled(Ls, S, Smax, 0, ea.EA_KV_BF16, ws, evs[i], stream, _arr=arr)
+    torch.cuda.synchronize()
+    k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    k2 = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    peaks = load_peaks()
+    k2_bytes = attn_kernel_bytes_per_layer(S) * n
+    achieved = k2_bytes / (k2 * 1e-3) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
+    if os.path.exists(tfile):
+        tj = json.load(open(tfile))
+        if tj.get("S") == S and tj.get("Smax") == Smax and tj.get("layers") == n and tj.get("current", False):
+            traffic = tj.get("bytes_per_launch")
+
+    # ---- end to end through the C ABI with host buffers: H2D of q/k/v, call, D2H of out
+    pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
+    hq = [pin(x.q_raw) for x in xs]
+    hk = [pin(x.k_raw) for x in xs]
+    hv = [pin(x.v_raw) for x in xs]
+    ho = [torch.empty(HQ, T, D, dtype=torch.bfloat16).pin_memory() for _ in xs]
+
+    def e2e_step():
+        for i, L in enumerate(Ls):
+            L.q_raw.copy_(hq[i], non_blocking=True)
+            L.k_raw.copy_(hk[i], non_blocking=True)
+            L.v_raw.copy_(hv[i], non_blocking=True)
+        step()
+        for i, L in enumerate(Ls):
+            ho[i].copy_(L.out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
+    h2d = sum(t.numel() * 2 for t in hq + hk + hv)
+    d2h = sum(t.numel() * 2 for t in ho)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = oracle_sample(S, Smax, 8, 10.0)
+        cpu = {"value": smp["us_per_layer"], "unit": "us/layer", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{smp['layers']} layer evaluations over 8 distinct layers of the workload "
+                         f"({smp['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = all cores)"}
+
+    if rank == 0:
+        step_bytes = algo_bytes_per_layer(S) * n
+        line = {
+            "metric": METRIC, "value": us_layer, "unit": "us/layer", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(args),
+            "step_hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9 * world,
+            "step_roofline_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "kernel": "attention_kernel", "peak_src": peaks["src"],
+                         "bytes_per_launch": k2_bytes, "ms_per_launch": k2},
+            "kernels_ms": {"prologue": k1, "attention": k2, "merge": k3},
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_ms * 1e3 / (n * world), "unit": "us/layer", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps * ((n + 63) // 64),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,414 @@
+// api.cu — host side of libexpert_attn.so: argument validation, launch planning, TMA tensor-map
+// encoding (cached), workspace layout and the three launches (prologue, attention, merge)
+// chained with programmatic dependent launch. See include/expert_attn.h for the contract.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "expert_attn.h"
+#include "internal.cuh"
+
+namespace ea {
+__global__ void prologue_kernel(const __grid_constant__ PrologueParams p);
+__global__ void attention_kernel(const __grid_constant__ AttnParams p);
+__global__ void merge_kernel(const __grid_constant__ MergeParams p);
+__global__ void quantize_cache_kernel(const __nv_bfloat16* src, uint8_t* dst, float* scales,
+                                      int n_rows, int Smax);
+size_t attention_smem_bytes();
+int attention_threads();
+}  // namespace ea
+
+namespace {
+
+using namespace ea;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  bool ok = false;
+  int sm_count = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+int g_splits = 0;
+
+// Queries (once per device) the SM count and that the device is an sm_103 part, and raises
+// the attention kernel's dynamic shared-memory limit.
+bool device_info(int* dev_out, DeviceInfo* info) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        major == 10 && minor == 3 && sms > 0) {
+      d.sm_count = sms;
+      d.ok = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(attention_smem_bytes())) == cudaSuccess;
+    }
+    cudaGetLastError();
+  }
+  *dev_out = dev;
+  *info = d;
+  return d.ok;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// Map of cache rows [0, S) of one bf16 cache [8][Smax][128]: dims {128, S, 8}, strides {256 B,
+// Smax*256 B}, box {64, 128, 1} with 128-byte swizzle. Rows >= S are outside the map, so a
+// partially covered tile arrives zero-filled and hidden rows are never read.
+struct MapKey {
+  const void* ptr;
+  int S, Smax;
+  bool operator==(const MapKey& o) const { return ptr == o.ptr && S == o.S && Smax == o.Smax; }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    return std::hash<const void*>()(k.ptr) ^ (static_cast<size_t>(k.S) * 0x9E3779B97F4A7C15ull) ^
+           (static_cast<size_t>(k.Smax) << 1);
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+bool cache_map(const void* base, int S, int Smax, CUtensorMap* out) {
+  const MapKey key{base, S, Smax};
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD),
+                              static_cast<cuuint64_t>(S > 0 ? S : 1),
+                              static_cast<cuuint64_t>(kHkv)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(Smax) * kD * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kKeyTile), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_maps.size() > 16384) g_maps.clear();
+  g_maps[key] = m;
+  *out = m;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pure argument checks (no CUDA call), so that they also run on machines without a GPU.
+int validate(const ea_layer_args* a, int n_layers, int S, int Smax, int rope_delta, int kv_dtype,
+             const void* ws, bool need_ws) {
+  if (a == nullptr || n_layers < 1) return EA_ERR_INVALID_ARG;
+  if (kv_dtype != EA_KV_BF16 && kv_dtype != EA_KV_FP8_E4M3) return EA_ERR_INVALID_ARG;
+  const int row_align = kv_dtype == EA_KV_BF16 ? kTok : kScaleBlock;
+  if (Smax < 2 * kTok || Smax % row_align != 0 || Smax > (1 << 22)) return EA_ERR_INVALID_ARG;
+  if (S < 0 || S > Smax - kTok) return EA_ERR_INVALID_ARG;
+  const long long p0 = static_cast<long long>(S) + rope_delta;
+  if (p0 <= -(1LL << 24) + kTok || p0 + kTok >= (1LL << 24)) return EA_ERR_INVALID_ARG;
+  if (need_ws && ws == nullptr) return EA_ERR_INVALID_ARG;
+  if (need_ws && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return EA_ERR_MISALIGNED;
+  for (int l = 0; l < n_layers; ++l) {
+    const ea_layer_args& x = a[l];
+    const void* req[] = {x.q_raw, x.k_raw, x.v_raw, x.q_gamma, x.k_gamma, x.k_cache, x.v_cache, x.out};
+    for (const void* p : req) {
+      if (p == nullptr) return EA_ERR_INVALID_ARG;
+      if (!aligned16(p)) return EA_ERR_MISALIGNED;
+    }
+    if (x.q_rope != nullptr && !aligned16(x.q_rope)) return EA_ERR_MISALIGNED;
+    if (kv_dtype == EA_KV_FP8_E4M3) {
+      if (x.k_scale == nullptr || x.v_scale == nullptr) return EA_ERR_INVALID_ARG;
+      if ((reinterpret_cast<uintptr_t>(x.k_scale) & 3u) || (reinterpret_cast<uintptr_t>(x.v_scale) & 3u))
+        return EA_ERR_MISALIGNED;
+    }
+  }
+  return EA_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// RoPE inverse frequencies theta^(-2j/128) = 5e6^(-j/64), j < 64, as fp32 (hi, lo) pairs.
+void rope_inv_freq(float* hi, float* lo) {
+  for (int j = 0; j < kD / 2; ++j) {
+    const double inv = std::pow(5.0e6, -static_cast<double>(j) / (kD / 2));
+    hi[j] = static_cast<float>(inv);
+    lo[j] = static_cast<float>(inv - static_cast<double>(hi[j]));
+  }
+}
+
+int n_ctas_for(long long W, int sm_count) {
+  int n = g_splits > 0 && g_splits < sm_count ? g_splits : sm_count;
+  if (static_cast<long long>(n) > W) n = static_cast<int>(W);
+  return n < 1 ? 1 : n;
+}
+
+int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
+                    uint8_t* ws, const WsLayout& wl, cudaStream_t st) {
+  PrologueParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  for (int l = 0; l < n; ++l) {
+    PrologueLayer& d = pp.layer[l];
+    d.q_raw = static_cast<const __nv_bfloat16*>(a[l].q_raw);
+    d.k_raw = static_cast<const __nv_bfloat16*>(a[l].k_raw);
+    d.v_raw = static_cast<const __nv_bfloat16*>(a[l].v_raw);
+    d.q_gamma = static_cast<const __nv_bfloat16*>(a[l].q_gamma);
+    d.k_gamma = static_cast<const __nv_bfloat16*>(a[l].k_gamma);
+    d.k_cache = a[l].k_cache;
+    d.v_cache = a[l].v_cache;
+    d.k_scale = a[l].k_scale;
+    d.v_scale = a[l].v_scale;
+    d.q_rope = static_cast<__nv_bfloat16*>(a[l].q_rope);
+  }
+  rope_inv_freq(pp.inv_hi, pp.inv_lo);
+  pp.q_ws = ws + wl.q_off;
+  pp.tail_ws = ws + wl.tail_off;
+  pp.n_layers = n;
+  pp.S = S;
+  pp.Smax = Smax;
+  pp.rope_delta = rope_delta;
+  pp.fp8 = fp8 ? 1 : 0;
+  prologue_kernel<<<n * kHkv, 256, 0, st>>>(pp);
+  return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
+                 uint8_t* ws, const WsLayout& wl, const DeviceInfo& di, cudaStream_t st,
+                 cudaEvent_t const* ev) {
+  if (fp8) return EA_ERR_UNSUPPORTED;  // FP8 attention kernel: not part of this build yet
+  const bool pdl = ev == nullptr;
+  if (ev && ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return EA_ERR_CUDA;
+  int rc = launch_prologue(a, n, S, Smax, rope_delta, fp8, ws, wl, st);
+  if (rc != EA_OK) return rc;
+  if (ev && ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return EA_ERR_CUDA;
+
+  static AttnParams ap;  // large (~19 KB): kept off the stack; guarded by g_launch_mu
+  static MergeParams mp;
+  static std::mutex g_launch_mu;
+  std::lock_guard<std::mutex> lk(g_launch_mu);
+  std::memset(&ap, 0, sizeof(ap));
+  for (int l = 0; l < n; ++l) {
+    if (!cache_map(a[l].k_cache, S, Smax, &ap.kmap[l]) ||
+        !cache_map(a[l].v_cache, S, Smax, &ap.vmap[l]))
+      return EA_ERR_CUDA;
+    ap.out[l] = static_cast<__nv_bfloat16*>(a[l].out);
+  }
+  const int n_main = (S + kKeyTile - 1) / kKeyTile;
+  ap.T = n_main + 1;
+  ap.n_main = n_main;
+  ap.S = S;
+  ap.Smax = Smax;
+  ap.W = static_cast<long long>(n) * kHkv * ap.T;
+  ap.q_ws = ws + wl.q_off;
+  ap.tail_ws = ws + wl.tail_off;
+  ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
+  ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
+  ap.status = reinterpret_cast<uint32_t*>(ws);
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+  const int n_ctas = n_ctas_for(ap.W, di.sm_count);
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(n_ctas);
+  cfg.blockDim = dim3(attention_threads());
+  cfg.dynamicSmemBytes = attention_smem_bytes();
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, attention_kernel, ap) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  if (ev && ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return EA_ERR_CUDA;
+
+  std::memset(&mp, 0, sizeof(mp));
+  for (int l = 0; l < n; ++l) mp.out[l] = ap.out[l];
+  mp.part_o = ap.part_o;
+  mp.part_lse = ap.part_lse;
+  mp.W = ap.W;
+  mp.T = ap.T;
+  mp.n_ctas = n_ctas;
+  cfg.gridDim = dim3(n * kHkv);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel, mp) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  if (ev && ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return EA_ERR_CUDA;
+  return EA_OK;
+}
+
+int run_layers(const ea_layer_args* a, int n_layers, int S, int Smax, int rope_delta, int kv_dtype,
+               void* workspace, size_t ws_bytes, ea_stream_t stream, cudaEvent_t const* ev) {
+  int rc = validate(a, n_layers, S, Smax, rope_delta, kv_dtype, workspace, true);
+  if (rc != EA_OK) return rc;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  const int per = n_layers < kMaxLayersPerLaunch ? n_layers : kMaxLayersPerLaunch;
+  const WsLayout wl = ws_layout(per, di.sm_count);
+  if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (int l0 = 0; l0 < n_layers; l0 += per) {
+    const int n = n_layers - l0 < per ? n_layers - l0 : per;
+    rc = launch_chunk(a + l0, n, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3, ws, wl, di, st,
+                      l0 == 0 ? ev : nullptr);
+    if (rc != EA_OK) return rc;
+  }
+  return EA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t expert_attn_workspace_size(int n_layers, int Smax, int kv_dtype) {
+  if (n_layers < 1 || Smax < 2 * kTok) return 0;
+  if (kv_dtype != EA_KV_BF16 && kv_dtype != EA_KV_FP8_E4M3) return 0;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return 0;
+  const int per = n_layers < kMaxLayersPerLaunch ? n_layers : kMaxLayersPerLaunch;
+  return ws_layout(per, di.sm_count).total;
+}
+
+int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < 1024) return EA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, 1024, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return EA_OK;
+}
+
+int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
+                         void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  int rc = validate(a, 1, S, Smax, rope_delta, kv_dtype, workspace, true);
+  if (rc != EA_OK) return rc;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  const WsLayout wl = ws_layout(1, di.sm_count);
+  if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
+  return launch_prologue(a, 1, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3,
+                         static_cast<uint8_t*>(workspace), wl, static_cast<cudaStream_t>(stream));
+}
+
+int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
+                      void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  return run_layers(a, 1, S, Smax, rope_delta, kv_dtype, workspace, ws_bytes, stream, nullptr);
+}
+
+int expert_attn_layers(const ea_layer_args* layers, int n_layers, int S, int Smax, int rope_delta,
+                       int kv_dtype, void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  return run_layers(layers, n_layers, S, Smax, rope_delta, kv_dtype, workspace, ws_bytes, stream,
+                    nullptr);
+}
+
+int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S, int Smax,
+                                int rope_delta, int kv_dtype, void* workspace, size_t ws_bytes,
+                                ea_stream_t stream, void* const events[4]) {
+  if (events == nullptr) return EA_ERR_INVALID_ARG;
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i) ev[i] = static_cast<cudaEvent_t>(events[i]);
+  return run_layers(layers, n_layers, S, Smax, rope_delta, kv_dtype, workspace, ws_bytes, stream, ev);
+}
+
+int expert_attn_quantize_cache(const void* src_bf16, int n_rows, int Smax, void* dst_codes,
+                               float* scales, ea_stream_t stream) {
+  if (src_bf16 == nullptr || dst_codes == nullptr || scales == nullptr) return EA_ERR_INVALID_ARG;
+  if (Smax < 2 * kTok || Smax % kScaleBlock != 0 || Smax > (1 << 22)) return EA_ERR_INVALID_ARG;
+  if (n_rows < 0 || n_rows > Smax - kTok) return EA_ERR_INVALID_ARG;
+  if (!aligned16(src_bf16) || !aligned16(dst_codes) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return EA_ERR_MISALIGNED;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return EA_OK;
+  quantize_cache_kernel<<<kHkv * (Smax / kScaleBlock), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(src_bf16), static_cast<uint8_t*>(dst_codes), scales, n_rows,
+      Smax);
+  return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+int expert_attn_set_splits(int n_ctas_or_0_for_auto) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  const int prev = g_splits;
+  g_splits = n_ctas_or_0_for_auto > 0 ? n_ctas_or_0_for_auto : 0;
+  return prev;
+}
+
+int expert_attn_read_status(const void* workspace, ea_stream_t stream, int* status_out,
+                            uint32_t* bits_out) {
+  if (workspace == nullptr || status_out == nullptr) return EA_ERR_INVALID_ARG;
+  uint32_t bits = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  *status_out = bits == 0 ? EA_OK : EA_ERR_TIMEOUT;
+  if (bits_out) *bits_out = bits;
+  return EA_OK;
+}
+
+const char* expert_attn_status_string(int status) {
+  switch (status) {
+    case EA_OK: return "EA_OK";
+    case EA_ERR_INVALID_ARG: return "EA_ERR_INVALID_ARG: invalid argument";
+    case EA_ERR_MISALIGNED: return "EA_ERR_MISALIGNED: pointer not aligned as required";
+    case EA_ERR_UNSUPPORTED: return "EA_ERR_UNSUPPORTED: no sm_103 device or unsupported variant";
+    case EA_ERR_WORKSPACE: return "EA_ERR_WORKSPACE: workspace too small";
+    case EA_ERR_CUDA: return "EA_ERR_CUDA: CUDA call or kernel launch failed";
+    case EA_ERR_TIMEOUT: return "EA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// internal.cuh — constants, kernel parameter blocks and the workspace layout shared by the
+// kernels and the host side of libexpert_attn.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ea {
+
+// Problem dimensions (alpamayo_tt/EXPERT_NOTES.md, section "Layouts"): 16 query heads, 8 KV
+// heads, head width 128, 64 expert tokens. Folding the two query heads of a GQA group over the
+// token axis gives 128 query rows per KV head (section "Attention over the VLM cache").
+constexpr int kHq = 16;
+constexpr int kHkv = 8;
+constexpr int kD = 128;
+constexpr int kTok = 64;
+constexpr int kRows = 128;        // folded query rows per KV head: row r = (h % 2) * 64 + t
+constexpr int kKeyTile = 128;     // cache rows per key tile
+constexpr int kMaxLayersPerLaunch = 64;
+constexpr int kScaleBlock = 128;  // FP8 scale granularity (rows)
+
+// Bytes of one staged operand tile in the 128-byte-swizzled K-major layout: two 64-column
+// halves ("atoms"), each [rows][128 bytes]; inside every 8-row group of 1024 bytes the 16-byte
+// chunks of row r are permuted as chunk' = chunk ^ (r % 8).
+constexpr uint32_t kQTileBytes = kRows * kD * 2;          // 32 KB: roped Q of one (layer, kv head)
+constexpr uint32_t kTailHalfBytes = kTok * kD * 2;        // 16 KB: own K (or V) rows, 64 x 128
+constexpr uint32_t kTailUnitBytes = 2 * kTailHalfBytes;   // K then V
+
+// Status bits recorded in the workspace when a bounded wait gives up.
+enum : uint32_t {
+  kErrProducerWait = 1u << 0,
+  kErrMmaWait = 1u << 1,
+  kErrSoftmaxWait = 1u << 2,
+  kErrDrain = 1u << 3,
+};
+
+// ------------------------------------------------------------------------- workspace layout
+//   [0, 1024)                    status word (first 4 bytes), rest reserved
+//   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; f16 FP8)
+//   tail    n_layers * 8 * 32 KB  own K rows then own V rows per (layer, kv head), swizzled
+//   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
+//   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
+struct WsLayout {
+  size_t q_off, tail_off, part_o_off, part_lse_off, total;
+};
+
+inline WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
+  WsLayout w;
+  size_t off = 1024;
+  w.q_off = off;
+  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
+  w.tail_off = off;
+  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kTailUnitBytes;
+  w.part_o_off = off;
+  off += static_cast<size_t>(max_ctas) * 2 * kRows * kD * sizeof(float);
+  w.part_lse_off = off;
+  off += static_cast<size_t>(max_ctas) * 2 * kRows * sizeof(float);
+  w.total = (off + 1023) & ~static_cast<size_t>(1023);
+  return w;
+}
+
+// ------------------------------------------------------------------------ parameter blocks
+struct PrologueLayer {
+  const __nv_bfloat16* q_raw;
+  const __nv_bfloat16* k_raw;
+  const __nv_bfloat16* v_raw;
+  const __nv_bfloat16* q_gamma;
+  const __nv_bfloat16* k_gamma;
+  void* k_cache;
+  void* v_cache;
+  float* k_scale;
+  float* v_scale;
+  __nv_bfloat16* q_rope;
+};
+
+struct PrologueParams {
+  PrologueLayer layer[kMaxLayersPerLaunch];
+  float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
+  float inv_lo[kD / 2];
+  uint8_t* q_ws;
+  uint8_t* tail_ws;
+  int n_layers, S, Smax, rope_delta, fp8;
+};
+
+struct AttnParams {
+  CUtensorMap kmap[kMaxLayersPerLaunch];  // cache rows [0, S) of K: dims {128, S, 8}, box {64,128,1}
+  CUtensorMap vmap[kMaxLayersPerLaunch];
+  __nv_bfloat16* out[kMaxLayersPerLaunch];
+  const uint8_t* kc8[kMaxLayersPerLaunch];  // FP8: e4m3 caches and scales (unused for bf16)
+  const uint8_t* vc8[kMaxLayersPerLaunch];
+  const float* ks[kMaxLayersPerLaunch];
+  const float* vs[kMaxLayersPerLaunch];
+  const uint8_t* q_ws;
+  const uint8_t* tail_ws;
+  float* part_o;
+  float* part_lse;
+  uint32_t* status;
+  long long W;         // total key tiles = n_layers * 8 * T
+  int T;               // key tiles per (layer, kv head): n_main cache tiles + 1 own-row tile
+  int n_main;          // ceil(S / 128)
+  int S, Smax;
+  float scale_log2;    // log2(e) / sqrt(128)
+};
+
+struct MergeParams {
+  __nv_bfloat16* out[kMaxLayersPerLaunch];
+  const float* part_o;
+  const float* part_lse;
+  long long W;
+  int T;
+  int n_ctas;
+};
+
+// The key tiles of all (layer, kv head) units, in unit-major order, are cut into n_ctas
+// contiguous ranges; CTA c owns tiles [c*W/n, (c+1)*W/n).
+__host__ __device__ inline long long cta_tile_start(int c, long long W, int n_ctas) {
+  return static_cast<long long>(c) * W / n_ctas;
+}
+
+}  // namespace ea

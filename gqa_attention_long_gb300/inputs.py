@@ -109,3 +109,18 @@ CONFIGS = {
 
 def config_seed(config: int, layer: int) -> int:
     return 0 if config == 0 else 1000 * config + layer
+
+
+def layer_inputs_on_device(seed: int, S: int, Smax: int, device, hidden_fill: float = 7.0) -> LayerInputs:
+    """Same distributions as :func:`layer_inputs`, drawn directly on ``device`` with a seeded
+    generator of that device (used to fill the many layers of a full-size step quickly; the
+    values differ from the CPU draw of the same seed)."""
+    assert 0 <= S <= Smax - T and Smax % T == 0
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    bf = torch.bfloat16
+    r = lambda *shape: torch.randn(*shape, generator=g, device=device)  # noqa: E731
+    x = LayerInputs(r(HQ, T, D).to(bf), r(HKV, T, D).to(bf), r(HKV, T, D).to(bf),
+                    (1.0 + 0.1 * r(D)).to(bf), (1.0 + 0.1 * r(D)).to(bf),
+                    r(HKV, Smax, D).to(bf), r(HKV, Smax, D).to(bf), int(S), int(Smax))
+    fill_hidden(x.k_cache, x.v_cache, S, Smax, hidden_fill, seed)
+    return x

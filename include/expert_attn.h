@@ -1,0 +1,133 @@
+/*
+ * expert_attn.h — C ABI of the GB300 (sm_103a) expert-attention library, libexpert_attn.so.
+ *
+ * The operation (alpamayo_tt/expert.py, TTExpert.layer and TTExpert.attention_core;
+ * alpamayo_tt/EXPERT_NOTES.md, sections "Layouts" and "Attention over the VLM cache: masking
+ * approach"): per layer, 64 expert tokens with 16 query heads and 8 KV heads of width 128
+ *   1. RMS-normalise every q and k head row over its 128 channels with a multiplicative gain
+ *      (eps 1e-6) and rotate it with the HF rotate_half RoPE, theta 5e6, at position
+ *      t + rope_delta + S for token t;
+ *   2. write the 64 roped k rows and the 64 raw v rows into rows [Smax-64, Smax) of the
+ *      layer's K and V caches;
+ *   3. let every token attend, non-causally, to cache rows [0, S) and to those 64 own rows
+ *      (rows [S, Smax-64) are hidden: they are never read nor written); query head h uses
+ *      KV head h/2, the score scale is 1/sqrt(128), softmax statistics are kept in fp32.
+ *
+ * Layouts (all row-major, little-endian, no padding):
+ *   q_raw    bf16 [16][64][128]   head-major (q_raw[h][t][d])
+ *   k_raw    bf16 [8][64][128]
+ *   v_raw    bf16 [8][64][128]
+ *   q_gamma  bf16 [128]           q_norm gain;   k_gamma bf16 [128] k_norm gain
+ *   k_cache  [8][Smax][128]       bf16, or e4m3 bytes for EA_KV_FP8_E4M3; v_cache likewise
+ *   k_scale  fp32 [8][Smax/128 + 1] (FP8 only): column b scales rows [128b, 128b+128);
+ *            column Smax/128 scales the 64 own rows [Smax-64, Smax). v_scale likewise.
+ *   out      bf16 [16][64][128]   attention output, head-major
+ *   q_rope   optional bf16 [16][64][128]: the normalised, roped q (NULL to skip)
+ *
+ * Ownership: the caller owns every buffer. The library allocates no device memory. It
+ * writes only out, q_rope, the workspace, cache rows [Smax-64, Smax) and (FP8) the last
+ * scale column. Calls are asynchronous on the given stream (a cudaStream_t, NULL = legacy
+ * default stream). Calls that share one workspace must not overlap on the GPU.
+ *
+ * Errors: argument errors return before anything is launched. EA_ERR_CUDA reports a failed
+ * launch. A kernel that gives up a bounded wait records EA_ERR_TIMEOUT in the workspace's
+ * status word, which expert_attn_read_status returns.
+ */
+#ifndef EXPERT_ATTN_H
+#define EXPERT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EA_OK = 0,
+  EA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, S out of [0, Smax-64], ... */
+  EA_ERR_MISALIGNED = 2,   /* a pointer is not aligned as documented below */
+  EA_ERR_UNSUPPORTED = 3,  /* no sm_103 GPU, or a dtype / size this build does not cover */
+  EA_ERR_WORKSPACE = 4,    /* workspace smaller than expert_attn_workspace_size() */
+  EA_ERR_CUDA = 5,         /* a CUDA runtime call or a launch failed */
+  EA_ERR_TIMEOUT = 6       /* a kernel gave up a bounded wait (see expert_attn_read_status) */
+} ea_status;
+
+typedef enum { EA_KV_BF16 = 0, EA_KV_FP8_E4M3 = 1 } ea_kv_dtype;
+
+/* A cudaStream_t, passed as an opaque pointer so that this header needs no CUDA header. */
+typedef void* ea_stream_t;
+
+/* One layer's buffers (device pointers). Alignment: every pointer 16 bytes; Smax a multiple
+ * of 64 (bf16) or 128 (FP8). */
+typedef struct {
+  const void* q_raw;
+  const void* k_raw;
+  const void* v_raw;
+  const void* q_gamma;
+  const void* k_gamma;
+  void* k_cache;
+  void* v_cache;
+  float* k_scale; /* FP8 only, else NULL */
+  float* v_scale; /* FP8 only, else NULL */
+  void* out;
+  void* q_rope;   /* optional, may be NULL */
+} ea_layer_args;
+
+/* Bytes of device workspace needed by a call over n_layers layers on the current device
+ * (0 if no suitable device is present). The workspace must be 256-byte aligned and, before
+ * its first use, cleared with expert_attn_workspace_init. */
+size_t expert_attn_workspace_size(int n_layers, int Smax, int kv_dtype);
+
+/* Clears the workspace's status word (asynchronous on stream). */
+int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream);
+
+/* Steps 1 + 2 only (alpamayo_tt/expert.py, TTExpert.layer: q/k rms_norm, rotary_embedding_hf,
+ * fill_cache): norm and rope q and k of one layer, write the own k/v rows into the cache tail
+ * (FP8: quantised with their own scale slot), and stage the roped q in the workspace (and in
+ * a->q_rope when it is not NULL). Requires 0 <= S <= Smax-64 and |S + rope_delta| + 64 < 2^24. */
+int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
+                         void* workspace, size_t ws_bytes, ea_stream_t stream);
+
+/* Steps 1-3 for one layer (the unit TTExpert.layer_fn can hand to a fused kernel): prologue,
+ * split-KV attention on the tensor cores, log-sum-exp merge; writes a->out. */
+int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
+                      void* workspace, size_t ws_bytes, ea_stream_t stream);
+
+/* Steps 1-3 for n_layers independent layers in one call (the 64 layers of one Euler step,
+ * alpamayo_tt/expert.py, TTExpert._forward_dev), all with the same S, Smax and rope_delta.
+ * layers is a HOST array of n_layers entries. Launches three kernels per 64 layers. */
+int expert_attn_layers(const ea_layer_args* layers, int n_layers, int S, int Smax, int rope_delta,
+                       int kv_dtype, void* workspace, size_t ws_bytes, ea_stream_t stream);
+
+/* As expert_attn_layers, and records four cudaEvent_t (passed as void*, each may be NULL) on
+ * the stream: before the prologue, before the attention kernel, after it, after the merge.
+ * Recording events between the kernels removes their launch overlap; use it to time kernels. */
+int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S, int Smax,
+                                int rope_delta, int kv_dtype, void* workspace, size_t ws_bytes,
+                                ea_stream_t stream, void* const events[4]);
+
+/* FP8 cache producer: quantises rows [0, n_rows) of one bf16 cache [8][Smax][128] into e4m3
+ * codes (round to nearest even, saturating) with one fp32 scale amax/448 per (kv head, 128-row
+ * block) over the block's rows below n_rows (1 when amax is 0). Rows >= n_rows and their
+ * scale columns are not written. Requires Smax % 128 == 0, 0 <= n_rows <= Smax-64. */
+int expert_attn_quantize_cache(const void* src_bf16, int n_rows, int Smax, void* dst_codes,
+                               float* scales, ea_stream_t stream);
+
+/* Tuning knob: number of persistent attention CTAs (0 = one per SM, the default). Values above
+ * the SM count are clamped. Process-wide. Returns the previous setting. */
+int expert_attn_set_splits(int n_ctas_or_0_for_auto);
+
+/* Synchronises the stream and returns the status recorded in the workspace by the kernels
+ * (EA_OK or EA_ERR_TIMEOUT) in *status_out; the raw status bits go to *bits_out if not NULL. */
+int expert_attn_read_status(const void* workspace, ea_stream_t stream, int* status_out,
+                            uint32_t* bits_out);
+
+/* A static string naming a status code. */
+const char* expert_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXPERT_ATTN_H */

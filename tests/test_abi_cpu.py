@@ -1,0 +1,91 @@
+"""The C-ABI library loads, exports every function include/expert_attn.h declares, and rejects
+bad arguments on the host before any CUDA work (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_attention_long_gb300 as ea
+from gqa_attention_long_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "expert_attn.h")
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not os.path.exists(_lib.LIB_PATH):
+        from gqa_attention_long_gb300 import build
+        build.build()
+    return ea.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(expert_attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("expert_attn_prologue", "expert_attn_layer", "expert_attn_layers",
+              "expert_attn_workspace_size", "expert_attn_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(h):
+    for n in declared_functions():
+        assert hasattr(h, n), n
+
+
+def test_status_strings(h):
+    for rc in range(7):
+        assert ea.expert_attn_status_string(rc).startswith("EA_")
+    assert ea.expert_attn_status_string(99) == "unknown status"
+
+
+def _args(**over):
+    a = (_lib.EaLayerArgs * 1)()
+    for n, _ in _lib.EaLayerArgs._fields_:
+        setattr(a[0], n, 0x10000)  # aligned fake device pointers: never dereferenced by validation
+    a[0].k_scale = a[0].v_scale = a[0].q_rope = None
+    for k, v in over.items():
+        setattr(a[0], k, v)
+    return a
+
+
+@pytest.mark.parametrize("S,Smax,dt,rc", [
+    (449, 512, 0, _lib.EA_ERR_INVALID_ARG),    # S > Smax - 64
+    (-1, 512, 0, _lib.EA_ERR_INVALID_ARG),
+    (10, 500, 0, _lib.EA_ERR_INVALID_ARG),     # Smax not a multiple of 64
+    (10, 576, 1, _lib.EA_ERR_INVALID_ARG),     # FP8 needs Smax % 128 == 0 (and scales)
+    (10, 512, 7, _lib.EA_ERR_INVALID_ARG),     # unknown dtype
+])
+def test_bad_sizes_rejected(h, S, Smax, dt, rc):
+    assert h.expert_attn_layer(_args(), S, Smax, 0, dt, ctypes.c_void_p(0x100000), 1 << 30, None) == rc
+
+
+def test_null_and_misaligned_pointers_rejected(h):
+    ws = ctypes.c_void_p(0x100000)
+    assert h.expert_attn_layer(_args(q_raw=None), 10, 512, 0, 0, ws, 1 << 30, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_attn_layer(_args(k_cache=0x10008), 10, 512, 0, 0, ws, 1 << 30, None) == _lib.EA_ERR_MISALIGNED
+    assert h.expert_attn_layer(_args(), 10, 512, 0, 0, ctypes.c_void_p(0x100010), 1 << 30, None) == _lib.EA_ERR_MISALIGNED
+    assert h.expert_attn_layer(_args(), 10, 512, 0, 0, None, 1 << 30, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_attn_layers(_args(), 0, 10, 512, 0, 0, ws, 1 << 30, None) == _lib.EA_ERR_INVALID_ARG
+    # positions beyond fp32-exact integers are refused
+    assert h.expert_attn_layer(_args(), 10, 512, 1 << 24, 0, ws, 1 << 30, None) == _lib.EA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_tensors(h):
+    import torch
+    t = torch.zeros(16, 64, 128, dtype=torch.bfloat16)
+    L = ea.LayerBuffers(q_raw=t, k_raw=t[:8], v_raw=t[:8], q_gamma=t[0, 0], k_gamma=t[0, 0],
+                        k_cache=t, v_cache=t, out=t)
+    with pytest.raises(TypeError):
+        ea.expert_attn_layer(L, 0, 128, 0, 0, torch.zeros(16, dtype=torch.uint8))
+
+
+def test_set_splits_roundtrip(h):
+    prev = ea.expert_attn_set_splits(7)
+    assert ea.expert_attn_set_splits(prev) == 7
