@@ -183,8 +183,10 @@ int n_ctas_for(long long W, int sm_count) {
   return n < 1 ? 1 : n;
 }
 
+// The prologue is launched with programmatic stream serialization: its CTAs may become resident
+// while the preceding kernel drains, and wait (griddepcontrol.wait) for it before touching memory.
 int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
-                    uint8_t* ws, const WsLayout& wl, cudaStream_t st) {
+                    uint8_t* ws, const WsLayout& wl, cudaStream_t st, bool pdl) {
   PrologueParams pp;
   std::memset(&pp, 0, sizeof(pp));
   for (int l = 0; l < n; ++l) {
@@ -208,8 +210,21 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
   pp.Smax = Smax;
   pp.rope_delta = rope_delta;
   pp.fp8 = fp8 ? 1 : 0;
-  prologue_kernel<<<n * kHkv, 256, 0, st>>>(pp);
-  return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(n * kHkv);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, prologue_kernel, pp) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return EA_OK;
 }
 
 int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
@@ -218,7 +233,7 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   if (fp8) return EA_ERR_UNSUPPORTED;  // FP8 attention kernel: not part of this build yet
   const bool pdl = ev == nullptr;
   if (ev && ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return EA_ERR_CUDA;
-  int rc = launch_prologue(a, n, S, Smax, rope_delta, fp8, ws, wl, st);
+  int rc = launch_prologue(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl);
   if (rc != EA_OK) return rc;
   if (ev && ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return EA_ERR_CUDA;
 
@@ -271,8 +286,20 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   mp.W = ap.W;
   mp.T = ap.T;
   mp.n_ctas = n_ctas;
-  cfg.gridDim = dim3(n * kHkv);
-  cfg.blockDim = dim3(128);
+  // units whose tiles straddle a CTA boundary; the others are finished by the attention kernel
+  mp.n_split = 0;
+  for (int u = 0; u < n * kHkv; ++u) {
+    const long long first = static_cast<long long>(u) * ap.T, last = first + ap.T - 1;
+    int c = static_cast<int>(first * n_ctas / ap.W);
+    while (c + 1 < n_ctas && cta_tile_start(c + 1, ap.W, n_ctas) <= first) ++c;
+    while (c > 0 && cta_tile_start(c, ap.W, n_ctas) > first) --c;
+    if (c + 1 < n_ctas && cta_tile_start(c + 1, ap.W, n_ctas) <= last)
+      mp.split_unit[mp.n_split++] = static_cast<uint16_t>(u);
+  }
+  // Always launched (one idle CTA when nothing is split), so that the next call's prologue
+  // always follows a merge kernel, which triggers it only after the attention grid is done.
+  cfg.gridDim = dim3(mp.n_split > 0 ? mp.n_split * (kRows / kMergeRowsPerCta) : 1);
+  cfg.blockDim = dim3(32 * kMergeRowsPerCta);
   cfg.dynamicSmemBytes = 0;
   if (cudaLaunchKernelEx(&cfg, merge_kernel, mp) != cudaSuccess) {
     cudaGetLastError();
@@ -336,7 +363,7 @@ int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta
   const WsLayout wl = ws_layout(1, di.sm_count);
   if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
   return launch_prologue(a, 1, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3,
-                         static_cast<uint8_t*>(workspace), wl, static_cast<cudaStream_t>(stream));
+                         static_cast<uint8_t*>(workspace), wl, static_cast<cudaStream_t>(stream), true);
 }
 
 int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,

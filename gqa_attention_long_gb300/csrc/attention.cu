@@ -245,7 +245,9 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
   auto wait_pv = [&](uint32_t k) -> bool {
     if (pv_seen > k) return true;
     pv_seen = k + 1;
-    return bounded_wait(cx.bar(B_ODONE), k & 1, cx.abort_flag, cx.status, kErrSoftmaxWait);
+    // warp-uniform outcome: the TMEM loads and shuffles that follow need the full warp
+    return __all_sync(0xffffffffu, bounded_wait(cx.bar(B_ODONE), k & 1, cx.abort_flag, cx.status,
+                                                kErrSoftmaxWait));
   };
 
   while (ok && next_seg(t, cx.end, p.T, s)) {
@@ -255,8 +257,8 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
     for (int i = 0; i < nt; ++i) {
       const int j = s.j0 + i;
       const uint32_t sb = n_s & 1;
-      ok = bounded_wait(cx.bar(B_SFULL + sb), (n_s >> 1) & 1, cx.abort_flag, cx.status,
-                        kErrSoftmaxWait);
+      ok = __all_sync(0xffffffffu, bounded_wait(cx.bar(B_SFULL + sb), (n_s >> 1) & 1,
+                                                cx.abort_flag, cx.status, kErrSoftmaxWait));
       if (!ok) break;
       ++n_s;
       tc_fence_after();
@@ -373,7 +375,7 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
       }
     }
     if (!full)
-      p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = m_ref + __log2f(lsum);
+      p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = m_ref + log2f(lsum);
     tc_fence_before();
     pv_total += nt;
     ++seg;

@@ -104,6 +104,10 @@ struct AttnParams {
   float scale_log2;    // log2(e) / sqrt(128)
 };
 
+// Units whose key tiles span more than one CTA range; the merge kernel visits only these.
+constexpr int kMaxSplitUnits = kMaxLayersPerLaunch * kHkv;
+constexpr int kMergeRowsPerCta = 8;  // one warp per folded row
+
 struct MergeParams {
   __nv_bfloat16* out[kMaxLayersPerLaunch];
   const float* part_o;
@@ -111,6 +115,8 @@ struct MergeParams {
   long long W;
   int T;
   int n_ctas;
+  int n_split;
+  uint16_t split_unit[kMaxSplitUnits];
 };
 
 // The key tiles of all (layer, kv head) units, in unit-major order, are cut into n_ctas

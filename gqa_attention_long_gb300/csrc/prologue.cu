@@ -40,14 +40,17 @@ __device__ __forceinline__ void rope_cos_sin(int pos, float inv_hi, float inv_lo
   sincosf(r, &s, &c);
 }
 
-__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* src, float (&x)[8]) {
-  const uint4 v = *reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&x)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     x[2 * e] = __uint_as_float(w[e] << 16);
     x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
   }
+}
+
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* src, float (&x)[8]) {
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(src), x);
 }
 
 __device__ __forceinline__ uint4 pack8(const float (&y)[8], bool f16) {
@@ -117,8 +120,10 @@ __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& 
 }  // namespace
 
 __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ PrologueParams p) {
-  // Let the attention kernel's CTAs start their set-up; they wait for this grid's memory
-  // before reading anything written here.
+  // Launched programmatically after the previous kernel in the stream: wait for it (it may have
+  // produced q/k/v, or still read the workspace), then let the attention kernel's CTAs start
+  // their set-up; they wait for this grid before reading anything written here.
+  pdl_wait_primary();
   pdl_launch_dependents();
   __shared__ float red[8];
 
@@ -146,6 +151,18 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   float kr[4][8], vr[4][8];  // kept for the FP8 path, whose scale needs all 64 rows first
   float kmax = 0.f, vmax = 0.f;
 
+  // All raw rows of this thread's 4 tokens are requested before any arithmetic, so that the
+  // loads overlap instead of paying one memory latency per token.
+  uint4 rq[4][2], rk[4], rv[4];
+#pragma unroll
+  for (int tt = 0; tt < 4; ++tt) {
+    const int t = hw + 16 * tt;
+    rq[tt][0] = *reinterpret_cast<const uint4*>(L.q_raw + (static_cast<size_t>(2 * g) * kTok + t) * kD + d0);
+    rq[tt][1] = *reinterpret_cast<const uint4*>(L.q_raw + (static_cast<size_t>(2 * g + 1) * kTok + t) * kD + d0);
+    rk[tt] = *reinterpret_cast<const uint4*>(L.k_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0);
+    rv[tt] = *reinterpret_cast<const uint4*>(L.v_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0);
+  }
+
 #pragma unroll
   for (int tt = 0; tt < 4; ++tt) {
     const int t = hw + 16 * tt;
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
     for (int hh = 0; hh < 2; ++hh) {
       const int h = 2 * g + hh;
       float x[8], y[8];
-      load_bf16x8(L.q_raw + (static_cast<size_t>(h) * kTok + t) * kD + d0, x);
+      unpack_bf16x8(rq[tt][hh], x);
       norm_rope(x, gq, cs, sn, upper, y);
       const int r = hh * kTok + t;
       *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = pack8(y, fp8);
@@ -167,10 +184,9 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
             pack8(y, false);
     }
     float x[8];
-    load_bf16x8(L.k_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0, x);
+    unpack_bf16x8(rk[tt], x);
     norm_rope(x, gk, cs, sn, upper, kr[tt]);
-    const uint4 vraw =
-        *reinterpret_cast<const uint4*>(L.v_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0);
+    const uint4 vraw = rv[tt];
     const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
     const uint32_t so = swz_off(t, i, kTailHalfBytes / 2);
     if (!fp8) {
@@ -180,7 +196,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
       *reinterpret_cast<uint4*>(tdst + so) = kb;
       *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + so) = vraw;
     } else {
-      load_bf16x8(L.v_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0, vr[tt]);
+      unpack_bf16x8(vraw, vr[tt]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         kmax = fmaxf(kmax, fabsf(kr[tt][e]));

@@ -12,16 +12,26 @@ generated ones) and is not available, so a standard-normal bf16 cache stands in 
 Hidden rows [S, Smax-64) are filled with a constant (the pages' tests use 7.0) or with
 arbitrary garbage to check that they are never read.
 
-Everything is drawn on the CPU with ``torch.Generator`` so that a given seed yields the same
-bytes on every machine.
+Everything is drawn on the CPU from numpy's PCG64 bit generator (a platform-independent
+integer stream; normals by its ziggurat in float64) and then rounded to bf16, so a given seed
+yields the same bytes on x86 and on Arm. (torch's CPU ``randn`` is not bit-identical across
+instruction sets: its vectorised transform differs in the last bits, which flips the bf16
+rounding of a few values.)
 """
 from __future__ import annotations
 
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 HQ, HKV, D, T = 16, 8, 128, 64
+
+
+def _bf16(a: np.ndarray) -> torch.Tensor:
+    """float64 samples -> float32 -> bf16 tensor. Both casts are IEEE round-to-nearest-even
+    conversions, so the result is the same on every platform."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
 
 
 @dataclass
@@ -47,15 +57,14 @@ def layer_inputs(seed: int, S: int, Smax: int, hidden_fill: float | str = 7.0,
     rewritten by the path anyway).
     """
     assert 0 <= S <= Smax - T and Smax % T == 0
-    g = torch.Generator().manual_seed(int(seed))
-    bf = torch.bfloat16
-    q_raw = torch.randn(HQ, T, D, generator=g).to(bf)
-    k_raw = torch.randn(HKV, T, D, generator=g).to(bf)
-    v_raw = torch.randn(HKV, T, D, generator=g).to(bf)
-    q_gamma = (1.0 + 0.1 * torch.randn(D, generator=g)).to(bf)
-    k_gamma = (1.0 + 0.1 * torch.randn(D, generator=g)).to(bf)
-    k_cache = torch.randn(HKV, Smax, D, generator=g).to(bf)
-    v_cache = torch.randn(HKV, Smax, D, generator=g).to(bf)
+    rng = np.random.Generator(np.random.PCG64(int(seed)))
+    q_raw = _bf16(rng.standard_normal((HQ, T, D)))
+    k_raw = _bf16(rng.standard_normal((HKV, T, D)))
+    v_raw = _bf16(rng.standard_normal((HKV, T, D)))
+    q_gamma = _bf16(1.0 + 0.1 * rng.standard_normal(D))
+    k_gamma = _bf16(1.0 + 0.1 * rng.standard_normal(D))
+    k_cache = _bf16(rng.standard_normal((HKV, Smax, D)))
+    v_cache = _bf16(rng.standard_normal((HKV, Smax, D)))
     fill_hidden(k_cache, v_cache, S, Smax, hidden_fill, seed)
     if tail_fill is not None:
         k_cache[:, Smax - T:] = tail_fill
@@ -71,9 +80,9 @@ def fill_hidden(k_cache: torch.Tensor, v_cache: torch.Tensor, S: int, Smax: int,
         return
     if isinstance(hidden_fill, str):
         if hidden_fill == "garbage":
-            g = torch.Generator().manual_seed(int(seed) + 7919)
+            rng = np.random.Generator(np.random.PCG64(int(seed) + 7919))
             for c in (k_cache, v_cache):
-                c[:, lo:hi] = (1e4 * torch.randn(c.shape[0], hi - lo, c.shape[2], generator=g)).to(c.dtype)
+                c[:, lo:hi] = _bf16(1e4 * rng.standard_normal((c.shape[0], hi - lo, c.shape[2]))).to(c.device)
         elif hidden_fill == "nan":
             k_cache[:, lo:hi] = float("nan")
             v_cache[:, lo:hi] = float("nan")

@@ -37,10 +37,13 @@ def test_prologue_matches_oracle_and_touches_only_the_tail():
     ea.expert_attn_prologue(L, S, Smax, delta, ea.EA_KV_BF16, ws)
     torch.cuda.synchronize()
     r = oracle_layer(x, rope_delta=delta)
+    # fp32 evaluation of O(1) terms errs by ~1e-6 absolute; near-zero outputs (cancellation in
+    # the rotation) have a bf16 step far below that, hence the absolute slack.
     q = f64(L.q_rope)
-    assert np.all(np.abs(q - r["q"]) <= bf16_ulp(r["q"]) * 1.001 + 1e-30)
+    assert np.all(np.abs(q - r["q"]) <= bf16_ulp(r["q"]) + 1e-5)
+    assert np.mean(np.abs(q - r["q"]) <= 0.5 * bf16_ulp(r["q"]) + 1e-6) > 0.999
     k_tail = f64(L.k_cache[:, Smax - 64:])
-    assert np.all(np.abs(k_tail - r["k"]) <= bf16_ulp(r["k"]) * 1.001 + 1e-30)
+    assert np.all(np.abs(k_tail - r["k"]) <= bf16_ulp(r["k"]) + 1e-5)
     assert np.mean(k_tail == r["k_store"]) > 0.99  # equal to the oracle's bf16 store but for ties
     assert torch.equal(L.v_cache[:, Smax - 64:], x.v_raw.cuda())
     assert torch.equal(L.k_cache[:, :Smax - 64], k_before[:, :Smax - 64])
@@ -107,7 +110,7 @@ def test_many_layers_one_call():
 
 @pytest.mark.parametrize("splits", [1, 5, 37, 0])
 def test_split_count_does_not_change_the_result(splits):
-    x = layer_inputs(11, 2000, 2048)
+    x = layer_inputs(11, 2000, 2112)
     ea.expert_attn_set_splits(splits)
     try:
         L = run_layer(x)
