@@ -439,3 +439,61 @@ const char* expert_attn_status_string(int status) {
 }
 
 }  // extern "C"
+
+// -------------------------------------------------------------- no-allocation variant
+// expert_attn_layers_noalloc runs the same three launches as expert_attn_layers, with the
+// workspace replaced by a static device array. Host code must not use the array's name as a
+// pointer (that is a host-side stand-in); its device address is looked up once per device.
+namespace {
+
+constexpr size_t noalloc_bytes() {
+  return ((1024 + 2 * static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kQTileBytes +
+           static_cast<size_t>(EA_NOALLOC_MAX_CTAS) * 2 * kRows * (kD + 1) * sizeof(float)) +
+          1023) & ~static_cast<size_t>(1023);
+}
+static_assert(noalloc_bytes() == EA_NOALLOC_SCRATCH_BYTES, "scratch size in the header is stale");
+static_assert(kQTileBytes == kTailUnitBytes, "q and tail staging have the same size per unit");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EA_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_ptr[kMaxDevices];
+
+// Device address of the scratch on the current device (looked up on first use per device).
+void* noalloc_scratch(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S,
+                                          int Smax, int rope_delta, int kv_dtype,
+                                          ea_stream_t stream) {
+  int rc = validate(layers, n_layers, S, Smax, rope_delta, kv_dtype, nullptr, false);
+  if (rc != EA_OK) return rc;
+  if (n_layers > EA_NOALLOC_MAX_LAYERS) return EA_ERR_WORKSPACE;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  DeviceInfo capped = di;
+  if (capped.sm_count > EA_NOALLOC_MAX_CTAS) capped.sm_count = EA_NOALLOC_MAX_CTAS;
+  const WsLayout wl = ws_layout(n_layers, capped.sm_count);
+  if (wl.total > EA_NOALLOC_SCRATCH_BYTES) return EA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
+  if (ws == nullptr) return EA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 1024, st) != cudaSuccess) {  // the status word must start at 0
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return launch_chunk(layers, n_layers, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3, ws, wl,
+                      capped, st, nullptr);
+}

@@ -126,6 +126,31 @@ int expert_attn_read_status(const void* workspace, ea_stream_t stream, int* stat
 /* A static string naming a status code. */
 const char* expert_attn_status_string(int status);
 
+/* ---- Variant without a caller-provided workspace (the pages have no counterpart to this).
+ *
+ * Some callers cannot allocate device memory at all: a plugin hosted by an engine that owns the
+ * whole device-memory budget and hands plugins no allocator, or a latency-critical loop where
+ * cudaMalloc / cudaFree are banned because they can synchronise the device. This entry point
+ * serves them: it does exactly what expert_attn_layers does, but its scratch (staged roped q,
+ * own rows, split partials, status word) lives in one static device array compiled into the
+ * library, EA_NOALLOC_SCRATCH_BYTES large, which every GPU that loads the library holds until the
+ * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Limits: at most EA_NOALLOC_MAX_LAYERS layers per call (more return EA_ERR_WORKSPACE before
+ * anything is launched) and at most EA_NOALLOC_MAX_CTAS attention CTAs (fewer than one per SM on
+ * a GB300, so it is slower than expert_attn_layers for large steps).
+ * Set-up: the first call on a device looks up the array's device address on that device (which
+ * must be current); make that first call before any stream capture.
+ * Sharing: all calls in the process share the array and find the previous call's contents in
+ * it; each call clears the status word itself. Calls that overlap on the GPU (for example on
+ * two streams) race on the array and must be avoided. Timeouts of bounded waits are recorded
+ * in the array's status word and are not reported by this call. */
+#define EA_NOALLOC_MAX_LAYERS 4
+#define EA_NOALLOC_MAX_CTAS 64
+#define EA_NOALLOC_SCRATCH_BYTES 10552320u /* status 1 KB + 4 x 512 KB + 64 x 2 x 66 KB */
+int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S, int Smax,
+                               int rope_delta, int kv_dtype, ea_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
