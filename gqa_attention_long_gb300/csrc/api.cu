@@ -1,6 +1,6 @@
 // api.cu — host side of libexpert_attn.so: argument validation, launch planning, TMA tensor-map
-// encoding (cached), workspace layout and the three launches (prologue, attention, merge)
-// chained with programmatic dependent launch. See include/expert_attn.h for the contract.
+// encoding (cached), workspace layout and the two launches (prologue, attention with its
+// merge) chained with programmatic dependent launch. See include/expert_attn.h for the contract.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -13,9 +13,8 @@
 #include "internal.cuh"
 
 namespace ea {
-__global__ void prologue_kernel(const __grid_constant__ PrologueParams p);
+cudaError_t launch_prologue_kernel(const PrologueParams& pp, bool fp8, cudaLaunchConfig_t cfg);
 __global__ void attention_kernel(const __grid_constant__ AttnParams p);
-__global__ void merge_kernel(const __grid_constant__ MergeParams p);
 __global__ void quantize_cache_kernel(const __nv_bfloat16* src, uint8_t* dst, float* scales,
                                       int n_rows, int Smax);
 size_t attention_smem_bytes();
@@ -205,6 +204,7 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
   rope_inv_freq(pp.inv_hi, pp.inv_lo);
   pp.q_ws = ws + wl.q_off;
   pp.tail_ws = ws + wl.tail_off;
+  pp.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
   pp.n_layers = n;
   pp.S = S;
   pp.Smax = Smax;
@@ -215,12 +215,10 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(n * kHkv);
-  cfg.blockDim = dim3(256);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, prologue_kernel, pp) != cudaSuccess) {
+  if (launch_prologue_kernel(pp, fp8, cfg) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
@@ -238,7 +236,6 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   if (ev && ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return EA_ERR_CUDA;
 
   static AttnParams ap;  // large (~19 KB): kept off the stack; guarded by g_launch_mu
-  static MergeParams mp;
   static std::mutex g_launch_mu;
   std::lock_guard<std::mutex> lk(g_launch_mu);
   std::memset(&ap, 0, sizeof(ap));
@@ -258,6 +255,7 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   ap.tail_ws = ws + wl.tail_off;
   ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
   ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
+  ap.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
   ap.status = reinterpret_cast<uint32_t*>(ws);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
   const int n_ctas = n_ctas_for(ap.W, di.sm_count);
@@ -278,33 +276,7 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
     return EA_ERR_CUDA;
   }
   if (ev && ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return EA_ERR_CUDA;
-
-  std::memset(&mp, 0, sizeof(mp));
-  for (int l = 0; l < n; ++l) mp.out[l] = ap.out[l];
-  mp.part_o = ap.part_o;
-  mp.part_lse = ap.part_lse;
-  mp.W = ap.W;
-  mp.T = ap.T;
-  mp.n_ctas = n_ctas;
-  // units whose tiles straddle a CTA boundary; the others are finished by the attention kernel
-  mp.n_split = 0;
-  for (int u = 0; u < n * kHkv; ++u) {
-    const long long first = static_cast<long long>(u) * ap.T, last = first + ap.T - 1;
-    int c = static_cast<int>(first * n_ctas / ap.W);
-    while (c + 1 < n_ctas && cta_tile_start(c + 1, ap.W, n_ctas) <= first) ++c;
-    while (c > 0 && cta_tile_start(c, ap.W, n_ctas) > first) --c;
-    if (c + 1 < n_ctas && cta_tile_start(c + 1, ap.W, n_ctas) <= last)
-      mp.split_unit[mp.n_split++] = static_cast<uint16_t>(u);
-  }
-  // Always launched (one idle CTA when nothing is split), so that the next call's prologue
-  // always follows a merge kernel, which triggers it only after the attention grid is done.
-  cfg.gridDim = dim3(mp.n_split > 0 ? mp.n_split * (kRows / kMergeRowsPerCta) : 1);
-  cfg.blockDim = dim3(32 * kMergeRowsPerCta);
-  cfg.dynamicSmemBytes = 0;
-  if (cudaLaunchKernelEx(&cfg, merge_kernel, mp) != cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
+  // The log-sum-exp merge runs inside the attention kernel; the fourth event follows directly.
   if (ev && ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return EA_ERR_CUDA;
   return EA_OK;
 }
@@ -447,7 +419,8 @@ const char* expert_attn_status_string(int status) {
 namespace {
 
 constexpr size_t noalloc_bytes() {
-  return ((1024 + 2 * static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kQTileBytes +
+  return ((1024 + static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(uint32_t) +
+           2 * static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kQTileBytes +
            static_cast<size_t>(EA_NOALLOC_MAX_CTAS) * 2 * kRows * (kD + 1) * sizeof(float)) +
           1023) & ~static_cast<size_t>(1023);
 }

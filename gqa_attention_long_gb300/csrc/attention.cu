@@ -10,41 +10,47 @@
 // 64-row tile of own rows) are laid out unit-major and cut into one contiguous range per CTA
 // (grid = number of SMs, one CTA per SM). A CTA walks its range as "segments" (the part of one
 // unit inside the range). A segment that covers a whole unit writes the bf16 output directly;
-// a partial one writes a normalised fp32 partial plus its log2-sum-exp for the merge kernel.
+// a partial one writes a normalised fp32 partial plus its log2-sum-exp per row, and the thread
+// that writes the last missing partial of a row (an atomic arrival count; nobody waits) merges:
+//   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s O_s / sum_s w_s  (log-sum-exp merge).
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3  softmax: thread r owns folded row r (= TMEM lane r); online softmax in fp32 with
-//              lazy rescaling of the TMEM accumulator, P written to shared memory as bf16
-//   warp 4     producer: one thread issues bulk copies (roped Q, own rows, both pre-swizzled in
-//              the workspace) and 3-D TMA loads of cache K/V tiles into a 4-slot ring
-//   warp 5     MMA: one thread issues tcgen05.mma (S = Q K^T into one of two TMEM score buffers,
-//              O += P V into the TMEM accumulator) and tcgen05.commit to the barriers
-// Shared memory: Q x2 (64 KB), P (32 KB), K/V ring 4 x 32 KB, barriers. TMEM: 512 columns
-// (two 128-column score buffers and one 128-column fp32 accumulator).
+//              lazy rescaling of the TMEM accumulator; P written back to TMEM as bf16 over the
+//              scores it came from, and read from there by the PV MMA
+//   warp 4     K/V producer: one thread issues 3-D TMA loads of cache K/V tiles and bulk copies
+//              of the own rows (pre-swizzled in the workspace) into a 5-slot ring
+//   warp 5     MMA: one thread issues tcgen05.mma (S = Q K^T from shared memory into one of two
+//              TMEM score buffers; O += P V with P from TMEM and V from shared memory into the TMEM
+//              accumulator) and tcgen05.commit to the barriers
+//   warp 6     Q loader: one thread brings each segment's roped Q (32 KB, pre-swizzled) into one
+//              of two buffers, one segment ahead, so the K/V stream never waits for it
+// Shared memory: Q x2 (64 KB), K/V ring 5 x 32 KB, barriers. TMEM: 512 columns (two 128-column
+// score/P buffers and one 128-column fp32 accumulator).
 #include "internal.cuh"
 #include "ptx.cuh"
 
 namespace ea {
 namespace attn {
 
-constexpr int kThreads = 192;
-constexpr int kRing = 4;
+constexpr int kThreads = 224;
+constexpr int kRing = 5;
 constexpr uint32_t kSlotBytes = 32768;  // one K or V tile: 128 rows x 256 bytes, two 16 KB atoms
 constexpr uint32_t kAtom = kSlotBytes / 2;
-constexpr uint32_t SM_Q = 0;
-constexpr uint32_t SM_P = 2 * kQTileBytes;
-constexpr uint32_t SM_RING = SM_P + kQTileBytes;
+constexpr uint32_t SM_Q = 0;  // two Q buffers
+constexpr uint32_t SM_RING = SM_Q + 2 * kQTileBytes;
 constexpr uint32_t SM_BAR = SM_RING + kRing * kSlotBytes;
 enum : int {
   B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing, B_SFULL = 4 + 2 * kRing,
-  B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 1, B_DRAIN = B_ODONE + 1, kNumBars = B_DRAIN + 1
+  B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_DRAIN = B_ODONE + 2, kNumBars = B_DRAIN + 1
 };
 constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;  // + slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
 
-constexpr uint32_t TM_S = 0;    // score buffers at columns 0 and 128
+constexpr uint32_t TM_S = 0;    // score buffers at columns 0 and 128; P(i) overwrites the first
+                                // 64 columns of the buffer that held S(i) (bf16 pairs)
 constexpr uint32_t TM_O = 256;  // output accumulator, columns 256..383
 constexpr uint32_t kTmemCols = 512;
 
@@ -52,6 +58,7 @@ struct Seg {
   int u, j0, j1;  // unit and its key-tile range [j0, j1)
 };
 
+// Next segment of a CTA's tile range, in range order: t is the next tile, end the range end.
 __device__ __forceinline__ bool next_seg(long long& t, long long end, int T, Seg& s) {
   if (t >= end) return false;
   s.u = static_cast<int>(t / T);
@@ -77,21 +84,11 @@ __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
   const uint64_t pol_stream = l2_policy_evict_first();  // cache tiles are read exactly once
   const uint64_t pol_keep = l2_policy_evict_last();
   uint32_t ring = 0;
-  int seg = 0, q_loads = 0;
   bool ok = true;
   long long t = cx.start;
   Seg s;
   while (ok && next_seg(t, cx.end, p.T, s)) {
     const int l = s.u / kHkv, g = s.u % kHkv;
-    const int qb = seg & 1;
-    if (seg >= 2)
-      ok = bounded_wait(cx.bar(B_QEMPTY + qb), ((seg >> 1) - 1) & 1, cx.abort_flag, cx.status,
-                        kErrProducerWait);
-    if (!ok) break;
-    mbar_expect_tx(cx.bar(B_QFULL + qb), kQTileBytes);
-    bulk_load(cx.sbase + SM_Q + qb * kQTileBytes, p.q_ws + static_cast<size_t>(s.u) * kQTileBytes,
-              kQTileBytes, cx.bar(B_QFULL + qb), pol_keep);
-    ++q_loads;
     for (int j = s.j0; j < s.j1 && ok; ++j) {
       for (int h = 0; h < 2; ++h) {  // h = 0: K tile, h = 1: V tile
         const uint32_t slot = ring % kRing, round = ring / kRing;
@@ -119,7 +116,6 @@ __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
         ++ring;
       }
     }
-    ++seg;
   }
   pdl_launch_dependents();
   if (!ok) {
@@ -128,8 +124,30 @@ __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
       const uint32_t pos = ring - 1 - k;
       if (!drain_wait(cx.bar(B_KVFULL + pos % kRing), (pos / kRing) & 1)) atomicOr(cx.status, kErrDrain);
     }
+  }
+}
+
+// ------------------------------------------------------------------------------- Q loader
+__device__ __noinline__ void q_loader(const AttnParams& p, const Ctx& cx) {
+  const uint64_t pol_keep = l2_policy_evict_last();
+  int seg = 0;
+  bool ok = true;
+  long long t = cx.start;
+  Seg s;
+  while (ok && next_seg(t, cx.end, p.T, s)) {
+    const int qb = seg & 1;
+    if (seg >= 2)  // the last QK^T of segment seg-2 has consumed buffer qb
+      ok = bounded_wait(cx.bar(B_QEMPTY + qb), ((seg >> 1) - 1) & 1, cx.abort_flag, cx.status,
+                        kErrProducerWait);
+    if (!ok) break;
+    mbar_expect_tx(cx.bar(B_QFULL + qb), kQTileBytes);
+    bulk_load(cx.sbase + SM_Q + qb * kQTileBytes, p.q_ws + static_cast<size_t>(s.u) * kQTileBytes,
+              kQTileBytes, cx.bar(B_QFULL + qb), pol_keep);
+    ++seg;
+  }
+  if (!ok) {  // let the last load into each buffer land
     for (int b = 0; b < 2; ++b) {
-      int last = q_loads - 1;  // last segment whose Q went into buffer b
+      int last = seg - 1;
       if ((last & 1) != b) --last;
       if (last >= 0 && !drain_wait(cx.bar(B_QFULL + b), (last >> 1) & 1))
         atomicOr(cx.status, kErrDrain);
@@ -163,6 +181,12 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
         const uint32_t pos = ring + 2 * i, slot = pos % kRing;
         ok = bounded_wait(cx.bar(B_KVFULL + slot), (pos / kRing) & 1, cx.abort_flag, cx.status,
                           kErrMmaWait);
+        // QK(n) overwrites the score buffer whose first columns hold P(n-2), the A operand of
+        // PV(n-2): wait until that MMA has completed (even/odd PVs complete on separate
+        // barriers; this thread observes every PV completion in order).
+        if (ok && n_qk >= 2)
+          ok = bounded_wait(cx.bar(B_ODONE + ((n_qk - 2) & 1)), ((n_qk - 2) >> 1) & 1,
+                            cx.abort_flag, cx.status, kErrMmaWait);
         if (!ok) break;
         tc_fence_after();
         const uint32_t kaddr = cx.sbase + SM_RING + slot * kSlotBytes;
@@ -181,7 +205,10 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
       }
       if (i > 0) {
         const int ii = i - 1, j = s.j0 + ii;
-        ok = bounded_wait(cx.bar(B_PFULL), n_pv & 1, cx.abort_flag, cx.status, kErrMmaWait);
+        // P of even and odd tiles arrive on separate barriers: a softmax warp may run one tile
+        // ahead of another, and its arrivals must not complete the slower warps' phase
+        ok = bounded_wait(cx.bar(B_PFULL + (n_pv & 1)), (n_pv >> 1) & 1, cx.abort_flag, cx.status,
+                          kErrMmaWait);
         if (!ok) break;
         const uint32_t pos = ring + 2 * ii + 1, slot = pos % kRing;
         ok = bounded_wait(cx.bar(B_KVFULL + slot), (pos / kRing) & 1, cx.abort_flag, cx.status,
@@ -190,13 +217,16 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
         tc_fence_after();
         const uint32_t vaddr = cx.sbase + SM_RING + slot * kSlotBytes;
         const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
+        // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together)
+        const uint32_t pcol = cx.tmem + TM_S + (n_pv & 1) * 128;
         for (int kk = 0; kk < nk; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (kQTileBytes / 2) + (kk & 3) * 32;  // P, K-major
-          const uint32_t boff = kk * 16 * 128;                                // V, 16 key rows
-          umma_f16_ss(cx.tmem + TM_O, sw128_desc(cx.sbase + SM_P + aoff, 16, 1024),
-                      sw128_desc(vaddr + boff, kAtom, 1024), kIdescPV, (ii > 0 || kk > 0));
+          const uint32_t boff = kk * 16 * 128;  // V, 16 key rows per step
+          umma_f16_ts(cx.tmem + TM_O, pcol + kk * 8, sw128_desc(vaddr + boff, kAtom, 1024),
+                      kIdescPV, (ii > 0 || kk > 0));
         }
-        umma_commit(cx.bar(B_ODONE));
+        // even and odd PVs complete on separate barriers: a waiter that knows PV k-2 is done
+        // can then always tell PV k's completion from an older phase
+        umma_commit(cx.bar(B_ODONE + (n_pv & 1)));
         umma_commit(cx.bar(B_KVEMPTY + slot));
         ++n_pv;
       }
@@ -229,25 +259,85 @@ __device__ __forceinline__ void rescale_O(uint32_t taddr, float alpha) {
   tmem_wait_st();
 }
 
+// Log-sum-exp merge of folded row r of unit u from the partials of every CTA that holds a part
+// of it (their rows are visible: each thread wrote its row, fenced, then counted it). Reads
+// bypass L1 (ld.global.cg): the rows were written by other SMs.
+__device__ __noinline__ void merge_unit_row(const AttnParams& p, int u, int r) {
+  __threadfence();
+  const int n = gridDim.x;
+  const long long first = static_cast<long long>(u) * p.T;
+  const int c0 = cta_of_tile(first, p.W, n), c1 = cta_of_tile(first + p.T - 1, p.W, n);
+  const int nparts = c1 - c0 + 1;
+  float M = -INFINITY;
+  for (int c = c0; c <= c1; ++c)
+    M = fmaxf(M, __ldcg(p.part_lse + part_index(c, first, p.W, n) * kRows + r));
+  float L = 0.f;
+  for (int c = c0; c <= c1; ++c) L += ex2_approx(__ldcg(p.part_lse + part_index(c, first, p.W, n) * kRows + r) - M);
+  const float invL = 1.0f / L;
+  __nv_bfloat16* orow = p.out[u / kHkv] + (static_cast<size_t>(u % kHkv) * kRows + r) * kD;
+  // Four chunks of 32 columns; per chunk, the rows of two parts are requested together (16
+  // independent 16-byte loads in flight per thread) before they are accumulated.
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 1
+    for (int q0 = 0; q0 < nparts; q0 += 2) {
+      float4 o[2][8];
+      float w[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        w[q] = 0.f;
+        if (q0 + q < nparts) {
+          const size_t pi = part_index(c0 + q0 + q, first, p.W, n);
+          w[q] = ex2_approx(__ldcg(p.part_lse + pi * kRows + r) - M) * invL;
+          const float4* src = reinterpret_cast<const float4*>(p.part_o + (pi * kRows + r) * kD + ch * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[q][k] = __ldcg(src + k);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          acc[4 * k] = fmaf(w[q], o[q][k].x, acc[4 * k]);
+          acc[4 * k + 1] = fmaf(w[q], o[q][k].y, acc[4 * k + 1]);
+          acc[4 * k + 2] = fmaf(w[q], o[q][k].z, acc[4 * k + 2]);
+          acc[4 * k + 3] = fmaf(w[q], o[q][k].w, acc[4 * k + 3]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 wv;
+      wv.x = pack_bf16x2(acc[8 * q + 0], acc[8 * q + 1]);
+      wv.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
+      wv.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
+      wv.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
+      *reinterpret_cast<uint4*>(orow + ch * 32 + 8 * q) = wv;
+    }
+  }
+}
+
 __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
   const int r = threadIdx.x;  // folded row = TMEM lane
   const uint32_t lane_addr = static_cast<uint32_t>(threadIdx.x & ~31) << 16;
   const float c = p.scale_log2;
-  const uint32_t prow = cx.sbase + SM_P + static_cast<uint32_t>(r) * 128u;
-  const uint32_t rsw = static_cast<uint32_t>(r & 7);
-  uint32_t n_s = 0, pv_seen = 0, pv_total = 0;
-  int seg = 0;
-  bool ok = true;
+  uint32_t n_s = 0, pv_total = 0;
+  bool ok = true, first_seg = true;
   long long t = cx.start;
   Seg s;
 
-  // Waits for PV number k of this CTA (all PVs before it are known to be complete).
+  // Waits for PV number k of this CTA. Callers know that PV k-2 is complete (S(i) ready implies
+  // every PV issued before QK(i), i.e. up to PV(i-2)), so the parity of PV k's barrier (even and
+  // odd PVs use separate barriers) identifies its completion unambiguously.
   auto wait_pv = [&](uint32_t k) -> bool {
-    if (pv_seen > k) return true;
-    pv_seen = k + 1;
     // warp-uniform outcome: the TMEM loads and shuffles that follow need the full warp
-    return __all_sync(0xffffffffu, bounded_wait(cx.bar(B_ODONE), k & 1, cx.abort_flag, cx.status,
-                                                kErrSoftmaxWait));
+    return __all_sync(0xffffffffu, bounded_wait(cx.bar(B_ODONE + (k & 1)), (k >> 1) & 1,
+                                                cx.abort_flag, cx.status, kErrSoftmaxWait));
   };
 
   while (ok && next_seg(t, cx.end, p.T, s)) {
@@ -260,6 +350,7 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
       ok = __all_sync(0xffffffffu, bounded_wait(cx.bar(B_SFULL + sb), (n_s >> 1) & 1,
                                                 cx.abort_flag, cx.status, kErrSoftmaxWait));
       if (!ok) break;
+      __syncwarp();
       ++n_s;
       tc_fence_after();
       const bool tail = j >= p.n_main;
@@ -290,12 +381,17 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
           for (int e = 0; e < 32; ++e)
             if (key0 + ch * 32 + e >= p.S) v[ch][e] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // row max with 8 independent accumulators (a single chain would serialise 128 fmax)
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[ch][e]));
-      const float mt = mx * c;
+        for (int e = 0; e < 32; e += 2)
+          mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
       const bool need = (i == 0) || (mt > m_ref + kLazy);
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = fmaxf(m_ref, mt);
@@ -310,43 +406,55 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
         m_ref = m_new;
       }
       const float neg = -m_ref;
-      float tsum = 0.f;
+      float ts8[8];  // row sum with 8 independent accumulators
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ts8[k] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), c, neg));
           const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), c, neg));
-          tsum += p0 + p1;
+          ts8[e & 7] += p0 + p1;
           v[ch][e] = pack_bf16x2(p0, p1);  // packed P overwrites the consumed scores
         }
-      lsum += tsum;
-      if (i > 0) {
-        ok = wait_pv(pv_total + i - 1);  // PV(i-1) has finished reading the P buffer
-        if (!ok) break;
-      }
-      const int nq = tail ? 8 : 16;  // 16-byte chunks of 8 keys
+      lsum += ((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]));
+      // P(i) goes to TMEM over the columns of S(i), already read: 64 keys per 32 columns. The
+      // buffer's previous P, P(i-2), was consumed by PV(i-2), which completed before QK(i).
+      const uint32_t pa = cx.tmem + lane_addr + TM_S + sb * 128;
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (q < nq) {
-          const uint32_t addr = prow + (q >> 3) * (kQTileBytes / 2) + (((q & 7) ^ rsw) << 4);
-          const int ch = q >> 2, k4 = (q & 3) * 4;
-          st_shared_v4(addr, v[ch][k4], v[ch][k4 + 1], v[ch][k4 + 2], v[ch][k4 + 3]);
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = v[0][e];
+          pk[16 + e] = v[1][e];
         }
+        tmem_st32(pa, pk);
       }
-      fence_proxy_async_smem();
+      if (!tail) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = v[2][e];
+          pk[16 + e] = v[3][e];
+        }
+        tmem_st32(pa + 32, pk);
+      }
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(cx.bar(B_PFULL));
+      mbar_arrive(cx.bar(B_PFULL + sb));
     }
     if (!ok) break;
 
-    // ---- epilogue: O / l of this segment
-    ok = wait_pv(pv_total + nt - 1);
+    // ---- epilogue: O / l of this segment (its last two PVs may still be running)
+    if (nt >= 2) ok = wait_pv(pv_total + nt - 2);
+    if (ok) ok = wait_pv(pv_total + nt - 1);
     if (!ok) break;
     tc_fence_after();
     const float inv = 1.0f / lsum;
     const bool full = (s.j0 == 0 && s.j1 == p.T);
-    const int slot = seg == 0 ? 0 : 1;  // a partial segment is the CTA's first or its last
+    const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
+    first_seg = false;
     float* po = p.part_o + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r) * kD;
     __nv_bfloat16* orow = p.out[l] + (static_cast<size_t>(g) * kRows + r) * kD;
 #pragma unroll
@@ -374,11 +482,23 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
         }
       }
     }
-    if (!full)
+    if (!full) {
       p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = m_ref + log2f(lsum);
+      // Count this partial row; the thread that brings the count to the number of parts of the
+      // unit merges the row. No thread waits for another.
+      __threadfence();
+      const long long first = static_cast<long long>(s.u) * p.T;
+      const int nparts = cta_of_tile(first + p.T - 1, p.W, gridDim.x) -
+                         cta_of_tile(first, p.W, gridDim.x) + 1;
+      if (atomicAdd(p.row_cnt + static_cast<size_t>(s.u) * kRows + r, 1u) + 1u ==
+          static_cast<uint32_t>(nparts))
+        merge_unit_row(p, s.u, r);
+      // Only some lanes merged: reconverge before the next tcgen05.ld/st (.sync.aligned, they
+      // need the whole warp to execute them together).
+      __syncwarp();
+    }
     tc_fence_before();
     pv_total += nt;
-    ++seg;
   }
 }
 
@@ -403,14 +523,16 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(cx.bar(B_QFULL + b), 1);
       mbar_init(cx.bar(B_QEMPTY + b), 1);
-      mbar_init(cx.bar(B_SFULL + b), 1);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(cx.bar(B_SFULL + b), 1);
     for (int b = 0; b < kRing; ++b) {
       mbar_init(cx.bar(B_KVFULL + b), 1);
       mbar_init(cx.bar(B_KVEMPTY + b), 1);
     }
     mbar_init(cx.bar(B_PFULL), 128);
+    mbar_init(cx.bar(B_PFULL + 1), 128);
     mbar_init(cx.bar(B_ODONE), 1);
+    mbar_init(cx.bar(B_ODONE + 1), 1);
     mbar_init(cx.bar(B_DRAIN), 1);
     *cx.abort_flag = 0u;
     fence_mbar_init();
@@ -423,13 +545,17 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  // Everything below depends on the prologue (staged Q and own rows, zeroed arrival counts).
+  pdl_wait_primary();
 
   if (warp < 4) {
     softmax_warps(p, cx);
   } else if (warp == 4) {
     if (lane == 0) producer(p, cx);
-  } else {
+  } else if (warp == 5) {
     if (lane == 0) mma_issuer(p, cx);
+  } else {
+    if (lane == 0) q_loader(p, cx);
   }
 
   tc_fence_before();

@@ -38,17 +38,20 @@ enum : uint32_t {
 
 // ------------------------------------------------------------------------- workspace layout
 //   [0, 1024)                    status word (first 4 bytes), rest reserved
+//   cnt     n_layers * 8 * 128 uint32  per-(unit, row) count of partial rows written
 //   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; f16 FP8)
 //   tail    n_layers * 8 * 32 KB  own K rows then own V rows per (layer, kv head), swizzled
 //   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
 struct WsLayout {
-  size_t q_off, tail_off, part_o_off, part_lse_off, total;
+  size_t cnt_off, q_off, tail_off, part_o_off, part_lse_off, total;
 };
 
 inline WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
   WsLayout w;
   size_t off = 1024;
+  w.cnt_off = off;
+  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kRows * sizeof(uint32_t);
   w.q_off = off;
   off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
   w.tail_off = off;
@@ -81,6 +84,7 @@ struct PrologueParams {
   float inv_lo[kD / 2];
   uint8_t* q_ws;
   uint8_t* tail_ws;
+  uint32_t* row_cnt;
   int n_layers, S, Smax, rope_delta, fp8;
 };
 
@@ -96,6 +100,7 @@ struct AttnParams {
   const uint8_t* tail_ws;
   float* part_o;
   float* part_lse;
+  uint32_t* row_cnt;   // [unit][128] count of partial rows written (zeroed by the prologue)
   uint32_t* status;
   long long W;         // total key tiles = n_layers * 8 * T
   int T;               // key tiles per (layer, kv head): n_main cache tiles + 1 own-row tile
@@ -104,25 +109,25 @@ struct AttnParams {
   float scale_log2;    // log2(e) / sqrt(128)
 };
 
-// Units whose key tiles span more than one CTA range; the merge kernel visits only these.
-constexpr int kMaxSplitUnits = kMaxLayersPerLaunch * kHkv;
-constexpr int kMergeRowsPerCta = 8;  // one warp per folded row
-
-struct MergeParams {
-  __nv_bfloat16* out[kMaxLayersPerLaunch];
-  const float* part_o;
-  const float* part_lse;
-  long long W;
-  int T;
-  int n_ctas;
-  int n_split;
-  uint16_t split_unit[kMaxSplitUnits];
-};
-
 // The key tiles of all (layer, kv head) units, in unit-major order, are cut into n_ctas
 // contiguous ranges; CTA c owns tiles [c*W/n, (c+1)*W/n).
 __host__ __device__ inline long long cta_tile_start(int c, long long W, int n_ctas) {
   return static_cast<long long>(c) * W / n_ctas;
+}
+
+// The CTA whose range holds tile x.
+__host__ __device__ inline int cta_of_tile(long long x, long long W, int n_ctas) {
+  int c = static_cast<int>((x * n_ctas) / W);
+  while (c + 1 < n_ctas && cta_tile_start(c + 1, W, n_ctas) <= x) ++c;
+  while (c > 0 && cta_tile_start(c, W, n_ctas) > x) --c;
+  return c;
+}
+
+// Partial slot of CTA c for the unit whose first tile is `first`: a partial segment is either
+// the CTA's first segment (slot 0: the CTA's range starts inside or at the start of the unit)
+// or its last one (slot 1).
+__host__ __device__ inline size_t part_index(int c, long long first, long long W, int n_ctas) {
+  return static_cast<size_t>(c) * 2 + (cta_tile_start(c, W, n_ctas) >= first ? 0 : 1);
 }
 
 }  // namespace ea

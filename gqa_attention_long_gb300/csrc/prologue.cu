@@ -6,10 +6,11 @@
 // rotary_embedding_hf, typecast to the cache dtype, fill_cache at row Smax-64) and
 // TTExpert.set_context (positions i + rope_delta + S); alpamayo_tt/EXPERT_NOTES.md, "Layouts".
 //
-// One CTA per (layer, kv head g): it handles q heads 2g and 2g+1, k head g and v head g. A
-// half-warp owns one token at a time; lane i of the half-warp holds channels [8i, 8i+8), so a
-// RoPE pair (d, d+64) sits in lanes i and i+8 and is exchanged with one shuffle. Every global
-// access is a 16-byte vector access.
+// A CTA handles q heads 2g and 2g+1, k head g and v head g of one layer, for 16 tokens (bf16
+// cache) or all 64 (FP8 cache). A half-warp owns one token at a time; lane i of the half-warp
+// holds channels [8i, 8i+8), so a RoPE pair (d, d+64) sits in lanes i and i+8 and is exchanged
+// with one shuffle. Every global access is a 16-byte vector access. It also zeroes the unit's
+// per-row arrival counters used by the attention kernel's merge.
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
@@ -119,7 +120,11 @@ __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& 
 
 }  // namespace
 
-__global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ PrologueParams p) {
+// TPH = tokens per half-warp: 1 for bf16 caches (four light CTAs per unit, so that many CTAs
+// are resident per SM), 4 for FP8 caches (one CTA per unit: the own-row scale needs the amax
+// over all 64 tokens of the head).
+template <int TPH>
+__global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__ PrologueParams p) {
   // Launched programmatically after the previous kernel in the stream: wait for it (it may have
   // produced q/k/v, or still read the workspace), then let the attention kernel's CTAs start
   // their set-up; they wait for this grid before reading anything written here.
@@ -127,9 +132,13 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   pdl_launch_dependents();
   __shared__ float red[8];
 
-  const int l = blockIdx.x / kHkv, g = blockIdx.x % kHkv;
+  constexpr int kCtasPerUnit = 4 / TPH;
+  const int unit_id = blockIdx.x / kCtasPerUnit;
+  const int quarter = blockIdx.x % kCtasPerUnit;
+  const int l = unit_id / kHkv, g = unit_id % kHkv;
   const PrologueLayer& L = p.layer[l];
-  const int hw = threadIdx.x >> 4;   // half-warp: tokens hw, hw+16, hw+32, hw+48
+  const int hw = threadIdx.x >> 4;   // half-warp: tokens t0 + hw + 16 tt
+  const int t0 = quarter * 16;
   const int i = threadIdx.x & 15;    // channels [8i, 8i+8)
   const int d0 = 8 * i;
   const bool upper = i >= 8;
@@ -145,18 +154,19 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
     il[e] = p.inv_lo[(d0 & 63) + e];
   }
   const size_t unit = static_cast<size_t>(l) * kHkv + g;
+  if (quarter == 0 && threadIdx.x < kRows) p.row_cnt[unit * kRows + threadIdx.x] = 0u;
   uint8_t* qdst = p.q_ws + unit * kQTileBytes;
   uint8_t* tdst = p.tail_ws + unit * kTailUnitBytes;
 
-  float kr[4][8], vr[4][8];  // kept for the FP8 path, whose scale needs all 64 rows first
+  float kr[TPH][8], vr[TPH][8];  // kept for the FP8 path, whose scale needs all 64 rows first
   float kmax = 0.f, vmax = 0.f;
 
   // All raw rows of this thread's 4 tokens are requested before any arithmetic, so that the
   // loads overlap instead of paying one memory latency per token.
-  uint4 rq[4][2], rk[4], rv[4];
+  uint4 rq[TPH][2], rk[TPH], rv[TPH];
 #pragma unroll
-  for (int tt = 0; tt < 4; ++tt) {
-    const int t = hw + 16 * tt;
+  for (int tt = 0; tt < TPH; ++tt) {
+    const int t = t0 + hw + 16 * tt;
     rq[tt][0] = *reinterpret_cast<const uint4*>(L.q_raw + (static_cast<size_t>(2 * g) * kTok + t) * kD + d0);
     rq[tt][1] = *reinterpret_cast<const uint4*>(L.q_raw + (static_cast<size_t>(2 * g + 1) * kTok + t) * kD + d0);
     rk[tt] = *reinterpret_cast<const uint4*>(L.k_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0);
@@ -164,8 +174,8 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   }
 
 #pragma unroll
-  for (int tt = 0; tt < 4; ++tt) {
-    const int t = hw + 16 * tt;
+  for (int tt = 0; tt < TPH; ++tt) {
+    const int t = t0 + hw + 16 * tt;
     const int pos = t + p.rope_delta + p.S;
     float cs[8], sn[8];
 #pragma unroll
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
       }
     }
   }
-  if (!fp8) return;
+  if (TPH != 4 || !fp8) return;
 
   // FP8 cache: the 64 own rows of this head share one scale slot, column Smax/128.
   kmax = block_max_256(kmax, red);
@@ -217,8 +227,8 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
     L.v_scale[g * ncol + ncol - 1] = vsc;
   }
 #pragma unroll
-  for (int tt = 0; tt < 4; ++tt) {
-    const int t = hw + 16 * tt;
+  for (int tt = 0; tt < TPH; ++tt) {
+    const int t = t0 + hw + 16 * tt;
     const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
     const uint32_t so = swz_off(t, i, kTailHalfBytes / 2);
     uint2 c;
@@ -230,6 +240,14 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
     *reinterpret_cast<uint2*>(static_cast<uint8_t*>(L.v_cache) + row * kD + d0) = c;
     *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + so) = w;
   }
+}
+
+// Host-side launcher (the kernel template is instantiated and launched in this file).
+cudaError_t launch_prologue_kernel(const PrologueParams& pp, bool fp8, cudaLaunchConfig_t cfg) {
+  cfg.gridDim = dim3(pp.n_layers * kHkv * (fp8 ? 1 : 4));  // FP8: one CTA per unit; bf16: four
+  cfg.blockDim = dim3(256);
+  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_kernel_t<4>, pp)
+             : cudaLaunchKernelEx(&cfg, prologue_kernel_t<1>, pp);
 }
 
 }  // namespace ea

@@ -90,19 +90,20 @@ int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1-3 for one layer (the unit TTExpert.layer_fn can hand to a fused kernel): prologue,
- * split-KV attention on the tensor cores, log-sum-exp merge; writes a->out. */
+ * then split-KV attention on the tensor cores with its log-sum-exp merge; writes a->out. */
 int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
                       void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1-3 for n_layers independent layers in one call (the 64 layers of one Euler step,
  * alpamayo_tt/expert.py, TTExpert._forward_dev), all with the same S, Smax and rope_delta.
- * layers is a HOST array of n_layers entries. Launches three kernels per 64 layers. */
+ * layers is a HOST array of n_layers entries. Launches two kernels per 64 layers. */
 int expert_attn_layers(const ea_layer_args* layers, int n_layers, int S, int Smax, int rope_delta,
                        int kv_dtype, void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* As expert_attn_layers, and records four cudaEvent_t (passed as void*, each may be NULL) on
- * the stream: before the prologue, before the attention kernel, after it, after the merge.
- * Recording events between the kernels removes their launch overlap; use it to time kernels. */
+ * the stream: before the prologue, before the attention kernel, after it, and once more (the
+ * merge runs inside the attention kernel, so the last two coincide). Recording events between
+ * the kernels removes their launch overlap; use it to time the kernels. */
 int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                 int rope_delta, int kv_dtype, void* workspace, size_t ws_bytes,
                                 ea_stream_t stream, void* const events[4]);
@@ -147,7 +148,7 @@ const char* expert_attn_status_string(int status);
  * in the array's status word and are not reported by this call. */
 #define EA_NOALLOC_MAX_LAYERS 4
 #define EA_NOALLOC_MAX_CTAS 64
-#define EA_NOALLOC_SCRATCH_BYTES 10552320u /* status 1 KB + 4 x 512 KB + 64 x 2 x 66 KB */
+#define EA_NOALLOC_SCRATCH_BYTES 10568704u /* status 1 KB + 4 x (16 KB + 512 KB) + 64 x 2 x 66 KB */
 int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                int rope_delta, int kv_dtype, ea_stream_t stream);
 
