@@ -6,11 +6,11 @@
 // rotary_embedding_hf, typecast to the cache dtype, fill_cache at row Smax-64) and
 // TTExpert.set_context (positions i + rope_delta + S); alpamayo_tt/EXPERT_NOTES.md, "Layouts".
 //
-// A CTA handles q heads 2g and 2g+1, k head g and v head g of one layer, for 16 tokens (bf16
-// cache) or all 64 (FP8 cache). A half-warp owns one token at a time; lane i of the half-warp
-// holds channels [8i, 8i+8), so a RoPE pair (d, d+64) sits in lanes i and i+8 and is exchanged
-// with one shuffle. Every global access is a 16-byte vector access. It also zeroes the unit's
-// per-row arrival counters used by the attention kernel's merge.
+// A CTA handles q heads 2g and 2g+1, k head g and v head g of one layer, for 32 tokens (bf16
+// cache) or all 64 (FP8 cache). An octet (8 lanes) owns one token at a time; lane i holds
+// channels [8i, 8i+8) and their RoPE partners [64+8i, 64+8i+8), so the rotation is in-thread and
+// the norm needs three shuffles. Every global access is a 16-byte vector access. It also zeroes
+// the unit's per-row arrival counters used by the attention kernel's merge.
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
@@ -62,24 +62,25 @@ __device__ __forceinline__ uint4 pack8(const float (&y)[8], bool f16) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// RMSNorm over the 128 channels held by a half-warp (8 per lane), then rotate_half RoPE.
-__device__ __forceinline__ void norm_rope(const float (&x)[8], const float (&gam)[8],
-                                          const float (&cs)[8], const float (&sn)[8], bool upper,
-                                          float (&y)[8]) {
+// RMSNorm over the 128 channels of one row held by an octet (lane i: channels [8i, 8i+8) in lo
+// and their RoPE partners [64+8i, 64+8i+8) in hi), then rotate_half RoPE, all in-thread:
+//   y[d] = n[d] cos - n[d+64] sin,   y[d+64] = n[d+64] cos + n[d] sin   (d < 64).
+__device__ __forceinline__ void norm_rope(const float (&xl)[8], const float (&xh)[8],
+                                          const float (&gl)[8], const float (&gh)[8],
+                                          const float (&cs)[8], const float (&sn)[8],
+                                          float (&yl)[8], float (&yh)[8]) {
   float ss = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+  for (int e = 0; e < 8; ++e) ss = fmaf(xl[e], xl[e], fmaf(xh[e], xh[e], ss));
 #pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+  for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
   const float rs = rsqrtf(ss * (1.0f / kD) + 1e-6f);
-  float n[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) n[e] = x[e] * rs * gam[e];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const float partner = __shfl_xor_sync(0xffffffffu, n[e], 8);
-    // d < 64:  y[d] = n[d] cos - n[d+64] sin;   d >= 64: y[d] = n[d] cos + n[d-64] sin
-    y[e] = upper ? fmaf(n[e], cs[e], partner * sn[e]) : fmaf(n[e], cs[e], -partner * sn[e]);
+    const float nl = xl[e] * rs * gl[e];
+    const float nh = xh[e] * rs * gh[e];
+    yl[e] = fmaf(nl, cs[e], -nh * sn[e]);
+    yh[e] = fmaf(nh, cs[e], nl * sn[e]);
   }
 }
 
@@ -120,10 +121,9 @@ __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& 
 
 }  // namespace
 
-// TPH = tokens per half-warp: 1 for bf16 caches (four light CTAs per unit, so that many CTAs
-// are resident per SM), 4 for FP8 caches (one CTA per unit: the own-row scale needs the amax
-// over all 64 tokens of the head).
-template <int TPH>
+// TPO = tokens per octet: 1 for bf16 caches (two CTAs per unit), 2 for FP8 caches (one CTA per
+// unit: the own-row scale needs the amax over all 64 tokens of the head).
+template <int TPO>
 __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__ PrologueParams p) {
   // Launched programmatically after the previous kernel in the stream: wait for it (it may have
   // produced q/k/v, or still read the workspace), then let the attention kernel's CTAs start
@@ -132,50 +132,57 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
   pdl_launch_dependents();
   __shared__ float red[8];
 
-  constexpr int kCtasPerUnit = 4 / TPH;
+  constexpr int kCtasPerUnit = 2 / TPO;
   const int unit_id = blockIdx.x / kCtasPerUnit;
-  const int quarter = blockIdx.x % kCtasPerUnit;
+  const int part = blockIdx.x % kCtasPerUnit;
   const int l = unit_id / kHkv, g = unit_id % kHkv;
   const PrologueLayer& L = p.layer[l];
-  const int hw = threadIdx.x >> 4;   // half-warp: tokens t0 + hw + 16 tt
-  const int t0 = quarter * 16;
-  const int i = threadIdx.x & 15;    // channels [8i, 8i+8)
-  const int d0 = 8 * i;
-  const bool upper = i >= 8;
+  const int oc = threadIdx.x >> 3;   // octet: tokens t0 + oc + 32 tt
+  const int i = threadIdx.x & 7;     // channels [8i, 8i+8) and [64+8i, 64+8i+8)
+  const int dl = 8 * i, dh = 64 + 8 * i;
+  const int t0 = part * 32;
   const bool fp8 = p.fp8 != 0;
   const int Smax = p.Smax;
 
-  float gq[8], gk[8], ih[8], il[8];
-  load_bf16x8(L.q_gamma + d0, gq);
-  load_bf16x8(L.k_gamma + d0, gk);
+  float gql[8], gqh[8], gkl[8], gkh[8], ih[8], il[8];
+  load_bf16x8(L.q_gamma + dl, gql);
+  load_bf16x8(L.q_gamma + dh, gqh);
+  load_bf16x8(L.k_gamma + dl, gkl);
+  load_bf16x8(L.k_gamma + dh, gkh);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    ih[e] = p.inv_hi[(d0 & 63) + e];
-    il[e] = p.inv_lo[(d0 & 63) + e];
+    ih[e] = p.inv_hi[dl + e];
+    il[e] = p.inv_lo[dl + e];
   }
   const size_t unit = static_cast<size_t>(l) * kHkv + g;
-  if (quarter == 0 && threadIdx.x < kRows) p.row_cnt[unit * kRows + threadIdx.x] = 0u;
+  if (part == 0 && threadIdx.x < kRows) p.row_cnt[unit * kRows + threadIdx.x] = 0u;
   uint8_t* qdst = p.q_ws + unit * kQTileBytes;
   uint8_t* tdst = p.tail_ws + unit * kTailUnitBytes;
 
-  float kr[TPH][8], vr[TPH][8];  // kept for the FP8 path, whose scale needs all 64 rows first
+  float krl[TPO][8], krh[TPO][8], vrl[TPO][8], vrh[TPO][8];  // kept for the FP8 scale
   float kmax = 0.f, vmax = 0.f;
 
-  // All raw rows of this thread's 4 tokens are requested before any arithmetic, so that the
-  // loads overlap instead of paying one memory latency per token.
-  uint4 rq[TPH][2], rk[TPH], rv[TPH];
+  // All raw rows of this thread's tokens are requested before any arithmetic.
+  uint4 rq[TPO][2][2], rk[TPO][2], rv[TPO][2];
 #pragma unroll
-  for (int tt = 0; tt < TPH; ++tt) {
-    const int t = t0 + hw + 16 * tt;
-    rq[tt][0] = *reinterpret_cast<const uint4*>(L.q_raw + (static_cast<size_t>(2 * g) * kTok + t) * kD + d0);
-    rq[tt][1] = *reinterpret_cast<const uint4*>(L.q_raw + (static_cast<size_t>(2 * g + 1) * kTok + t) * kD + d0);
-    rk[tt] = *reinterpret_cast<const uint4*>(L.k_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0);
-    rv[tt] = *reinterpret_cast<const uint4*>(L.v_raw + (static_cast<size_t>(g) * kTok + t) * kD + d0);
+  for (int tt = 0; tt < TPO; ++tt) {
+    const int t = t0 + oc + 32 * tt;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __nv_bfloat16* src = L.q_raw + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
+      rq[tt][hh][0] = *reinterpret_cast<const uint4*>(src + dl);
+      rq[tt][hh][1] = *reinterpret_cast<const uint4*>(src + dh);
+    }
+    const size_t kv = (static_cast<size_t>(g) * kTok + t) * kD;
+    rk[tt][0] = *reinterpret_cast<const uint4*>(L.k_raw + kv + dl);
+    rk[tt][1] = *reinterpret_cast<const uint4*>(L.k_raw + kv + dh);
+    rv[tt][0] = *reinterpret_cast<const uint4*>(L.v_raw + kv + dl);
+    rv[tt][1] = *reinterpret_cast<const uint4*>(L.v_raw + kv + dh);
   }
 
 #pragma unroll
-  for (int tt = 0; tt < TPH; ++tt) {
-    const int t = t0 + hw + 16 * tt;
+  for (int tt = 0; tt < TPO; ++tt) {
+    const int t = t0 + oc + 32 * tt;
     const int pos = t + p.rope_delta + p.S;
     float cs[8], sn[8];
 #pragma unroll
@@ -184,37 +191,48 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int h = 2 * g + hh;
-      float x[8], y[8];
-      unpack_bf16x8(rq[tt][hh], x);
-      norm_rope(x, gq, cs, sn, upper, y);
+      float xl[8], xh[8], yl[8], yh[8];
+      unpack_bf16x8(rq[tt][hh][0], xl);
+      unpack_bf16x8(rq[tt][hh][1], xh);
+      norm_rope(xl, xh, gql, gqh, cs, sn, yl, yh);
       const int r = hh * kTok + t;
-      *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = pack8(y, fp8);
-      if (L.q_rope != nullptr)
-        *reinterpret_cast<uint4*>(L.q_rope + (static_cast<size_t>(h) * kTok + t) * kD + d0) =
-            pack8(y, false);
+      *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = pack8(yl, fp8);
+      *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = pack8(yh, fp8);
+      if (L.q_rope != nullptr) {
+        __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(h) * kTok + t) * kD;
+        *reinterpret_cast<uint4*>(qr + dl) = pack8(yl, false);
+        *reinterpret_cast<uint4*>(qr + dh) = pack8(yh, false);
+      }
     }
-    float x[8];
-    unpack_bf16x8(rk[tt], x);
-    norm_rope(x, gk, cs, sn, upper, kr[tt]);
-    const uint4 vraw = rv[tt];
+    float xl[8], xh[8];
+    unpack_bf16x8(rk[tt][0], xl);
+    unpack_bf16x8(rk[tt][1], xh);
+    norm_rope(xl, xh, gkl, gkh, cs, sn, krl[tt], krh[tt]);
     const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-    const uint32_t so = swz_off(t, i, kTailHalfBytes / 2);
+    const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
     if (!fp8) {
-      const uint4 kb = pack8(kr[tt], false);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(L.k_cache) + row * kD + d0) = kb;
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(L.v_cache) + row * kD + d0) = vraw;
-      *reinterpret_cast<uint4*>(tdst + so) = kb;
-      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + so) = vraw;
+      const uint4 kl = pack8(krl[tt], false), kh = pack8(krh[tt], false);
+      __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(L.k_cache) + row * kD;
+      __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(L.v_cache) + row * kD;
+      *reinterpret_cast<uint4*>(kc + dl) = kl;
+      *reinterpret_cast<uint4*>(kc + dh) = kh;
+      *reinterpret_cast<uint4*>(vc + dl) = rv[tt][0];
+      *reinterpret_cast<uint4*>(vc + dh) = rv[tt][1];
+      *reinterpret_cast<uint4*>(tdst + sol) = kl;
+      *reinterpret_cast<uint4*>(tdst + soh) = kh;
+      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = rv[tt][0];
+      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = rv[tt][1];
     } else {
-      unpack_bf16x8(vraw, vr[tt]);
+      unpack_bf16x8(rv[tt][0], vrl[tt]);
+      unpack_bf16x8(rv[tt][1], vrh[tt]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        kmax = fmaxf(kmax, fabsf(kr[tt][e]));
-        vmax = fmaxf(vmax, fabsf(vr[tt][e]));
+        kmax = fmaxf(kmax, fmaxf(fabsf(krl[tt][e]), fabsf(krh[tt][e])));
+        vmax = fmaxf(vmax, fmaxf(fabsf(vrl[tt][e]), fabsf(vrh[tt][e])));
       }
     }
   }
-  if (TPH != 4 || !fp8) return;
+  if (TPO != 2 || !fp8) return;
 
   // FP8 cache: the 64 own rows of this head share one scale slot, column Smax/128.
   kmax = block_max_256(kmax, red);
@@ -227,26 +245,34 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
     L.v_scale[g * ncol + ncol - 1] = vsc;
   }
 #pragma unroll
-  for (int tt = 0; tt < TPH; ++tt) {
-    const int t = t0 + hw + 16 * tt;
+  for (int tt = 0; tt < TPO; ++tt) {
+    const int t = t0 + oc + 32 * tt;
     const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-    const uint32_t so = swz_off(t, i, kTailHalfBytes / 2);
+    const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
     uint2 c;
     uint4 w;
-    quant8(kr[tt], ksc, c, w);
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(L.k_cache) + row * kD + d0) = c;
-    *reinterpret_cast<uint4*>(tdst + so) = w;
-    quant8(vr[tt], vsc, c, w);
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(L.v_cache) + row * kD + d0) = c;
-    *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + so) = w;
+    uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + row * kD;
+    uint8_t* vc = static_cast<uint8_t*>(L.v_cache) + row * kD;
+    quant8(krl[tt], ksc, c, w);
+    *reinterpret_cast<uint2*>(kc + dl) = c;
+    *reinterpret_cast<uint4*>(tdst + sol) = w;
+    quant8(krh[tt], ksc, c, w);
+    *reinterpret_cast<uint2*>(kc + dh) = c;
+    *reinterpret_cast<uint4*>(tdst + soh) = w;
+    quant8(vrl[tt], vsc, c, w);
+    *reinterpret_cast<uint2*>(vc + dl) = c;
+    *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = w;
+    quant8(vrh[tt], vsc, c, w);
+    *reinterpret_cast<uint2*>(vc + dh) = c;
+    *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = w;
   }
 }
 
 // Host-side launcher (the kernel template is instantiated and launched in this file).
 cudaError_t launch_prologue_kernel(const PrologueParams& pp, bool fp8, cudaLaunchConfig_t cfg) {
-  cfg.gridDim = dim3(pp.n_layers * kHkv * (fp8 ? 1 : 4));  // FP8: one CTA per unit; bf16: four
+  cfg.gridDim = dim3(pp.n_layers * kHkv * (fp8 ? 1 : 2));  // FP8: one CTA per unit; bf16: two
   cfg.blockDim = dim3(256);
-  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_kernel_t<4>, pp)
+  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_kernel_t<2>, pp)
              : cudaLaunchKernelEx(&cfg, prologue_kernel_t<1>, pp);
 }
 
