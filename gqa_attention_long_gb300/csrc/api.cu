@@ -14,11 +14,10 @@
 
 namespace ea {
 cudaError_t launch_prologue_kernel(const PrologueParams& pp, bool fp8, cudaLaunchConfig_t cfg);
-__global__ void attention_kernel(const __grid_constant__ AttnParams p);
+cudaError_t attention_set_attributes();
+cudaError_t launch_attention_kernel(const AttnParams& ap, bool f8, cudaLaunchConfig_t cfg);
 __global__ void quantize_cache_kernel(const __nv_bfloat16* src, uint8_t* dst, float* scales,
                                       int n_rows, int Smax);
-size_t attention_smem_bytes();
-int attention_threads();
 }  // namespace ea
 
 namespace {
@@ -54,8 +53,7 @@ bool device_info(int* dev_out, DeviceInfo* info) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
         major == 10 && minor == 3 && sms > 0) {
       d.sm_count = sms;
-      d.ok = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(attention_smem_bytes())) == cudaSuccess;
+      d.ok = attention_set_attributes() == cudaSuccess;
     }
     cudaGetLastError();
   }
@@ -90,18 +88,22 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
   const void* ptr;
   int S, Smax;
-  bool operator==(const MapKey& o) const { return ptr == o.ptr && S == o.S && Smax == o.Smax; }
+  bool f8;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && S == o.S && Smax == o.Smax && f8 == o.f8;
+  }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     return std::hash<const void*>()(k.ptr) ^ (static_cast<size_t>(k.S) * 0x9E3779B97F4A7C15ull) ^
-           (static_cast<size_t>(k.Smax) << 1);
+           (static_cast<size_t>(k.Smax) << 1) ^ (k.f8 ? 0x5bd1e995ull : 0);
   }
 };
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-bool cache_map(const void* base, int S, int Smax, CUtensorMap* out) {
-  const MapKey key{base, S, Smax};
+// bf16 cache: box {64 channels, 128 rows, 1}; e4m3 cache: box {128 channels (bytes), 128, 1}.
+bool cache_map(const void* base, int S, int Smax, bool f8, CUtensorMap* out) {
+  const MapKey key{base, S, Smax, f8};
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_maps.find(key);
@@ -117,11 +119,13 @@ bool cache_map(const void* base, int S, int Smax, CUtensorMap* out) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD),
                               static_cast<cuuint64_t>(S > 0 ? S : 1),
                               static_cast<cuuint64_t>(kHkv)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                                 static_cast<cuuint64_t>(Smax) * kD * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kKeyTile), 1};
+  const cuuint64_t esz = f8 ? 1 : 2;
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * esz,
+                                 static_cast<cuuint64_t>(Smax) * kD * esz};
+  const cuuint32_t box[3] = {f8 ? 128u : 64u, static_cast<cuuint32_t>(kKeyTile), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  if (fn(&m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+         const_cast<void*>(base), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
@@ -205,6 +209,8 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
   pp.q_ws = ws + wl.q_off;
   pp.tail_ws = ws + wl.tail_off;
   pp.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
+  pp.q_scale = reinterpret_cast<float*>(ws + wl.qscale_off);
+  pp.sv_ref = reinterpret_cast<float*>(ws + wl.svref_off);
   pp.n_layers = n;
   pp.S = S;
   pp.Smax = Smax;
@@ -228,7 +234,6 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
 int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
                  uint8_t* ws, const WsLayout& wl, const DeviceInfo& di, cudaStream_t st,
                  cudaEvent_t const* ev) {
-  if (fp8) return EA_ERR_UNSUPPORTED;  // FP8 attention kernel: not part of this build yet
   const bool pdl = ev == nullptr;
   if (ev && ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return EA_ERR_CUDA;
   int rc = launch_prologue(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl);
@@ -240,10 +245,12 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   std::lock_guard<std::mutex> lk(g_launch_mu);
   std::memset(&ap, 0, sizeof(ap));
   for (int l = 0; l < n; ++l) {
-    if (!cache_map(a[l].k_cache, S, Smax, &ap.kmap[l]) ||
-        !cache_map(a[l].v_cache, S, Smax, &ap.vmap[l]))
+    if (!cache_map(a[l].k_cache, S, Smax, fp8, &ap.kmap[l]) ||
+        !cache_map(a[l].v_cache, S, Smax, fp8, &ap.vmap[l]))
       return EA_ERR_CUDA;
     ap.out[l] = static_cast<__nv_bfloat16*>(a[l].out);
+    ap.ks[l] = a[l].k_scale;
+    ap.vs[l] = a[l].v_scale;
   }
   const int n_main = (S + kKeyTile - 1) / kKeyTile;
   ap.T = n_main + 1;
@@ -256,6 +263,9 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
   ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
   ap.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
+  ap.q_scale = reinterpret_cast<const float*>(ws + wl.qscale_off);
+  ap.sv_ref = reinterpret_cast<const float*>(ws + wl.svref_off);
+  ap.ncol = Smax / kScaleBlock + 1;
   ap.status = reinterpret_cast<uint32_t*>(ws);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
   const int n_ctas = n_ctas_for(ap.W, di.sm_count);
@@ -266,12 +276,10 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(n_ctas);
-  cfg.blockDim = dim3(attention_threads());
-  cfg.dynamicSmemBytes = attention_smem_bytes();
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, attention_kernel, ap) != cudaSuccess) {
+  if (launch_attention_kernel(ap, fp8, cfg) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
@@ -420,6 +428,7 @@ namespace {
 
 constexpr size_t noalloc_bytes() {
   return ((1024 + static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(uint32_t) +
+           static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(float) + 1024 +
            2 * static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kQTileBytes +
            static_cast<size_t>(EA_NOALLOC_MAX_CTAS) * 2 * kRows * (kD + 1) * sizeof(float)) +
           1023) & ~static_cast<size_t>(1023);

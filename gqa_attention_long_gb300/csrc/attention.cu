@@ -34,23 +34,42 @@ namespace ea {
 namespace attn {
 
 constexpr int kThreads = 224;
-constexpr int kRing = 5;
-constexpr uint32_t kSlotBytes = 32768;  // one K or V tile: 128 rows x 256 bytes, two 16 KB atoms
-constexpr uint32_t kAtom = kSlotBytes / 2;
-constexpr uint32_t SM_Q = 0;  // two Q buffers
-constexpr uint32_t SM_RING = SM_Q + 2 * kQTileBytes;
-constexpr uint32_t SM_BAR = SM_RING + kRing * kSlotBytes;
-enum : int {
-  B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing, B_SFULL = 4 + 2 * kRing,
-  B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_DRAIN = B_ODONE + 2, kNumBars = B_DRAIN + 1
+
+// Shared-memory layout of one CTA. bf16 cache: a K or V tile is 128 rows x 256 bytes, stored as
+// two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom.
+template <bool F8>
+struct Lay {
+  static constexpr uint32_t kQ = kQTileBytes;  // one roped Q tile (e4m3: high then low codes)
+  static constexpr uint32_t kSlot = F8 ? 16384u : 32768u;           // one K or V tile
+  static constexpr uint32_t kAtom = 16384u;                         // bf16: second channel half
+  static constexpr uint32_t kTail = F8 ? kTailHalfBytesF8 : kTailHalfBytes;  // 64 own rows
+  static constexpr int kRing = F8 ? 10 : 5;
+  static constexpr uint32_t SM_Q = 0;  // two Q buffers
+  static constexpr uint32_t SM_RING = SM_Q + 2 * kQ;
+  static constexpr uint32_t SM_BAR = SM_RING + kRing * kSlot;
+  static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing,
+                       B_SFULL = 4 + 2 * kRing, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
+                       B_DRAIN = B_ODONE + 2, kNumBars = B_DRAIN + 1;
+  static constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
+  static constexpr uint32_t SM_ABORT = SM_TMEM + 4;
+  static constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;  // + slack to align the base
+  static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
 };
-constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
-constexpr uint32_t SM_ABORT = SM_TMEM + 4;
-constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;  // + slack to align the base to 1024 bytes
-static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
+
+#define EA_LAYOUT_ALIASES                                                                  \
+  using LY = Lay<F8>;                                                                      \
+  constexpr int kRing = LY::kRing;                                                         \
+  constexpr uint32_t kSlotBytes = LY::kSlot, kAtom = LY::kAtom, kQB = LY::kQ;              \
+  constexpr uint32_t SM_Q = LY::SM_Q, SM_RING = LY::SM_RING;                               \
+  constexpr int B_QFULL = LY::B_QFULL, B_QEMPTY = LY::B_QEMPTY, B_KVFULL = LY::B_KVFULL,   \
+                B_KVEMPTY = LY::B_KVEMPTY, B_SFULL = LY::B_SFULL, B_PFULL = LY::B_PFULL,    \
+                B_ODONE = LY::B_ODONE, B_DRAIN = LY::B_DRAIN;                              \
+  (void)kRing; (void)kSlotBytes; (void)kAtom; (void)kQB; (void)SM_Q; (void)SM_RING;         \
+  (void)B_QFULL; (void)B_QEMPTY; (void)B_KVFULL; (void)B_KVEMPTY; (void)B_SFULL;            \
+  (void)B_PFULL; (void)B_ODONE; (void)B_DRAIN
 
 constexpr uint32_t TM_S = 0;    // score buffers at columns 0 and 128; P(i) overwrites the first
-                                // 64 columns of the buffer that held S(i) (bf16 pairs)
+                                // columns of the buffer that held S(i)
 constexpr uint32_t TM_O = 256;  // output accumulator, columns 256..383
 constexpr uint32_t kTmemCols = 512;
 
@@ -75,11 +94,14 @@ struct Ctx {
   volatile uint32_t* abort_flag;
   uint32_t* status;
   long long start, end;
-  __device__ __forceinline__ uint32_t bar(int i) const { return sbase + SM_BAR + 8u * i; }
+  uint32_t bar_base;  // shared address of barrier 0
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar_base + 8u * i; }
 };
 
 // ------------------------------------------------------------------------------- producer
+template <bool F8>
 __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
+  EA_LAYOUT_ALIASES;
   pdl_wait_primary();  // roped Q and own rows are written by the prologue kernel
   const uint64_t pol_stream = l2_policy_evict_first();  // cache tiles are read exactly once
   const uint64_t pol_keep = l2_policy_evict_last();
@@ -104,14 +126,19 @@ __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
           mbar_expect_tx(fb, kSlotBytes);
           const CUtensorMap* m = h ? &p.vmap[l] : &p.kmap[l];
           tma_load_3d(dst, m, fb, 0, j * kKeyTile, g, pol_stream);
-          tma_load_3d(dst + kAtom, m, fb, 64, j * kKeyTile, g, pol_stream);
+          if constexpr (!F8) tma_load_3d(dst + kAtom, m, fb, 64, j * kKeyTile, g, pol_stream);
         } else {
-          // the 64 own rows, staged pre-swizzled by the prologue: two 8 KB atoms
-          mbar_expect_tx(fb, kTailHalfBytes);
+          // the 64 own rows, staged pre-swizzled by the prologue
           const uint8_t* src =
               p.tail_ws + static_cast<size_t>(s.u) * kTailUnitBytes + h * kTailHalfBytes;
-          bulk_load(dst, src, kTailHalfBytes / 2, fb, pol_keep);
-          bulk_load(dst + kAtom, src + kTailHalfBytes / 2, kTailHalfBytes / 2, fb, pol_keep);
+          if constexpr (F8) {  // one 8 KB atom block: 64 rows x 128 bytes
+            mbar_expect_tx(fb, kTailHalfBytesF8);
+            bulk_load(dst, src, kTailHalfBytesF8, fb, pol_keep);
+          } else {  // two 8 KB atom blocks, one per channel half
+            mbar_expect_tx(fb, kTailHalfBytes);
+            bulk_load(dst, src, kTailHalfBytes / 2, fb, pol_keep);
+            bulk_load(dst + kAtom, src + kTailHalfBytes / 2, kTailHalfBytes / 2, fb, pol_keep);
+          }
         }
         ++ring;
       }
@@ -128,7 +155,9 @@ __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------------------- Q loader
+template <bool F8>
 __device__ __noinline__ void q_loader(const AttnParams& p, const Ctx& cx) {
+  EA_LAYOUT_ALIASES;
   const uint64_t pol_keep = l2_policy_evict_last();
   int seg = 0;
   bool ok = true;
@@ -140,9 +169,9 @@ __device__ __noinline__ void q_loader(const AttnParams& p, const Ctx& cx) {
       ok = bounded_wait(cx.bar(B_QEMPTY + qb), ((seg >> 1) - 1) & 1, cx.abort_flag, cx.status,
                         kErrProducerWait);
     if (!ok) break;
-    mbar_expect_tx(cx.bar(B_QFULL + qb), kQTileBytes);
-    bulk_load(cx.sbase + SM_Q + qb * kQTileBytes, p.q_ws + static_cast<size_t>(s.u) * kQTileBytes,
-              kQTileBytes, cx.bar(B_QFULL + qb), pol_keep);
+    mbar_expect_tx(cx.bar(B_QFULL + qb), kQB);
+    bulk_load(cx.sbase + SM_Q + qb * kQB, p.q_ws + static_cast<size_t>(s.u) * kQTileBytes, kQB,
+              cx.bar(B_QFULL + qb), pol_keep);
     ++seg;
   }
   if (!ok) {  // let the last load into each buffer land
@@ -159,10 +188,13 @@ __device__ __noinline__ void q_loader(const AttnParams& p, const Ctx& cx) {
 // Issue order per segment: QK(0), then for i >= 1: QK(i), PV(i-1); finally PV(nt-1). So QK(i+1)
 // is issued only after PV(i-1), whose P came from the softmax of tile i-1: by then the score
 // buffer that QK(i+1) overwrites has been read, and every completed S(i) implies PV(i-2) done.
+template <bool F8>
 __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
-  constexpr uint32_t kIdescQK128 = umma_idesc_f16(128, 128, true, false, false);
-  constexpr uint32_t kIdescQK64 = umma_idesc_f16(128, 64, true, false, false);
-  constexpr uint32_t kIdescPV = umma_idesc_f16(128, 128, true, false, true);  // V is MN-major
+  EA_LAYOUT_ALIASES;
+  // bf16: format code 1 (kind::f16); e4m3: format code 0 (kind::f8f6f4). V is MN-major.
+  constexpr uint32_t kIdescQK128 = umma_idesc_f16(128, 128, !F8, false, false);
+  constexpr uint32_t kIdescQK64 = umma_idesc_f16(128, 64, !F8, false, false);
+  constexpr uint32_t kIdescPV = umma_idesc_f16(128, 128, !F8, false, true);
   uint32_t ring = 0, n_qk = 0, n_pv = 0;
   int seg = 0;
   bool ok = true;
@@ -173,7 +205,7 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
     ok = bounded_wait(cx.bar(B_QFULL + qb), (seg >> 1) & 1, cx.abort_flag, cx.status, kErrMmaWait);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t qaddr = cx.sbase + SM_Q + qb * kQTileBytes;
+    const uint32_t qaddr = cx.sbase + SM_Q + qb * kQB;
     const int nt = s.j1 - s.j0;
     for (int i = 0; i <= nt && ok; ++i) {
       if (i < nt) {
@@ -192,11 +224,20 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
         const uint32_t kaddr = cx.sbase + SM_RING + slot * kSlotBytes;
         const uint32_t d = cx.tmem + TM_S + (n_qk & 1) * 128;
         const uint32_t idesc = j < p.n_main ? kIdescQK128 : kIdescQK64;
+        if constexpr (F8) {
+          // 4 steps of 32 channels within the 128-byte atom, for the high Q codes and then the
+          // low ones (same scale), both accumulating into S
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 8 steps of 16 channels; 4 per 64-channel atom
-          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-          umma_f16_ss(d, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024),
-                      idesc, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_f8_ss(d, sw128_desc(qaddr + (kk >> 2) * kQTileBytesF8 + (kk & 3) * 32, 16, 1024),
+                       sw128_desc(kaddr + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // 8 steps of 16 channels; 4 per 64-channel atom
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_f16_ss(d, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024),
+                        idesc, kk > 0);
+          }
         }
         umma_commit(cx.bar(B_SFULL + (n_qk & 1)));
         umma_commit(cx.bar(B_KVEMPTY + slot));
@@ -216,13 +257,23 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
         if (!ok) break;
         tc_fence_after();
         const uint32_t vaddr = cx.sbase + SM_RING + slot * kSlotBytes;
-        const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
-        // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together)
+        // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together);
+        // a K step spans 8 TMEM columns in both formats (16 bf16 or 32 e4m3 keys)
         const uint32_t pcol = cx.tmem + TM_S + (n_pv & 1) * 128;
-        for (int kk = 0; kk < nk; ++kk) {
-          const uint32_t boff = kk * 16 * 128;  // V, 16 key rows per step
-          umma_f16_ts(cx.tmem + TM_O, pcol + kk * 8, sw128_desc(vaddr + boff, kAtom, 1024),
-                      kIdescPV, (ii > 0 || kk > 0));
+        if constexpr (F8) {
+          // 32 keys per step (the own-row tile has 64 keys); V: 32 key rows of 128 bytes per
+          // step. The high P codes sit in columns [0, 32), the low ones in [32, 64).
+          const int nk = j < p.n_main ? 4 : 2;
+          for (int kk = 0; kk < 2 * nk; ++kk) {
+            const int ks = kk < nk ? kk : kk - nk;
+            umma_f8_ts(cx.tmem + TM_O, pcol + (kk < nk ? 0 : 32) + ks * 8,
+                       sw128_desc(vaddr + ks * 32 * 128, 16, 1024), kIdescPV, (ii > 0 || kk > 0));
+          }
+        } else {
+          const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
+          for (int kk = 0; kk < nk; ++kk)        // V: 16 key rows of 128 bytes per step and atom
+            umma_f16_ts(cx.tmem + TM_O, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024),
+                        kIdescPV, (ii > 0 || kk > 0));
         }
         // even and odd PVs complete on separate barriers: a waiter that knows PV k-2 is done
         // can then always tell PV k's completion from an older phase
@@ -322,7 +373,9 @@ __device__ __noinline__ void merge_unit_row(const AttnParams& p, int u, int r) {
   }
 }
 
+template <bool F8>
 __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
+  EA_LAYOUT_ALIASES;
   const int r = threadIdx.x;  // folded row = TMEM lane
   const uint32_t lane_addr = static_cast<uint32_t>(threadIdx.x & ~31) << 16;
   const float c = p.scale_log2;
@@ -344,6 +397,12 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
     const int l = s.u / kHkv, g = s.u % kHkv;
     const int nt = s.j1 - s.j0;
     float m_ref = -INFINITY, lsum = 0.f;
+    // FP8: e4m3 Q row scale, and the unit's reference V scale (P is stored relative to it)
+    float sq = 1.f, svr = 1.f;
+    if constexpr (F8) {
+      sq = p.q_scale[static_cast<size_t>(s.u) * kRows + r];
+      svr = p.sv_ref[s.u];
+    }
     for (int i = 0; i < nt; ++i) {
       const int j = s.j0 + i;
       const uint32_t sb = n_s & 1;
@@ -390,8 +449,19 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
           mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
+      // per-tile factors: scores in log2 units are s * ct; FP8 adds the block scales, and P is
+      // stored as 2^(x - m) * (sv / svr) (exponent offset lgv) so that its e4m3 codes carry the
+      // tile's V scale relative to the unit's largest one; the row sum counts 2^(x - m).
+      float ct = c, lgv = 0.f, lmul = 1.f;
+      if constexpr (F8) {
+        const int col = tail ? p.ncol - 1 : j;
+        const float sk = p.ks[l][g * p.ncol + col], sv = p.vs[l][g * p.ncol + col];
+        ct = c * sq * sk;
+        lgv = __log2f(sv / svr);
+        lmul = svr / sv;
+      }
       const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * ct;
       const bool need = (i == 0) || (mt > m_ref + kLazy);
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = fmaxf(m_ref, mt);
@@ -405,24 +475,68 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
         lsum *= alpha;
         m_ref = m_new;
       }
-      const float neg = -m_ref;
+      const float neg = lgv - m_ref;
       float ts8[8];  // row sum with 8 independent accumulators
 #pragma unroll
       for (int k = 0; k < 8; ++k) ts8[k] = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), c, neg));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), c, neg));
-          ts8[e & 7] += p0 + p1;
-          v[ch][e] = pack_bf16x2(p0, p1);  // packed P overwrites the consumed scores
-        }
-      lsum += ((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]));
-      // P(i) goes to TMEM over the columns of S(i), already read: 64 keys per 32 columns. The
-      // buffer's previous P, P(i-2), was consumed by PV(i-2), which completed before QK(i).
       const uint32_t pa = cx.tmem + lane_addr + TM_S + sb * 128;
-      {
+      // P(i) goes to TMEM over the columns of S(i), already read. The buffer's previous P,
+      // P(i-2), was consumed by PV(i-2), which completed before QK(i).
+      if constexpr (F8) {
+        // four e4m3 codes per column: P as high codes in columns [0, 32) and low codes (the
+        // residual) in [32, 64); the own-row tile (64 keys) uses 16 columns of each
+        uint32_t lo[4][8];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e]), ct, neg));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 1]), ct, neg));
+            const float p2 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 2]), ct, neg));
+            const float p3 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 3]), ct, neg));
+            ts8[e] += (p0 + p1) + (p2 + p3);
+            uint32_t hi;
+            pack_e4m3x4_hilo(p0, p1, p2, p3, hi, lo[ch][e]);
+            v[ch][e] = hi;  // packed P overwrites the consumed scores
+          }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          pk[e] = v[0][e];
+          pk[8 + e] = v[1][e];
+        }
+        tmem_st16(pa, pk);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          pk[e] = lo[0][e];
+          pk[8 + e] = lo[1][e];
+        }
+        tmem_st16(pa + 32, pk);
+        if (!tail) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pk[e] = v[2][e];
+            pk[8 + e] = v[3][e];
+          }
+          tmem_st16(pa + 16, pk);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pk[e] = lo[2][e];
+            pk[8 + e] = lo[3][e];
+          }
+          tmem_st16(pa + 48, pk);
+        }
+      } else {
+        // bf16 pairs: 128 keys in 64 columns (own-row tile: 32)
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), ct, neg));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), ct, neg));
+            ts8[e & 7] += p0 + p1;
+            v[ch][e] = pack_bf16x2(p0, p1);  // packed P overwrites the consumed scores
+          }
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -430,16 +544,16 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
           pk[16 + e] = v[1][e];
         }
         tmem_st32(pa, pk);
-      }
-      if (!tail) {
-        uint32_t pk[32];
+        if (!tail) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pk[e] = v[2][e];
-          pk[16 + e] = v[3][e];
+          for (int e = 0; e < 16; ++e) {
+            pk[e] = v[2][e];
+            pk[16 + e] = v[3][e];
+          }
+          tmem_st32(pa + 32, pk);
         }
-        tmem_st32(pa + 32, pk);
       }
+      lsum += (((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]))) * lmul;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(cx.bar(B_PFULL + sb));
@@ -451,7 +565,7 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
     if (ok) ok = wait_pv(pv_total + nt - 1);
     if (!ok) break;
     tc_fence_after();
-    const float inv = 1.0f / lsum;
+    const float inv = svr / lsum;  // FP8: P was stored relative to the reference V scale
     const bool full = (s.j0 == 0 && s.j1 == p.T);
     const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
     first_seg = false;
@@ -505,16 +619,19 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
 }  // namespace attn
 
 // ------------------------------------------------------------------------------------ kernel
+template <bool F8>
 __global__ void __launch_bounds__(attn::kThreads, 1)
     attention_kernel(const __grid_constant__ AttnParams p) {
   using namespace attn;
+  EA_LAYOUT_ALIASES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx cx;
   cx.sbase = smem_u32(smem);
-  cx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_ABORT);
+  cx.bar_base = cx.sbase + LY::SM_BAR;
+  cx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + LY::SM_ABORT);
   cx.status = p.status;
   cx.start = cta_tile_start(blockIdx.x, p.W, gridDim.x);
   cx.end = cta_tile_start(blockIdx.x + 1, p.W, gridDim.x);
@@ -523,39 +640,37 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(cx.bar(B_QFULL + b), 1);
       mbar_init(cx.bar(B_QEMPTY + b), 1);
+      mbar_init(cx.bar(B_SFULL + b), 1);
+      mbar_init(cx.bar(B_PFULL + b), 128);
+      mbar_init(cx.bar(B_ODONE + b), 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(cx.bar(B_SFULL + b), 1);
     for (int b = 0; b < kRing; ++b) {
       mbar_init(cx.bar(B_KVFULL + b), 1);
       mbar_init(cx.bar(B_KVEMPTY + b), 1);
     }
-    mbar_init(cx.bar(B_PFULL), 128);
-    mbar_init(cx.bar(B_PFULL + 1), 128);
-    mbar_init(cx.bar(B_ODONE), 1);
-    mbar_init(cx.bar(B_ODONE + 1), 1);
     mbar_init(cx.bar(B_DRAIN), 1);
     *cx.abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(cx.sbase + SM_TMEM, kTmemCols);
+    tmem_alloc(cx.sbase + LY::SM_TMEM, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + LY::SM_TMEM);
   // Everything below depends on the prologue (staged Q and own rows, zeroed arrival counts).
   pdl_wait_primary();
 
   if (warp < 4) {
-    softmax_warps(p, cx);
+    softmax_warps<F8>(p, cx);
   } else if (warp == 4) {
-    if (lane == 0) producer(p, cx);
+    if (lane == 0) producer<F8>(p, cx);
   } else if (warp == 5) {
-    if (lane == 0) mma_issuer(p, cx);
+    if (lane == 0) mma_issuer<F8>(p, cx);
   } else {
-    if (lane == 0) q_loader(p, cx);
+    if (lane == 0) q_loader<F8>(p, cx);
   }
 
   tc_fence_before();
@@ -564,9 +679,22 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   if (warp == 5) tmem_dealloc(cx.tmem, kTmemCols);
 }
 
-}  // namespace ea
+// Host side: attributes and launch of the two instances (kept in this file, where the kernel
+// template is instantiated).
+cudaError_t attention_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(attention_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(attn::Lay<false>::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(attn::Lay<true>::kSmemBytes));
+}
 
-namespace ea {
-size_t attention_smem_bytes() { return attn::kSmemBytes; }
-int attention_threads() { return attn::kThreads; }
+cudaError_t launch_attention_kernel(const AttnParams& ap, bool f8, cudaLaunchConfig_t cfg) {
+  cfg.blockDim = dim3(attn::kThreads);
+  cfg.dynamicSmemBytes = f8 ? attn::Lay<true>::kSmemBytes : attn::Lay<false>::kSmemBytes;
+  return f8 ? cudaLaunchKernelEx(&cfg, attention_kernel<true>, ap)
+            : cudaLaunchKernelEx(&cfg, attention_kernel<false>, ap);
+}
+
 }  // namespace ea

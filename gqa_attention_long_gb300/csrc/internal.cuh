@@ -27,6 +27,10 @@ constexpr int kScaleBlock = 128;  // FP8 scale granularity (rows)
 constexpr uint32_t kQTileBytes = kRows * kD * 2;          // 32 KB: roped Q of one (layer, kv head)
 constexpr uint32_t kTailHalfBytes = kTok * kD * 2;        // 16 KB: own K (or V) rows, 64 x 128
 constexpr uint32_t kTailUnitBytes = 2 * kTailHalfBytes;   // K then V
+// FP8 (e4m3) variant: one 128-byte swizzle atom per row, so a Q tile is 16 KB and the 64 own K
+// (or V) rows 8 KB, stored at the start of the same workspace slots as the bf16 ones.
+constexpr uint32_t kQTileBytesF8 = kRows * kD;
+constexpr uint32_t kTailHalfBytesF8 = kTok * kD;
 
 // Status bits recorded in the workspace when a bounded wait gives up.
 enum : uint32_t {
@@ -39,12 +43,14 @@ enum : uint32_t {
 // ------------------------------------------------------------------------- workspace layout
 //   [0, 1024)                    status word (first 4 bytes), rest reserved
 //   cnt     n_layers * 8 * 128 uint32  per-(unit, row) count of partial rows written
+//   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
+//   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
 //   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; f16 FP8)
 //   tail    n_layers * 8 * 32 KB  own K rows then own V rows per (layer, kv head), swizzled
 //   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
 struct WsLayout {
-  size_t cnt_off, q_off, tail_off, part_o_off, part_lse_off, total;
+  size_t cnt_off, qscale_off, svref_off, q_off, tail_off, part_o_off, part_lse_off, total;
 };
 
 inline WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
@@ -52,6 +58,10 @@ inline WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
   size_t off = 1024;
   w.cnt_off = off;
   off += static_cast<size_t>(n_layers_per_launch) * kHkv * kRows * sizeof(uint32_t);
+  w.qscale_off = off;
+  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kRows * sizeof(float);
+  w.svref_off = off;
+  off += ((static_cast<size_t>(n_layers_per_launch) * kHkv * sizeof(float)) + 1023) & ~static_cast<size_t>(1023);
   w.q_off = off;
   off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
   w.tail_off = off;
@@ -85,6 +95,8 @@ struct PrologueParams {
   uint8_t* q_ws;
   uint8_t* tail_ws;
   uint32_t* row_cnt;
+  float* q_scale;  // FP8: [unit][128] scale of each e4m3 Q row
+  float* sv_ref;   // FP8: [unit] reference V scale
   int n_layers, S, Smax, rope_delta, fp8;
 };
 
@@ -92,20 +104,21 @@ struct AttnParams {
   CUtensorMap kmap[kMaxLayersPerLaunch];  // cache rows [0, S) of K: dims {128, S, 8}, box {64,128,1}
   CUtensorMap vmap[kMaxLayersPerLaunch];
   __nv_bfloat16* out[kMaxLayersPerLaunch];
-  const uint8_t* kc8[kMaxLayersPerLaunch];  // FP8: e4m3 caches and scales (unused for bf16)
-  const uint8_t* vc8[kMaxLayersPerLaunch];
-  const float* ks[kMaxLayersPerLaunch];
+  const float* ks[kMaxLayersPerLaunch];      // FP8: block scales [8][Smax/128 + 1] (else null)
   const float* vs[kMaxLayersPerLaunch];
   const uint8_t* q_ws;
   const uint8_t* tail_ws;
   float* part_o;
   float* part_lse;
   uint32_t* row_cnt;   // [unit][128] count of partial rows written (zeroed by the prologue)
+  const float* q_scale;  // FP8: [unit][128]
+  const float* sv_ref;   // FP8: [unit]
   uint32_t* status;
   long long W;         // total key tiles = n_layers * 8 * T
   int T;               // key tiles per (layer, kv head): n_main cache tiles + 1 own-row tile
   int n_main;          // ceil(S / 128)
   int S, Smax;
+  int ncol;            // FP8: scale columns per kv head, Smax/128 + 1 (the last one: own rows)
   float scale_log2;    // log2(e) / sqrt(128)
 };
 

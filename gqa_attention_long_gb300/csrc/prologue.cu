@@ -103,6 +103,31 @@ __device__ __forceinline__ float block_max_256(float v, float* red) {
   return r;
 }
 
+// Byte offset of the 8 e4m3 values of channels [8k, 8k+8) (k < 16) of row r in an e4m3 tile
+// with one 128-byte swizzle atom per row: 16-byte chunk k/2, half k%2, chunk' = chunk ^ (r % 8).
+__device__ __forceinline__ uint32_t swz8_off(int r, int k) {
+  return static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>((k >> 1) ^ (r & 7)) << 4) +
+         static_cast<uint32_t>(k & 1) * 8u;
+}
+
+// 8 fp32 values * inv_scale -> a high and a low set of 8 e4m3 codes with the same scale:
+// hi = e4m3(y / s), lo = e4m3(y / s - value(hi)). hi + lo carries about twice the mantissa bits
+// of one e4m3 code, and both can feed MMAs that accumulate into the same result.
+__device__ __forceinline__ void quant8_hilo(const float (&y)[8], float inv_scale, uint2& hi,
+                                            uint2& lo) {
+  uint32_t ch[4], cl[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = y[2 * e] * inv_scale, b = y[2 * e + 1] * inv_scale;
+    const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const float2 hv = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3)));
+    ch[e] = h;
+    cl[e] = __nv_cvt_float2_to_fp8x2(make_float2(a - hv.x, b - hv.y), __NV_SATFINITE, __NV_E4M3);
+  }
+  hi = make_uint2(ch[0] | (ch[1] << 16), ch[2] | (ch[3] << 16));
+  lo = make_uint2(cl[0] | (cl[1] << 16), cl[2] | (cl[3] << 16));
+}
+
 // 8 fp32 values / scale -> 8 e4m3 codes (RNE, satfinite) and their exact f16 widening.
 __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& codes, uint4& wide) {
   uint32_t c[4];
@@ -196,8 +221,28 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
       unpack_bf16x8(rq[tt][hh][1], xh);
       norm_rope(xl, xh, gql, gqh, cs, sn, yl, yh);
       const int r = hh * kTok + t;
-      *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = pack8(yl, fp8);
-      *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = pack8(yh, fp8);
+      if constexpr (TPO == 2) {
+        // FP8 path: the row is stored as two sets of e4m3 codes (high, low) with one scale
+        // amax / 448
+        float am = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fmaxf(fabsf(yl[e]), fabsf(yh[e])));
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
+        const float sq = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
+        const float isq = am > 0.f ? 448.0f / am : 1.0f;
+        uint2 hi, lo;  // high codes in the first 16 KB of the unit's slot, low codes in the second
+        quant8_hilo(yl, isq, hi, lo);
+        *reinterpret_cast<uint2*>(qdst + swz8_off(r, i)) = hi;
+        *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i)) = lo;
+        quant8_hilo(yh, isq, hi, lo);
+        *reinterpret_cast<uint2*>(qdst + swz8_off(r, i + 8)) = hi;
+        *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i + 8)) = lo;
+        if (i == 0) p.q_scale[unit * kRows + r] = sq;
+      } else {
+        *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = pack8(yl, false);
+        *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = pack8(yh, false);
+      }
       if (L.q_rope != nullptr) {
         __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(h) * kTok + t) * kD;
         *reinterpret_cast<uint4*>(qr + dl) = pack8(yl, false);
@@ -232,39 +277,44 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
       }
     }
   }
-  if (TPO != 2 || !fp8) return;
-
-  // FP8 cache: the 64 own rows of this head share one scale slot, column Smax/128.
-  kmax = block_max_256(kmax, red);
-  vmax = block_max_256(vmax, red);
-  const float ksc = kmax > 0.f ? __fdiv_rn(kmax, 448.0f) : 1.0f;
-  const float vsc = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
-  const int ncol = Smax / kScaleBlock + 1;
-  if (threadIdx.x == 0) {
-    L.k_scale[g * ncol + ncol - 1] = ksc;
-    L.v_scale[g * ncol + ncol - 1] = vsc;
-  }
+  if constexpr (TPO == 2) {
+    // FP8 cache: the 64 own rows of this head share one scale slot, column Smax/128.
+    kmax = block_max_256(kmax, red);
+    vmax = block_max_256(vmax, red);
+    const float ksc = kmax > 0.f ? __fdiv_rn(kmax, 448.0f) : 1.0f;
+    const float vsc = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
+    const int ncol = Smax / kScaleBlock + 1;
+    // reference V scale of the unit: the largest over the cache blocks it reads and its own rows
+    const int n_main = (p.S + kKeyTile - 1) / kKeyTile;
+    float vr = vsc;
+    for (int b = threadIdx.x; b < n_main; b += 256) vr = fmaxf(vr, L.v_scale[g * ncol + b]);
+    vr = block_max_256(vr, red);
+    if (threadIdx.x == 0) {
+      L.k_scale[g * ncol + ncol - 1] = ksc;
+      L.v_scale[g * ncol + ncol - 1] = vsc;
+      p.sv_ref[unit] = vr;
+    }
 #pragma unroll
-  for (int tt = 0; tt < TPO; ++tt) {
-    const int t = t0 + oc + 32 * tt;
-    const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-    const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
-    uint2 c;
-    uint4 w;
-    uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + row * kD;
-    uint8_t* vc = static_cast<uint8_t*>(L.v_cache) + row * kD;
-    quant8(krl[tt], ksc, c, w);
-    *reinterpret_cast<uint2*>(kc + dl) = c;
-    *reinterpret_cast<uint4*>(tdst + sol) = w;
-    quant8(krh[tt], ksc, c, w);
-    *reinterpret_cast<uint2*>(kc + dh) = c;
-    *reinterpret_cast<uint4*>(tdst + soh) = w;
-    quant8(vrl[tt], vsc, c, w);
-    *reinterpret_cast<uint2*>(vc + dl) = c;
-    *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = w;
-    quant8(vrh[tt], vsc, c, w);
-    *reinterpret_cast<uint2*>(vc + dh) = c;
-    *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = w;
+    for (int tt = 0; tt < TPO; ++tt) {
+      const int t = t0 + oc + 32 * tt;
+      const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
+      uint2 c;
+      uint4 w;
+      uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + row * kD;
+      uint8_t* vc = static_cast<uint8_t*>(L.v_cache) + row * kD;
+      quant8(krl[tt], ksc, c, w);
+      *reinterpret_cast<uint2*>(kc + dl) = c;
+      *reinterpret_cast<uint2*>(tdst + swz8_off(t, i)) = c;
+      quant8(krh[tt], ksc, c, w);
+      *reinterpret_cast<uint2*>(kc + dh) = c;
+      *reinterpret_cast<uint2*>(tdst + swz8_off(t, i + 8)) = c;
+      quant8(vrl[tt], vsc, c, w);
+      *reinterpret_cast<uint2*>(vc + dl) = c;
+      *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i)) = c;
+      quant8(vrh[tt], vsc, c, w);
+      *reinterpret_cast<uint2*>(vc + dh) = c;
+      *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i + 8)) = c;
+    }
   }
 }
 
