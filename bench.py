@@ -25,6 +25,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from gqa_attention_long_gb300._lib import split_units  # noqa: E402
 from gqa_attention_long_gb300.inputs import config_seed, layer_inputs, layer_inputs_on_device  # noqa: E402
 
 METRIC = "µs/layer & achieved HBM GB/s (% roofline), expert attention, S=4700 Smax=8192"
@@ -40,6 +41,21 @@ def algo_bytes_per_layer(S: int, b: int = 2) -> int:
 def attn_kernel_bytes_per_layer(S: int, b: int = 2) -> int:
     """Algorithmic bytes of the attention kernel alone: live cache K/V rows, own K/V rows, output."""
     return 2 * HKV * S * D * b + 2 * HKV * T * D * b + HQ * T * D * 2
+
+
+def algo_bytes_per_layer_fp8(S: int) -> int:
+    """As algo_bytes_per_layer for an e4m3 cache (1-byte K/V codes; block scales negligible)."""
+    return 2 * HKV * S * D + 2 * (2 * HKV * T * D) + (HQ + 2 * HKV) * T * D * 2 + HQ * T * D * 2
+
+
+def launches_per_call(n_layers: int, S: int, sm_count: int) -> int:
+    """Kernels one expert_attn_layers call launches: per chunk of 64 layers the prologue, the
+    attention kernel and, when a CTA boundary cuts a unit, the merge kernel."""
+    total = 0
+    for l0 in range(0, n_layers, 64):
+        n = min(64, n_layers - l0)
+        total += 2 + (1 if split_units(n, S, sm_count) else 0)
+    return total
 
 
 def flops_per_layer(S: int) -> int:
@@ -209,6 +225,7 @@ def main():
     ap.add_argument("--Smax", type=int, default=8192)
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the FP8 and single-layer extras")
     ap.add_argument("--splits", type=int, default=0, help="attention CTAs (0 = one per SM)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -273,6 +290,7 @@ def main():
     torch.cuda.synchronize()
     k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     k2 = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     peaks = load_peaks()
     k2_bytes = attn_kernel_bytes_per_layer(S) * n
     achieved = k2_bytes / (k2 * 1e-3) / 1e9
@@ -301,6 +319,61 @@ def main():
     h2d = h_act.numel() * h_act.element_size()
     d2h = h_out.numel() * h_out.element_size()
 
+    # ---- FP8 (e4m3) cache variant of the same step: caches quantised on the device by the library
+    fp8 = None
+    if not args.no_extras:
+        ncol = Smax // 128 + 1
+        L8 = []
+        for x, L in zip(xs, Ls):
+            kq = torch.empty(HKV, Smax, D, dtype=torch.uint8, device=dev)
+            vq = torch.empty(HKV, Smax, D, dtype=torch.uint8, device=dev)
+            ks = torch.empty(HKV, ncol, dtype=torch.float32, device=dev)
+            vs = torch.empty(HKV, ncol, dtype=torch.float32, device=dev)
+            ea.expert_attn_quantize_cache(x.k_cache, S, Smax, kq, ks)
+            ea.expert_attn_quantize_cache(x.v_cache, S, Smax, vq, vs)
+            L8.append(ea.LayerBuffers(q_raw=L.q_raw, k_raw=L.k_raw, v_raw=L.v_raw, q_gamma=L.q_gamma,
+                                      k_gamma=L.k_gamma, k_cache=kq, v_cache=vq, k_scale=ks, v_scale=vs,
+                                      out=L.out))
+        ws8 = ea.alloc_workspace(n, Smax, ea.EA_KV_FP8_E4M3)
+        arr8 = ea.make_args(L8, Smax, ea.EA_KV_FP8_E4M3)
+        for _ in range(args.warmup):
+            ea.expert_attn_layers(L8, S, Smax, 0, ea.EA_KV_FP8_E4M3, ws8, stream, _arr=arr8)
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            ea.expert_attn_layers(L8, S, Smax, 0, ea.EA_KV_FP8_E4M3, ws8, stream, _arr=arr8)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        st8, bits8 = ea.expert_attn_read_status(ws8)
+        if st8 != 0:
+            raise RuntimeError(f"fp8 kernel status bits {bits8:#x}")
+        ms8 = g0.elapsed_time(g1) / args.steps
+        b8 = algo_bytes_per_layer_fp8(S) * n
+        fp8 = {"workload": f"{n}-layer step, S={S}, Smax={Smax}, e4m3 cache", "us_per_layer": ms8 * 1e3 / n,
+               "ms_per_step": ms8, "step_hbm_gbs": b8 / (ms8 * 1e-3) / 1e9,
+               "step_roofline_frac": b8 / (ms8 * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        del L8, ws8
+
+    # ---- one layer per call (the pages' per-layer measurement), rotating over 8 distinct layers
+    single = None
+    if not args.no_extras and n >= 8:
+        ws1 = ea.alloc_workspace(1, Smax)
+        arrs = [ea.make_args([Ls[l]], Smax, ea.EA_KV_BF16) for l in range(8)]
+        for l in range(8):
+            ea.expert_attn_layers([Ls[l]], S, Smax, 0, ea.EA_KV_BF16, ws1, stream, _arr=arrs[l])
+        torch.cuda.synchronize()
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 8 * max(4, args.steps // 2)
+        h0.record(stream)
+        for k in range(reps):
+            ea.expert_attn_layers([Ls[k % 8]], S, Smax, 0, ea.EA_KV_BF16, ws1, stream, _arr=arrs[k % 8])
+        h1.record(stream)
+        torch.cuda.synchronize()
+        us1 = h0.elapsed_time(h1) * 1e3 / reps
+        single = {"workload": f"one layer per call, S={S}, Smax={Smax}, bf16 cache, 8 layers rotated (> L2)",
+                  "us_per_layer": us1, "hbm_gbs": algo_bytes_per_layer(S) / (us1 * 1e-6) / 1e9}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         smp = oracle_sample(S, Smax, 8, 10.0)
@@ -320,12 +393,14 @@ def main():
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "attention_kernel", "peak_src": peaks["src"],
                          "bytes_per_launch": k2_bytes, "ms_per_launch": k2},
-            "kernels_ms": {"prologue": k1, "attention_with_merge": k2},
+            "kernels_ms": {"prologue": k1, "attention": k2, "merge": k3},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_ms * 1e3 / (n * world), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * args.steps * ((n + 63) // 64),
+            "gpu_launches": args.steps * launches_per_call(n, S, torch.cuda.get_device_properties(dev).multi_processor_count),
             "cpu_baseline": cpu,
+            "fp8_step": fp8,
+            "single_layer": single,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -9,5 +9,5 @@ from ._lib import (  # noqa: F401
     expert_attn_layer, expert_attn_layers, expert_attn_layers_profiled, expert_attn_prologue,
     expert_attn_quantize_cache, expert_attn_read_status, expert_attn_set_splits,
     expert_attn_status_string, expert_attn_workspace_init, expert_attn_workspace_size, lib,
-    make_args,
+    make_args, split_units,
 )

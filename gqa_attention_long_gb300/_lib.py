@@ -201,6 +201,22 @@ def expert_attn_quantize_cache(src: torch.Tensor, n_rows: int, Smax: int, dst: t
         _ptr(scales, "scales", torch.float32, 8 * (Smax // 128 + 1)), _stream(stream)))
 
 
+def split_units(n_layers: int, S: int, n_ctas: int) -> list[int]:
+    """Units (layer * 8 + kv head) whose key tiles the attention kernel's partition cuts between
+    CTAs, i.e. the units the merge kernel combines; the same plan the library makes for a chunk
+    of n_layers (<= 64) layers on n_ctas persistent CTAs (capped by the number of key tiles).
+    Host-side planning only (no GPU): used to count launches and by tests."""
+    T = (S + 127) // 128 + 1
+    W = n_layers * 8 * T
+    n = max(1, min(n_ctas, 257, W))
+    units: list[int] = []
+    for b in range(1, n):
+        tb = b * W // n
+        if tb % T and (not units or units[-1] != tb // T):
+            units.append(tb // T)
+    return units
+
+
 def expert_attn_set_splits(n_ctas_or_0_for_auto: int) -> int:
     return int(lib().expert_attn_set_splits(int(n_ctas_or_0_for_auto)))
 

@@ -1,6 +1,7 @@
 // api.cu — host side of libexpert_attn.so: argument validation, launch planning, TMA tensor-map
-// encoding (cached), workspace layout and the two launches (prologue, attention with its
-// merge) chained with programmatic dependent launch. See include/expert_attn.h for the contract.
+// encoding (cached), workspace layout and the three launches per chunk of layers (prologue,
+// attention, log-sum-exp merge of the split units) chained with programmatic dependent launch.
+// See include/expert_attn.h for the contract.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -13,9 +14,13 @@
 #include "internal.cuh"
 
 namespace ea {
-cudaError_t launch_prologue_kernel(const PrologueParams& pp, bool fp8, cudaLaunchConfig_t cfg);
+template <int CAP>
+cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, cudaLaunchConfig_t cfg);
 cudaError_t attention_set_attributes();
-cudaError_t launch_attention_kernel(const AttnParams& ap, bool f8, cudaLaunchConfig_t cfg);
+template <int CAP>
+cudaError_t launch_attention_kernel(const AttnParams<CAP>& ap, bool f8, cudaLaunchConfig_t cfg);
+template <int CAP>
+cudaError_t launch_merge_kernel(const MergeParams<CAP>& mp, cudaLaunchConfig_t cfg);
 __global__ void quantize_cache_kernel(const __nv_bfloat16* src, uint8_t* dst, float* scales,
                                       int n_rows, int Smax);
 }  // namespace ea
@@ -182,15 +187,28 @@ void rope_inv_freq(float* hi, float* lo) {
 
 int n_ctas_for(long long W, int sm_count) {
   int n = g_splits > 0 && g_splits < sm_count ? g_splits : sm_count;
+  if (n > kMaxSplitUnits + 1) n = kMaxSplitUnits + 1;  // at most one split unit per boundary
   if (static_cast<long long>(n) > W) n = static_cast<int>(W);
   return n < 1 ? 1 : n;
 }
 
+cudaLaunchConfig_t launch_config(cudaStream_t st, cudaLaunchAttribute* attr, bool pdl) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
 // The prologue is launched with programmatic stream serialization: its CTAs may become resident
 // while the preceding kernel drains, and wait (griddepcontrol.wait) for it before touching memory.
-int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
-                    uint8_t* ws, const WsLayout& wl, cudaStream_t st, bool pdl) {
-  PrologueParams pp;
+template <int CAP>
+int launch_prologue_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
+                      uint8_t* ws, const WsLayout& wl, cudaStream_t st, bool pdl) {
+  PrologueParams<CAP> pp;
   std::memset(&pp, 0, sizeof(pp));
   for (int l = 0; l < n; ++l) {
     PrologueLayer& d = pp.layer[l];
@@ -208,7 +226,6 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
   rope_inv_freq(pp.inv_hi, pp.inv_lo);
   pp.q_ws = ws + wl.q_off;
   pp.tail_ws = ws + wl.tail_off;
-  pp.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
   pp.q_scale = reinterpret_cast<float*>(ws + wl.qscale_off);
   pp.sv_ref = reinterpret_cast<float*>(ws + wl.svref_off);
   pp.n_layers = n;
@@ -217,32 +234,47 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
   pp.rope_delta = rope_delta;
   pp.fp8 = fp8 ? 1 : 0;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (launch_prologue_kernel(pp, fp8, cfg) != cudaSuccess) {
+  if (launch_prologue_kernel<CAP>(pp, fp8, launch_config(st, attr, pdl)) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
   return EA_OK;
 }
 
-int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
-                 uint8_t* ws, const WsLayout& wl, const DeviceInfo& di, cudaStream_t st,
-                 cudaEvent_t const* ev) {
+int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
+                    uint8_t* ws, const WsLayout& wl, cudaStream_t st, bool pdl) {
+  return n <= kSmallCap ? launch_prologue_t<kSmallCap>(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl)
+                        : launch_prologue_t<kMaxLayersPerLaunch>(a, n, S, Smax, rope_delta, fp8, ws,
+                                                                 wl, st, pdl);
+}
+
+// Attention parameter blocks are large (~19 KB at full capacity): kept off the stack, one per
+// capacity, guarded by their own mutex.
+template <int CAP>
+struct LaunchBlocks {
+  AttnParams<CAP> ap;
+  MergeParams<CAP> mp;
+  std::mutex mu;
+};
+template <int CAP>
+LaunchBlocks<CAP>& launch_blocks() {
+  static LaunchBlocks<CAP> b;
+  return b;
+}
+
+template <int CAP>
+int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
+                   uint8_t* ws, const WsLayout& wl, const DeviceInfo& di, cudaStream_t st,
+                   cudaEvent_t const* ev) {
   const bool pdl = ev == nullptr;
   if (ev && ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return EA_ERR_CUDA;
-  int rc = launch_prologue(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl);
+  int rc = launch_prologue_t<CAP>(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl);
   if (rc != EA_OK) return rc;
   if (ev && ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return EA_ERR_CUDA;
 
-  static AttnParams ap;  // large (~19 KB): kept off the stack; guarded by g_launch_mu
-  static std::mutex g_launch_mu;
-  std::lock_guard<std::mutex> lk(g_launch_mu);
+  LaunchBlocks<CAP>& lb = launch_blocks<CAP>();
+  std::lock_guard<std::mutex> lk(lb.mu);
+  AttnParams<CAP>& ap = lb.ap;
   std::memset(&ap, 0, sizeof(ap));
   for (int l = 0; l < n; ++l) {
     if (!cache_map(a[l].k_cache, S, Smax, fp8, &ap.kmap[l]) ||
@@ -262,7 +294,6 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   ap.tail_ws = ws + wl.tail_off;
   ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
   ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
-  ap.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
   ap.q_scale = reinterpret_cast<const float*>(ws + wl.qscale_off);
   ap.sv_ref = reinterpret_cast<const float*>(ws + wl.svref_off);
   ap.ncol = Smax / kScaleBlock + 1;
@@ -271,22 +302,48 @@ int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta,
   const int n_ctas = n_ctas_for(ap.W, di.sm_count);
 
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = launch_config(st, attr, pdl);
   cfg.gridDim = dim3(n_ctas);
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (launch_attention_kernel(ap, fp8, cfg) != cudaSuccess) {
+  if (launch_attention_kernel<CAP>(ap, fp8, cfg) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
   if (ev && ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return EA_ERR_CUDA;
-  // The log-sum-exp merge runs inside the attention kernel; the fourth event follows directly.
+
+  // Units cut by a CTA boundary (each listed once, in order) are merged by K3.
+  MergeParams<CAP>& mp = lb.mp;
+  mp.n_split = 0;
+  for (int b = 1; b < n_ctas; ++b) {
+    const long long tb = cta_tile_start(b, ap.W, n_ctas);
+    if (tb % ap.T == 0) continue;
+    const int u = static_cast<int>(tb / ap.T);
+    if (mp.n_split > 0 && mp.unit[mp.n_split - 1].u == u) continue;
+    const long long first = static_cast<long long>(u) * ap.T;
+    SplitUnit& su = mp.unit[mp.n_split++];
+    su.u = u;
+    su.c0 = static_cast<short>(cta_of_tile(first, ap.W, n_ctas));
+    su.nparts = static_cast<short>(cta_of_tile(first + ap.T - 1, ap.W, n_ctas) - su.c0 + 1);
+    su.slot0 = cta_tile_start(su.c0, ap.W, n_ctas) >= first ? 0 : 1;
+  }
+  if (mp.n_split > 0) {
+    for (int l = 0; l < n; ++l) mp.out[l] = ap.out[l];
+    mp.part_o = ap.part_o;
+    mp.part_lse = ap.part_lse;
+    if (launch_merge_kernel<CAP>(mp, launch_config(st, attr, pdl)) != cudaSuccess) {
+      cudaGetLastError();
+      return EA_ERR_CUDA;
+    }
+  }
   if (ev && ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return EA_ERR_CUDA;
   return EA_OK;
+}
+
+int launch_chunk(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
+                 uint8_t* ws, const WsLayout& wl, const DeviceInfo& di, cudaStream_t st,
+                 cudaEvent_t const* ev) {
+  return n <= kSmallCap
+             ? launch_chunk_t<kSmallCap>(a, n, S, Smax, rope_delta, fp8, ws, wl, di, st, ev)
+             : launch_chunk_t<kMaxLayersPerLaunch>(a, n, S, Smax, rope_delta, fp8, ws, wl, di, st, ev);
 }
 
 int run_layers(const ea_layer_args* a, int n_layers, int S, int Smax, int rope_delta, int kv_dtype,
@@ -421,14 +478,13 @@ const char* expert_attn_status_string(int status) {
 }  // extern "C"
 
 // -------------------------------------------------------------- no-allocation variant
-// expert_attn_layers_noalloc runs the same three launches as expert_attn_layers, with the
+// expert_attn_layers_noalloc runs the same launches as expert_attn_layers, with the
 // workspace replaced by a static device array. Host code must not use the array's name as a
 // pointer (that is a host-side stand-in); its device address is looked up once per device.
 namespace {
 
 constexpr size_t noalloc_bytes() {
-  return ((1024 + static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(uint32_t) +
-           static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(float) + 1024 +
+  return ((1024 + static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(float) + 1024 +
            2 * static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kQTileBytes +
            static_cast<size_t>(EA_NOALLOC_MAX_CTAS) * 2 * kRows * (kD + 1) * sizeof(float)) +
           1023) & ~static_cast<size_t>(1023);

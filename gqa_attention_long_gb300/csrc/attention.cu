@@ -1,4 +1,4 @@
-// attention.cu — K2: persistent split-KV expert attention on the sm_103a tensor cores (bf16 cache).
+// attention.cu — K2: persistent split-KV expert attention on the sm_103a tensor cores.
 //
 // What it computes (alpamayo_tt/expert.py, TTExpert.attention_core; alpamayo_tt/EXPERT_NOTES.md,
 // "Attention over the VLM cache: masking approach"): for every (layer, kv head g) unit, the 128
@@ -10,30 +10,38 @@
 // 64-row tile of own rows) are laid out unit-major and cut into one contiguous range per CTA
 // (grid = number of SMs, one CTA per SM). A CTA walks its range as "segments" (the part of one
 // unit inside the range). A segment that covers a whole unit writes the bf16 output directly;
-// a partial one writes a normalised fp32 partial plus its log2-sum-exp per row, and the thread
-// that writes the last missing partial of a row (an atomic arrival count; nobody waits) merges:
-//   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s O_s / sum_s w_s  (log-sum-exp merge).
+// a partial one writes a normalised fp32 partial plus its log2-sum-exp per row, which the
+// log-sum-exp merge kernel (merge.cu) combines once this grid has finished.
 //
-// Warp roles (224 threads):
-//   warps 0-3  softmax: thread r owns folded row r (= TMEM lane r); online softmax in fp32 with
-//              lazy rescaling of the TMEM accumulator; P written back to TMEM as bf16 over the
-//              scores it came from, and read from there by the PV MMA
-//   warp 4     K/V producer: one thread issues 3-D TMA loads of cache K/V tiles and bulk copies
-//              of the own rows (pre-swizzled in the workspace) into a 5-slot ring
-//   warp 5     MMA: one thread issues tcgen05.mma (S = Q K^T from shared memory into one of two
-//              TMEM score buffers; O += P V with P from TMEM and V from shared memory into the TMEM
-//              accumulator) and tcgen05.commit to the barriers
-//   warp 6     Q loader: one thread brings each segment's roped Q (32 KB, pre-swizzled) into one
+// Two key streams per CTA: the CTA's tiles alternate between stream 0 (even tile count) and
+// stream 1 (odd), each with its own TMEM score buffer, its own TMEM accumulator and its own
+// softmax warpgroup with its own running max and sum, so that one warpgroup's exponentials
+// overlap the other's TMEM traffic and waits (the softmax, not the tensor core, limits a CTA).
+// At the end of a segment the two warpgroups exchange their row statistics through shared
+// memory and each writes half of the output columns of the combined rows.
+//
+// Warp roles (352 threads):
+//   warps 0-3, 4-7  softmax of stream 0, 1: thread r of a warpgroup owns folded row r (= TMEM
+//              lane r); online softmax in fp32 with lazy rescaling of its TMEM accumulator; P
+//              written back to TMEM as bf16 (e4m3) over the scores it came from, and read from
+//              there by the PV MMA
+//   warp 8     K/V producer: one thread issues 3-D TMA loads of cache K/V tiles and bulk copies
+//              of the own rows (pre-swizzled in the workspace) into the ring
+//   warp 9     MMA: one thread issues tcgen05.mma (S = Q K^T from shared memory into the score
+//              buffer of the tile's stream; O += P V with P from TMEM and V from shared memory
+//              into the stream's accumulator) and tcgen05.commit to the barriers
+//   warp 10    Q loader: one thread brings each segment's roped Q (32 KB, pre-swizzled) into one
 //              of two buffers, one segment ahead, so the K/V stream never waits for it
-// Shared memory: Q x2 (64 KB), K/V ring 5 x 32 KB, barriers. TMEM: 512 columns (two 128-column
-// score/P buffers and one 128-column fp32 accumulator).
+// Shared memory: Q x2 (64 KB), K/V ring (160 KB), barriers, a 1 KB row-statistics exchange.
+// TMEM: 512 columns (two 128-column score/P buffers, two 128-column fp32 accumulators).
 #include "internal.cuh"
 #include "ptx.cuh"
 
 namespace ea {
 namespace attn {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;
 
 // Shared-memory layout of one CTA. bf16 cache: a K or V tile is 128 rows x 256 bytes, stored as
 // two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom.
@@ -47,10 +55,14 @@ struct Lay {
   static constexpr uint32_t SM_Q = 0;  // two Q buffers
   static constexpr uint32_t SM_RING = SM_Q + 2 * kQ;
   static constexpr uint32_t SM_BAR = SM_RING + kRing * kSlot;
+  // per-stream barriers (SFULL, PFULL, ODONE) are indexed by the stream; X1, X2 and OFREE
+  // complete once per segment (row-statistics exchange and release of the accumulators)
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing,
                        B_SFULL = 4 + 2 * kRing, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-                       B_DRAIN = B_ODONE + 2, kNumBars = B_DRAIN + 1;
-  static constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
+                       B_X1 = B_ODONE + 2, B_X2 = B_X1 + 1, B_OFREE = B_X2 + 1,
+                       B_DRAIN = B_OFREE + 1, kNumBars = B_DRAIN + 1;
+  static constexpr uint32_t SM_XCH = SM_BAR + kNumBars * 8;  // float2 per folded row
+  static constexpr uint32_t SM_TMEM = SM_XCH + kRows * 8;
   static constexpr uint32_t SM_ABORT = SM_TMEM + 4;
   static constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;  // + slack to align the base
   static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
@@ -63,14 +75,15 @@ struct Lay {
   constexpr uint32_t SM_Q = LY::SM_Q, SM_RING = LY::SM_RING;                               \
   constexpr int B_QFULL = LY::B_QFULL, B_QEMPTY = LY::B_QEMPTY, B_KVFULL = LY::B_KVFULL,   \
                 B_KVEMPTY = LY::B_KVEMPTY, B_SFULL = LY::B_SFULL, B_PFULL = LY::B_PFULL,    \
-                B_ODONE = LY::B_ODONE, B_DRAIN = LY::B_DRAIN;                              \
+                B_ODONE = LY::B_ODONE, B_X1 = LY::B_X1, B_X2 = LY::B_X2,                   \
+                B_OFREE = LY::B_OFREE, B_DRAIN = LY::B_DRAIN;                              \
   (void)kRing; (void)kSlotBytes; (void)kAtom; (void)kQB; (void)SM_Q; (void)SM_RING;         \
   (void)B_QFULL; (void)B_QEMPTY; (void)B_KVFULL; (void)B_KVEMPTY; (void)B_SFULL;            \
-  (void)B_PFULL; (void)B_ODONE; (void)B_DRAIN
+  (void)B_PFULL; (void)B_ODONE; (void)B_X1; (void)B_X2; (void)B_OFREE; (void)B_DRAIN
 
-constexpr uint32_t TM_S = 0;    // score buffers at columns 0 and 128; P(i) overwrites the first
-                                // columns of the buffer that held S(i)
-constexpr uint32_t TM_O = 256;  // output accumulator, columns 256..383
+constexpr uint32_t TM_S = 0;    // score buffers of streams 0 and 1 at columns 0 and 128; P(n)
+                                // overwrites the first columns of the buffer that held S(n)
+constexpr uint32_t TM_O = 256;  // accumulators of streams 0 and 1 at columns 256 and 384
 constexpr uint32_t kTmemCols = 512;
 
 struct Seg {
@@ -89,6 +102,7 @@ __device__ __forceinline__ bool next_seg(long long& t, long long end, int T, Seg
 }
 
 struct Ctx {
+  uint8_t* smem;  // generic address of the aligned shared-memory base
   uint32_t sbase;
   uint32_t tmem;
   volatile uint32_t* abort_flag;
@@ -99,8 +113,8 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------------------- producer
-template <bool F8>
-__device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
+template <bool F8, class PP>
+__device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
   pdl_wait_primary();  // roped Q and own rows are written by the prologue kernel
   const uint64_t pol_stream = l2_policy_evict_first();  // cache tiles are read exactly once
@@ -155,8 +169,8 @@ __device__ __noinline__ void producer(const AttnParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------------------- Q loader
-template <bool F8>
-__device__ __noinline__ void q_loader(const AttnParams& p, const Ctx& cx) {
+template <bool F8, class PP>
+__device__ __noinline__ void q_loader(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
   const uint64_t pol_keep = l2_policy_evict_last();
   int seg = 0;
@@ -185,11 +199,13 @@ __device__ __noinline__ void q_loader(const AttnParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------------------------ MMA
-// Issue order per segment: QK(0), then for i >= 1: QK(i), PV(i-1); finally PV(nt-1). So QK(i+1)
-// is issued only after PV(i-1), whose P came from the softmax of tile i-1: by then the score
-// buffer that QK(i+1) overwrites has been read, and every completed S(i) implies PV(i-2) done.
-template <bool F8>
-__device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
+// Issue order per segment: QK(0), then for i >= 1: QK(i), PV(i-1); finally PV(nt-1). Tile n of
+// the CTA (counted over all its segments) belongs to stream n & 1: QK(n) writes that stream's
+// score buffer, PV(n) accumulates into that stream's accumulator. QK(n) is issued only after
+// PV(n-2), the previous MMA that read the same buffer, has completed; so a completed S(n)
+// also tells the softmax that every earlier PV of its stream is done.
+template <bool F8, class PP>
+__device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
   // bf16: format code 1 (kind::f16); e4m3: format code 0 (kind::f8f6f4). V is MN-major.
   constexpr uint32_t kIdescQK128 = umma_idesc_f16(128, 128, !F8, false, false);
@@ -246,8 +262,8 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
       }
       if (i > 0) {
         const int ii = i - 1, j = s.j0 + ii;
-        // P of even and odd tiles arrive on separate barriers: a softmax warp may run one tile
-        // ahead of another, and its arrivals must not complete the slower warps' phase
+        // P of even and odd tiles (streams 0 and 1) arrive on separate barriers, each from its
+        // own softmax warpgroup
         ok = bounded_wait(cx.bar(B_PFULL + (n_pv & 1)), (n_pv >> 1) & 1, cx.abort_flag, cx.status,
                           kErrMmaWait);
         if (!ok) break;
@@ -260,20 +276,22 @@ __device__ __noinline__ void mma_issuer(const AttnParams& p, const Ctx& cx) {
         // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together);
         // a K step spans 8 TMEM columns in both formats (16 bf16 or 32 e4m3 keys)
         const uint32_t pcol = cx.tmem + TM_S + (n_pv & 1) * 128;
+        // the first PV of each stream in a segment (segment tiles 0 and 1) starts a fresh sum
+        const uint32_t ocol = cx.tmem + TM_O + (n_pv & 1) * 128;
         if constexpr (F8) {
           // 32 keys per step (the own-row tile has 64 keys); V: 32 key rows of 128 bytes per
           // step. The high P codes sit in columns [0, 32), the low ones in [32, 64).
           const int nk = j < p.n_main ? 4 : 2;
           for (int kk = 0; kk < 2 * nk; ++kk) {
             const int ks = kk < nk ? kk : kk - nk;
-            umma_f8_ts(cx.tmem + TM_O, pcol + (kk < nk ? 0 : 32) + ks * 8,
-                       sw128_desc(vaddr + ks * 32 * 128, 16, 1024), kIdescPV, (ii > 0 || kk > 0));
+            umma_f8_ts(ocol, pcol + (kk < nk ? 0 : 32) + ks * 8,
+                       sw128_desc(vaddr + ks * 32 * 128, 16, 1024), kIdescPV, (ii > 1 || kk > 0));
           }
         } else {
           const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
           for (int kk = 0; kk < nk; ++kk)        // V: 16 key rows of 128 bytes per step and atom
-            umma_f16_ts(cx.tmem + TM_O, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024),
-                        kIdescPV, (ii > 0 || kk > 0));
+            umma_f16_ts(ocol, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024),
+                        kIdescPV, (ii > 1 || kk > 0));
         }
         // even and odd PVs complete on separate barriers: a waiter that knows PV k-2 is done
         // can then always tell PV k's completion from an older phase
@@ -310,87 +328,25 @@ __device__ __forceinline__ void rescale_O(uint32_t taddr, float alpha) {
   tmem_wait_st();
 }
 
-// Log-sum-exp merge of folded row r of unit u from the partials of every CTA that holds a part
-// of it (their rows are visible: each thread wrote its row, fenced, then counted it). Reads
-// bypass L1 (ld.global.cg): the rows were written by other SMs.
-__device__ __noinline__ void merge_unit_row(const AttnParams& p, int u, int r) {
-  __threadfence();
-  const int n = gridDim.x;
-  const long long first = static_cast<long long>(u) * p.T;
-  const int c0 = cta_of_tile(first, p.W, n), c1 = cta_of_tile(first + p.T - 1, p.W, n);
-  const int nparts = c1 - c0 + 1;
-  float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c)
-    M = fmaxf(M, __ldcg(p.part_lse + part_index(c, first, p.W, n) * kRows + r));
-  float L = 0.f;
-  for (int c = c0; c <= c1; ++c) L += ex2_approx(__ldcg(p.part_lse + part_index(c, first, p.W, n) * kRows + r) - M);
-  const float invL = 1.0f / L;
-  __nv_bfloat16* orow = p.out[u / kHkv] + (static_cast<size_t>(u % kHkv) * kRows + r) * kD;
-  // Four chunks of 32 columns; per chunk, the rows of two parts are requested together (16
-  // independent 16-byte loads in flight per thread) before they are accumulated.
-#pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {
-    float acc[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-#pragma unroll 1
-    for (int q0 = 0; q0 < nparts; q0 += 2) {
-      float4 o[2][8];
-      float w[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        w[q] = 0.f;
-        if (q0 + q < nparts) {
-          const size_t pi = part_index(c0 + q0 + q, first, p.W, n);
-          w[q] = ex2_approx(__ldcg(p.part_lse + pi * kRows + r) - M) * invL;
-          const float4* src = reinterpret_cast<const float4*>(p.part_o + (pi * kRows + r) * kD + ch * 32);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) o[q][k] = __ldcg(src + k);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) o[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          acc[4 * k] = fmaf(w[q], o[q][k].x, acc[4 * k]);
-          acc[4 * k + 1] = fmaf(w[q], o[q][k].y, acc[4 * k + 1]);
-          acc[4 * k + 2] = fmaf(w[q], o[q][k].z, acc[4 * k + 2]);
-          acc[4 * k + 3] = fmaf(w[q], o[q][k].w, acc[4 * k + 3]);
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 wv;
-      wv.x = pack_bf16x2(acc[8 * q + 0], acc[8 * q + 1]);
-      wv.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
-      wv.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
-      wv.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
-      *reinterpret_cast<uint4*>(orow + ch * 32 + 8 * q) = wv;
-    }
-  }
-}
-
-template <bool F8>
-__device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
+template <bool F8, class PP>
+__device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
-  const int r = threadIdx.x;  // folded row = TMEM lane
-  const uint32_t lane_addr = static_cast<uint32_t>(threadIdx.x & ~31) << 16;
+  const int k = threadIdx.x >> 7;   // stream of this warpgroup
+  const int r = threadIdx.x & 127;  // folded row = TMEM lane
+  const uint32_t lane_addr = static_cast<uint32_t>(r & ~31) << 16;
+  const uint32_t s_col = TM_S + k * 128, o_col = TM_O + k * 128;
+  const uint32_t pa_base = cx.tmem + lane_addr + s_col;  // P(n) of this stream
   const float c = p.scale_log2;
-  uint32_t n_s = 0, pv_total = 0;
+  float2* xch = reinterpret_cast<float2*>(cx.smem + LY::SM_XCH);
+  uint32_t base = 0, seg = 0;  // tiles of this CTA before the current segment; segment count
   bool ok = true, first_seg = true;
   long long t = cx.start;
   Seg s;
 
-  // Waits for PV number k of this CTA. Callers know that PV k-2 is complete (S(i) ready implies
-  // every PV issued before QK(i), i.e. up to PV(i-2)), so the parity of PV k's barrier (even and
-  // odd PVs use separate barriers) identifies its completion unambiguously.
-  auto wait_pv = [&](uint32_t k) -> bool {
-    // warp-uniform outcome: the TMEM loads and shuffles that follow need the full warp
-    return __all_sync(0xffffffffu, bounded_wait(cx.bar(B_ODONE + (k & 1)), (k >> 1) & 1,
-                                                cx.abort_flag, cx.status, kErrSoftmaxWait));
+  // warp-uniform outcome: the TMEM loads and shuffles that follow need the full warp
+  auto wait_bar = [&](int b, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, bounded_wait(cx.bar(b), parity, cx.abort_flag, cx.status,
+                                                kErrSoftmaxWait));
   };
 
   while (ok && next_seg(t, cx.end, p.T, s)) {
@@ -403,52 +359,50 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
       sq = p.q_scale[static_cast<size_t>(s.u) * kRows + r];
       svr = p.sv_ref[s.u];
     }
-    for (int i = 0; i < nt; ++i) {
+    int last_n = -1;  // last tile of this stream in the segment (-1: none yet)
+    // segment tile i is CTA tile base + i and belongs to stream (base + i) & 1
+    for (int i = (k - static_cast<int>(base)) & 1; i < nt; i += 2) {
+      const int n = static_cast<int>(base) + i;
       const int j = s.j0 + i;
-      const uint32_t sb = n_s & 1;
-      ok = __all_sync(0xffffffffu, bounded_wait(cx.bar(B_SFULL + sb), (n_s >> 1) & 1,
-                                                cx.abort_flag, cx.status, kErrSoftmaxWait));
+      ok = wait_bar(B_SFULL + k, (n >> 1) & 1);
       if (!ok) break;
-      __syncwarp();
-      ++n_s;
       tc_fence_after();
       const bool tail = j >= p.n_main;
-      const uint32_t sa = cx.tmem + lane_addr + TM_S + sb * 128;
-      uint32_t v[4][32];
-      tmem_ld32(sa, v[0]);
-      tmem_ld32(sa + 32, v[1]);
-      if (!tail) {
-        tmem_ld32(sa + 64, v[2]);
-        tmem_ld32(sa + 96, v[3]);
-      }
-      tmem_wait_ld();
-      reg_fence32(v[0]);
-      reg_fence32(v[1]);
-      if (!tail) {
-        reg_fence32(v[2]);
-        reg_fence32(v[3]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[2][e] = v[3][e] = __float_as_uint(-INFINITY);
-      }
-      // keys >= S of the last cache tile (zero-filled by TMA) are masked out
+      const uint32_t sa = cx.tmem + lane_addr + s_col;
+      // The score row is read in two passes of 64-column pairs (max, then exponentials), so
+      // that no more than 64 scores are live per thread: two softmax warpgroups share the
+      // register file. A cache tile has two pairs, the own-row tile (64 keys) one.
+      const int npair = tail ? 1 : 2;
       const int key0 = j * kKeyTile;
-      if (!tail && key0 + kKeyTile > p.S) {
+      const bool ragged = !tail && key0 + kKeyTile > p.S;  // keys >= S (zero-filled) are masked
+      auto load_pair = [&](int pr, uint32_t (&v)[2][32]) {
+        tmem_ld32(sa + 64 * pr, v[0]);
+        tmem_ld32(sa + 64 * pr + 32, v[1]);
+        tmem_wait_ld();
+        reg_fence32(v[0]);
+        reg_fence32(v[1]);
+        if (ragged) {
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
+          for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + ch * 32 + e >= p.S) v[ch][e] = __float_as_uint(-INFINITY);
-      }
+            for (int e = 0; e < 32; ++e)
+              if (key0 + 64 * pr + 32 * ch + e >= p.S) v[ch][e] = __float_as_uint(-INFINITY);
+        }
+      };
       // row max with 8 independent accumulators (a single chain would serialise 128 fmax)
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+      for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+#pragma unroll 1
+      for (int pr = 0; pr < npair; ++pr) {
+        uint32_t v[2][32];
+        load_pair(pr, v);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
+        for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
+          for (int e = 0; e < 32; e += 2)
+            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
+      }
       // per-tile factors: scores in log2 units are s * ct; FP8 adds the block scales, and P is
       // stored as 2^(x - m) * (sv / svr) (exponent offset lgv) so that its e4m3 codes carry the
       // tile's V scale relative to the unit's largest one; the row sum counts 2^(x - m).
@@ -462,166 +416,160 @@ __device__ __noinline__ void softmax_warps(const AttnParams& p, const Ctx& cx) {
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * ct;
-      const bool need = (i == 0) || (mt > m_ref + kLazy);
+      const bool need = (last_n < 0) || (mt > m_ref + kLazy);
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = fmaxf(m_ref, mt);
         const float alpha = ex2_approx(m_ref - m_new);
-        if (i > 0) {
-          ok = wait_pv(pv_total + i - 1);  // the accumulator holds tiles < i
-          if (!ok) break;
-          tc_fence_after();
-          rescale_O(cx.tmem + lane_addr + TM_O, alpha);
-        }
+        // S(n) is complete, so PV(n-2) and every earlier PV of this stream are done: the
+        // accumulator is stable and holds this stream's tiles before n
+        if (last_n >= 0) rescale_O(cx.tmem + lane_addr + o_col, alpha);
         lsum *= alpha;
         m_ref = m_new;
       }
       const float neg = lgv - m_ref;
       float ts8[8];  // row sum with 8 independent accumulators
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ts8[k] = 0.f;
-      const uint32_t pa = cx.tmem + lane_addr + TM_S + sb * 128;
-      // P(i) goes to TMEM over the columns of S(i), already read. The buffer's previous P,
-      // P(i-2), was consumed by PV(i-2), which completed before QK(i).
-      if constexpr (F8) {
-        // four e4m3 codes per column: P as high codes in columns [0, 32) and low codes (the
-        // residual) in [32, 64); the own-row tile (64 keys) uses 16 columns of each
-        uint32_t lo[4][8];
+      for (int q = 0; q < 8; ++q) ts8[q] = 0.f;
+      // P(n) goes to TMEM over the columns of S(n). Pair pr's P lands in columns that hold
+      // scores of pairs <= pr, already read (bf16: columns [32 pr, 32 pr + 32); e4m3: high
+      // codes in [16 pr, 16 pr + 16), low codes in [32 + 16 pr, 32 + 16 pr + 16)). The buffer's
+      // previous P, P(n-2), was consumed by PV(n-2), which completed before QK(n).
+#pragma unroll 1
+      for (int pr = 0; pr < npair; ++pr) {
+        uint32_t v[2][32];
+        load_pair(pr, v);
+        if constexpr (F8) {
+          // four e4m3 codes per column; the low codes carry the residual of the high ones
+          uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
+          for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e]), ct, neg));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 1]), ct, neg));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 2]), ct, neg));
-            const float p3 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 3]), ct, neg));
-            ts8[e] += (p0 + p1) + (p2 + p3);
-            uint32_t hi;
-            pack_e4m3x4_hilo(p0, p1, p2, p3, hi, lo[ch][e]);
-            v[ch][e] = hi;  // packed P overwrites the consumed scores
-          }
-        uint32_t pk[16];
+            for (int e = 0; e < 8; ++e) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e]), ct, neg));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 1]), ct, neg));
+              const float p2 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 2]), ct, neg));
+              const float p3 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 3]), ct, neg));
+              ts8[e] += (p0 + p1) + (p2 + p3);
+              pack_e4m3x4_hilo(p0, p1, p2, p3, hi[8 * ch + e], lo[8 * ch + e]);
+            }
+          tmem_st16(pa_base + 16 * pr, hi);
+          tmem_st16(pa_base + 32 + 16 * pr, lo);
+        } else {
+          // bf16 pairs: column c holds keys 2c and 2c + 1
+          uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pk[e] = v[0][e];
-          pk[8 + e] = v[1][e];
-        }
-        tmem_st16(pa, pk);
+          for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pk[e] = lo[0][e];
-          pk[8 + e] = lo[1][e];
-        }
-        tmem_st16(pa + 32, pk);
-        if (!tail) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pk[e] = v[2][e];
-            pk[8 + e] = v[3][e];
-          }
-          tmem_st16(pa + 16, pk);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pk[e] = lo[2][e];
-            pk[8 + e] = lo[3][e];
-          }
-          tmem_st16(pa + 48, pk);
-        }
-      } else {
-        // bf16 pairs: 128 keys in 64 columns (own-row tile: 32)
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), ct, neg));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), ct, neg));
-            ts8[e & 7] += p0 + p1;
-            v[ch][e] = pack_bf16x2(p0, p1);  // packed P overwrites the consumed scores
-          }
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pk[e] = v[0][e];
-          pk[16 + e] = v[1][e];
-        }
-        tmem_st32(pa, pk);
-        if (!tail) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            pk[e] = v[2][e];
-            pk[16 + e] = v[3][e];
-          }
-          tmem_st32(pa + 32, pk);
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), ct, neg));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), ct, neg));
+              ts8[e & 7] += p0 + p1;
+              pk[16 * ch + e] = pack_bf16x2(p0, p1);
+            }
+          tmem_st32(pa_base + 32 * pr, pk);
         }
       }
       lsum += (((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]))) * lmul;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(cx.bar(B_PFULL + sb));
+      mbar_arrive(cx.bar(B_PFULL + k));
+      last_n = n;
     }
     if (!ok) break;
 
-    // ---- epilogue: O / l of this segment (its last two PVs may still be running)
-    if (nt >= 2) ok = wait_pv(pv_total + nt - 2);
-    if (ok) ok = wait_pv(pv_total + nt - 1);
-    if (!ok) break;
+    // ---- epilogue. Each stream waits for its last PV (the one before it is done: S(last)
+    // completed after it). Stream 1 hands its (max, sum) to stream 0, which forms the row's
+    // weights w_k = 2^(m_k - M) * svr / L and hands them back; each warpgroup then writes the
+    // combined rows' output columns [64 k, 64 k + 64). A stream without tiles in the segment
+    // has m = -inf and weight 0 and its accumulator is not read.
+    if (last_n >= 0) {
+      ok = wait_bar(B_ODONE + k, (last_n >> 1) & 1);
+      if (!ok) break;
+    }
+    const uint32_t sp = seg & 1;
+    const bool has0 = nt >= 2 || (base & 1) == 0, has1 = nt >= 2 || (base & 1) == 1;
+    float w0, w1, lse_row = 0.f;
+    if (k == 1) {
+      xch[r] = make_float2(m_ref, lsum);
+      mbar_arrive(cx.bar(B_X1));
+      ok = wait_bar(B_X2, sp);
+      if (!ok) break;
+      const float2 w = xch[r];
+      w0 = w.x;
+      w1 = w.y;
+    } else {
+      ok = wait_bar(B_X1, sp);
+      if (!ok) break;
+      const float2 o = xch[r];  // stream 1's (max, sum)
+      const float M = fmaxf(m_ref, o.x);
+      const float a0 = has0 ? ex2_approx(m_ref - M) : 0.f;
+      const float a1 = has1 ? ex2_approx(o.x - M) : 0.f;
+      const float L = lsum * a0 + o.y * a1;
+      const float inv = svr / L;  // FP8: P was stored relative to the reference V scale
+      w0 = a0 * inv;
+      w1 = a1 * inv;
+      lse_row = M + log2f(L);
+      xch[r] = make_float2(w0, w1);
+      mbar_arrive(cx.bar(B_X2));
+    }
     tc_fence_after();
-    const float inv = svr / lsum;  // FP8: P was stored relative to the reference V scale
     const bool full = (s.j0 == 0 && s.j1 == p.T);
     const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
     first_seg = false;
-    float* po = p.part_o + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r) * kD;
-    __nv_bfloat16* orow = p.out[l] + (static_cast<size_t>(g) * kRows + r) * kD;
+    float* po = p.part_o + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r) * kD + 64 * k;
+    __nv_bfloat16* orow = p.out[l] + (static_cast<size_t>(g) * kRows + r) * kD + 64 * k;
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      uint32_t o[32];
-      tmem_ld32(cx.tmem + lane_addr + TM_O + ch * 32, o);
-      tmem_wait_ld();
-      reg_fence32(o);
+    for (int ch = 0; ch < 2; ++ch) {
+      const uint32_t col = cx.tmem + lane_addr + TM_O + 64 * k + 32 * ch;
+      float o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {  // the two streams' accumulators, one after the other
+        if (st == 0 ? !has0 : !has1) continue;
+        uint32_t x[32];
+        tmem_ld32(col + 128 * st, x);
+        tmem_wait_ld();
+        reg_fence32(x);
+        const float w = st == 0 ? w0 : w1;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = fmaf(__uint_as_float(x[e]), w, o[e]);
+      }
       if (full) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          w.x = pack_bf16x2(o[8 * q + 0], o[8 * q + 1]);
+          w.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
+          w.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
+          w.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
           *reinterpret_cast<uint4*>(orow + ch * 32 + 8 * q) = w;
         }
       } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 w = make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                                 __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
-          *reinterpret_cast<float4*>(po + ch * 32 + 4 * q) = w;
-        }
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(po + ch * 32 + 4 * q) =
+              make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
     }
-    if (!full) {
-      p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = m_ref + log2f(lsum);
-      // Count this partial row; the thread that brings the count to the number of parts of the
-      // unit merges the row. No thread waits for another.
-      __threadfence();
-      const long long first = static_cast<long long>(s.u) * p.T;
-      const int nparts = cta_of_tile(first + p.T - 1, p.W, gridDim.x) -
-                         cta_of_tile(first, p.W, gridDim.x) + 1;
-      if (atomicAdd(p.row_cnt + static_cast<size_t>(s.u) * kRows + r, 1u) + 1u ==
-          static_cast<uint32_t>(nparts))
-        merge_unit_row(p, s.u, r);
-      // Only some lanes merged: reconverge before the next tcgen05.ld/st (.sync.aligned, they
-      // need the whole warp to execute them together).
-      __syncwarp();
-    }
+    if (!full && k == 0) p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = lse_row;
+    // Both halves of every row are written and both accumulators read: release them to the
+    // next segment's PVs (their P arrives only after this barrier).
     tc_fence_before();
-    pv_total += nt;
+    mbar_arrive(cx.bar(B_OFREE));
+    ok = wait_bar(B_OFREE, sp);
+    if (!ok) break;
+    base += nt;
+    ++seg;
   }
 }
 
 }  // namespace attn
 
 // ------------------------------------------------------------------------------------ kernel
-template <bool F8>
+template <bool F8, int CAP>
 __global__ void __launch_bounds__(attn::kThreads, 1)
-    attention_kernel(const __grid_constant__ AttnParams p) {
+    attention_kernel(const __grid_constant__ AttnParams<CAP> p) {
   using namespace attn;
   EA_LAYOUT_ALIASES;
   extern __shared__ uint8_t smem_raw[];
@@ -629,6 +577,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx cx;
+  cx.smem = smem;
   cx.sbase = smem_u32(smem);
   cx.bar_base = cx.sbase + LY::SM_BAR;
   cx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + LY::SM_ABORT);
@@ -644,6 +593,9 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       mbar_init(cx.bar(B_PFULL + b), 128);
       mbar_init(cx.bar(B_ODONE + b), 1);
     }
+    mbar_init(cx.bar(B_X1), 128);
+    mbar_init(cx.bar(B_X2), 128);
+    mbar_init(cx.bar(B_OFREE), kSoftmaxThreads);
     for (int b = 0; b < kRing; ++b) {
       mbar_init(cx.bar(B_KVFULL + b), 1);
       mbar_init(cx.bar(B_KVEMPTY + b), 1);
@@ -652,7 +604,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     *cx.abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(cx.sbase + LY::SM_TMEM, kTmemCols);
     tmem_relinquish();
   }
@@ -663,11 +615,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   // Everything below depends on the prologue (staged Q and own rows, zeroed arrival counts).
   pdl_wait_primary();
 
-  if (warp < 4) {
+  if (warp < 8) {
     softmax_warps<F8>(p, cx);
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     if (lane == 0) producer<F8>(p, cx);
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) mma_issuer<F8>(p, cx);
   } else {
     if (lane == 0) q_loader<F8>(p, cx);
@@ -676,25 +628,35 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(cx.tmem, kTmemCols);
+  if (warp == 9) tmem_dealloc(cx.tmem, kTmemCols);
 }
 
-// Host side: attributes and launch of the two instances (kept in this file, where the kernel
+// Host side: attributes and launch of the four instances (kept in this file, where the kernel
 // template is instantiated).
-cudaError_t attention_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(attn::Lay<false>::kSmemBytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(attn::Lay<true>::kSmemBytes));
+template <bool F8, int CAP>
+static cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(attention_kernel<F8, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(attn::Lay<F8>::kSmemBytes));
 }
 
-cudaError_t launch_attention_kernel(const AttnParams& ap, bool f8, cudaLaunchConfig_t cfg) {
+cudaError_t attention_set_attributes() {
+  cudaError_t e = set_smem_attr<false, kSmallCap>();
+  if (e == cudaSuccess) e = set_smem_attr<true, kSmallCap>();
+  if (e == cudaSuccess) e = set_smem_attr<false, kMaxLayersPerLaunch>();
+  if (e == cudaSuccess) e = set_smem_attr<true, kMaxLayersPerLaunch>();
+  return e;
+}
+
+template <int CAP>
+cudaError_t launch_attention_kernel(const AttnParams<CAP>& ap, bool f8, cudaLaunchConfig_t cfg) {
   cfg.blockDim = dim3(attn::kThreads);
   cfg.dynamicSmemBytes = f8 ? attn::Lay<true>::kSmemBytes : attn::Lay<false>::kSmemBytes;
-  return f8 ? cudaLaunchKernelEx(&cfg, attention_kernel<true>, ap)
-            : cudaLaunchKernelEx(&cfg, attention_kernel<false>, ap);
+  return f8 ? cudaLaunchKernelEx(&cfg, attention_kernel<true, CAP>, ap)
+            : cudaLaunchKernelEx(&cfg, attention_kernel<false, CAP>, ap);
 }
+template cudaError_t launch_attention_kernel<kSmallCap>(const AttnParams<kSmallCap>&, bool,
+                                                        cudaLaunchConfig_t);
+template cudaError_t launch_attention_kernel<kMaxLayersPerLaunch>(
+    const AttnParams<kMaxLayersPerLaunch>&, bool, cudaLaunchConfig_t);
 
 }  // namespace ea

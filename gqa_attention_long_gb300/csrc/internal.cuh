@@ -19,6 +19,9 @@ constexpr int kTok = 64;
 constexpr int kRows = 128;        // folded query rows per KV head: row r = (h % 2) * 64 + t
 constexpr int kKeyTile = 128;     // cache rows per key tile
 constexpr int kMaxLayersPerLaunch = 64;
+// Kernel parameter blocks come in two capacities: calls with few layers use the small one, so
+// that their launches carry ~2 KB of parameters instead of ~19 KB.
+constexpr int kSmallCap = 8;
 constexpr int kScaleBlock = 128;  // FP8 scale granularity (rows)
 
 // Bytes of one staged operand tile in the 128-byte-swizzled K-major layout: two 64-column
@@ -42,7 +45,6 @@ enum : uint32_t {
 
 // ------------------------------------------------------------------------- workspace layout
 //   [0, 1024)                    status word (first 4 bytes), rest reserved
-//   cnt     n_layers * 8 * 128 uint32  per-(unit, row) count of partial rows written
 //   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
 //   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
 //   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; f16 FP8)
@@ -50,14 +52,12 @@ enum : uint32_t {
 //   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
 struct WsLayout {
-  size_t cnt_off, qscale_off, svref_off, q_off, tail_off, part_o_off, part_lse_off, total;
+  size_t qscale_off, svref_off, q_off, tail_off, part_o_off, part_lse_off, total;
 };
 
 inline WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
   WsLayout w;
   size_t off = 1024;
-  w.cnt_off = off;
-  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kRows * sizeof(uint32_t);
   w.qscale_off = off;
   off += static_cast<size_t>(n_layers_per_launch) * kHkv * kRows * sizeof(float);
   w.svref_off = off;
@@ -88,29 +88,29 @@ struct PrologueLayer {
   __nv_bfloat16* q_rope;
 };
 
+template <int CAP>
 struct PrologueParams {
-  PrologueLayer layer[kMaxLayersPerLaunch];
+  PrologueLayer layer[CAP];
   float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
   float inv_lo[kD / 2];
   uint8_t* q_ws;
   uint8_t* tail_ws;
-  uint32_t* row_cnt;
   float* q_scale;  // FP8: [unit][128] scale of each e4m3 Q row
   float* sv_ref;   // FP8: [unit] reference V scale
   int n_layers, S, Smax, rope_delta, fp8;
 };
 
+template <int CAP>
 struct AttnParams {
-  CUtensorMap kmap[kMaxLayersPerLaunch];  // cache rows [0, S) of K: dims {128, S, 8}, box {64,128,1}
-  CUtensorMap vmap[kMaxLayersPerLaunch];
-  __nv_bfloat16* out[kMaxLayersPerLaunch];
-  const float* ks[kMaxLayersPerLaunch];      // FP8: block scales [8][Smax/128 + 1] (else null)
-  const float* vs[kMaxLayersPerLaunch];
+  CUtensorMap kmap[CAP];  // cache rows [0, S) of K: dims {128, S, 8}, box {64,128,1}
+  CUtensorMap vmap[CAP];
+  __nv_bfloat16* out[CAP];
+  const float* ks[CAP];      // FP8: block scales [8][Smax/128 + 1] (else null)
+  const float* vs[CAP];
   const uint8_t* q_ws;
   const uint8_t* tail_ws;
   float* part_o;
   float* part_lse;
-  uint32_t* row_cnt;   // [unit][128] count of partial rows written (zeroed by the prologue)
   const float* q_scale;  // FP8: [unit][128]
   const float* sv_ref;   // FP8: [unit]
   uint32_t* status;
@@ -120,6 +120,27 @@ struct AttnParams {
   int S, Smax;
   int ncol;            // FP8: scale columns per kv head, Smax/128 + 1 (the last one: own rows)
   float scale_log2;    // log2(e) / sqrt(128)
+};
+
+// Units split across CTAs, merged by the LSE merge kernel: at most one per CTA boundary.
+constexpr int kMaxSplitUnits = 256;
+
+// One split unit: its parts are CTAs c0 .. c0 + nparts - 1; the partial of CTA c sits in slot
+// 2 c + 0, except the first CTA's, which sits in slot 2 c0 + slot0 (1 when the unit is that
+// CTA's last segment, its range having started in an earlier unit).
+struct SplitUnit {
+  int u;
+  short c0, nparts;
+  int slot0;
+};
+
+template <int CAP>
+struct MergeParams {
+  __nv_bfloat16* out[CAP];
+  const float* part_o;
+  const float* part_lse;
+  int n_split;
+  SplitUnit unit[kMaxSplitUnits];  // the split units, in order
 };
 
 // The key tiles of all (layer, kv head) units, in unit-major order, are cut into n_ctas
@@ -134,13 +155,6 @@ __host__ __device__ inline int cta_of_tile(long long x, long long W, int n_ctas)
   while (c + 1 < n_ctas && cta_tile_start(c + 1, W, n_ctas) <= x) ++c;
   while (c > 0 && cta_tile_start(c, W, n_ctas) > x) --c;
   return c;
-}
-
-// Partial slot of CTA c for the unit whose first tile is `first`: a partial segment is either
-// the CTA's first segment (slot 0: the CTA's range starts inside or at the start of the unit)
-// or its last one (slot 1).
-__host__ __device__ inline size_t part_index(int c, long long first, long long W, int n_ctas) {
-  return static_cast<size_t>(c) * 2 + (cta_tile_start(c, W, n_ctas) >= first ? 0 : 1);
 }
 
 }  // namespace ea

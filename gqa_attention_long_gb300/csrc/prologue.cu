@@ -148,8 +148,8 @@ __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& 
 
 // TPO = tokens per octet: 1 for bf16 caches (two CTAs per unit), 2 for FP8 caches (one CTA per
 // unit: the own-row scale needs the amax over all 64 tokens of the head).
-template <int TPO>
-__global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__ PrologueParams p) {
+template <int TPO, int CAP>
+__global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__ PrologueParams<CAP> p) {
   // Launched programmatically after the previous kernel in the stream: wait for it (it may have
   // produced q/k/v, or still read the workspace), then let the attention kernel's CTAs start
   // their set-up; they wait for this grid before reading anything written here.
@@ -180,7 +180,6 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
     il[e] = p.inv_lo[dl + e];
   }
   const size_t unit = static_cast<size_t>(l) * kHkv + g;
-  if (part == 0 && threadIdx.x < kRows) p.row_cnt[unit * kRows + threadIdx.x] = 0u;
   uint8_t* qdst = p.q_ws + unit * kQTileBytes;
   uint8_t* tdst = p.tail_ws + unit * kTailUnitBytes;
 
@@ -318,12 +317,17 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
   }
 }
 
-// Host-side launcher (the kernel template is instantiated and launched in this file).
-cudaError_t launch_prologue_kernel(const PrologueParams& pp, bool fp8, cudaLaunchConfig_t cfg) {
+// Host-side launchers (the kernel template is instantiated and launched in this file).
+template <int CAP>
+cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, cudaLaunchConfig_t cfg) {
   cfg.gridDim = dim3(pp.n_layers * kHkv * (fp8 ? 1 : 2));  // FP8: one CTA per unit; bf16: two
   cfg.blockDim = dim3(256);
-  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_kernel_t<2>, pp)
-             : cudaLaunchKernelEx(&cfg, prologue_kernel_t<1>, pp);
+  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_kernel_t<2, CAP>, pp)
+             : cudaLaunchKernelEx(&cfg, prologue_kernel_t<1, CAP>, pp);
 }
+template cudaError_t launch_prologue_kernel<kSmallCap>(const PrologueParams<kSmallCap>&, bool,
+                                                       cudaLaunchConfig_t);
+template cudaError_t launch_prologue_kernel<kMaxLayersPerLaunch>(
+    const PrologueParams<kMaxLayersPerLaunch>&, bool, cudaLaunchConfig_t);
 
 }  // namespace ea

@@ -90,20 +90,22 @@ int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1-3 for one layer (the unit TTExpert.layer_fn can hand to a fused kernel): prologue,
- * then split-KV attention on the tensor cores with its log-sum-exp merge; writes a->out. */
+ * then split-KV attention on the tensor cores, then the log-sum-exp merge of the key ranges
+ * that were split across SMs; writes a->out. */
 int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
                       void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1-3 for n_layers independent layers in one call (the 64 layers of one Euler step,
  * alpamayo_tt/expert.py, TTExpert._forward_dev), all with the same S, Smax and rope_delta.
- * layers is a HOST array of n_layers entries. Launches two kernels per 64 layers. */
+ * layers is a HOST array of n_layers entries. Launches three kernels per 64 layers (the merge
+ * is skipped when no unit is split). */
 int expert_attn_layers(const ea_layer_args* layers, int n_layers, int S, int Smax, int rope_delta,
                        int kv_dtype, void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* As expert_attn_layers, and records four cudaEvent_t (passed as void*, each may be NULL) on
- * the stream: before the prologue, before the attention kernel, after it, and once more (the
- * merge runs inside the attention kernel, so the last two coincide). Recording events between
- * the kernels removes their launch overlap; use it to time the kernels. */
+ * the stream, around the first 64 layers: before the prologue, before the attention kernel,
+ * after it, and after the merge kernel. Recording events between the kernels removes their
+ * launch overlap; use it to time the kernels. */
 int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                 int rope_delta, int kv_dtype, void* workspace, size_t ws_bytes,
                                 ea_stream_t stream, void* const events[4]);
@@ -148,7 +150,7 @@ const char* expert_attn_status_string(int status);
  * in the array's status word and are not reported by this call. */
 #define EA_NOALLOC_MAX_LAYERS 4
 #define EA_NOALLOC_MAX_CTAS 64
-#define EA_NOALLOC_SCRATCH_BYTES 10586112u /* 1 KB + 4 layers x 520 KB + 1 KB + 64 CTAs x 129 KB */
+#define EA_NOALLOC_SCRATCH_BYTES 10569728u /* 1 KB + 4 layers x 516 KB + 1 KB + 64 CTAs x 129 KB */
 int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                int rope_delta, int kv_dtype, ea_stream_t stream);
 

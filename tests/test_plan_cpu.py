@@ -1,0 +1,41 @@
+"""Host-side launch planning (no GPU): the list of units that the attention kernel's partition
+cuts between CTAs, which the merge kernel combines, checked against a brute-force count of the
+CTAs whose tile range meets each unit."""
+import random
+
+import pytest
+
+from gqa_attention_long_gb300 import split_units
+
+
+def brute_force(n_layers, S, n_ctas):
+    T = (S + 127) // 128 + 1
+    W = n_layers * 8 * T
+    n = max(1, min(n_ctas, 257, W))
+    ranges = [(c * W // n, (c + 1) * W // n) for c in range(n)]
+    out = []
+    for u in range(n_layers * 8):
+        lo, hi = u * T, (u + 1) * T
+        parts = sum(1 for a, b in ranges if a < hi and b > lo and b > a)
+        if parts >= 2:
+            out.append(u)
+    return out
+
+
+@pytest.mark.parametrize("n_layers,S,n_ctas", [(1, 4700, 152), (64, 4700, 152), (64, 8128, 152),
+                                               (8, 1024, 152), (1, 0, 152), (2, 300, 5), (64, 4700, 1),
+                                               (64, 4700, 64), (3, 129, 37)])
+def test_split_units_match_brute_force(n_layers, S, n_ctas):
+    assert split_units(n_layers, S, n_ctas) == brute_force(n_layers, S, n_ctas)
+
+
+def test_split_units_random():
+    rng = random.Random(7)
+    for _ in range(200):
+        n_layers, S, n_ctas = rng.randint(1, 64), rng.randint(0, 8128), rng.randint(1, 300)
+        assert split_units(n_layers, S, n_ctas) == brute_force(n_layers, S, n_ctas)
+
+
+def test_single_layer_splits_every_unit():
+    # one layer over all 152 SMs: every (kv head) unit spans ~19 CTAs and needs the merge
+    assert split_units(1, 4700, 152) == list(range(8))
