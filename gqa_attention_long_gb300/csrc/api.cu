@@ -15,7 +15,9 @@
 
 namespace ea {
 template <int CAP>
-cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, cudaLaunchConfig_t cfg);
+cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, int sm_count,
+                                   cudaLaunchConfig_t cfg);
+cudaError_t prologue_set_attributes();
 cudaError_t attention_set_attributes();
 template <int CAP>
 cudaError_t launch_attention_kernel(const AttnParams<CAP>& ap, bool f8, cudaLaunchConfig_t cfg);
@@ -58,7 +60,7 @@ bool device_info(int* dev_out, DeviceInfo* info) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
         major == 10 && minor == 3 && sms > 0) {
       d.sm_count = sms;
-      d.ok = attention_set_attributes() == cudaSuccess;
+      d.ok = attention_set_attributes() == cudaSuccess && prologue_set_attributes() == cudaSuccess;
     }
     cudaGetLastError();
   }
@@ -207,7 +209,7 @@ cudaLaunchConfig_t launch_config(cudaStream_t st, cudaLaunchAttribute* attr, boo
 // while the preceding kernel drains, and wait (griddepcontrol.wait) for it before touching memory.
 template <int CAP>
 int launch_prologue_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
-                      uint8_t* ws, const WsLayout& wl, cudaStream_t st, bool pdl) {
+                      uint8_t* ws, const WsLayout& wl, int sm_count, cudaStream_t st, bool pdl) {
   PrologueParams<CAP> pp;
   std::memset(&pp, 0, sizeof(pp));
   for (int l = 0; l < n; ++l) {
@@ -228,13 +230,15 @@ int launch_prologue_t(const ea_layer_args* a, int n, int S, int Smax, int rope_d
   pp.tail_ws = ws + wl.tail_off;
   pp.q_scale = reinterpret_cast<float*>(ws + wl.qscale_off);
   pp.sv_ref = reinterpret_cast<float*>(ws + wl.svref_off);
+  pp.unit_sync = reinterpret_cast<uint32_t*>(ws + wl.sync_off);
+  pp.status = reinterpret_cast<uint32_t*>(ws);
   pp.n_layers = n;
   pp.S = S;
   pp.Smax = Smax;
   pp.rope_delta = rope_delta;
   pp.fp8 = fp8 ? 1 : 0;
   cudaLaunchAttribute attr[1];
-  if (launch_prologue_kernel<CAP>(pp, fp8, launch_config(st, attr, pdl)) != cudaSuccess) {
+  if (launch_prologue_kernel<CAP>(pp, fp8, sm_count, launch_config(st, attr, pdl)) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
@@ -242,10 +246,11 @@ int launch_prologue_t(const ea_layer_args* a, int n, int S, int Smax, int rope_d
 }
 
 int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_delta, bool fp8,
-                    uint8_t* ws, const WsLayout& wl, cudaStream_t st, bool pdl) {
-  return n <= kSmallCap ? launch_prologue_t<kSmallCap>(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl)
-                        : launch_prologue_t<kMaxLayersPerLaunch>(a, n, S, Smax, rope_delta, fp8, ws,
-                                                                 wl, st, pdl);
+                    uint8_t* ws, const WsLayout& wl, int sm_count, cudaStream_t st, bool pdl) {
+  return n <= kSmallCap
+             ? launch_prologue_t<kSmallCap>(a, n, S, Smax, rope_delta, fp8, ws, wl, sm_count, st, pdl)
+             : launch_prologue_t<kMaxLayersPerLaunch>(a, n, S, Smax, rope_delta, fp8, ws, wl, sm_count,
+                                                      st, pdl);
 }
 
 // Attention parameter blocks are large (~19 KB at full capacity): kept off the stack, one per
@@ -268,7 +273,7 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
                    cudaEvent_t const* ev) {
   const bool pdl = ev == nullptr;
   if (ev && ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return EA_ERR_CUDA;
-  int rc = launch_prologue_t<CAP>(a, n, S, Smax, rope_delta, fp8, ws, wl, st, pdl);
+  int rc = launch_prologue_t<CAP>(a, n, S, Smax, rope_delta, fp8, ws, wl, di.sm_count, st, pdl);
   if (rc != EA_OK) return rc;
   if (ev && ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return EA_ERR_CUDA;
 
@@ -297,22 +302,16 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
   ap.q_scale = reinterpret_cast<const float*>(ws + wl.qscale_off);
   ap.sv_ref = reinterpret_cast<const float*>(ws + wl.svref_off);
   ap.ncol = Smax / kScaleBlock + 1;
+  ap.unit_sync = reinterpret_cast<uint32_t*>(ws + wl.sync_off);
   ap.status = reinterpret_cast<uint32_t*>(ws);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
   const int n_ctas = n_ctas_for(ap.W, di.sm_count);
 
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(st, attr, pdl);
-  cfg.gridDim = dim3(n_ctas);
-  if (launch_attention_kernel<CAP>(ap, fp8, cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
-  if (ev && ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return EA_ERR_CUDA;
-
-  // Units cut by a CTA boundary (each listed once, in order) are merged by K3.
+  // Units cut by a CTA boundary (each listed once, in order). When every one of them has two
+  // parts, the attention kernel merges them itself; otherwise K3 does.
   MergeParams<CAP>& mp = lb.mp;
   mp.n_split = 0;
+  bool all_two = true;
   for (int b = 1; b < n_ctas; ++b) {
     const long long tb = cta_tile_start(b, ap.W, n_ctas);
     if (tb % ap.T == 0) continue;
@@ -324,8 +323,20 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
     su.c0 = static_cast<short>(cta_of_tile(first, ap.W, n_ctas));
     su.nparts = static_cast<short>(cta_of_tile(first + ap.T - 1, ap.W, n_ctas) - su.c0 + 1);
     su.slot0 = cta_tile_start(su.c0, ap.W, n_ctas) >= first ? 0 : 1;
+    all_two = all_two && su.nparts == 2;
   }
-  if (mp.n_split > 0) {
+  ap.fused_merge = all_two ? 1 : 0;
+
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(st, attr, pdl);
+  cfg.gridDim = dim3(n_ctas);
+  if (launch_attention_kernel<CAP>(ap, fp8, cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  if (ev && ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return EA_ERR_CUDA;
+
+  if (mp.n_split > 0 && !ap.fused_merge) {
     for (int l = 0; l < n; ++l) mp.out[l] = ap.out[l];
     mp.part_o = ap.part_o;
     mp.part_lse = ap.part_lse;
@@ -400,7 +411,8 @@ int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta
   const WsLayout wl = ws_layout(1, di.sm_count);
   if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
   return launch_prologue(a, 1, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3,
-                         static_cast<uint8_t*>(workspace), wl, static_cast<cudaStream_t>(stream), true);
+                         static_cast<uint8_t*>(workspace), wl, di.sm_count,
+                         static_cast<cudaStream_t>(stream), true);
 }
 
 int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
@@ -484,10 +496,7 @@ const char* expert_attn_status_string(int status) {
 namespace {
 
 constexpr size_t noalloc_bytes() {
-  return ((1024 + static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kRows * sizeof(float) + 1024 +
-           2 * static_cast<size_t>(EA_NOALLOC_MAX_LAYERS) * kHkv * kQTileBytes +
-           static_cast<size_t>(EA_NOALLOC_MAX_CTAS) * 2 * kRows * (kD + 1) * sizeof(float)) +
-          1023) & ~static_cast<size_t>(1023);
+  return ws_layout(EA_NOALLOC_MAX_LAYERS, EA_NOALLOC_MAX_CTAS).total;
 }
 static_assert(noalloc_bytes() == EA_NOALLOC_SCRATCH_BYTES, "scratch size in the header is stale");
 static_assert(kQTileBytes == kTailUnitBytes, "q and tail staging have the same size per unit");

@@ -60,9 +60,11 @@ struct Lay {
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing,
                        B_SFULL = 4 + 2 * kRing, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
                        B_X1 = B_ODONE + 2, B_X2 = B_X1 + 1, B_OFREE = B_X2 + 1,
-                       B_DRAIN = B_OFREE + 1, kNumBars = B_DRAIN + 1;
-  static constexpr uint32_t SM_XCH = SM_BAR + kNumBars * 8;  // float2 per folded row
-  static constexpr uint32_t SM_TMEM = SM_XCH + kRows * 8;
+                       B_STAGED = B_OFREE + 1, B_DRAIN = B_STAGED + 2, kNumBars = B_DRAIN + 1;
+  static constexpr uint32_t SM_XCH = SM_BAR + kNumBars * 8;  // three floats per folded row
+  static constexpr uint32_t SM_ROLE = SM_XCH + kRows * 12;    // in-kernel merge role
+  static constexpr uint32_t SM_SFLAG = SM_ROLE + 4;            // per Q buffer: output staged
+  static constexpr uint32_t SM_TMEM = SM_SFLAG + 8;
   static constexpr uint32_t SM_ABORT = SM_TMEM + 4;
   static constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;  // + slack to align the base
   static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
@@ -76,10 +78,11 @@ struct Lay {
   constexpr int B_QFULL = LY::B_QFULL, B_QEMPTY = LY::B_QEMPTY, B_KVFULL = LY::B_KVFULL,   \
                 B_KVEMPTY = LY::B_KVEMPTY, B_SFULL = LY::B_SFULL, B_PFULL = LY::B_PFULL,    \
                 B_ODONE = LY::B_ODONE, B_X1 = LY::B_X1, B_X2 = LY::B_X2,                   \
-                B_OFREE = LY::B_OFREE, B_DRAIN = LY::B_DRAIN;                              \
+                B_OFREE = LY::B_OFREE, B_STAGED = LY::B_STAGED, B_DRAIN = LY::B_DRAIN;      \
   (void)kRing; (void)kSlotBytes; (void)kAtom; (void)kQB; (void)SM_Q; (void)SM_RING;         \
   (void)B_QFULL; (void)B_QEMPTY; (void)B_KVFULL; (void)B_KVEMPTY; (void)B_SFULL;            \
-  (void)B_PFULL; (void)B_ODONE; (void)B_X1; (void)B_X2; (void)B_OFREE; (void)B_DRAIN
+  (void)B_PFULL; (void)B_ODONE; (void)B_X1; (void)B_X2; (void)B_OFREE; (void)B_STAGED;          \
+  (void)B_DRAIN
 
 constexpr uint32_t TM_S = 0;    // score buffers of streams 0 and 1 at columns 0 and 128; P(n)
                                 // overwrites the first columns of the buffer that held S(n)
@@ -173,21 +176,44 @@ template <bool F8, class PP>
 __device__ __noinline__ void q_loader(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
   const uint64_t pol_keep = l2_policy_evict_last();
+  volatile uint32_t* sflag = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_SFLAG);
   int seg = 0;
+  int hist_u[2] = {0, 0};  // units of the last two segments, by Q buffer
   bool ok = true;
   long long t = cx.start;
   Seg s;
+  // A segment that produced bf16 output rows staged them in its Q buffer (row-major, the 32 KB
+  // block of out that its unit owns): store them with one bulk copy, and let the buffer be
+  // refilled only once the copy has read it.
+  auto drain_staged = [&](int sg) -> bool {
+    const int b = sg & 1;
+    if (!bounded_wait(cx.bar(B_STAGED + b), (sg >> 1) & 1, cx.abort_flag, cx.status, kErrProducerWait))
+      return false;
+    if (sflag[b] != 0u) {
+      const int u = hist_u[b];
+      bulk_store(p.out[u / kHkv] + static_cast<size_t>(u % kHkv) * kRows * kD,
+                 cx.sbase + SM_Q + b * kQB, kRows * kD * 2);
+      bulk_commit();
+    }
+    bulk_wait_read0();
+    return true;
+  };
   while (ok && next_seg(t, cx.end, p.T, s)) {
     const int qb = seg & 1;
-    if (seg >= 2)  // the last QK^T of segment seg-2 has consumed buffer qb
+    if (seg >= 2) {  // segment seg-2 has finished with buffer qb (its last QK and its output)
       ok = bounded_wait(cx.bar(B_QEMPTY + qb), ((seg >> 1) - 1) & 1, cx.abort_flag, cx.status,
                         kErrProducerWait);
+      if (ok) ok = drain_staged(seg - 2);
+    }
     if (!ok) break;
+    hist_u[qb] = s.u;
     mbar_expect_tx(cx.bar(B_QFULL + qb), kQB);
     bulk_load(cx.sbase + SM_Q + qb * kQB, p.q_ws + static_cast<size_t>(s.u) * kQTileBytes, kQB,
               cx.bar(B_QFULL + qb), pol_keep);
     ++seg;
   }
+  for (int sg = seg >= 2 ? seg - 2 : 0; ok && sg < seg; ++sg) ok = drain_staged(sg);
+  bulk_wait_all0();
   if (!ok) {  // let the last load into each buffer land
     for (int b = 0; b < 2; ++b) {
       int last = seg - 1;
@@ -262,6 +288,13 @@ __device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
       }
       if (i > 0) {
         const int ii = i - 1, j = s.j0 + ii;
+        // the first PV of a segment overwrites both accumulators' previous contents: wait until
+        // the softmax warpgroups have read the previous segment's (OFREE completes once per
+        // segment)
+        if (ii == 0 && seg > 0) {
+          ok = bounded_wait(cx.bar(B_OFREE), (seg - 1) & 1, cx.abort_flag, cx.status, kErrMmaWait);
+          if (!ok) break;
+        }
         // P of even and odd tiles (streams 0 and 1) arrive on separate barriers, each from its
         // own softmax warpgroup
         ok = bounded_wait(cx.bar(B_PFULL + (n_pv & 1)), (n_pv >> 1) & 1, cx.abort_flag, cx.status,
@@ -337,7 +370,9 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
   const uint32_t s_col = TM_S + k * 128, o_col = TM_O + k * 128;
   const uint32_t pa_base = cx.tmem + lane_addr + s_col;  // P(n) of this stream
   const float c = p.scale_log2;
-  float2* xch = reinterpret_cast<float2*>(cx.smem + LY::SM_XCH);
+  float* xw = reinterpret_cast<float*>(cx.smem + LY::SM_XCH) + 3 * r;  // this row's exchange slot
+  volatile uint32_t* role = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_ROLE);
+  volatile uint32_t* sflag = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_SFLAG);
   uint32_t base = 0, seg = 0;  // tiles of this CTA before the current segment; segment count
   bool ok = true, first_seg = true;
   long long t = cx.start;
@@ -360,10 +395,23 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
       svr = p.sv_ref[s.u];
     }
     int last_n = -1;  // last tile of this stream in the segment (-1: none yet)
+    // In-kernel merge of a two-part unit (see the epilogue): the leader counts this part's
+    // arrival now and polls the other part's ready flag once per tile, each load consumed one
+    // tile later, so that neither round trip lands on the epilogue.
+    const bool full = (s.j0 == 0 && s.j1 == p.T);
+    const bool fused = !full && p.fused_merge != 0;
+    const bool leader = threadIdx.x == 0;
+    uint32_t* usync = p.unit_sync + 2 * static_cast<size_t>(s.u);  // [arrivals, ready]
+    uint32_t arr_old = 0u, flag_pend = 0u, flag_seen = 0u;
+    if (fused && leader) arr_old = atomicAdd(usync, 1u);
     // segment tile i is CTA tile base + i and belongs to stream (base + i) & 1
     for (int i = (k - static_cast<int>(base)) & 1; i < nt; i += 2) {
       const int n = static_cast<int>(base) + i;
       const int j = s.j0 + i;
+      if (fused && leader) {
+        flag_seen |= flag_pend;
+        flag_pend = ld_relaxed_gpu(usync + 1);
+      }
       ok = wait_bar(B_SFULL + k, (n >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
@@ -482,48 +530,110 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
     // weights w_k = 2^(m_k - M) * svr / L and hands them back; each warpgroup then writes the
     // combined rows' output columns [64 k, 64 k + 64). A stream without tiles in the segment
     // has m = -inf and weight 0 and its accumulator is not read.
+    //
+    // A partial segment of a two-part unit (fused_merge) is merged here: the part whose CTA
+    // arrives second (a per-unit atomic count) waits for the first part's ready flag, then
+    // weights its own rows by 2^(lse - M2) and the first part's normalised partial by
+    // 2^(lse_1 - M2) (M2 the larger lse, both over their sum) and writes the bf16 output. The
+    // first part writes its partial and raises the flag; it never waits for the other.
     if (last_n >= 0) {
       ok = wait_bar(B_ODONE + k, (last_n >> 1) & 1);
       if (!ok) break;
     }
     const uint32_t sp = seg & 1;
     const bool has0 = nt >= 2 || (base & 1) == 0, has1 = nt >= 2 || (base & 1) == 1;
-    float w0, w1, lse_row = 0.f;
+    const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
+    first_seg = false;
+    // the other part of a two-part unit: its CTA and partial slot
+    const long long ufirst = static_cast<long long>(s.u) * p.T;
+    int other = 0, other_slot = 0;
+    if (fused) {
+      const int c0 = cta_of_tile(ufirst, p.W, gridDim.x);
+      other = static_cast<int>(blockIdx.x) == c0 ? c0 + 1 : c0;
+      other_slot = cta_tile_start(other, p.W, gridDim.x) >= ufirst ? 0 : 1;
+    }
+    float w0, w1, w2 = 0.f, lse_row = 0.f;
+    bool second = false;
     if (k == 1) {
-      xch[r] = make_float2(m_ref, lsum);
+      xw[0] = m_ref;
+      xw[1] = lsum;
       mbar_arrive(cx.bar(B_X1));
       ok = wait_bar(B_X2, sp);
       if (!ok) break;
-      const float2 w = xch[r];
-      w0 = w.x;
-      w1 = w.y;
+      w0 = xw[0];
+      w1 = xw[1];
+      w2 = xw[2];
+      // only a second part gives the other part's partial a weight (2^(lse_1 - M2) / sum > 0);
+      // the role word itself may already belong to the next segment
+      second = w2 != 0.f;
     } else {
+      if (leader) {  // the leader also arrives on X1 (its count is 128 + 1), with the role
+        uint32_t rl = 0u;
+        if (fused && arr_old == 1u) {  // second part: wait until the first part's partial is out
+          if ((flag_seen | flag_pend) != 0u) {
+            fence_acq_rel_gpu();  // with the relaxed read that saw the flag: an acquire
+            rl = 1u;
+          } else {
+            rl = bounded_flag_wait(usync + 1, cx.abort_flag, cx.status, kErrMergeWait) ? 1u : 2u;
+          }
+        }
+        *role = rl;
+        mbar_arrive(cx.bar(B_X1));
+      }
       ok = wait_bar(B_X1, sp);
       if (!ok) break;
-      const float2 o = xch[r];  // stream 1's (max, sum)
-      const float M = fmaxf(m_ref, o.x);
+      const uint32_t rl = *role;
+      if (rl == 2u) {
+        ok = false;
+        break;
+      }
+      second = rl == 1u;
+      const float mo = xw[0], lo = xw[1];  // stream 1's (max, sum)
+      const float M = fmaxf(m_ref, mo);
       const float a0 = has0 ? ex2_approx(m_ref - M) : 0.f;
-      const float a1 = has1 ? ex2_approx(o.x - M) : 0.f;
-      const float L = lsum * a0 + o.y * a1;
+      const float a1 = has1 ? ex2_approx(mo - M) : 0.f;
+      const float L = lsum * a0 + lo * a1;
       const float inv = svr / L;  // FP8: P was stored relative to the reference V scale
       w0 = a0 * inv;
       w1 = a1 * inv;
       lse_row = M + log2f(L);
-      xch[r] = make_float2(w0, w1);
+      if (second) {
+        const float lse_o =
+            __ldcg(p.part_lse + (static_cast<size_t>(other) * 2 + other_slot) * kRows + r);
+        const float M2 = fmaxf(lse_row, lse_o);
+        const float ea = ex2_approx(lse_row - M2), eb = ex2_approx(lse_o - M2);
+        const float rs = 1.0f / (ea + eb);
+        w0 *= ea * rs;
+        w1 *= ea * rs;
+        w2 = eb * rs;
+      }
+      xw[0] = w0;
+      xw[1] = w1;
+      xw[2] = w2;
       mbar_arrive(cx.bar(B_X2));
     }
     tc_fence_after();
-    const bool full = (s.j0 == 0 && s.j1 == p.T);
-    const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
-    first_seg = false;
-    float* po = p.part_o + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r) * kD + 64 * k;
-    __nv_bfloat16* orow = p.out[l] + (static_cast<size_t>(g) * kRows + r) * kD + 64 * k;
+    // ---- this warpgroup's 64 columns of both accumulators, combined (a second part starts from
+    // the first part's weighted partial)
+    const float* pother =
+        p.part_o + ((static_cast<size_t>(other) * 2 + other_slot) * kRows + r) * kD + 64 * k;
+    float o[2][32];
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       const uint32_t col = cx.tmem + lane_addr + TM_O + 64 * k + 32 * ch;
-      float o[32];
+      if (second) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(pother + ch * 32) + q);
+          o[ch][4 * q] = v.x * w2;
+          o[ch][4 * q + 1] = v.y * w2;
+          o[ch][4 * q + 2] = v.z * w2;
+          o[ch][4 * q + 3] = v.w * w2;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[ch][e] = 0.f;
+      }
 #pragma unroll
       for (int st = 0; st < 2; ++st) {  // the two streams' accumulators, one after the other
         if (st == 0 ? !has0 : !has1) continue;
@@ -533,31 +643,68 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
         reg_fence32(x);
         const float w = st == 0 ? w0 : w1;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = fmaf(__uint_as_float(x[e]), w, o[e]);
+        for (int e = 0; e < 32; ++e) o[ch][e] = fmaf(__uint_as_float(x[e]), w, o[ch][e]);
       }
-      if (full) {
+    }
+    // The accumulators are read: release them to the next segment's PVs (the MMA issuer waits
+    // for all 256 arrivals before the first one).
+    tc_fence_before();
+    mbar_arrive(cx.bar(B_OFREE));
+    const bool staged = full || second;
+    if (staged) {
+      // bf16 rows into this segment's Q buffer (its last QK is done), row-major like the unit's
+      // block of out: row r, columns [64 k, 64 k + 64) at byte r * 256 + 128 k. Store q of a
+      // thread writes chunk q ^ (r % 8) (columns 8 c .. 8 c + 7, c = q ^ (r % 8)), so that the
+      // eight rows of a warp quarter hit eight different bank groups; the chunks are permuted
+      // into that order in registers by three conditional swap stages. The Q loader stores the
+      // block with one bulk copy.
+      uint32_t w[8][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16x2(o[8 * q + 0], o[8 * q + 1]);
-          w.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
-          w.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
-          w.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
-          *reinterpret_cast<uint4*>(orow + ch * 32 + 8 * q) = w;
+      for (int c = 0; c < 8; ++c)
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          w[c][h] = pack_bf16x2(o[c >> 2][8 * (c & 3) + 2 * h], o[c >> 2][8 * (c & 3) + 2 * h + 1]);
+      const int m = r & 7;
+#pragma unroll
+      for (int bit = 1; bit < 8; bit <<= 1) {
+        const bool sw = (m & bit) != 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (c & bit) continue;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const uint32_t a0 = w[c][h], a1 = w[c | bit][h];
+            w[c][h] = sw ? a1 : a0;
+            w[c | bit][h] = sw ? a0 : a1;
+          }
         }
-      } else {
+      }
+      const uint32_t srow = cx.sbase + SM_Q + (seg & 1) * kQB + r * (kD * 2) + k * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(srow + 16 * (q ^ m), w[q][0], w[q][1], w[q][2], w[q][3]);
+      fence_proxy_async_smem();  // visible to the bulk copy (async proxy)
+    } else {
+      float* po = p.part_o + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r) * kD + 64 * k;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<float4*>(po + ch * 32 + 4 * q) =
-              make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      }
+              make_float4(o[ch][4 * q], o[ch][4 * q + 1], o[ch][4 * q + 2], o[ch][4 * q + 3]);
+      if (k == 0) p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = lse_row;
+      if (fused) __threadfence();  // the partial is visible before the flag
     }
-    if (!full && k == 0) p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = lse_row;
-    // Both halves of every row are written and both accumulators read: release them to the
-    // next segment's PVs (their P arrives only after this barrier).
-    tc_fence_before();
-    mbar_arrive(cx.bar(B_OFREE));
-    ok = wait_bar(B_OFREE, sp);
+    if (leader) sflag[seg & 1] = staged ? 1u : 0u;
+    mbar_arrive(cx.bar(B_STAGED + (seg & 1)));
+    // The leader of a first part waits until every half row of the partial is out, then raises
+    // the unit's ready flag.
+    if (!staged && fused && leader) {
+      ok = bounded_wait(cx.bar(B_STAGED + (seg & 1)), (seg >> 1) & 1, cx.abort_flag, cx.status,
+                        kErrSoftmaxWait);
+      if (ok) st_release_gpu(usync + 1, 1u);
+    }
+    ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     base += nt;
     ++seg;
@@ -593,9 +740,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       mbar_init(cx.bar(B_PFULL + b), 128);
       mbar_init(cx.bar(B_ODONE + b), 1);
     }
-    mbar_init(cx.bar(B_X1), 128);
+    mbar_init(cx.bar(B_X1), 128 + 1);  // stream 1's threads and stream 0's leader
     mbar_init(cx.bar(B_X2), 128);
     mbar_init(cx.bar(B_OFREE), kSoftmaxThreads);
+    mbar_init(cx.bar(B_STAGED), kSoftmaxThreads);
+    mbar_init(cx.bar(B_STAGED + 1), kSoftmaxThreads);
     for (int b = 0; b < kRing; ++b) {
       mbar_init(cx.bar(B_KVFULL + b), 1);
       mbar_init(cx.bar(B_KVEMPTY + b), 1);

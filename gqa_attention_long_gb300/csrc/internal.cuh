@@ -41,10 +41,14 @@ enum : uint32_t {
   kErrMmaWait = 1u << 1,
   kErrSoftmaxWait = 1u << 2,
   kErrDrain = 1u << 3,
+  kErrPrologueWait = 1u << 4,
+  kErrMergeWait = 1u << 5,
 };
 
 // ------------------------------------------------------------------------- workspace layout
 //   [0, 1024)                    status word (first 4 bytes), rest reserved
+//   sync    n_layers * 8 * 2 uint32  per unit: arrival count and partial-ready flag of the
+//                                   in-kernel merge of two-part units (zeroed by the prologue)
 //   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
 //   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
 //   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; f16 FP8)
@@ -52,12 +56,15 @@ enum : uint32_t {
 //   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
 struct WsLayout {
-  size_t qscale_off, svref_off, q_off, tail_off, part_o_off, part_lse_off, total;
+  size_t sync_off, qscale_off, svref_off, q_off, tail_off, part_o_off, part_lse_off, total;
 };
 
-inline WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
-  WsLayout w;
+constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
+  WsLayout w{};
   size_t off = 1024;
+  w.sync_off = off;
+  off += ((static_cast<size_t>(n_layers_per_launch) * kHkv * 2 * sizeof(uint32_t)) + 1023) &
+         ~static_cast<size_t>(1023);
   w.qscale_off = off;
   off += static_cast<size_t>(n_layers_per_launch) * kHkv * kRows * sizeof(float);
   w.svref_off = off;
@@ -97,6 +104,8 @@ struct PrologueParams {
   uint8_t* tail_ws;
   float* q_scale;  // FP8: [unit][128] scale of each e4m3 Q row
   float* sv_ref;   // FP8: [unit] reference V scale
+  uint32_t* unit_sync;  // [unit][2]: zeroed here for the attention kernel's in-kernel merge
+  uint32_t* status;  // workspace status word (bounded-wait failures)
   int n_layers, S, Smax, rope_delta, fp8;
 };
 
@@ -113,12 +122,14 @@ struct AttnParams {
   float* part_lse;
   const float* q_scale;  // FP8: [unit][128]
   const float* sv_ref;   // FP8: [unit]
+  uint32_t* unit_sync;   // [unit][2]: arrival count, partial-ready flag (in-kernel merge)
   uint32_t* status;
   long long W;         // total key tiles = n_layers * 8 * T
   int T;               // key tiles per (layer, kv head): n_main cache tiles + 1 own-row tile
   int n_main;          // ceil(S / 128)
   int S, Smax;
   int ncol;            // FP8: scale columns per kv head, Smax/128 + 1 (the last one: own rows)
+  int fused_merge;     // every split unit has two parts: the second one merges in-kernel
   float scale_log2;    // log2(e) / sqrt(128)
 };
 

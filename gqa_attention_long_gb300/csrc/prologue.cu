@@ -6,11 +6,15 @@
 // rotary_embedding_hf, typecast to the cache dtype, fill_cache at row Smax-64) and
 // TTExpert.set_context (positions i + rope_delta + S); alpamayo_tt/EXPERT_NOTES.md, "Layouts".
 //
-// A CTA handles q heads 2g and 2g+1, k head g and v head g of one layer, for 32 tokens (bf16
-// cache) or all 64 (FP8 cache). An octet (8 lanes) owns one token at a time; lane i holds
-// channels [8i, 8i+8) and their RoPE partners [64+8i, 64+8i+8), so the rotation is in-thread and
-// the norm needs three shuffles. Every global access is a 16-byte vector access. It also zeroes
-// the unit's per-row arrival counters used by the attention kernel's merge.
+// An octet (8 lanes) owns one token at a time; lane i holds channels [8i, 8i+8) and their RoPE
+// partners [64+8i, 64+8i+8), so the rotation is in-thread and the norm needs three shuffles.
+// Every global access is a 16-byte vector access.
+//   bf16 cache: persistent CTAs (one per SM) of 256 threads walk a range of (layer, g) units (q
+//     heads 2g, 2g+1, k head g, v head g; all 64 tokens, two per octet), computing the tokens'
+//     cos/sin once (positions are the same in every layer and head); the raw rows arrive by
+//     bulk copy into a shared-memory ring several units ahead.
+//   FP8 cache: a CTA of 256 threads owns one (layer, g) unit and all 64 tokens (two per octet):
+//     the own rows' scale needs the amax over all of them.
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
@@ -146,6 +150,141 @@ __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& 
 
 }  // namespace
 
+// bf16 kernel: persistent CTAs of 256 threads walk a contiguous range of (layer, g) units. The
+// raw rows of a unit (q heads 2g and 2g+1: 32 KB, k head g: 16 KB, v head g: 16 KB, each one
+// contiguous block) arrive by bulk copy in a three-slot shared-memory ring, so that up to
+// 192 KB of loads per SM are in flight while the threads work on an earlier unit.
+constexpr int kPRing = 3;
+constexpr uint32_t kPUnitBytes = 65536;
+constexpr uint32_t kPBarOff = kPRing * kPUnitBytes;
+constexpr uint32_t kPSmemBytes = kPBarOff + 8 * kPRing + 16;
+
+// Grid: min(number of SMs, units); block 256 = 32 octets, each owning tokens oc and oc + 32.
+template <int CAP>
+__global__ void __launch_bounds__(256, 1) prologue_bf16_kernel(const __grid_constant__ PrologueParams<CAP> p) {
+  extern __shared__ __align__(128) uint8_t psm[];
+  const uint32_t sbase = smem_u32(psm);
+  const uint32_t bar0 = sbase + kPBarOff;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(psm + kPBarOff + 8 * kPRing);
+  const int n_units = p.n_layers * kHkv;
+  const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * n_units / gridDim.x);
+  const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_units / gridDim.x);
+  const int oc = threadIdx.x >> 3;  // octet: tokens oc and oc + 32
+  const int i = threadIdx.x & 7;    // channels [8i, 8i+8) and [64+8i, 64+8i+8)
+  const int dl = 8 * i, dh = 64 + 8 * i;
+  const int Smax = p.Smax;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPRing; ++s) mbar_init(bar0 + 8 * s, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Launched programmatically after the previous kernel in the stream: wait for it (it may have
+  // produced q/k/v, or still read the workspace), then let the attention kernel's CTAs start
+  // their set-up; they wait for this grid before reading anything written here.
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  for (int x = threadIdx.x; x < 2 * (u1 - u0); x += 256) p.unit_sync[2 * u0 + x] = 0u;
+
+  const uint64_t pol = l2_policy_evict_first();  // raw rows are read once
+  auto issue = [&](int k) {  // one thread: bulk loads of unit u0 + k into slot k % kPRing
+    const int u = u0 + k, g = u % kHkv;
+    const PrologueLayer& L = p.layer[u / kHkv];
+    const uint32_t dst = sbase + (k % kPRing) * kPUnitBytes, bar = bar0 + 8 * (k % kPRing);
+    mbar_expect_tx(bar, kPUnitBytes);
+    bulk_load(dst, L.q_raw + static_cast<size_t>(2 * g) * kTok * kD, 32768, bar, pol);
+    bulk_load(dst + 32768, L.k_raw + static_cast<size_t>(g) * kTok * kD, 16384, bar, pol);
+    bulk_load(dst + 49152, L.v_raw + static_cast<size_t>(g) * kTok * kD, 16384, bar, pol);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (; issued < kPRing && u0 + issued < u1; ++issued) issue(issued);
+
+  // cos/sin of this thread's two tokens at its eight frequencies (the same in every unit)
+  float cs[2][8], sn[2][8];
+#pragma unroll
+  for (int tt = 0; tt < 2; ++tt) {
+    const int pos = oc + 32 * tt + p.rope_delta + p.S;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_cos_sin(pos, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[tt][e], sn[tt][e]);
+  }
+
+  float gql[8], gqh[8], gkl[8], gkh[8];
+  int cur_l = -1;
+  bool ok = true;
+  int k = 0;
+  for (; u0 + k < u1; ++k) {
+    const int u = u0 + k, l = u / kHkv, g = u % kHkv;
+    ok = __syncthreads_and(bounded_wait(bar0 + 8 * (k % kPRing), (k / kPRing) & 1, abort_flag, p.status,
+                                        kErrPrologueWait)) != 0;
+    if (!ok) break;
+    const PrologueLayer& L = p.layer[l];
+    if (l != cur_l) {
+      load_bf16x8(L.q_gamma + dl, gql);
+      load_bf16x8(L.q_gamma + dh, gqh);
+      load_bf16x8(L.k_gamma + dl, gkl);
+      load_bf16x8(L.k_gamma + dh, gkh);
+      cur_l = l;
+    }
+    const uint8_t* src = psm + (k % kPRing) * kPUnitBytes;
+    uint8_t* qdst = p.q_ws + static_cast<size_t>(u) * kQTileBytes;
+    uint8_t* tdst = p.tail_ws + static_cast<size_t>(u) * kTailUnitBytes;
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      const int t = oc + 32 * tt;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint8_t* row = src + (hh * kTok + t) * (kD * 2);
+        float xl[8], xh[8], yl[8], yh[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dl * 2), xl);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dh * 2), xh);
+        norm_rope(xl, xh, gql, gqh, cs[tt], sn[tt], yl, yh);
+        const int r = hh * kTok + t;
+        const uint4 ql = pack8(yl, false), qh = pack8(yh, false);
+        *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = ql;
+        *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = qh;
+        if (L.q_rope != nullptr) {
+          __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
+          *reinterpret_cast<uint4*>(qr + dl) = ql;
+          *reinterpret_cast<uint4*>(qr + dh) = qh;
+        }
+      }
+      const uint8_t* krow = src + 32768 + t * (kD * 2);
+      const uint8_t* vrow = src + 49152 + t * (kD * 2);
+      float xl[8], xh[8], kl[8], kh[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl * 2), xl);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh * 2), xh);
+      norm_rope(xl, xh, gkl, gkh, cs[tt], sn[tt], kl, kh);
+      const uint4 kpl = pack8(kl, false), kph = pack8(kh, false);
+      const uint4 vpl = *reinterpret_cast<const uint4*>(vrow + dl * 2);
+      const uint4 vph = *reinterpret_cast<const uint4*>(vrow + dh * 2);
+      const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
+      __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(L.k_cache) + crow * kD;
+      __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(L.v_cache) + crow * kD;
+      *reinterpret_cast<uint4*>(kc + dl) = kpl;
+      *reinterpret_cast<uint4*>(kc + dh) = kph;
+      *reinterpret_cast<uint4*>(vc + dl) = vpl;
+      *reinterpret_cast<uint4*>(vc + dh) = vph;
+      const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
+      *reinterpret_cast<uint4*>(tdst + sol) = kpl;
+      *reinterpret_cast<uint4*>(tdst + soh) = kph;
+      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = vpl;
+      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = vph;
+    }
+    __syncthreads();  // every thread is done with the slot
+    if (threadIdx.x == 0 && u0 + issued < u1) {
+      fence_proxy_async_smem();  // generic-proxy reads of the slot before the async-proxy refill
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (!ok && threadIdx.x == 0) {
+    // let the copies already issued land before the CTA gives its shared memory back
+    for (int kk = k; kk < issued; ++kk)
+      if (!drain_wait(bar0 + 8 * (kk % kPRing), (kk / kPRing) & 1)) atomicOr(p.status, kErrDrain);
+  }
+}
+
 // TPO = tokens per octet: 1 for bf16 caches (two CTAs per unit), 2 for FP8 caches (one CTA per
 // unit: the own-row scale needs the amax over all 64 tokens of the head).
 template <int TPO, int CAP>
@@ -156,6 +295,8 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
   pdl_wait_primary();
   pdl_launch_dependents();
   __shared__ float red[8];
+  if (threadIdx.x < 2 && blockIdx.x % (2 / TPO) == 0)
+    p.unit_sync[2 * (blockIdx.x / (2 / TPO)) + threadIdx.x] = 0u;
 
   constexpr int kCtasPerUnit = 2 / TPO;
   const int unit_id = blockIdx.x / kCtasPerUnit;
@@ -319,15 +460,31 @@ __global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__
 
 // Host-side launchers (the kernel template is instantiated and launched in this file).
 template <int CAP>
-cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, cudaLaunchConfig_t cfg) {
-  cfg.gridDim = dim3(pp.n_layers * kHkv * (fp8 ? 1 : 2));  // FP8: one CTA per unit; bf16: two
+cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, int sm_count,
+                                   cudaLaunchConfig_t cfg) {
+  if (fp8) {
+    cfg.gridDim = dim3(pp.n_layers * kHkv);  // one CTA per unit
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, prologue_kernel_t<2, CAP>, pp);
+  }
+  const int n_units = pp.n_layers * kHkv;
+  cfg.gridDim = dim3(n_units < sm_count ? n_units : sm_count);
   cfg.blockDim = dim3(256);
-  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_kernel_t<2, CAP>, pp)
-             : cudaLaunchKernelEx(&cfg, prologue_kernel_t<1, CAP>, pp);
+  cfg.dynamicSmemBytes = kPSmemBytes;
+  return cudaLaunchKernelEx(&cfg, prologue_bf16_kernel<CAP>, pp);
 }
-template cudaError_t launch_prologue_kernel<kSmallCap>(const PrologueParams<kSmallCap>&, bool,
+
+cudaError_t prologue_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(prologue_bf16_kernel<kSmallCap>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prologue_bf16_kernel<kMaxLayersPerLaunch>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+}
+
+template cudaError_t launch_prologue_kernel<kSmallCap>(const PrologueParams<kSmallCap>&, bool, int,
                                                        cudaLaunchConfig_t);
 template cudaError_t launch_prologue_kernel<kMaxLayersPerLaunch>(
-    const PrologueParams<kMaxLayersPerLaunch>&, bool, cudaLaunchConfig_t);
+    const PrologueParams<kMaxLayersPerLaunch>&, bool, int, cudaLaunchConfig_t);
 
 }  // namespace ea

@@ -73,6 +73,38 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// Waits until a global flag (written by another CTA with release semantics) is non-zero, with
+// the same limits and failure handling as bounded_wait.
+__device__ __forceinline__ bool bounded_flag_wait(const uint32_t* flag, volatile uint32_t* abort_flag,
+                                                  uint32_t* status, uint32_t err_bit) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < 0x80000000u; ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0u) return true;
+    if ((it & 15u) == 15u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+    __nanosleep(100);
+  }
+  *abort_flag = 1u;
+  atomicOr(status, err_bit);
+  return false;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Time-bounded wait that ignores the abort flag: used while tearing down after an abort, to
 // let copies and MMAs that are still in flight land before shared memory and TMEM are freed.
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -116,6 +148,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+// Contiguous bulk copy shared -> global (16-byte aligned addresses, size a multiple of 16), in
+// the issuing thread's bulk group; bulk_wait_read0 returns once every committed store has read
+// its shared-memory source, bulk_wait_all0 once the stores are complete.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
