@@ -44,17 +44,20 @@ constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 
 // Shared-memory layout of one CTA. bf16 cache: a K or V tile is 128 rows x 256 bytes, stored as
-// two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom.
+// two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom;
+// each stream also has a 32 KB buffer where its softmax warpgroup widens the V tile to f16 (the
+// bf16 tile layout), the B operand of the f16 PV MMA.
 template <bool F8>
 struct Lay {
   static constexpr uint32_t kQ = kQTileBytes;  // one roped Q tile (e4m3: high then low codes)
   static constexpr uint32_t kSlot = F8 ? 16384u : 32768u;           // one K or V tile
-  static constexpr uint32_t kAtom = 16384u;                         // bf16: second channel half
+  static constexpr uint32_t kAtom = 16384u;                         // 16-bit tiles: second channel half
   static constexpr uint32_t kTail = F8 ? kTailHalfBytesF8 : kTailHalfBytes;  // 64 own rows
-  static constexpr int kRing = F8 ? 10 : 5;
+  static constexpr int kRing = F8 ? 6 : 5;  // e4m3: even, so ring slot parity = K (even) / V (odd)
   static constexpr uint32_t SM_Q = 0;  // two Q buffers
   static constexpr uint32_t SM_RING = SM_Q + 2 * kQ;
-  static constexpr uint32_t SM_BAR = SM_RING + kRing * kSlot;
+  static constexpr uint32_t SM_V16 = SM_RING + kRing * kSlot;  // e4m3: two widened V tiles
+  static constexpr uint32_t SM_BAR = SM_V16 + (F8 ? 2u * 32768u : 0u);
   // per-stream barriers (SFULL, PFULL, ODONE) are indexed by the stream; X1, X2 and OFREE
   // complete once per segment (row-statistics exchange and release of the accumulators)
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing,
@@ -74,12 +77,12 @@ struct Lay {
   using LY = Lay<F8>;                                                                      \
   constexpr int kRing = LY::kRing;                                                         \
   constexpr uint32_t kSlotBytes = LY::kSlot, kAtom = LY::kAtom, kQB = LY::kQ;              \
-  constexpr uint32_t SM_Q = LY::SM_Q, SM_RING = LY::SM_RING;                               \
+  constexpr uint32_t SM_Q = LY::SM_Q, SM_RING = LY::SM_RING, SM_V16 = LY::SM_V16;          \
   constexpr int B_QFULL = LY::B_QFULL, B_QEMPTY = LY::B_QEMPTY, B_KVFULL = LY::B_KVFULL,   \
                 B_KVEMPTY = LY::B_KVEMPTY, B_SFULL = LY::B_SFULL, B_PFULL = LY::B_PFULL,    \
                 B_ODONE = LY::B_ODONE, B_X1 = LY::B_X1, B_X2 = LY::B_X2,                   \
                 B_OFREE = LY::B_OFREE, B_STAGED = LY::B_STAGED, B_DRAIN = LY::B_DRAIN;      \
-  (void)kRing; (void)kSlotBytes; (void)kAtom; (void)kQB; (void)SM_Q; (void)SM_RING;         \
+  (void)kRing; (void)kSlotBytes; (void)kAtom; (void)kQB; (void)SM_Q; (void)SM_RING; (void)SM_V16; \
   (void)B_QFULL; (void)B_QEMPTY; (void)B_KVFULL; (void)B_KVEMPTY; (void)B_SFULL;            \
   (void)B_PFULL; (void)B_ODONE; (void)B_X1; (void)B_X2; (void)B_OFREE; (void)B_STAGED;          \
   (void)B_DRAIN
@@ -236,6 +239,7 @@ __device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
   // bf16: format code 1 (kind::f16); e4m3: format code 0 (kind::f8f6f4). V is MN-major.
   constexpr uint32_t kIdescQK128 = umma_idesc_f16(128, 128, !F8, false, false);
   constexpr uint32_t kIdescQK64 = umma_idesc_f16(128, 64, !F8, false, false);
+  // PV: bf16 P and V, or (e4m3 cache) f16 P and the f16-widened V; V is MN-major
   constexpr uint32_t kIdescPV = umma_idesc_f16(128, 128, !F8, false, true);
   uint32_t ring = 0, n_qk = 0, n_pv = 0;
   int seg = 0;
@@ -301,35 +305,28 @@ __device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
                           kErrMmaWait);
         if (!ok) break;
         const uint32_t pos = ring + 2 * ii + 1, slot = pos % kRing;
-        ok = bounded_wait(cx.bar(B_KVFULL + slot), (pos / kRing) & 1, cx.abort_flag, cx.status,
-                          kErrMmaWait);
+        // bf16: V is read from its ring slot; e4m3: from the stream's widened copy, written by
+        // the softmax warpgroup before it arrived on PFULL (which also released the slot)
+        if constexpr (!F8)
+          ok = bounded_wait(cx.bar(B_KVFULL + slot), (pos / kRing) & 1, cx.abort_flag, cx.status,
+                            kErrMmaWait);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t vaddr = cx.sbase + SM_RING + slot * kSlotBytes;
-        // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together);
-        // a K step spans 8 TMEM columns in both formats (16 bf16 or 32 e4m3 keys)
+        const uint32_t vaddr = F8 ? cx.sbase + SM_V16 + (n_pv & 1) * 32768u
+                                  : cx.sbase + SM_RING + slot * kSlotBytes;
+        // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together),
+        // as 16-bit pairs: a K step of 16 keys spans 8 TMEM columns
         const uint32_t pcol = cx.tmem + TM_S + (n_pv & 1) * 128;
         // the first PV of each stream in a segment (segment tiles 0 and 1) starts a fresh sum
         const uint32_t ocol = cx.tmem + TM_O + (n_pv & 1) * 128;
-        if constexpr (F8) {
-          // 32 keys per step (the own-row tile has 64 keys); V: 32 key rows of 128 bytes per
-          // step. The high P codes sit in columns [0, 32), the low ones in [32, 64).
-          const int nk = j < p.n_main ? 4 : 2;
-          for (int kk = 0; kk < 2 * nk; ++kk) {
-            const int ks = kk < nk ? kk : kk - nk;
-            umma_f8_ts(ocol, pcol + (kk < nk ? 0 : 32) + ks * 8,
-                       sw128_desc(vaddr + ks * 32 * 128, 16, 1024), kIdescPV, (ii > 1 || kk > 0));
-          }
-        } else {
-          const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
-          for (int kk = 0; kk < nk; ++kk)        // V: 16 key rows of 128 bytes per step and atom
-            umma_f16_ts(ocol, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024),
-                        kIdescPV, (ii > 1 || kk > 0));
-        }
+        const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
+        for (int kk = 0; kk < nk; ++kk)        // V: 16 key rows of 128 bytes per step and atom
+          umma_f16_ts(ocol, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024), kIdescPV,
+                      (ii > 1 || kk > 0));
         // even and odd PVs complete on separate barriers: a waiter that knows PV k-2 is done
         // can then always tell PV k's completion from an older phase
         umma_commit(cx.bar(B_ODONE + (n_pv & 1)));
-        umma_commit(cx.bar(B_KVEMPTY + slot));
+        if constexpr (!F8) umma_commit(cx.bar(B_KVEMPTY + slot));
         ++n_pv;
       }
     }
@@ -412,6 +409,38 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
         flag_seen |= flag_pend;
         flag_pend = ld_relaxed_gpu(usync + 1);
       }
+      if constexpr (F8) {
+        // e4m3 cache: widen V(n) to f16 in the stream's buffer while QK(n) runs. The buffer
+        // held V(n-2): wait until PV(n-2) has read it (PV(n-4) is known complete, since S(n-2)
+        // was). V(n) is ring position 2n + 1; the slot is released once it has been read.
+        if (n >= 2) ok = wait_bar(B_ODONE + k, ((n - 2) >> 1) & 1);
+        const uint32_t vpos = 2 * static_cast<uint32_t>(n) + 1, vslot = vpos % kRing;
+        if (ok) ok = wait_bar(B_KVFULL + vslot, (vpos / kRing) & 1);
+        if (!ok) break;
+        if (j < p.n_main || r < kTok) {  // the own-row tile has 64 keys
+          const uint32_t src = cx.sbase + SM_RING + vslot * kSlotBytes + r * 128;
+          const uint32_t dst = cx.sbase + SM_V16 + k * 32768u + r * 128;
+          const int sw = r & 7;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: channels 16c .. 16c + 15
+            const uint4 v = ld_shared_v4(src + 16 * (c ^ sw));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              h[2 * q] = cvt_f16x2_e4m3x2(static_cast<uint16_t>(w[q] & 0xFFFFu));
+              h[2 * q + 1] = cvt_f16x2_e4m3x2(static_cast<uint16_t>(w[q] >> 16));
+            }
+            // f16 channels 16c .. 16c + 15: atom c / 4, 8-channel chunks 2 (c % 4) and + 1
+            const uint32_t atom = dst + (c >> 2) * kAtom;
+            const int d0 = 2 * (c & 3);
+            st_shared_v4(atom + 16 * (d0 ^ sw), h[0], h[1], h[2], h[3]);
+            st_shared_v4(atom + 16 * ((d0 + 1) ^ sw), h[4], h[5], h[6], h[7]);
+          }
+        }
+        fence_proxy_async_smem();  // the f16 tile is read by the tensor core (async proxy)
+        mbar_arrive(cx.bar(B_KVEMPTY + vslot));
+      }
       ok = wait_bar(B_SFULL + k, (n >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
@@ -452,8 +481,9 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
             mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
       }
       // per-tile factors: scores in log2 units are s * ct; FP8 adds the block scales, and P is
-      // stored as 2^(x - m) * (sv / svr) (exponent offset lgv) so that its e4m3 codes carry the
-      // tile's V scale relative to the unit's largest one; the row sum counts 2^(x - m).
+      // stored as 2^(x - m) * (sv / svr) (exponent offset lgv) so that it carries the tile's V
+      // scale relative to the unit's largest one (V itself stays as its e4m3 code values); the
+      // row sum counts 2^(x - m).
       float ct = c, lgv = 0.f, lmul = 1.f;
       if constexpr (F8) {
         const int col = tail ? p.ncol - 1 : j;
@@ -478,44 +508,26 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
       float ts8[8];  // row sum with 8 independent accumulators
 #pragma unroll
       for (int q = 0; q < 8; ++q) ts8[q] = 0.f;
-      // P(n) goes to TMEM over the columns of S(n). Pair pr's P lands in columns that hold
-      // scores of pairs <= pr, already read (bf16: columns [32 pr, 32 pr + 32); e4m3: high
-      // codes in [16 pr, 16 pr + 16), low codes in [32 + 16 pr, 32 + 16 pr + 16)). The buffer's
-      // previous P, P(n-2), was consumed by PV(n-2), which completed before QK(n).
+      // P(n) goes to TMEM over the columns of S(n). Pair pr's P lands in columns [32 pr,
+      // 32 pr + 32), which hold scores of pairs <= pr, already read. The buffer's previous P,
+      // P(n-2), was consumed by PV(n-2), which completed before QK(n).
 #pragma unroll 1
       for (int pr = 0; pr < npair; ++pr) {
         uint32_t v[2][32];
         load_pair(pr, v);
-        if constexpr (F8) {
-          // four e4m3 codes per column; the low codes carry the residual of the high ones
-          uint32_t hi[16], lo[16];
+        // 16-bit pairs (bf16; f16 for an e4m3 cache, whose V is widened to f16): column c of
+        // the pair block holds keys 2c and 2c + 1
+        uint32_t pk[32];
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
+        for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e]), ct, neg));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 1]), ct, neg));
-              const float p2 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 2]), ct, neg));
-              const float p3 = ex2_approx(fmaf(__uint_as_float(v[ch][4 * e + 3]), ct, neg));
-              ts8[e] += (p0 + p1) + (p2 + p3);
-              pack_e4m3x4_hilo(p0, p1, p2, p3, hi[8 * ch + e], lo[8 * ch + e]);
-            }
-          tmem_st16(pa_base + 16 * pr, hi);
-          tmem_st16(pa_base + 32 + 16 * pr, lo);
-        } else {
-          // bf16 pairs: column c holds keys 2c and 2c + 1
-          uint32_t pk[32];
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), ct, neg));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), ct, neg));
-              ts8[e & 7] += p0 + p1;
-              pk[16 * ch + e] = pack_bf16x2(p0, p1);
-            }
-          tmem_st32(pa_base + 32 * pr, pk);
-        }
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), ct, neg));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), ct, neg));
+            ts8[e & 7] += p0 + p1;
+            pk[16 * ch + e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          }
+        tmem_st32(pa_base + 32 * pr, pk);
       }
       lsum += (((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]))) * lmul;
       tmem_wait_st();
@@ -747,7 +759,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     mbar_init(cx.bar(B_STAGED + 1), kSoftmaxThreads);
     for (int b = 0; b < kRing; ++b) {
       mbar_init(cx.bar(B_KVFULL + b), 1);
-      mbar_init(cx.bar(B_KVEMPTY + b), 1);
+      // e4m3: a V slot (odd) is released by the 128 threads of the warpgroup that widened it
+      mbar_init(cx.bar(B_KVEMPTY + b), F8 && (b & 1) ? 128 : 1);
     }
     mbar_init(cx.bar(B_DRAIN), 1);
     *cx.abort_flag = 0u;

@@ -376,6 +376,20 @@ __device__ __forceinline__ void pack_e4m3x4_hilo(float a, float b, float c, floa
   hi = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
   lo = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
 }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// Two e4m3 codes (low byte first) -> their exact f16 values (low half first).
+__device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
