@@ -9,12 +9,11 @@
 // An octet (8 lanes) owns one token at a time; lane i holds channels [8i, 8i+8) and their RoPE
 // partners [64+8i, 64+8i+8), so the rotation is in-thread and the norm needs three shuffles.
 // Every global access is a 16-byte vector access.
-//   bf16 cache: persistent CTAs (one per SM) of 256 threads walk a range of (layer, g) units (q
-//     heads 2g, 2g+1, k head g, v head g; all 64 tokens, two per octet), computing the tokens'
-//     cos/sin once (positions are the same in every layer and head); the raw rows arrive by
-//     bulk copy into a shared-memory ring several units ahead.
-//   FP8 cache: a CTA of 256 threads owns one (layer, g) unit and all 64 tokens (two per octet):
-//     the own rows' scale needs the amax over all of them.
+// Persistent CTAs (one per SM) of 256 threads walk a range of (layer, g) units (q heads 2g,
+// 2g+1, k head g, v head g; all 64 tokens, two per octet), computing the tokens' cos/sin once
+// (positions are the same in every layer and head); the raw rows arrive by bulk copy into a
+// shared-memory ring several units ahead. With an e4m3 cache the own K and V rows of a head
+// share one scale over all 64 tokens, a CTA-wide maximum.
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
@@ -160,8 +159,11 @@ constexpr uint32_t kPBarOff = kPRing * kPUnitBytes;
 constexpr uint32_t kPSmemBytes = kPBarOff + 8 * kPRing + 16;
 
 // Grid: min(number of SMs, units); block 256 = 32 octets, each owning tokens oc and oc + 32.
-template <int CAP>
-__global__ void __launch_bounds__(256, 1) prologue_bf16_kernel(const __grid_constant__ PrologueParams<CAP> p) {
+// F8: the e4m3 cache variant (Q as high and low codes with a per-row scale; the own K and V rows
+// quantised with one scale per head over all 64 tokens: CTA-wide maxima).
+template <bool F8, int CAP>
+__global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_constant__ PrologueParams<CAP> p) {
+  __shared__ float red[8];
   extern __shared__ __align__(128) uint8_t psm[];
   const uint32_t sbase = smem_u32(psm);
   const uint32_t bar0 = sbase + kPBarOff;
@@ -229,6 +231,8 @@ __global__ void __launch_bounds__(256, 1) prologue_bf16_kernel(const __grid_cons
     const uint8_t* src = psm + (k % kPRing) * kPUnitBytes;
     uint8_t* qdst = p.q_ws + static_cast<size_t>(u) * kQTileBytes;
     uint8_t* tdst = p.tail_ws + static_cast<size_t>(u) * kTailUnitBytes;
+    float krl[2][8], krh[2][8], vrl[2][8], vrh[2][8];  // FP8: kept for the heads' scales
+    float kmax = 0.f, vmax = 0.f;
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
       const int t = oc + 32 * tt;
@@ -241,8 +245,27 @@ __global__ void __launch_bounds__(256, 1) prologue_bf16_kernel(const __grid_cons
         norm_rope(xl, xh, gql, gqh, cs[tt], sn[tt], yl, yh);
         const int r = hh * kTok + t;
         const uint4 ql = pack8(yl, false), qh = pack8(yh, false);
-        *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = ql;
-        *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = qh;
+        if constexpr (F8) {
+          // the row as two sets of e4m3 codes (high, low) with one scale amax / 448
+          float am = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) am = fmaxf(am, fmaxf(fabsf(yl[e]), fabsf(yh[e])));
+#pragma unroll
+          for (int m = 4; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
+          const float sq = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
+          const float isq = am > 0.f ? 448.0f / am : 1.0f;
+          uint2 hi, lo;  // high codes in the first 16 KB of the unit's slot, low codes in the second
+          quant8_hilo(yl, isq, hi, lo);
+          *reinterpret_cast<uint2*>(qdst + swz8_off(r, i)) = hi;
+          *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i)) = lo;
+          quant8_hilo(yh, isq, hi, lo);
+          *reinterpret_cast<uint2*>(qdst + swz8_off(r, i + 8)) = hi;
+          *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i + 8)) = lo;
+          if (i == 0) p.q_scale[static_cast<size_t>(u) * kRows + r] = sq;
+        } else {
+          *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = ql;
+          *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = qh;
+        }
         if (L.q_rope != nullptr) {
           __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
           *reinterpret_cast<uint4*>(qr + dl) = ql;
@@ -251,25 +274,74 @@ __global__ void __launch_bounds__(256, 1) prologue_bf16_kernel(const __grid_cons
       }
       const uint8_t* krow = src + 32768 + t * (kD * 2);
       const uint8_t* vrow = src + 49152 + t * (kD * 2);
-      float xl[8], xh[8], kl[8], kh[8];
+      float xl[8], xh[8];
       unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl * 2), xl);
       unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh * 2), xh);
-      norm_rope(xl, xh, gkl, gkh, cs[tt], sn[tt], kl, kh);
-      const uint4 kpl = pack8(kl, false), kph = pack8(kh, false);
+      norm_rope(xl, xh, gkl, gkh, cs[tt], sn[tt], krl[tt], krh[tt]);
       const uint4 vpl = *reinterpret_cast<const uint4*>(vrow + dl * 2);
       const uint4 vph = *reinterpret_cast<const uint4*>(vrow + dh * 2);
-      const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-      __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(L.k_cache) + crow * kD;
-      __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(L.v_cache) + crow * kD;
-      *reinterpret_cast<uint4*>(kc + dl) = kpl;
-      *reinterpret_cast<uint4*>(kc + dh) = kph;
-      *reinterpret_cast<uint4*>(vc + dl) = vpl;
-      *reinterpret_cast<uint4*>(vc + dh) = vph;
-      const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
-      *reinterpret_cast<uint4*>(tdst + sol) = kpl;
-      *reinterpret_cast<uint4*>(tdst + soh) = kph;
-      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = vpl;
-      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = vph;
+      if constexpr (F8) {
+        unpack_bf16x8(vpl, vrl[tt]);
+        unpack_bf16x8(vph, vrh[tt]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kmax = fmaxf(kmax, fmaxf(fabsf(krl[tt][e]), fabsf(krh[tt][e])));
+          vmax = fmaxf(vmax, fmaxf(fabsf(vrl[tt][e]), fabsf(vrh[tt][e])));
+        }
+      } else {
+        const uint4 kpl = pack8(krl[tt], false), kph = pack8(krh[tt], false);
+        const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(L.k_cache) + crow * kD;
+        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(L.v_cache) + crow * kD;
+        *reinterpret_cast<uint4*>(kc + dl) = kpl;
+        *reinterpret_cast<uint4*>(kc + dh) = kph;
+        *reinterpret_cast<uint4*>(vc + dl) = vpl;
+        *reinterpret_cast<uint4*>(vc + dh) = vph;
+        const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
+        *reinterpret_cast<uint4*>(tdst + sol) = kpl;
+        *reinterpret_cast<uint4*>(tdst + soh) = kph;
+        *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = vpl;
+        *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = vph;
+      }
+    }
+    if constexpr (F8) {
+      // e4m3 cache: the 64 own rows of this head share one scale slot, column Smax/128; the
+      // unit's reference V scale is the largest over the cache blocks it reads and its own rows
+      kmax = block_max_256(kmax, red);
+      vmax = block_max_256(vmax, red);
+      const float ksc = kmax > 0.f ? __fdiv_rn(kmax, 448.0f) : 1.0f;
+      const float vsc = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
+      const int ncol = Smax / kScaleBlock + 1;
+      const int n_main = (p.S + kKeyTile - 1) / kKeyTile;
+      float vr = vsc;
+      for (int b = threadIdx.x; b < n_main; b += 256) vr = fmaxf(vr, L.v_scale[g * ncol + b]);
+      vr = block_max_256(vr, red);
+      if (threadIdx.x == 0) {
+        L.k_scale[g * ncol + ncol - 1] = ksc;
+        L.v_scale[g * ncol + ncol - 1] = vsc;
+        p.sv_ref[u] = vr;
+      }
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int t = oc + 32 * tt;
+        const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
+        uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + crow * kD;
+        uint8_t* vc = static_cast<uint8_t*>(L.v_cache) + crow * kD;
+        uint2 c;
+        uint4 w;
+        quant8(krl[tt], ksc, c, w);
+        *reinterpret_cast<uint2*>(kc + dl) = c;
+        *reinterpret_cast<uint2*>(tdst + swz8_off(t, i)) = c;
+        quant8(krh[tt], ksc, c, w);
+        *reinterpret_cast<uint2*>(kc + dh) = c;
+        *reinterpret_cast<uint2*>(tdst + swz8_off(t, i + 8)) = c;
+        quant8(vrl[tt], vsc, c, w);
+        *reinterpret_cast<uint2*>(vc + dl) = c;
+        *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i)) = c;
+        quant8(vrh[tt], vsc, c, w);
+        *reinterpret_cast<uint2*>(vc + dh) = c;
+        *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i + 8)) = c;
+      }
     }
     __syncthreads();  // every thread is done with the slot
     if (threadIdx.x == 0 && u0 + issued < u1) {
@@ -285,201 +357,29 @@ __global__ void __launch_bounds__(256, 1) prologue_bf16_kernel(const __grid_cons
   }
 }
 
-// TPO = tokens per octet: 1 for bf16 caches (two CTAs per unit), 2 for FP8 caches (one CTA per
-// unit: the own-row scale needs the amax over all 64 tokens of the head).
-template <int TPO, int CAP>
-__global__ void __launch_bounds__(256) prologue_kernel_t(const __grid_constant__ PrologueParams<CAP> p) {
-  // Launched programmatically after the previous kernel in the stream: wait for it (it may have
-  // produced q/k/v, or still read the workspace), then let the attention kernel's CTAs start
-  // their set-up; they wait for this grid before reading anything written here.
-  pdl_wait_primary();
-  pdl_launch_dependents();
-  __shared__ float red[8];
-  if (threadIdx.x < 2 && blockIdx.x % (2 / TPO) == 0)
-    p.unit_sync[2 * (blockIdx.x / (2 / TPO)) + threadIdx.x] = 0u;
-
-  constexpr int kCtasPerUnit = 2 / TPO;
-  const int unit_id = blockIdx.x / kCtasPerUnit;
-  const int part = blockIdx.x % kCtasPerUnit;
-  const int l = unit_id / kHkv, g = unit_id % kHkv;
-  const PrologueLayer& L = p.layer[l];
-  const int oc = threadIdx.x >> 3;   // octet: tokens t0 + oc + 32 tt
-  const int i = threadIdx.x & 7;     // channels [8i, 8i+8) and [64+8i, 64+8i+8)
-  const int dl = 8 * i, dh = 64 + 8 * i;
-  const int t0 = part * 32;
-  const bool fp8 = p.fp8 != 0;
-  const int Smax = p.Smax;
-
-  float gql[8], gqh[8], gkl[8], gkh[8], ih[8], il[8];
-  load_bf16x8(L.q_gamma + dl, gql);
-  load_bf16x8(L.q_gamma + dh, gqh);
-  load_bf16x8(L.k_gamma + dl, gkl);
-  load_bf16x8(L.k_gamma + dh, gkh);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    ih[e] = p.inv_hi[dl + e];
-    il[e] = p.inv_lo[dl + e];
-  }
-  const size_t unit = static_cast<size_t>(l) * kHkv + g;
-  uint8_t* qdst = p.q_ws + unit * kQTileBytes;
-  uint8_t* tdst = p.tail_ws + unit * kTailUnitBytes;
-
-  float krl[TPO][8], krh[TPO][8], vrl[TPO][8], vrh[TPO][8];  // kept for the FP8 scale
-  float kmax = 0.f, vmax = 0.f;
-
-  // All raw rows of this thread's tokens are requested before any arithmetic.
-  uint4 rq[TPO][2][2], rk[TPO][2], rv[TPO][2];
-#pragma unroll
-  for (int tt = 0; tt < TPO; ++tt) {
-    const int t = t0 + oc + 32 * tt;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const __nv_bfloat16* src = L.q_raw + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
-      rq[tt][hh][0] = *reinterpret_cast<const uint4*>(src + dl);
-      rq[tt][hh][1] = *reinterpret_cast<const uint4*>(src + dh);
-    }
-    const size_t kv = (static_cast<size_t>(g) * kTok + t) * kD;
-    rk[tt][0] = *reinterpret_cast<const uint4*>(L.k_raw + kv + dl);
-    rk[tt][1] = *reinterpret_cast<const uint4*>(L.k_raw + kv + dh);
-    rv[tt][0] = *reinterpret_cast<const uint4*>(L.v_raw + kv + dl);
-    rv[tt][1] = *reinterpret_cast<const uint4*>(L.v_raw + kv + dh);
-  }
-
-#pragma unroll
-  for (int tt = 0; tt < TPO; ++tt) {
-    const int t = t0 + oc + 32 * tt;
-    const int pos = t + p.rope_delta + p.S;
-    float cs[8], sn[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) rope_cos_sin(pos, ih[e], il[e], cs[e], sn[e]);
-
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = 2 * g + hh;
-      float xl[8], xh[8], yl[8], yh[8];
-      unpack_bf16x8(rq[tt][hh][0], xl);
-      unpack_bf16x8(rq[tt][hh][1], xh);
-      norm_rope(xl, xh, gql, gqh, cs, sn, yl, yh);
-      const int r = hh * kTok + t;
-      if constexpr (TPO == 2) {
-        // FP8 path: the row is stored as two sets of e4m3 codes (high, low) with one scale
-        // amax / 448
-        float am = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) am = fmaxf(am, fmaxf(fabsf(yl[e]), fabsf(yh[e])));
-#pragma unroll
-        for (int m = 4; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
-        const float sq = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
-        const float isq = am > 0.f ? 448.0f / am : 1.0f;
-        uint2 hi, lo;  // high codes in the first 16 KB of the unit's slot, low codes in the second
-        quant8_hilo(yl, isq, hi, lo);
-        *reinterpret_cast<uint2*>(qdst + swz8_off(r, i)) = hi;
-        *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i)) = lo;
-        quant8_hilo(yh, isq, hi, lo);
-        *reinterpret_cast<uint2*>(qdst + swz8_off(r, i + 8)) = hi;
-        *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i + 8)) = lo;
-        if (i == 0) p.q_scale[unit * kRows + r] = sq;
-      } else {
-        *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = pack8(yl, false);
-        *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = pack8(yh, false);
-      }
-      if (L.q_rope != nullptr) {
-        __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(h) * kTok + t) * kD;
-        *reinterpret_cast<uint4*>(qr + dl) = pack8(yl, false);
-        *reinterpret_cast<uint4*>(qr + dh) = pack8(yh, false);
-      }
-    }
-    float xl[8], xh[8];
-    unpack_bf16x8(rk[tt][0], xl);
-    unpack_bf16x8(rk[tt][1], xh);
-    norm_rope(xl, xh, gkl, gkh, cs, sn, krl[tt], krh[tt]);
-    const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-    const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
-    if (!fp8) {
-      const uint4 kl = pack8(krl[tt], false), kh = pack8(krh[tt], false);
-      __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(L.k_cache) + row * kD;
-      __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(L.v_cache) + row * kD;
-      *reinterpret_cast<uint4*>(kc + dl) = kl;
-      *reinterpret_cast<uint4*>(kc + dh) = kh;
-      *reinterpret_cast<uint4*>(vc + dl) = rv[tt][0];
-      *reinterpret_cast<uint4*>(vc + dh) = rv[tt][1];
-      *reinterpret_cast<uint4*>(tdst + sol) = kl;
-      *reinterpret_cast<uint4*>(tdst + soh) = kh;
-      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = rv[tt][0];
-      *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = rv[tt][1];
-    } else {
-      unpack_bf16x8(rv[tt][0], vrl[tt]);
-      unpack_bf16x8(rv[tt][1], vrh[tt]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        kmax = fmaxf(kmax, fmaxf(fabsf(krl[tt][e]), fabsf(krh[tt][e])));
-        vmax = fmaxf(vmax, fmaxf(fabsf(vrl[tt][e]), fabsf(vrh[tt][e])));
-      }
-    }
-  }
-  if constexpr (TPO == 2) {
-    // FP8 cache: the 64 own rows of this head share one scale slot, column Smax/128.
-    kmax = block_max_256(kmax, red);
-    vmax = block_max_256(vmax, red);
-    const float ksc = kmax > 0.f ? __fdiv_rn(kmax, 448.0f) : 1.0f;
-    const float vsc = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
-    const int ncol = Smax / kScaleBlock + 1;
-    // reference V scale of the unit: the largest over the cache blocks it reads and its own rows
-    const int n_main = (p.S + kKeyTile - 1) / kKeyTile;
-    float vr = vsc;
-    for (int b = threadIdx.x; b < n_main; b += 256) vr = fmaxf(vr, L.v_scale[g * ncol + b]);
-    vr = block_max_256(vr, red);
-    if (threadIdx.x == 0) {
-      L.k_scale[g * ncol + ncol - 1] = ksc;
-      L.v_scale[g * ncol + ncol - 1] = vsc;
-      p.sv_ref[unit] = vr;
-    }
-#pragma unroll
-    for (int tt = 0; tt < TPO; ++tt) {
-      const int t = t0 + oc + 32 * tt;
-      const size_t row = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-      uint2 c;
-      uint4 w;
-      uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + row * kD;
-      uint8_t* vc = static_cast<uint8_t*>(L.v_cache) + row * kD;
-      quant8(krl[tt], ksc, c, w);
-      *reinterpret_cast<uint2*>(kc + dl) = c;
-      *reinterpret_cast<uint2*>(tdst + swz8_off(t, i)) = c;
-      quant8(krh[tt], ksc, c, w);
-      *reinterpret_cast<uint2*>(kc + dh) = c;
-      *reinterpret_cast<uint2*>(tdst + swz8_off(t, i + 8)) = c;
-      quant8(vrl[tt], vsc, c, w);
-      *reinterpret_cast<uint2*>(vc + dl) = c;
-      *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i)) = c;
-      quant8(vrh[tt], vsc, c, w);
-      *reinterpret_cast<uint2*>(vc + dh) = c;
-      *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i + 8)) = c;
-    }
-  }
-}
-
-// Host-side launchers (the kernel template is instantiated and launched in this file).
 template <int CAP>
 cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, int sm_count,
                                    cudaLaunchConfig_t cfg) {
-  if (fp8) {
-    cfg.gridDim = dim3(pp.n_layers * kHkv);  // one CTA per unit
-    cfg.blockDim = dim3(256);
-    return cudaLaunchKernelEx(&cfg, prologue_kernel_t<2, CAP>, pp);
-  }
   const int n_units = pp.n_layers * kHkv;
   cfg.gridDim = dim3(n_units < sm_count ? n_units : sm_count);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = kPSmemBytes;
-  return cudaLaunchKernelEx(&cfg, prologue_bf16_kernel<CAP>, pp);
+  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_ring_kernel<true, CAP>, pp)
+             : cudaLaunchKernelEx(&cfg, prologue_ring_kernel<false, CAP>, pp);
+}
+
+template <bool F8, int CAP>
+static cudaError_t prologue_smem_attr() {
+  return cudaFuncSetAttribute(prologue_ring_kernel<F8, CAP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
 }
 
 cudaError_t prologue_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(prologue_bf16_kernel<kSmallCap>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prologue_bf16_kernel<kMaxLayersPerLaunch>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+  cudaError_t e = prologue_smem_attr<false, kSmallCap>();
+  if (e == cudaSuccess) e = prologue_smem_attr<true, kSmallCap>();
+  if (e == cudaSuccess) e = prologue_smem_attr<false, kMaxLayersPerLaunch>();
+  if (e == cudaSuccess) e = prologue_smem_attr<true, kMaxLayersPerLaunch>();
+  return e;
 }
 
 template cudaError_t launch_prologue_kernel<kSmallCap>(const PrologueParams<kSmallCap>&, bool, int,
