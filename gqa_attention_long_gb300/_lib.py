@@ -50,6 +50,7 @@ def lib() -> ctypes.CDLL:
             "expert_attn_set_splits": (I, [I]),
             "expert_attn_read_status": (I, [V, V, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_uint32)]),
             "expert_attn_status_string": (ctypes.c_char_p, [I]),
+            "expert_attn_selftest_wait_timeout": (I, [I, V, S, V]),
         }
         for name, (res, args) in sig.items():
             f = getattr(h, name)
@@ -219,6 +220,14 @@ def split_units(n_layers: int, S: int, n_ctas: int) -> list[int]:
 
 def expert_attn_set_splits(n_ctas_or_0_for_auto: int) -> int:
     return int(lib().expert_attn_set_splits(int(n_ctas_or_0_for_auto)))
+
+
+def expert_attn_selftest_wait_timeout(limit_us: int, ws: torch.Tensor, stream=None) -> None:
+    """Launches the library's bounded-wait self-test: a kernel wait that nothing satisfies
+    gives up after limit_us and records a timeout in the workspace's status word."""
+    p, n = _ws(ws)
+    _check("expert_attn_selftest_wait_timeout",
+           lib().expert_attn_selftest_wait_timeout(int(limit_us), p, n, _stream(stream)))
 
 
 def expert_attn_read_status(ws: torch.Tensor, stream=None) -> tuple[int, int]:

@@ -12,6 +12,7 @@
 
 #include "expert_attn.h"
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace ea {
 template <int CAP>
@@ -32,6 +33,30 @@ namespace {
 using namespace ea;
 
 constexpr int kMaxDevices = 64;
+
+// One thread waits, with a time limit, on an mbarrier that nothing arrives on: the bounded-wait
+// failure path of the library's kernels, made to run out on purpose (see the header).
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    bool done = false;
+    for (uint32_t it = 0; it < 0x80000000u; ++it) {
+      if (mbar_try_wait(b, 0)) {
+        done = true;
+        break;
+      }
+      if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
+    }
+    if (!done) atomicOr(status, kErrSelftestWait);
+  }
+}
 
 struct DeviceInfo {
   bool init = false;
@@ -472,6 +497,19 @@ int expert_attn_read_status(const void* workspace, ea_stream_t stream, int* stat
   *status_out = bits == 0 ? EA_OK : EA_ERR_TIMEOUT;
   if (bits_out) *bits_out = bits;
   return EA_OK;
+}
+
+int expert_attn_selftest_wait_timeout(int limit_us, void* workspace, size_t ws_bytes,
+                                      ea_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < 1024 || limit_us < 1 || limit_us > 2000000)
+    return EA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EA_ERR_MISALIGNED;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint32_t*>(workspace), static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
 const char* expert_attn_status_string(int status) {

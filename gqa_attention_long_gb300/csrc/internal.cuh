@@ -43,6 +43,7 @@ enum : uint32_t {
   kErrDrain = 1u << 3,
   kErrPrologueWait = 1u << 4,
   kErrMergeWait = 1u << 5,
+  kErrSelftestWait = 1u << 6,
 };
 
 // ------------------------------------------------------------------------- workspace layout

@@ -129,6 +129,15 @@ int expert_attn_read_status(const void* workspace, ea_stream_t stream, int* stat
 /* A static string naming a status code. */
 const char* expert_attn_status_string(int status);
 
+/* Failure-detection self-test (the pages have no counterpart): launches one CTA on the stream
+ * whose thread waits on a shared-memory barrier that nothing ever arrives on, giving up after
+ * limit_us microseconds (1 .. 2000000) exactly as the library's kernels give up a bounded wait:
+ * it records a timeout bit in the workspace's status word and returns (no trap, no hang), so
+ * that expert_attn_read_status then reports EA_ERR_TIMEOUT and the context stays usable.
+ * Returns EA_ERR_INVALID_ARG for a null workspace or an out-of-range limit. */
+int expert_attn_selftest_wait_timeout(int limit_us, void* workspace, size_t ws_bytes,
+                                      ea_stream_t stream);
+
 /* ---- Variant without a caller-provided workspace (the pages have no counterpart to this).
  *
  * Some callers cannot allocate device memory at all: a plugin hosted by an engine that owns the

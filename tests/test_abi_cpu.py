@@ -89,3 +89,13 @@ def test_binding_refuses_host_tensors(h):
 def test_set_splits_roundtrip(h):
     prev = ea.expert_attn_set_splits(7)
     assert ea.expert_attn_set_splits(prev) == 7
+
+
+def test_selftest_rejects_bad_arguments_without_gpu(h):
+    ws = ctypes.c_void_p(0x10000)
+    assert h.expert_attn_selftest_wait_timeout(0, ws, 1 << 20, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_attn_selftest_wait_timeout(2000001, ws, 1 << 20, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_attn_selftest_wait_timeout(1000, None, 1 << 20, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_attn_selftest_wait_timeout(1000, ws, 16, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_attn_selftest_wait_timeout(1000, ctypes.c_void_p(0x10010), 1 << 20, None) == \
+        _lib.EA_ERR_MISALIGNED
