@@ -374,6 +374,45 @@ def main():
         single = {"workload": f"one layer per call, S={S}, Smax={Smax}, bf16 cache, 8 layers rotated (> L2)",
                   "us_per_layer": us1, "hbm_gbs": algo_bytes_per_layer(S) / (us1 * 1e-6) / 1e9}
 
+    # ---- the sequential chain: 64 dependent layers (layer i+1's raw q is layer i's output, a
+    # stand-in for the wo/MLP between them), one expert_attn_layer call per layer, replayed as a
+    # CUDA graph; latency per layer
+    chain = None
+    if not args.no_extras:
+        Lc = [ea.LayerBuffers(q_raw=(outs[l - 1] if l > 0 else act[0, :HQ]), k_raw=act[l, HQ:HQ + HKV],
+                              v_raw=act[l, HQ + HKV:], q_gamma=Ls[l].q_gamma, k_gamma=Ls[l].k_gamma,
+                              k_cache=Ls[l].k_cache, v_cache=Ls[l].v_cache, out=outs[l]) for l in range(n)]
+        wsc = ea.alloc_workspace(1, Smax)
+        arrc = [ea.make_args([Lc[l]], Smax, ea.EA_KV_BF16) for l in range(n)]
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for l in range(n):  # warm-up outside the capture (tensor maps, attributes)
+                ea.expert_attn_layers([Lc[l]], S, Smax, 0, ea.EA_KV_BF16, wsc, side, _arr=arrc[l])
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for l in range(n):
+                ea.expert_attn_layers([Lc[l]], S, Smax, 0, ea.EA_KV_BF16, wsc, side, _arr=arrc[l])
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(side)
+        with torch.cuda.stream(side):
+            for _ in range(args.steps):
+                graph.replay()
+        c1.record(side)
+        torch.cuda.synchronize()
+        stc, bitsc = ea.expert_attn_read_status(wsc)
+        if stc != 0:
+            raise RuntimeError(f"chain kernel status bits {bitsc:#x}")
+        msc = c0.elapsed_time(c1) / args.steps
+        chain = {"workload": f"{n} dependent layers (layer i+1's raw q = layer i's output), one expert_attn_layer "
+                             f"call each, replayed as a CUDA graph; S={S}, Smax={Smax}, bf16 cache",
+                 "us_per_layer": msc * 1e3 / n, "ms_per_chain": msc,
+                 "launches_per_layer": launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count)}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         smp = oracle_sample(S, Smax, 8, 10.0)
@@ -401,6 +440,7 @@ def main():
             "cpu_baseline": cpu,
             "fp8_step": fp8,
             "single_layer": single,
+            "sequential_chain": chain,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

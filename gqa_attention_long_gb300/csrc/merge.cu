@@ -7,19 +7,19 @@
 //   M = max_s lse_s,   w_s = 2^(lse_s - M) / sum_t 2^(lse_t - M),   out = sum_s w_s O_s,
 // written as bf16 to out[layer][2g + r/64][r%64][:] (folded row r of kv head g).
 //
-// One warp per folded row; lane j owns columns [4j, 4j+4). Parts are taken eight at a time: every
-// lane requests the eight parts' lse values (broadcast loads) together with its eight float4s,
-// so a row costs one round trip to L2 per eight parts, and the running max and weight sum are
-// carried across batches (a unit has at most as many parts as there are CTAs: a single layer
-// spread over every SM has ~20).
+// One warp per folded row; lane j owns columns [4j, 4j+4). Parts are taken kBatch at a time
+// (8, or 24 when a unit has more than 8 parts): every lane requests the batch's lse values
+// (broadcast loads) together with its float4s, so a row costs one round trip to L2 per batch,
+// and the running max and weight sum are carried across batches (a unit has at most as many
+// parts as there are CTAs: a single layer spread over every SM has ~20, one batch of 24).
 #include "internal.cuh"
 #include "ptx.cuh"
 
 namespace ea {
 
-constexpr int kMergeWarps = 8;  // rows per CTA
+constexpr int kMergeWarps = 4;  // rows per CTA
 
-template <int CAP>
+template <int CAP, int kBatch>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ MergeParams<CAP> p) {
   // Launched programmatically after the attention kernel: let the next kernel in the stream set
   // up, then wait until every partial of the attention grid is written and visible.
@@ -34,11 +34,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
 
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int q0 = 0; q0 < nparts; q0 += 8) {
-    float lse[8];
-    float4 o[8];
+  for (int q0 = 0; q0 < nparts; q0 += kBatch) {
+    float lse[kBatch];
+    float4 o[kBatch];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < kBatch; ++e) {
       if (q0 + e < nparts) {
         const int q = q0 + e;
         const size_t pr = (static_cast<size_t>(c0 + q) * 2 + (q == 0 ? su.slot0 : 0)) * kRows + r;
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
     }
     float mb = lse[0];
 #pragma unroll
-    for (int e = 1; e < 8; ++e) mb = fmaxf(mb, lse[e]);
+    for (int e = 1; e < kBatch; ++e) mb = fmaxf(mb, lse[e]);
     const float Mn = fmaxf(M, mb);
     const float alpha = ex2_approx(M - Mn);  // 0 on the first batch (M = -inf)
     L *= alpha;
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
     acc.z *= alpha;
     acc.w *= alpha;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < kBatch; ++e) {
       const float w = ex2_approx(lse[e] - Mn);  // 0 for the padding entries
       L += w;
       acc.x = fmaf(w, o[e].x, acc.x);
@@ -87,7 +87,10 @@ template <int CAP>
 cudaError_t launch_merge_kernel(const MergeParams<CAP>& mp, cudaLaunchConfig_t cfg) {
   cfg.gridDim = dim3(mp.n_split * (kRows / kMergeWarps));
   cfg.blockDim = dim3(kMergeWarps * 32);
-  return cudaLaunchKernelEx(&cfg, merge_kernel<CAP>, mp);
+  int max_parts = 0;
+  for (int i = 0; i < mp.n_split; ++i) max_parts = mp.unit[i].nparts > max_parts ? mp.unit[i].nparts : max_parts;
+  return max_parts <= 8 ? cudaLaunchKernelEx(&cfg, merge_kernel<CAP, 8>, mp)
+                        : cudaLaunchKernelEx(&cfg, merge_kernel<CAP, 24>, mp);
 }
 template cudaError_t launch_merge_kernel<kSmallCap>(const MergeParams<kSmallCap>&, cudaLaunchConfig_t);
 template cudaError_t launch_merge_kernel<kMaxLayersPerLaunch>(const MergeParams<kMaxLayersPerLaunch>&,

@@ -158,19 +158,26 @@ constexpr uint32_t kPUnitBytes = 65536;
 constexpr uint32_t kPBarOff = kPRing * kPUnitBytes;
 constexpr uint32_t kPSmemBytes = kPBarOff + 8 * kPRing + 16;
 
-// Grid: min(number of SMs, units); block 256 = 32 octets, each owning tokens oc and oc + 32.
+// TPO = 2 (tokens per octet): grid min(number of SMs, units), block 256 = 32 octets, each owning
+// tokens oc and oc + 32 of every unit in the CTA's range. TPO = 1 (few units, bf16 only): two
+// CTAs per unit, each owning 32 tokens, one per octet; the per-thread work halves.
 // F8: the e4m3 cache variant (Q as high and low codes with a per-row scale; the own K and V rows
 // quantised with one scale per head over all 64 tokens: CTA-wide maxima).
-template <bool F8, int CAP>
+template <bool F8, int CAP, int TPO>
 __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_constant__ PrologueParams<CAP> p) {
+  static_assert(TPO == 2 || !F8, "the e4m3 own-row scale needs all 64 tokens in one CTA");
+  constexpr int kTpc = 32 * TPO;  // tokens per CTA and unit
   __shared__ float red[8];
   extern __shared__ __align__(128) uint8_t psm[];
   const uint32_t sbase = smem_u32(psm);
   const uint32_t bar0 = sbase + kPBarOff;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(psm + kPBarOff + 8 * kPRing);
   const int n_units = p.n_layers * kHkv;
-  const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * n_units / gridDim.x);
-  const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_units / gridDim.x);
+  const int u0 = TPO == 2 ? static_cast<int>(static_cast<long long>(blockIdx.x) * n_units / gridDim.x)
+                          : static_cast<int>(blockIdx.x >> 1);
+  const int u1 = TPO == 2 ? static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_units / gridDim.x)
+                          : u0 + 1;
+  const int t0 = TPO == 2 ? 0 : 32 * static_cast<int>(blockIdx.x & 1);  // first token of the CTA
   const int oc = threadIdx.x >> 3;  // octet: tokens oc and oc + 32
   const int i = threadIdx.x & 7;    // channels [8i, 8i+8) and [64+8i, 64+8i+8)
   const int dl = 8 * i, dh = 64 + 8 * i;
@@ -186,27 +193,35 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
   // their set-up; they wait for this grid before reading anything written here.
   pdl_wait_primary();
   pdl_launch_dependents();
-  for (int x = threadIdx.x; x < 2 * (u1 - u0); x += 256) p.unit_sync[2 * u0 + x] = 0u;
+  if (t0 == 0)
+    for (int x = threadIdx.x; x < 2 * (u1 - u0); x += 256) p.unit_sync[2 * u0 + x] = 0u;
 
   const uint64_t pol = l2_policy_evict_first();  // raw rows are read once
+  // slot layout: q head 2g rows, q head 2g+1 rows, k rows, v rows (kTpc rows of 256 B each)
+  constexpr uint32_t kRowsB = kTpc * kD * 2;
   auto issue = [&](int k) {  // one thread: bulk loads of unit u0 + k into slot k % kPRing
     const int u = u0 + k, g = u % kHkv;
     const PrologueLayer& L = p.layer[u / kHkv];
     const uint32_t dst = sbase + (k % kPRing) * kPUnitBytes, bar = bar0 + 8 * (k % kPRing);
-    mbar_expect_tx(bar, kPUnitBytes);
-    bulk_load(dst, L.q_raw + static_cast<size_t>(2 * g) * kTok * kD, 32768, bar, pol);
-    bulk_load(dst + 32768, L.k_raw + static_cast<size_t>(g) * kTok * kD, 16384, bar, pol);
-    bulk_load(dst + 49152, L.v_raw + static_cast<size_t>(g) * kTok * kD, 16384, bar, pol);
+    mbar_expect_tx(bar, 4 * kRowsB);
+    if (TPO == 2) {  // both q heads are one contiguous block
+      bulk_load(dst, L.q_raw + static_cast<size_t>(2 * g) * kTok * kD, 2 * kRowsB, bar, pol);
+    } else {
+      bulk_load(dst, L.q_raw + (static_cast<size_t>(2 * g) * kTok + t0) * kD, kRowsB, bar, pol);
+      bulk_load(dst + kRowsB, L.q_raw + (static_cast<size_t>(2 * g + 1) * kTok + t0) * kD, kRowsB, bar, pol);
+    }
+    bulk_load(dst + 2 * kRowsB, L.k_raw + (static_cast<size_t>(g) * kTok + t0) * kD, kRowsB, bar, pol);
+    bulk_load(dst + 3 * kRowsB, L.v_raw + (static_cast<size_t>(g) * kTok + t0) * kD, kRowsB, bar, pol);
   };
   int issued = 0;
   if (threadIdx.x == 0)
     for (; issued < kPRing && u0 + issued < u1; ++issued) issue(issued);
 
-  // cos/sin of this thread's two tokens at its eight frequencies (the same in every unit)
-  float cs[2][8], sn[2][8];
+  // cos/sin of this thread's tokens at its eight frequencies (the same in every unit)
+  float cs[TPO][8], sn[TPO][8];
 #pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
-    const int pos = oc + 32 * tt + p.rope_delta + p.S;
+  for (int tt = 0; tt < TPO; ++tt) {
+    const int pos = t0 + oc + 32 * tt + p.rope_delta + p.S;
 #pragma unroll
     for (int e = 0; e < 8; ++e) rope_cos_sin(pos, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[tt][e], sn[tt][e]);
   }
@@ -231,14 +246,14 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
     const uint8_t* src = psm + (k % kPRing) * kPUnitBytes;
     uint8_t* qdst = p.q_ws + static_cast<size_t>(u) * kQTileBytes;
     uint8_t* tdst = p.tail_ws + static_cast<size_t>(u) * kTailUnitBytes;
-    float krl[2][8], krh[2][8], vrl[2][8], vrh[2][8];  // FP8: kept for the heads' scales
+    float krl[TPO][8], krh[TPO][8], vrl[TPO][8], vrh[TPO][8];  // FP8: kept for the heads' scales
     float kmax = 0.f, vmax = 0.f;
 #pragma unroll
-    for (int tt = 0; tt < 2; ++tt) {
-      const int t = oc + 32 * tt;
+    for (int tt = 0; tt < TPO; ++tt) {
+      const int tl = oc + 32 * tt, t = t0 + tl;  // token within the CTA's block, within the unit
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const uint8_t* row = src + (hh * kTok + t) * (kD * 2);
+        const uint8_t* row = src + (hh * kTpc + tl) * (kD * 2);
         float xl[8], xh[8], yl[8], yh[8];
         unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dl * 2), xl);
         unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dh * 2), xh);
@@ -272,8 +287,8 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
           *reinterpret_cast<uint4*>(qr + dh) = qh;
         }
       }
-      const uint8_t* krow = src + 32768 + t * (kD * 2);
-      const uint8_t* vrow = src + 49152 + t * (kD * 2);
+      const uint8_t* krow = src + 2 * kRowsB + tl * (kD * 2);
+      const uint8_t* vrow = src + 3 * kRowsB + tl * (kD * 2);
       float xl[8], xh[8];
       unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl * 2), xl);
       unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh * 2), xh);
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
         p.sv_ref[u] = vr;
       }
 #pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
+      for (int tt = 0; tt < TPO; ++tt) {
         const int t = oc + 32 * tt;
         const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
         uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + crow * kD;
@@ -361,24 +376,33 @@ template <int CAP>
 cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, int sm_count,
                                    cudaLaunchConfig_t cfg) {
   const int n_units = pp.n_layers * kHkv;
-  cfg.gridDim = dim3(n_units < sm_count ? n_units : sm_count);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = kPSmemBytes;
-  return fp8 ? cudaLaunchKernelEx(&cfg, prologue_ring_kernel<true, CAP>, pp)
-             : cudaLaunchKernelEx(&cfg, prologue_ring_kernel<false, CAP>, pp);
+  if (fp8) {
+    cfg.gridDim = dim3(n_units < sm_count ? n_units : sm_count);
+    return cudaLaunchKernelEx(&cfg, prologue_ring_kernel<true, CAP, 2>, pp);
+  }
+  if (2 * n_units <= sm_count) {  // few units: two CTAs per unit, half the tokens each
+    cfg.gridDim = dim3(2 * n_units);
+    return cudaLaunchKernelEx(&cfg, prologue_ring_kernel<false, CAP, 1>, pp);
+  }
+  cfg.gridDim = dim3(n_units < sm_count ? n_units : sm_count);
+  return cudaLaunchKernelEx(&cfg, prologue_ring_kernel<false, CAP, 2>, pp);
 }
 
-template <bool F8, int CAP>
+template <bool F8, int CAP, int TPO>
 static cudaError_t prologue_smem_attr() {
-  return cudaFuncSetAttribute(prologue_ring_kernel<F8, CAP>,
+  return cudaFuncSetAttribute(prologue_ring_kernel<F8, CAP, TPO>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
 }
 
 cudaError_t prologue_set_attributes() {
-  cudaError_t e = prologue_smem_attr<false, kSmallCap>();
-  if (e == cudaSuccess) e = prologue_smem_attr<true, kSmallCap>();
-  if (e == cudaSuccess) e = prologue_smem_attr<false, kMaxLayersPerLaunch>();
-  if (e == cudaSuccess) e = prologue_smem_attr<true, kMaxLayersPerLaunch>();
+  cudaError_t e = prologue_smem_attr<false, kSmallCap, 2>();
+  if (e == cudaSuccess) e = prologue_smem_attr<false, kSmallCap, 1>();
+  if (e == cudaSuccess) e = prologue_smem_attr<true, kSmallCap, 2>();
+  if (e == cudaSuccess) e = prologue_smem_attr<false, kMaxLayersPerLaunch, 2>();
+  if (e == cudaSuccess) e = prologue_smem_attr<false, kMaxLayersPerLaunch, 1>();
+  if (e == cudaSuccess) e = prologue_smem_attr<true, kMaxLayersPerLaunch, 2>();
   return e;
 }
 
