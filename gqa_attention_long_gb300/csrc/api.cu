@@ -114,9 +114,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Map of cache rows [0, S) of one bf16 cache [8][Smax][128]: dims {128, S, 8}, strides {256 B,
-// Smax*256 B}, box {64, 128, 1} with 128-byte swizzle. Rows >= S are outside the map, so a
-// partially covered tile arrives zero-filled and hidden rows are never read.
+// Map of all Smax rows of one cache [8][Smax][128]: dims {128 channels, Smax, 8}, strides
+// {row bytes, Smax * row bytes}, 128-byte swizzle; it serves the cache tiles and, at row
+// Smax - 64, the own-row tile (its box rows past Smax arrive zero-filled). Keys >= S of the last
+// cache tile are masked by the softmax, and their V rows zeroed in shared memory.
 struct MapKey {
   const void* ptr;
   int S, Smax;
@@ -148,8 +149,7 @@ bool cache_map(const void* base, int S, int Smax, bool f8, CUtensorMap* out) {
   if (fn == nullptr) return false;
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD),
-                              static_cast<cuuint64_t>(S > 0 ? S : 1),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Smax),
                               static_cast<cuuint64_t>(kHkv)};
   const cuuint64_t esz = f8 ? 1 : 2;
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * esz,
@@ -252,7 +252,6 @@ int launch_prologue_t(const ea_layer_args* a, int n, int S, int Smax, int rope_d
   }
   rope_inv_freq(pp.inv_hi, pp.inv_lo);
   pp.q_ws = ws + wl.q_off;
-  pp.tail_ws = ws + wl.tail_off;
   pp.q_scale = reinterpret_cast<float*>(ws + wl.qscale_off);
   pp.sv_ref = reinterpret_cast<float*>(ws + wl.svref_off);
   pp.unit_sync = reinterpret_cast<uint32_t*>(ws + wl.sync_off);
@@ -321,7 +320,6 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
   ap.Smax = Smax;
   ap.W = static_cast<long long>(n) * kHkv * ap.T;
   ap.q_ws = ws + wl.q_off;
-  ap.tail_ws = ws + wl.tail_off;
   ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
   ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
   ap.q_scale = reinterpret_cast<const float*>(ws + wl.qscale_off);
@@ -537,7 +535,6 @@ constexpr size_t noalloc_bytes() {
   return ws_layout(EA_NOALLOC_MAX_LAYERS, EA_NOALLOC_MAX_CTAS).total;
 }
 static_assert(noalloc_bytes() == EA_NOALLOC_SCRATCH_BYTES, "scratch size in the header is stale");
-static_assert(kQTileBytes == kTailUnitBytes, "q and tail staging have the same size per unit");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[EA_NOALLOC_SCRATCH_BYTES];
 

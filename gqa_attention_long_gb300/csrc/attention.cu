@@ -52,7 +52,6 @@ struct Lay {
   static constexpr uint32_t kQ = kQTileBytes;  // one roped Q tile (e4m3: high then low codes)
   static constexpr uint32_t kSlot = F8 ? 16384u : 32768u;           // one K or V tile
   static constexpr uint32_t kAtom = 16384u;                         // 16-bit tiles: second channel half
-  static constexpr uint32_t kTail = F8 ? kTailHalfBytesF8 : kTailHalfBytes;  // 64 own rows
   static constexpr int kRing = F8 ? 6 : 5;  // e4m3: even, so ring slot parity = K (even) / V (odd)
   static constexpr uint32_t SM_Q = 0;  // two Q buffers
   static constexpr uint32_t SM_RING = SM_Q + 2 * kQ;
@@ -122,9 +121,8 @@ struct Ctx {
 template <bool F8, class PP>
 __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
-  pdl_wait_primary();  // roped Q and own rows are written by the prologue kernel
+  pdl_wait_primary();  // roped Q and the cache's own rows are written by the prologue kernel
   const uint64_t pol_stream = l2_policy_evict_first();  // cache tiles are read exactly once
-  const uint64_t pol_keep = l2_policy_evict_last();
   uint32_t ring = 0;
   bool ok = true;
   long long t = cx.start;
@@ -141,25 +139,14 @@ __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
         }
         const uint32_t dst = cx.sbase + SM_RING + slot * kSlotBytes;
         const uint32_t fb = cx.bar(B_KVFULL + slot);
-        if (j < p.n_main) {
-          // rows [128 j, 128 j + 128) of head g; rows >= S lie outside the map and arrive as 0
-          mbar_expect_tx(fb, kSlotBytes);
-          const CUtensorMap* m = h ? &p.vmap[l] : &p.kmap[l];
-          tma_load_3d(dst, m, fb, 0, j * kKeyTile, g, pol_stream);
-          if constexpr (!F8) tma_load_3d(dst + kAtom, m, fb, 64, j * kKeyTile, g, pol_stream);
-        } else {
-          // the 64 own rows, staged pre-swizzled by the prologue
-          const uint8_t* src =
-              p.tail_ws + static_cast<size_t>(s.u) * kTailUnitBytes + h * kTailHalfBytes;
-          if constexpr (F8) {  // one 8 KB atom block: 64 rows x 128 bytes
-            mbar_expect_tx(fb, kTailHalfBytesF8);
-            bulk_load(dst, src, kTailHalfBytesF8, fb, pol_keep);
-          } else {  // two 8 KB atom blocks, one per channel half
-            mbar_expect_tx(fb, kTailHalfBytes);
-            bulk_load(dst, src, kTailHalfBytes / 2, fb, pol_keep);
-            bulk_load(dst + kAtom, src + kTailHalfBytes / 2, kTailHalfBytes / 2, fb, pol_keep);
-          }
-        }
+        // cache tile j: rows [128 j, 128 j + 128) of head g (keys >= S of the last one are masked,
+        // and their V rows zeroed, by the softmax); own-row tile: rows [Smax - 64, Smax), written
+        // by the prologue, the box's rows past Smax arriving as zeros
+        const int row0 = j < p.n_main ? j * kKeyTile : p.Smax - kTok;
+        mbar_expect_tx(fb, kSlotBytes);
+        const CUtensorMap* m = h ? &p.vmap[l] : &p.kmap[l];
+        tma_load_3d(dst, m, fb, 0, row0, g, pol_stream);
+        if constexpr (!F8) tma_load_3d(dst + kAtom, m, fb, 64, row0, g, pol_stream);
         ++ring;
       }
     }
@@ -421,9 +408,12 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
           const uint32_t src = cx.sbase + SM_RING + vslot * kSlotBytes + r * 128;
           const uint32_t dst = cx.sbase + SM_V16 + k * 32768u + r * 128;
           const int sw = r & 7;
+          // rows of keys >= S in the last cache tile (hidden rows, any content) become zeros
+          const bool live = j >= p.n_main || j * kKeyTile + r < p.S;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: channels 16c .. 16c + 15
-            const uint4 v = ld_shared_v4(src + 16 * (c ^ sw));
+            uint4 v = ld_shared_v4(src + 16 * (c ^ sw));
+            if (!live) v = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t h[8];
 #pragma unroll
@@ -451,7 +441,7 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
       // register file. A cache tile has two pairs, the own-row tile (64 keys) one.
       const int npair = tail ? 1 : 2;
       const int key0 = j * kKeyTile;
-      const bool ragged = !tail && key0 + kKeyTile > p.S;  // keys >= S (zero-filled) are masked
+      const bool ragged = !tail && key0 + kKeyTile > p.S;  // keys >= S (hidden rows) are masked
       auto load_pair = [&](int pr, uint32_t (&v)[2][32]) {
         tmem_ld32(sa + 64 * pr, v[0]);
         tmem_ld32(sa + 64 * pr + 32, v[1]);
@@ -530,6 +520,24 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
         tmem_st32(pa_base + 32 * pr, pk);
       }
       lsum += (((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]))) * lmul;
+      if constexpr (!F8) {
+        if (ragged) {
+          // the last cache tile: V rows of keys >= S (hidden rows, any content, NaN included)
+          // become zeros before PV reads them, as P is 0 there
+          const uint32_t vpos = 2 * static_cast<uint32_t>(n) + 1, vslot = vpos % kRing;
+          ok = wait_bar(B_KVFULL + vslot, (vpos / kRing) & 1);
+          if (!ok) break;
+          if (key0 + r >= p.S) {
+            const uint32_t row = cx.sbase + SM_RING + vslot * kSlotBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              st_shared_v4(row + 16 * c, 0u, 0u, 0u, 0u);
+              st_shared_v4(row + kAtom + 16 * c, 0u, 0u, 0u, 0u);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(cx.bar(B_PFULL + k));

@@ -28,12 +28,9 @@ constexpr int kScaleBlock = 128;  // FP8 scale granularity (rows)
 // halves ("atoms"), each [rows][128 bytes]; inside every 8-row group of 1024 bytes the 16-byte
 // chunks of row r are permuted as chunk' = chunk ^ (r % 8).
 constexpr uint32_t kQTileBytes = kRows * kD * 2;          // 32 KB: roped Q of one (layer, kv head)
-constexpr uint32_t kTailHalfBytes = kTok * kD * 2;        // 16 KB: own K (or V) rows, 64 x 128
-constexpr uint32_t kTailUnitBytes = 2 * kTailHalfBytes;   // K then V
-// FP8 (e4m3) variant: one 128-byte swizzle atom per row, so a Q tile is 16 KB and the 64 own K
-// (or V) rows 8 KB, stored at the start of the same workspace slots as the bf16 ones.
+// FP8 (e4m3) variant: one 128-byte swizzle atom per row, so a Q tile is 16 KB (high codes, then
+// low codes in the next 16 KB of the same workspace slot).
 constexpr uint32_t kQTileBytesF8 = kRows * kD;
-constexpr uint32_t kTailHalfBytesF8 = kTok * kD;
 
 // Status bits recorded in the workspace when a bounded wait gives up.
 enum : uint32_t {
@@ -52,12 +49,12 @@ enum : uint32_t {
 //                                   in-kernel merge of two-part units (zeroed by the prologue)
 //   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
 //   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
-//   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; f16 FP8)
-//   tail    n_layers * 8 * 32 KB  own K rows then own V rows per (layer, kv head), swizzled
+//   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; e4m3
+//                                 high and low codes)
 //   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
 struct WsLayout {
-  size_t sync_off, qscale_off, svref_off, q_off, tail_off, part_o_off, part_lse_off, total;
+  size_t sync_off, qscale_off, svref_off, q_off, part_o_off, part_lse_off, total;
 };
 
 constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
@@ -72,8 +69,6 @@ constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
   off += ((static_cast<size_t>(n_layers_per_launch) * kHkv * sizeof(float)) + 1023) & ~static_cast<size_t>(1023);
   w.q_off = off;
   off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
-  w.tail_off = off;
-  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kTailUnitBytes;
   w.part_o_off = off;
   off += static_cast<size_t>(max_ctas) * 2 * kRows * kD * sizeof(float);
   w.part_lse_off = off;
@@ -102,7 +97,6 @@ struct PrologueParams {
   float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
   float inv_lo[kD / 2];
   uint8_t* q_ws;
-  uint8_t* tail_ws;
   float* q_scale;  // FP8: [unit][128] scale of each e4m3 Q row
   float* sv_ref;   // FP8: [unit] reference V scale
   uint32_t* unit_sync;  // [unit][2]: zeroed here for the attention kernel's in-kernel merge
@@ -112,13 +106,12 @@ struct PrologueParams {
 
 template <int CAP>
 struct AttnParams {
-  CUtensorMap kmap[CAP];  // cache rows [0, S) of K: dims {128, S, 8}, box {64,128,1}
+  CUtensorMap kmap[CAP];  // all Smax rows of K: dims {128, Smax, 8}, box {64 (e4m3: 128), 128, 1}
   CUtensorMap vmap[CAP];
   __nv_bfloat16* out[CAP];
   const float* ks[CAP];      // FP8: block scales [8][Smax/128 + 1] (else null)
   const float* vs[CAP];
   const uint8_t* q_ws;
-  const uint8_t* tail_ws;
   float* part_o;
   float* part_lse;
   const float* q_scale;  // FP8: [unit][128]

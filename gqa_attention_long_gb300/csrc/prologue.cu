@@ -245,7 +245,6 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
     }
     const uint8_t* src = psm + (k % kPRing) * kPUnitBytes;
     uint8_t* qdst = p.q_ws + static_cast<size_t>(u) * kQTileBytes;
-    uint8_t* tdst = p.tail_ws + static_cast<size_t>(u) * kTailUnitBytes;
     float krl[TPO][8], krh[TPO][8], vrl[TPO][8], vrh[TPO][8];  // FP8: kept for the heads' scales
     float kmax = 0.f, vmax = 0.f;
 #pragma unroll
@@ -312,11 +311,6 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
         *reinterpret_cast<uint4*>(kc + dh) = kph;
         *reinterpret_cast<uint4*>(vc + dl) = vpl;
         *reinterpret_cast<uint4*>(vc + dh) = vph;
-        const uint32_t sol = swz_off(t, i, kTailHalfBytes / 2), soh = swz_off(t, i + 8, kTailHalfBytes / 2);
-        *reinterpret_cast<uint4*>(tdst + sol) = kpl;
-        *reinterpret_cast<uint4*>(tdst + soh) = kph;
-        *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + sol) = vpl;
-        *reinterpret_cast<uint4*>(tdst + kTailHalfBytes + soh) = vph;
       }
     }
     if constexpr (F8) {
@@ -346,16 +340,12 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
         uint4 w;
         quant8(krl[tt], ksc, c, w);
         *reinterpret_cast<uint2*>(kc + dl) = c;
-        *reinterpret_cast<uint2*>(tdst + swz8_off(t, i)) = c;
         quant8(krh[tt], ksc, c, w);
         *reinterpret_cast<uint2*>(kc + dh) = c;
-        *reinterpret_cast<uint2*>(tdst + swz8_off(t, i + 8)) = c;
         quant8(vrl[tt], vsc, c, w);
         *reinterpret_cast<uint2*>(vc + dl) = c;
-        *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i)) = c;
         quant8(vrh[tt], vsc, c, w);
         *reinterpret_cast<uint2*>(vc + dh) = c;
-        *reinterpret_cast<uint2*>(tdst + kTailHalfBytes + swz8_off(t, i + 8)) = c;
       }
     }
     __syncthreads();  // every thread is done with the slot
