@@ -25,7 +25,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from gqa_attention_long_gb300._lib import split_units  # noqa: E402
+from gqa_attention_long_gb300._lib import kernels_per_call  # noqa: E402
 from gqa_attention_long_gb300.inputs import config_seed, layer_inputs, layer_inputs_on_device  # noqa: E402
 
 METRIC = "µs/layer & achieved HBM GB/s (% roofline), expert attention, S=4700 Smax=8192"
@@ -38,24 +38,16 @@ def algo_bytes_per_layer(S: int, b: int = 2) -> int:
     return 2 * HKV * S * D * b + 2 * (2 * HKV * T * D * b) + (HQ + 2 * HKV) * T * D * 2 + HQ * T * D * 2
 
 
-def attn_kernel_bytes_per_layer(S: int, b: int = 2) -> int:
-    """Algorithmic bytes of the attention kernel alone: live cache K/V rows, own K/V rows, output."""
-    return 2 * HKV * S * D * b + 2 * HKV * T * D * b + HQ * T * D * 2
-
-
 def algo_bytes_per_layer_fp8(S: int) -> int:
     """As algo_bytes_per_layer for an e4m3 cache (1-byte K/V codes; block scales negligible)."""
     return 2 * HKV * S * D + 2 * (2 * HKV * T * D) + (HQ + 2 * HKV) * T * D * 2 + HQ * T * D * 2
 
 
-def launches_per_call(n_layers: int, S: int, sm_count: int) -> int:
-    """Kernels one expert_attn_layers call launches: per chunk of 64 layers the prologue, the
-    attention kernel and, when a CTA boundary cuts a unit, the merge kernel."""
-    total = 0
-    for l0 in range(0, n_layers, 64):
-        n = min(64, n_layers - l0)
-        total += 2 + (1 if split_units(n, S, sm_count) else 0)
-    return total
+def launches_per_call(n_layers: int, S: int, sm_count: int, kv_dtype: int = 0) -> int:
+    """Kernels one expert_attn_layers call launches (the library's own plan, mirrored on the
+    host: bf16 attention kernel, plus the merge kernel when a split unit has more than two
+    parts; an e4m3 cache adds the prologue kernel)."""
+    return kernels_per_call(n_layers, S, sm_count, kv_dtype)
 
 
 def flops_per_layer(S: int) -> int:
@@ -280,7 +272,9 @@ def main():
     ms_step = ms_total / args.steps
     us_layer = ms_step * 1e3 / (n * world)
 
-    # ---- dominant kernel (attention) timed on its own with events between the kernels
+    # ---- dominant kernel (attention) timed on its own with events between the kernels; with a
+    # bf16 cache it is the whole layer (no prologue kernel; no merge kernel when every split
+    # unit has two parts), so its algorithmic bytes are the layer's
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for e in evs:  # torch creates the CUDA event on first record
         for x in e:
@@ -288,13 +282,13 @@ def main():
     for i in range(args.steps):
         ea.expert_attn_layers_profiled(Ls, S, Smax, 0, ea.EA_KV_BF16, ws, evs[i], stream, _arr=arr)
     torch.cuda.synchronize()
-    k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     k2 = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     peaks = load_peaks()
-    k2_bytes = attn_kernel_bytes_per_layer(S) * n
+    k2_bytes = algo_bytes_per_layer(S) * n
     achieved = k2_bytes / (k2 * 1e-3) / 1e9
     traffic = attention_traffic(S, Smax, n)
+    merge_launched = launches_per_call(n, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1
 
     # ---- end to end through the C ABI with host buffers: H2D of q/k/v, call, D2H of out
     h_act = act.cpu().pin_memory()
@@ -432,7 +426,7 @@ def main():
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "attention_kernel", "peak_src": peaks["src"],
                          "bytes_per_launch": k2_bytes, "ms_per_launch": k2},
-            "kernels_ms": {"prologue": k1, "attention": k2, "merge": k3},
+            "kernels_ms": {"attention": k2, "merge": k3 if merge_launched else None},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_ms * 1e3 / (n * world), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

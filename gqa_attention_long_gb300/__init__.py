@@ -9,6 +9,6 @@ from ._lib import (  # noqa: F401
     expert_attn_layer, expert_attn_layers, expert_attn_layers_profiled, expert_attn_prologue,
     expert_attn_quantize_cache, expert_attn_read_status, expert_attn_selftest_wait_timeout,
     expert_attn_set_splits,
-    expert_attn_status_string, expert_attn_workspace_init, expert_attn_workspace_size, lib,
-    make_args, split_units,
+    expert_attn_status_string, expert_attn_workspace_init, expert_attn_workspace_size,
+    kernels_per_call, lib, make_args, split_parts, split_units,
 )

@@ -218,6 +218,38 @@ def split_units(n_layers: int, S: int, n_ctas: int) -> list[int]:
     return units
 
 
+def split_parts(n_layers: int, S: int, n_ctas: int) -> list[tuple[int, int]]:
+    """split_units with each unit's number of parts (the CTAs whose tile range meets it)."""
+    T = (S + 127) // 128 + 1
+    W = n_layers * 8 * T
+    n = max(1, min(n_ctas, 257, W))
+
+    def cta_of_tile(x: int) -> int:
+        c = x * n // W
+        while c + 1 < n and (c + 1) * W // n <= x:
+            c += 1
+        while c > 0 and c * W // n > x:
+            c -= 1
+        return c
+
+    return [(u, cta_of_tile(u * T + T - 1) - cta_of_tile(u * T) + 1)
+            for u in split_units(n_layers, S, n_ctas)]
+
+
+def kernels_per_call(n_layers: int, S: int, n_ctas: int, kv_dtype: int = EA_KV_BF16) -> int:
+    """Kernels one expert_attn_layers call launches: per chunk of 64 layers the prologue kernel
+    (e4m3 cache only; the bf16 attention kernel does its own prologue), the attention kernel and,
+    when a split unit has more than two parts, the merge kernel (two-part units are merged inside
+    the attention kernel)."""
+    total = 0
+    for l0 in range(0, n_layers, 64):
+        n = min(64, n_layers - l0)
+        parts = split_parts(n, S, n_ctas)
+        total += (1 if kv_dtype == EA_KV_FP8_E4M3 else 0) + 1
+        total += 1 if parts and any(k != 2 for _, k in parts) else 0
+    return total
+
+
 def expert_attn_set_splits(n_ctas_or_0_for_auto: int) -> int:
     return int(lib().expert_attn_set_splits(int(n_ctas_or_0_for_auto)))
 

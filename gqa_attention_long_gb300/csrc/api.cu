@@ -1,6 +1,8 @@
 // api.cu — host side of libexpert_attn.so: argument validation, launch planning, TMA tensor-map
-// encoding (cached), workspace layout and the three launches per chunk of layers (prologue,
-// attention, log-sum-exp merge of the split units) chained with programmatic dependent launch.
+// encoding (cached), workspace layout and the launches per chunk of layers (e4m3 cache: the
+// prologue kernel; the attention kernel, which does the bf16 prologue itself; the log-sum-exp
+// merge of the split units when the attention kernel does not merge them) chained with
+// programmatic dependent launch.
 // See include/expert_attn.h for the contract.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -203,6 +205,10 @@ int validate(const ea_layer_args* a, int n_layers, int S, int Smax, int rope_del
 
 namespace {
 
+// Bytes that expert_attn_workspace_init zeroes: everything before the first region that the
+// kernels fully rewrite on every call.
+constexpr size_t kInitBytes = ws_layout(kMaxLayersPerLaunch, 1).qscale_off;
+
 // RoPE inverse frequencies theta^(-2j/128) = 5e6^(-j/64), j < 64, as fp32 (hi, lo) pairs.
 void rope_inv_freq(float* hi, float* lo) {
   for (int j = 0; j < kD / 2; ++j) {
@@ -297,8 +303,10 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
                    cudaEvent_t const* ev) {
   const bool pdl = ev == nullptr;
   if (ev && ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return EA_ERR_CUDA;
-  int rc = launch_prologue_t<CAP>(a, n, S, Smax, rope_delta, fp8, ws, wl, di.sm_count, st, pdl);
-  if (rc != EA_OK) return rc;
+  if (fp8) {  // bf16: the attention kernel norms and ropes q and k and writes the own rows itself
+    const int rc = launch_prologue_t<CAP>(a, n, S, Smax, rope_delta, fp8, ws, wl, di.sm_count, st, pdl);
+    if (rc != EA_OK) return rc;
+  }
   if (ev && ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return EA_ERR_CUDA;
 
   LaunchBlocks<CAP>& lb = launch_blocks<CAP>();
@@ -312,7 +320,17 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
     ap.out[l] = static_cast<__nv_bfloat16*>(a[l].out);
     ap.ks[l] = a[l].k_scale;
     ap.vs[l] = a[l].v_scale;
+    ap.q_raw[l] = static_cast<const __nv_bfloat16*>(a[l].q_raw);
+    ap.k_raw[l] = static_cast<const __nv_bfloat16*>(a[l].k_raw);
+    ap.v_raw[l] = static_cast<const __nv_bfloat16*>(a[l].v_raw);
+    ap.q_gamma[l] = static_cast<const __nv_bfloat16*>(a[l].q_gamma);
+    ap.k_gamma[l] = static_cast<const __nv_bfloat16*>(a[l].k_gamma);
+    ap.q_rope[l] = static_cast<__nv_bfloat16*>(a[l].q_rope);
+    ap.kc[l] = static_cast<__nv_bfloat16*>(a[l].k_cache);
+    ap.vc[l] = static_cast<__nv_bfloat16*>(a[l].v_cache);
   }
+  rope_inv_freq(ap.inv_hi, ap.inv_lo);
+  ap.rope_base = S + rope_delta;
   const int n_main = (S + kKeyTile - 1) / kKeyTile;
   ap.T = n_main + 1;
   ap.n_main = n_main;
@@ -417,7 +435,9 @@ size_t expert_attn_workspace_size(int n_layers, int Smax, int kv_dtype) {
 
 int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream) {
   if (workspace == nullptr || ws_bytes < 1024) return EA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(workspace, 0, 1024, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  // the status word and the in-kernel merge words of up to 64 layers per launch
+  const size_t n = ws_bytes < kInitBytes ? ws_bytes : kInitBytes;
+  if (cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
@@ -572,7 +592,8 @@ extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_lay
   uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
   if (ws == nullptr) return EA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 1024, st) != cudaSuccess) {  // the status word must start at 0
+  // the status word and the in-kernel merge words start at 0
+  if (cudaMemsetAsync(ws, 0, wl.qscale_off, st) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }

@@ -2,9 +2,10 @@
 //
 // What it computes (alpamayo_tt/expert.py, TTExpert.attention_core; alpamayo_tt/EXPERT_NOTES.md,
 // "Attention over the VLM cache: masking approach"): for every (layer, kv head g) unit, the 128
-// folded query rows (q heads 2g and 2g+1 x 64 tokens, pre-roped by the prologue) attend to cache
-// rows [0, S) and to the 64 own rows, softmax(Q K^T / sqrt(128)) V. Hidden rows [S, Smax-64) are
-// never read; the mask is derived from row indices.
+// folded query rows (q heads 2g and 2g+1 x 64 tokens, RMSNormed and roped) attend to cache rows
+// [0, S) and to the 64 own rows, softmax(Q K^T / sqrt(128)) V. Hidden rows [S, Smax-64) are
+// masked; the mask is derived from row indices. With a bf16 cache the kernel also does the
+// layer's prologue itself (q/k RMSNorm, RoPE, own rows into the cache tail).
 //
 // Work decomposition: the key tiles of all units (ceil(S/128) tiles of 128 cache rows, then one
 // 64-row tile of own rows) are laid out unit-major and cut into one contiguous range per CTA
@@ -20,28 +21,37 @@
 // At the end of a segment the two warpgroups exchange their row statistics through shared
 // memory and each writes half of the output columns of the combined rows.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-3, 4-7  softmax of stream 0, 1: thread r of a warpgroup owns folded row r (= TMEM
 //              lane r); online softmax in fp32 with lazy rescaling of its TMEM accumulator; P
 //              written back to TMEM as bf16 (e4m3) over the scores it came from, and read from
 //              there by the PV MMA
-//   warp 8     K/V producer: one thread issues 3-D TMA loads of cache K/V tiles and bulk copies
-//              of the own rows (pre-swizzled in the workspace) into the ring
+//   warp 8     K/V producer: one thread issues 3-D TMA loads of the K/V tiles (cache rows, and the
+//              unit's own rows from the cache tail) into the ring
 //   warp 9     MMA: one thread issues tcgen05.mma (S = Q K^T from shared memory into the score
 //              buffer of the tile's stream; O += P V with P from TMEM and V from shared memory
 //              into the stream's accumulator) and tcgen05.commit to the barriers
-//   warp 10    Q loader: one thread brings each segment's roped Q (32 KB, pre-swizzled) into one
-//              of two buffers, one segment ahead, so the K/V stream never waits for it
+//   warps 10-11  bf16: Q and own-row prep (64 threads): per segment, RMSNorm + RoPE of the unit's
+//              raw q rows straight into one of two Q buffers, one segment ahead, so the K/V stream
+//              never waits for it; for the segment holding the own-row tile, the roped K and the V
+//              rows into the cache tail. e4m3: one thread of warp 10 bulk-copies the Q codes that
+//              the prologue kernel staged.
 // Shared memory: Q x2 (64 KB), K/V ring (160 KB), barriers, a 1 KB row-statistics exchange.
 // TMEM: 512 columns (two 128-column score/P buffers, two 128-column fp32 accumulators).
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace ea {
 namespace attn {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
+constexpr int kPrepThreads = 64;  // bf16: warps 10 and 11
 constexpr int kSoftmaxThreads = 256;
+// bf16: the producer warp and the prep warps start their memory traffic only once the softmax
+// threads have issued the loads of the first segment's raw q (named barrier 3), so that those
+// loads are not queued behind the K/V ring fill
+constexpr uint32_t kBarQFirst = 3, kBarQFirstThreads = kSoftmaxThreads + 32 + kPrepThreads;
 
 // Shared-memory layout of one CTA. bf16 cache: a K or V tile is 128 rows x 256 bytes, stored as
 // two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom;
@@ -62,7 +72,8 @@ struct Lay {
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4, B_KVEMPTY = 4 + kRing,
                        B_SFULL = 4 + 2 * kRing, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
                        B_X1 = B_ODONE + 2, B_X2 = B_X1 + 1, B_OFREE = B_X2 + 1,
-                       B_STAGED = B_OFREE + 1, B_DRAIN = B_STAGED + 2, kNumBars = B_DRAIN + 1;
+                       B_STAGED = B_OFREE + 1, B_TAILRDY = B_STAGED + 2, B_DRAIN = B_TAILRDY + 2,
+                       kNumBars = B_DRAIN + 1;
   static constexpr uint32_t SM_XCH = SM_BAR + kNumBars * 8;  // three floats per folded row
   static constexpr uint32_t SM_ROLE = SM_XCH + kRows * 12;    // in-kernel merge role
   static constexpr uint32_t SM_SFLAG = SM_ROLE + 4;            // per Q buffer: output staged
@@ -80,11 +91,12 @@ struct Lay {
   constexpr int B_QFULL = LY::B_QFULL, B_QEMPTY = LY::B_QEMPTY, B_KVFULL = LY::B_KVFULL,   \
                 B_KVEMPTY = LY::B_KVEMPTY, B_SFULL = LY::B_SFULL, B_PFULL = LY::B_PFULL,    \
                 B_ODONE = LY::B_ODONE, B_X1 = LY::B_X1, B_X2 = LY::B_X2,                   \
-                B_OFREE = LY::B_OFREE, B_STAGED = LY::B_STAGED, B_DRAIN = LY::B_DRAIN;      \
+                B_OFREE = LY::B_OFREE, B_STAGED = LY::B_STAGED, B_TAILRDY = LY::B_TAILRDY,  \
+                B_DRAIN = LY::B_DRAIN;                                                     \
   (void)kRing; (void)kSlotBytes; (void)kAtom; (void)kQB; (void)SM_Q; (void)SM_RING; (void)SM_V16; \
   (void)B_QFULL; (void)B_QEMPTY; (void)B_KVFULL; (void)B_KVEMPTY; (void)B_SFULL;            \
   (void)B_PFULL; (void)B_ODONE; (void)B_X1; (void)B_X2; (void)B_OFREE; (void)B_STAGED;          \
-  (void)B_DRAIN
+  (void)B_TAILRDY; (void)B_DRAIN
 
 constexpr uint32_t TM_S = 0;    // score buffers of streams 0 and 1 at columns 0 and 128; P(n)
                                 // overwrites the first columns of the buffer that held S(n)
@@ -121,15 +133,23 @@ struct Ctx {
 template <bool F8, class PP>
 __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
-  pdl_wait_primary();  // roped Q and the cache's own rows are written by the prologue kernel
+  pdl_wait_primary();  // e4m3: roped Q and the cache's own rows are written by the prologue kernel
   const uint64_t pol_stream = l2_policy_evict_first();  // cache tiles are read exactly once
-  uint32_t ring = 0;
+  uint32_t ring = 0, n_own = 0;
   bool ok = true;
   long long t = cx.start;
   Seg s;
   while (ok && next_seg(t, cx.end, p.T, s)) {
     const int l = s.u / kHkv, g = s.u % kHkv;
     for (int j = s.j0; j < s.j1 && ok; ++j) {
+      if (!F8 && j >= p.n_main) {
+        // bf16 own-row tile: its rows are written into the cache tail by this CTA's prep warps
+        ok = bounded_wait(cx.bar(B_TAILRDY + (n_own & 1)), (n_own >> 1) & 1, cx.abort_flag,
+                          cx.status, kErrProducerWait);
+        if (!ok) break;
+        fence_proxy_async_global();
+        ++n_own;
+      }
       for (int h = 0; h < 2; ++h) {  // h = 0: K tile, h = 1: V tile
         const uint32_t slot = ring % kRing, round = ring / kRing;
         if (round > 0) {
@@ -140,8 +160,8 @@ __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
         const uint32_t dst = cx.sbase + SM_RING + slot * kSlotBytes;
         const uint32_t fb = cx.bar(B_KVFULL + slot);
         // cache tile j: rows [128 j, 128 j + 128) of head g (keys >= S of the last one are masked,
-        // and their V rows zeroed, by the softmax); own-row tile: rows [Smax - 64, Smax), written
-        // by the prologue, the box's rows past Smax arriving as zeros
+        // and their V rows zeroed, by the softmax); own-row tile: rows [Smax - 64, Smax), the
+        // box's rows past Smax arriving as zeros
         const int row0 = j < p.n_main ? j * kKeyTile : p.Smax - kTok;
         mbar_expect_tx(fb, kSlotBytes);
         const CUtensorMap* m = h ? &p.vmap[l] : &p.kmap[l];
@@ -161,39 +181,44 @@ __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
   }
 }
 
-// ------------------------------------------------------------------------------- Q loader
+// ------------------------------------------------------------------- staged-output store
+// A segment that produced bf16 output rows staged them in its Q buffer (row-major, the 32 KB
+// block of out that its unit u owns): one thread stores them with one bulk copy and waits until
+// the copy has read the buffer, which may then be refilled.
+template <bool F8, class PP>
+__device__ __forceinline__ bool drain_staged(const PP& p, const Ctx& cx, int sg, int u) {
+  EA_LAYOUT_ALIASES;
+  const int b = sg & 1;
+  volatile uint32_t* sflag = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_SFLAG);
+  if (!bounded_wait(cx.bar(B_STAGED + b), (sg >> 1) & 1, cx.abort_flag, cx.status, kErrProducerWait))
+    return false;
+  if (sflag[b] != 0u) {
+    bulk_store(p.out[u / kHkv] + static_cast<size_t>(u % kHkv) * kRows * kD, cx.sbase + SM_Q + b * kQB,
+               kRows * kD * 2);
+    bulk_commit();
+  }
+  bulk_wait_read0();
+  return true;
+}
+
+// ------------------------------------------------------------------------ Q loader (e4m3)
+// One thread brings each segment's roped e4m3 Q (high and low codes, written by the prologue
+// kernel) into one of the two Q buffers, one segment ahead.
 template <bool F8, class PP>
 __device__ __noinline__ void q_loader(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
   const uint64_t pol_keep = l2_policy_evict_last();
-  volatile uint32_t* sflag = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_SFLAG);
   int seg = 0;
   int hist_u[2] = {0, 0};  // units of the last two segments, by Q buffer
   bool ok = true;
   long long t = cx.start;
   Seg s;
-  // A segment that produced bf16 output rows staged them in its Q buffer (row-major, the 32 KB
-  // block of out that its unit owns): store them with one bulk copy, and let the buffer be
-  // refilled only once the copy has read it.
-  auto drain_staged = [&](int sg) -> bool {
-    const int b = sg & 1;
-    if (!bounded_wait(cx.bar(B_STAGED + b), (sg >> 1) & 1, cx.abort_flag, cx.status, kErrProducerWait))
-      return false;
-    if (sflag[b] != 0u) {
-      const int u = hist_u[b];
-      bulk_store(p.out[u / kHkv] + static_cast<size_t>(u % kHkv) * kRows * kD,
-                 cx.sbase + SM_Q + b * kQB, kRows * kD * 2);
-      bulk_commit();
-    }
-    bulk_wait_read0();
-    return true;
-  };
   while (ok && next_seg(t, cx.end, p.T, s)) {
     const int qb = seg & 1;
     if (seg >= 2) {  // segment seg-2 has finished with buffer qb (its last QK and its output)
       ok = bounded_wait(cx.bar(B_QEMPTY + qb), ((seg >> 1) - 1) & 1, cx.abort_flag, cx.status,
                         kErrProducerWait);
-      if (ok) ok = drain_staged(seg - 2);
+      if (ok) ok = drain_staged<F8>(p, cx, seg - 2, hist_u[qb]);
     }
     if (!ok) break;
     hist_u[qb] = s.u;
@@ -202,7 +227,7 @@ __device__ __noinline__ void q_loader(const PP& p, const Ctx& cx) {
               cx.bar(B_QFULL + qb), pol_keep);
     ++seg;
   }
-  for (int sg = seg >= 2 ? seg - 2 : 0; ok && sg < seg; ++sg) ok = drain_staged(sg);
+  for (int sg = seg >= 2 ? seg - 2 : 0; ok && sg < seg; ++sg) ok = drain_staged<F8>(p, cx, sg, hist_u[sg & 1]);
   bulk_wait_all0();
   if (!ok) {  // let the last load into each buffer land
     for (int b = 0; b < 2; ++b) {
@@ -211,6 +236,323 @@ __device__ __noinline__ void q_loader(const PP& p, const Ctx& cx) {
       if (last >= 0 && !drain_wait(cx.bar(B_QFULL + b), (last >> 1) & 1))
         atomicOr(cx.status, kErrDrain);
     }
+  }
+}
+
+// ---------------------------------------------------------------- Q and own-row prep (bf16)
+// alpamayo_tt/expert.py, TTExpert.layer and TTExpert.set_context: per-head RMSNorm of q and k
+// (eps 1e-6, q_norm / k_norm gains), HF rotate_half RoPE at positions t + rope_delta + S, and the
+// own K/V rows written into the cache at rows [Smax - 64, Smax).
+//
+// Rows are handled by octets of threads: lane i of an octet holds channels [8i, 8i + 8) and
+// their RoPE partners [64 + 8i, 64 + 8i + 8), so that the rotation is in-thread and a row's norm
+// takes three shuffles; every global access is a 16-byte vector access. The roped Q goes to a Q
+// buffer in the 128-byte-swizzled K-major layout the QK MMA reads.
+//
+// The first segment's Q is prepared by the 256 softmax threads, which have nothing else to do
+// until its first scores; later segments' Q, one segment ahead of the MMA, and the own K/V rows
+// of the segment that holds a unit's own-row tile are prepared by warps 10 and 11. The loops
+// over rows are straight-line code, so that the rows' load, shuffle and arithmetic latencies
+// overlap.
+
+// Roped row (hh, tok) of q heads 2g, 2g + 1 from its raw chunks: stored into the Q buffer at
+// folded row hh * 64 + tok; returns the two output chunks.
+__device__ __forceinline__ void q_row_to_smem(uint32_t qbuf, int hh, int tok, int i, const uint4 lo,
+                                              const uint4 hi, const float (&gl)[8],
+                                              const float (&gh)[8], const float (&cs)[8],
+                                              const float (&sn)[8], uint4& ql, uint4& qh) {
+  float xl[8], xh[8], yl[8], yh[8];
+  unpack_bf16x8(lo, xl);
+  unpack_bf16x8(hi, xh);
+  norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
+  ql = pack8(yl, false);
+  qh = pack8(yh, false);
+  const int r = hh * kTok + tok;
+  st_shared_v4(qbuf + swz_off(r, i, kQTileBytes / 2), ql.x, ql.y, ql.z, ql.w);
+  st_shared_v4(qbuf + swz_off(r, i + 8, kQTileBytes / 2), qh.x, qh.y, qh.z, qh.w);
+}
+
+// cos/sin of token tok at the eight frequencies [8i, 8i + 8).
+template <class PP>
+__device__ __forceinline__ void token_cos_sin(const PP& p, int tok, int dl, float (&cs)[8],
+                                              float (&sn)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_base + tok, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[e], sn[e]);
+}
+
+// The first segment's Q by the 256 softmax threads (32 octets, octet oc: tokens oc and oc + 32
+// of both heads), into Q buffer 0, and, when that segment holds its unit's own-row tile, the
+// unit's roped K rows and V rows into the cache tail; one thread then signals QFULL (and
+// TAILRDY). A CTA's first segment can be short, so that its own rows are needed early.
+template <class PP>
+__device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
+  long long t = cx.start;
+  Seg s;
+  if (!next_seg(t, cx.end, p.T, s)) {
+    bar_arrive(kBarQFirst, kBarQFirstThreads);
+    return;
+  }
+  const int oc = threadIdx.x >> 3, i = threadIdx.x & 7;
+  const int dl = 8 * i, dh = 64 + 8 * i;
+  const int l = s.u / kHkv, g = s.u % kHkv;
+  const bool own = s.j1 == p.T;
+  const __nv_bfloat16* qsrc = p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD + oc * kD;
+  // both tokens' rows are requested at once (and the own k and v rows)
+  uint4 raw[2][2][2];  // [token][head][lo, hi]
+#pragma unroll
+  for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __nv_bfloat16* row = qsrc + static_cast<size_t>(hh * kTok + 32 * tt) * kD;
+      raw[tt][hh][0] = *reinterpret_cast<const uint4*>(row + dl);
+      raw[tt][hh][1] = *reinterpret_cast<const uint4*>(row + dh);
+    }
+  uint4 kv[2][2][2];  // [token][k, v][lo, hi]
+  const size_t unit_rows = static_cast<size_t>(g) * kTok * kD;
+  if (own) {
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      const size_t ro = unit_rows + static_cast<size_t>(oc + 32 * tt) * kD;
+      kv[tt][0][0] = *reinterpret_cast<const uint4*>(p.k_raw[l] + ro + dl);
+      kv[tt][0][1] = *reinterpret_cast<const uint4*>(p.k_raw[l] + ro + dh);
+      kv[tt][1][0] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dl);
+      kv[tt][1][1] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dh);
+    }
+  }
+  bar_arrive(kBarQFirst, kBarQFirstThreads);  // the loads are issued: the K/V stream may start
+  float gl[8], gh[8];
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gl);
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dh), gh);
+  const uint32_t qbuf = cx.sbase + Lay<false>::SM_Q;
+  // the optional roped q output is written by the CTA that holds the unit's own-row tile
+  __nv_bfloat16* qr0 = own ? p.q_rope[l] : nullptr;
+  if (qr0 != nullptr) qr0 += (static_cast<size_t>(2 * g) * kTok + oc) * kD;
+  // one token per pass (a short loop body, which stays in the instruction cache)
+#pragma unroll 1
+  for (int tt = 0; tt < 2; ++tt) {
+    uint4 cur[2][2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      cur[hh][0] = raw[0][hh][0];
+      cur[hh][1] = raw[0][hh][1];
+      raw[0][hh][0] = raw[1][hh][0];
+      raw[0][hh][1] = raw[1][hh][1];
+    }
+    const int tok = oc + 32 * tt;
+    float cs[8], sn[8];
+    token_cos_sin(p, tok, dl, cs, sn);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint4 ql, qh;
+      q_row_to_smem(qbuf, hh, tok, i, cur[hh][0], cur[hh][1], gl, gh, cs, sn, ql, qh);
+      if (qr0 != nullptr) {
+        __nv_bfloat16* qr = qr0 + static_cast<size_t>(hh * kTok + 32 * tt) * kD;
+        *reinterpret_cast<uint4*>(qr + dl) = ql;
+        *reinterpret_cast<uint4*>(qr + dh) = qh;
+      }
+    }
+  }
+  fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
+  bar_sync(2, kSoftmaxThreads);
+  if (threadIdx.x == 0) mbar_arrive(cx.bar(Lay<false>::B_QFULL));
+  if (own) {
+    // K rows: RMSNorm with the k_norm gain and RoPE; V rows as given; into cache rows
+    // Smax - 64 + t of head g
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gl);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gh);
+    const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
+#pragma unroll 1
+    for (int tt = 0; tt < 2; ++tt) {
+      uint4 cur[2][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        cur[h][0] = kv[0][h][0];
+        cur[h][1] = kv[0][h][1];
+        kv[0][h][0] = kv[1][h][0];
+        kv[0][h][1] = kv[1][h][1];
+      }
+      const int tok = oc + 32 * tt;
+      const size_t ro = tail + static_cast<size_t>(tok) * kD;
+      float cs[8], sn[8], xl[8], xh[8], yl[8], yh[8];
+      token_cos_sin(p, tok, dl, cs, sn);
+      unpack_bf16x8(cur[0][0], xl);
+      unpack_bf16x8(cur[0][1], xh);
+      norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = pack8(yl, false);
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = pack8(yh, false);
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = cur[1][0];
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = cur[1][1];
+    }
+    fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
+    bar_sync(2, kSoftmaxThreads);
+    if (threadIdx.x == 0) mbar_arrive(cx.bar(Lay<false>::B_TAILRDY));
+  }
+}
+
+// Warps 10 and 11 (64 threads, 8 octets; octet oc: tokens oc + 8 it, it < 8). A pass handles
+// one token, with the raw rows of the next kAhead tokens already requested.
+constexpr int kAhead = 1;
+template <class PP>
+__device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
+  constexpr bool F8 = false;
+  EA_LAYOUT_ALIASES;
+  const int px = static_cast<int>(threadIdx.x) - (kThreads - kPrepThreads);
+  const int oc = px >> 3, i = px & 7;
+  const int dl = 8 * i, dh = 64 + 8 * i;
+  int hist_u[2] = {0, 0};  // units of the last two segments, by Q buffer
+  int seg = 0, n_own = 0, cur_l = -1;
+  float gql[8], gqh[8];
+  bool ok = true;
+  long long t = cx.start;
+  Seg s;
+  // raw rows of a segment's unit into L2 ahead of their use: q (both heads, 32 KB) unless it is
+  // the first segment (read at once by the softmax threads), and k and v (16 KB each) if the
+  // segment holds the own-row tile
+  auto prefetch = [&](const Seg& x, bool q) {
+    const int l = x.u / kHkv, g = x.u % kHkv;
+    if (q) prefetch_l2_bulk(p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD, 2 * kTok * kD * 2);
+    if (x.j1 == p.T) {
+      prefetch_l2_bulk(p.k_raw[l] + static_cast<size_t>(g) * kTok * kD, kTok * kD * 2);
+      prefetch_l2_bulk(p.v_raw[l] + static_cast<size_t>(g) * kTok * kD, kTok * kD * 2);
+    }
+  };
+  while (next_seg(t, cx.end, p.T, s)) {
+    const int qb = seg & 1;
+    bool good = true;
+    if (px == 0) {
+      long long t2 = t;
+      Seg s2;
+      if (next_seg(t2, cx.end, p.T, s2)) prefetch(s2, true);
+      if (seg >= 2) {
+        // segment seg-2 has finished with buffer qb: its last QK is done and its output stored
+        good = bounded_wait(cx.bar(B_QEMPTY + qb), ((seg >> 1) - 1) & 1, cx.abort_flag, cx.status,
+                            kErrProducerWait);
+        if (good) good = drain_staged<F8>(p, cx, seg - 2, hist_u[qb]);
+      }
+    }
+    ok = bar_sync_and(1, kPrepThreads, good);
+    if (!ok) break;
+    hist_u[qb] = s.u;
+    const int l = s.u / kHkv, g = s.u % kHkv;
+    const bool own = s.j1 == p.T;  // this segment holds the unit's own-row tile
+    if (seg > 0) {
+      if (l != cur_l) {
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gql);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dh), gqh);
+        cur_l = l;
+      }
+      const __nv_bfloat16* qsrc = p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD;
+      __nv_bfloat16* qr0 = own ? p.q_rope[l] : nullptr;  // optional; one CTA per unit writes it
+      if (qr0 != nullptr) qr0 += static_cast<size_t>(2 * g) * kTok * kD;
+      const uint32_t qbuf = cx.sbase + SM_Q + qb * kQB;
+      // one token (both heads' rows) per pass, with the rows of the next kAhead tokens in flight
+      // (rotated through registers): a short loop body, which stays in the instruction cache
+      uint4 nx[kAhead][2][2];
+#pragma unroll
+      for (int a = 0; a < kAhead; ++a)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const __nv_bfloat16* row = qsrc + static_cast<size_t>(hh * kTok + oc + 8 * a) * kD;
+          nx[a][hh][0] = *reinterpret_cast<const uint4*>(row + dl);
+          nx[a][hh][1] = *reinterpret_cast<const uint4*>(row + dh);
+        }
+#pragma unroll 1
+      for (int it = 0; it < 8; ++it) {
+        const int tok = oc + 8 * it;
+        uint4 cur[2][2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          cur[hh][0] = nx[0][hh][0];
+          cur[hh][1] = nx[0][hh][1];
+#pragma unroll
+          for (int a = 0; a + 1 < kAhead; ++a) {
+            nx[a][hh][0] = nx[a + 1][hh][0];
+            nx[a][hh][1] = nx[a + 1][hh][1];
+          }
+        }
+        const int nt = oc + 8 * (it + kAhead < 8 ? it + kAhead : 7);  // past the end: token 7 again
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const __nv_bfloat16* row = qsrc + static_cast<size_t>(hh * kTok + nt) * kD;
+          nx[kAhead - 1][hh][0] = *reinterpret_cast<const uint4*>(row + dl);
+          nx[kAhead - 1][hh][1] = *reinterpret_cast<const uint4*>(row + dh);
+        }
+        float cs[8], sn[8];
+        token_cos_sin(p, tok, dl, cs, sn);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint4 ql, qh;
+          q_row_to_smem(qbuf, hh, tok, i, cur[hh][0], cur[hh][1], gql, gqh, cs, sn, ql, qh);
+          if (qr0 != nullptr) {
+            __nv_bfloat16* qr = qr0 + static_cast<size_t>(hh * kTok + tok) * kD;
+            *reinterpret_cast<uint4*>(qr + dl) = ql;
+            *reinterpret_cast<uint4*>(qr + dh) = qh;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
+      bar_sync(1, kPrepThreads);
+      if (px == 0) mbar_arrive(cx.bar(B_QFULL + qb));
+    }
+    if (own && seg == 0) ++n_own;  // written by the softmax threads
+    if (own && seg > 0) {
+      // K rows: RMSNorm with the k_norm gain and RoPE; V rows: as given; both into cache rows
+      // Smax - 64 + t of head g, which the producer then loads as the own-row tile
+      float gkl[8], gkh[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gkl);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gkh);
+      const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
+      const __nv_bfloat16* ksrc = p.k_raw[l] + static_cast<size_t>(g) * kTok * kD;
+      const __nv_bfloat16* vsrc = p.v_raw[l] + static_cast<size_t>(g) * kTok * kD;
+      __nv_bfloat16* kdst = p.kc[l] + tail;
+      __nv_bfloat16* vdst = p.vc[l] + tail;
+      uint4 nk[kAhead][2], nv[kAhead][2];  // rows of the next kAhead tokens, in flight
+#pragma unroll
+      for (int a = 0; a < kAhead; ++a) {
+        const size_t ro = static_cast<size_t>(oc + 8 * a) * kD;
+        nk[a][0] = *reinterpret_cast<const uint4*>(ksrc + ro + dl);
+        nk[a][1] = *reinterpret_cast<const uint4*>(ksrc + ro + dh);
+        nv[a][0] = *reinterpret_cast<const uint4*>(vsrc + ro + dl);
+        nv[a][1] = *reinterpret_cast<const uint4*>(vsrc + ro + dh);
+      }
+#pragma unroll 1
+      for (int it = 0; it < 8; ++it) {
+        const int tok = oc + 8 * it;
+        const uint4 k0 = nk[0][0], k1 = nk[0][1], v0 = nv[0][0], v1 = nv[0][1];
+#pragma unroll
+        for (int a = 0; a + 1 < kAhead; ++a) {
+          nk[a][0] = nk[a + 1][0];
+          nk[a][1] = nk[a + 1][1];
+          nv[a][0] = nv[a + 1][0];
+          nv[a][1] = nv[a + 1][1];
+        }
+        const size_t rn = static_cast<size_t>(oc + 8 * (it + kAhead < 8 ? it + kAhead : 7)) * kD;
+        nk[kAhead - 1][0] = *reinterpret_cast<const uint4*>(ksrc + rn + dl);
+        nk[kAhead - 1][1] = *reinterpret_cast<const uint4*>(ksrc + rn + dh);
+        nv[kAhead - 1][0] = *reinterpret_cast<const uint4*>(vsrc + rn + dl);
+        nv[kAhead - 1][1] = *reinterpret_cast<const uint4*>(vsrc + rn + dh);
+        const size_t ro = static_cast<size_t>(tok) * kD;
+        float cs[8], sn[8], xl[8], xh[8], yl[8], yh[8];
+        token_cos_sin(p, tok, dl, cs, sn);
+        unpack_bf16x8(k0, xl);
+        unpack_bf16x8(k1, xh);
+        norm_rope(xl, xh, gkl, gkh, cs, sn, yl, yh);
+        *reinterpret_cast<uint4*>(kdst + ro + dl) = pack8(yl, false);
+        *reinterpret_cast<uint4*>(kdst + ro + dh) = pack8(yh, false);
+        *reinterpret_cast<uint4*>(vdst + ro + dl) = v0;
+        *reinterpret_cast<uint4*>(vdst + ro + dh) = v1;
+      }
+      fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
+      bar_sync(1, kPrepThreads);
+      if (px == 0) mbar_arrive(cx.bar(B_TAILRDY + (n_own & 1)));
+      ++n_own;
+    }
+    ++seg;
+  }
+  if (px == 0) {
+    for (int sg = seg >= 2 ? seg - 2 : 0; ok && sg < seg; ++sg)
+      ok = drain_staged<F8>(p, cx, sg, hist_u[sg & 1]);
+    bulk_wait_all0();
   }
 }
 
@@ -596,6 +938,11 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
           } else {
             rl = bounded_flag_wait(usync + 1, cx.abort_flag, cx.status, kErrMergeWait) ? 1u : 2u;
           }
+          if (rl == 1u) {
+            // both parts are done with the unit's words: leave them zero for the next grid
+            reinterpret_cast<volatile uint32_t*>(usync)[0] = 0u;
+            reinterpret_cast<volatile uint32_t*>(usync)[1] = 0u;
+          }
         }
         *role = rl;
         mbar_arrive(cx.bar(B_X1));
@@ -754,7 +1101,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(cx.bar(B_QFULL + b), 1);
+      mbar_init(cx.bar(B_QFULL + b), 1);  // e4m3: the bulk copy; bf16: one thread per preparing group
+      mbar_init(cx.bar(B_TAILRDY + b), 1);
       mbar_init(cx.bar(B_QEMPTY + b), 1);
       mbar_init(cx.bar(B_SFULL + b), 1);
       mbar_init(cx.bar(B_PFULL + b), 128);
@@ -782,17 +1130,23 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + LY::SM_TMEM);
-  // Everything below depends on the prologue (staged Q and own rows, zeroed arrival counts).
+  // Everything below reads what earlier kernels in the stream wrote (layer inputs, caches; e4m3:
+  // the prologue's staged Q and own rows).
   pdl_wait_primary();
 
   if (warp < 8) {
+    if constexpr (!F8) first_q_prep(p, cx);
     softmax_warps<F8>(p, cx);
   } else if (warp == 8) {
+    if constexpr (!F8) bar_sync(kBarQFirst, kBarQFirstThreads);
     if (lane == 0) producer<F8>(p, cx);
   } else if (warp == 9) {
     if (lane == 0) mma_issuer<F8>(p, cx);
+  } else if constexpr (F8) {
+    if (warp == 10 && lane == 0) q_loader<F8>(p, cx);
   } else {
-    if (lane == 0) q_loader<F8>(p, cx);
+    bar_sync(kBarQFirst, kBarQFirstThreads);
+    prep_warps(p, cx);
   }
 
   tc_fence_before();

@@ -46,7 +46,7 @@ enum : uint32_t {
 // ------------------------------------------------------------------------- workspace layout
 //   [0, 1024)                    status word (first 4 bytes), rest reserved
 //   sync    n_layers * 8 * 2 uint32  per unit: arrival count and partial-ready flag of the
-//                                   in-kernel merge of two-part units (zeroed by the prologue)
+//                                   in-kernel merge of two-part units (zero between calls)
 //   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
 //   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
 //   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; e4m3
@@ -108,6 +108,18 @@ template <int CAP>
 struct AttnParams {
   CUtensorMap kmap[CAP];  // all Smax rows of K: dims {128, Smax, 8}, box {64 (e4m3: 128), 128, 1}
   CUtensorMap vmap[CAP];
+  // bf16: the layer's inputs, normed and roped inside the attention kernel
+  const __nv_bfloat16* q_raw[CAP];
+  const __nv_bfloat16* k_raw[CAP];
+  const __nv_bfloat16* v_raw[CAP];
+  const __nv_bfloat16* q_gamma[CAP];
+  const __nv_bfloat16* k_gamma[CAP];
+  __nv_bfloat16* q_rope[CAP];  // optional
+  __nv_bfloat16* kc[CAP];      // the caches, whose rows [Smax-64, Smax) the kernel writes
+  __nv_bfloat16* vc[CAP];
+  float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
+  float inv_lo[kD / 2];
+  int rope_base;         // S + rope_delta: token t sits at position rope_base + t
   __nv_bfloat16* out[CAP];
   const float* ks[CAP];      // FP8: block scales [8][Smax/128 + 1] (else null)
   const float* vs[CAP];

@@ -31,7 +31,9 @@
  *
  * Errors: argument errors return before anything is launched. EA_ERR_CUDA reports a failed
  * launch. A kernel that gives up a bounded wait records EA_ERR_TIMEOUT in the workspace's
- * status word, which expert_attn_read_status returns.
+ * status word, which expert_attn_read_status returns; the outputs of that call are then
+ * undefined, and the workspace must be cleared again with expert_attn_workspace_init before
+ * its next use.
  */
 #ifndef EXPERT_ATTN_H
 #define EXPERT_ATTN_H
@@ -79,7 +81,9 @@ typedef struct {
  * its first use, cleared with expert_attn_workspace_init. */
 size_t expert_attn_workspace_size(int n_layers, int Smax, int kv_dtype);
 
-/* Clears the workspace's status word (asynchronous on stream). */
+/* Clears the workspace's status word and the per-unit words of the attention kernel's
+ * in-kernel merge (asynchronous on stream). Every call leaves those words zero again unless it
+ * reports EA_ERR_TIMEOUT. */
 int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1 + 2 only (alpamayo_tt/expert.py, TTExpert.layer: q/k rms_norm, rotary_embedding_hf,
@@ -89,23 +93,26 @@ int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t str
 int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 
-/* Steps 1-3 for one layer (the unit TTExpert.layer_fn can hand to a fused kernel): prologue,
- * then split-KV attention on the tensor cores, then the log-sum-exp merge of the key ranges
- * that were split across SMs; writes a->out. */
+/* Steps 1-3 for one layer (the unit TTExpert.layer_fn can hand to a fused kernel): split-KV
+ * attention on the tensor cores, whose kernel also does steps 1 and 2 for a bf16 cache (an e4m3
+ * cache runs the prologue kernel first), then the log-sum-exp merge of the key ranges that were
+ * split across SMs over more than two CTAs; writes a->out and, if not NULL, a->q_rope. */
 int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
                       void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1-3 for n_layers independent layers in one call (the 64 layers of one Euler step,
  * alpamayo_tt/expert.py, TTExpert._forward_dev), all with the same S, Smax and rope_delta.
- * layers is a HOST array of n_layers entries. Launches three kernels per 64 layers (the merge
- * is skipped when no unit is split). */
+ * layers is a HOST array of n_layers entries. Per 64 layers it launches the attention kernel,
+ * after the prologue kernel for an e4m3 cache and before the merge kernel when some unit is
+ * split over more than two CTAs (two-part units are merged inside the attention kernel). */
 int expert_attn_layers(const ea_layer_args* layers, int n_layers, int S, int Smax, int rope_delta,
                        int kv_dtype, void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* As expert_attn_layers, and records four cudaEvent_t (passed as void*, each may be NULL) on
- * the stream, around the first 64 layers: before the prologue, before the attention kernel,
- * after it, and after the merge kernel. Recording events between the kernels removes their
- * launch overlap; use it to time the kernels. */
+ * the stream, around the first 64 layers: before the prologue kernel, before the attention
+ * kernel (right after the first event for a bf16 cache, which has no prologue kernel), after
+ * it, and after the merge kernel. Recording events between the kernels removes their launch
+ * overlap; use it to time the kernels. */
 int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                 int rope_delta, int kv_dtype, void* workspace, size_t ws_bytes,
                                 ea_stream_t stream, void* const events[4]);

@@ -157,3 +157,76 @@ def test_64_layer_step_full_size_sampled(S):
         assert_close(f64(Ls[l].out), oracle_layer(host)["out"], f"S={S} layer {l}")
     for L in Ls:
         assert torch.isfinite(L.out.float()).all()
+
+
+def test_layer_writes_q_rope_and_tail_itself():
+    """With a bf16 cache the attention kernel does the prologue: its roped q and cache tail are
+    those of the oracle (within a bf16 step) and the same bits as the standalone prologue's."""
+    S, Smax, delta = 700, 1024, -5
+    x = layer_inputs(21, S, Smax)
+    A = to_dev(x, want_q_rope=True)
+    B = to_dev(x, want_q_rope=True)
+    k_before, v_before = A.k_cache.clone(), A.v_cache.clone()
+    ws = ea.alloc_workspace(1, Smax)
+    ea.expert_attn_layer(A, S, Smax, delta, ea.EA_KV_BF16, ws)
+    ea.expert_attn_prologue(B, S, Smax, delta, ea.EA_KV_BF16, ws)
+    torch.cuda.synchronize()
+    check_status(ws)
+    r = oracle_layer(x, rope_delta=delta)
+    q = f64(A.q_rope)
+    assert np.all(np.abs(q - r["q"]) <= bf16_ulp(r["q"]) + 1e-5)
+    k_tail = f64(A.k_cache[:, Smax - 64:])
+    assert np.all(np.abs(k_tail - r["k"]) <= bf16_ulp(r["k"]) + 1e-5)
+    assert torch.equal(A.v_cache[:, Smax - 64:], x.v_raw.cuda())
+    assert torch.equal(A.q_rope.view(torch.int16), B.q_rope.view(torch.int16))
+    assert torch.equal(A.k_cache.view(torch.int16), B.k_cache.view(torch.int16))
+    assert torch.equal(A.k_cache[:, :Smax - 64], k_before[:, :Smax - 64])
+    assert torch.equal(A.v_cache[:, :Smax - 64], v_before[:, :Smax - 64])
+    assert_close(f64(A.out), r["out"])
+
+
+def test_q_rope_of_every_layer_in_a_split_call():
+    """Eight layers over few CTAs: units are cut between CTAs, and exactly one CTA per unit (the
+    one holding its own-row tile) writes that unit's roped q and cache tail."""
+    S, Smax, n = 900, 1024, 8
+    xs = [layer_inputs(600 + l, S, Smax) for l in range(n)]
+    Ls = [to_dev(x, want_q_rope=True) for x in xs]
+    ws = ea.alloc_workspace(n, Smax)
+    ea.expert_attn_set_splits(23)
+    try:
+        ea.expert_attn_layers(Ls, S, Smax, 2, ea.EA_KV_BF16, ws)
+        torch.cuda.synchronize()
+    finally:
+        ea.expert_attn_set_splits(0)
+    check_status(ws)
+    for x, L in zip(xs, Ls):
+        r = oracle_layer(x, rope_delta=2)
+        assert np.all(np.abs(f64(L.q_rope) - r["q"]) <= bf16_ulp(r["q"]) + 1e-5)
+        assert np.all(np.abs(f64(L.k_cache[:, Smax - 64:]) - r["k"]) <= bf16_ulp(r["k"]) + 1e-5)
+        assert_close(f64(L.out), r["out"])
+
+
+def test_repeated_calls_leave_merge_words_zero():
+    """Two-part units are merged inside the attention kernel through per-unit words in the
+    workspace; each call leaves them zero, so back-to-back calls on one workspace agree bit for
+    bit without re-initialising it."""
+    S, Smax, n = 1024, 2048, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    parts = ea.split_parts(n, S, sms)
+    assert parts and all(k == 2 for _, k in parts)  # the in-kernel merge is taken
+    dev = torch.device("cuda")
+    xs = [layer_inputs_on_device(9000 + l, S, Smax, dev) for l in range(n)]
+    Ls = [ea.LayerBuffers(q_raw=x.q_raw, k_raw=x.k_raw, v_raw=x.v_raw, q_gamma=x.q_gamma,
+                          k_gamma=x.k_gamma, k_cache=x.k_cache, v_cache=x.v_cache,
+                          out=torch.empty(16, 64, 128, dtype=torch.bfloat16, device=dev)) for x in xs]
+    ws = ea.alloc_workspace(n, Smax)
+    outs = []
+    for _ in range(3):
+        ea.expert_attn_layers(Ls, S, Smax, 0, ea.EA_KV_BF16, ws)
+        torch.cuda.synchronize()
+        check_status(ws)
+        assert int(ws[1024:1024 + n * 8 * 2 * 4].count_nonzero()) == 0
+        outs.append(torch.stack([L.out for L in Ls]).clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    host = type(xs[5])(**{k: (v.cpu() if torch.is_tensor(v) else v) for k, v in xs[5].__dict__.items()})
+    assert_close(f64(Ls[5].out), oracle_layer(host)["out"])
