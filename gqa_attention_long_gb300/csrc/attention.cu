@@ -982,8 +982,11 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
     tc_fence_after();
     // ---- this warpgroup's 64 columns of both accumulators, combined (a second part starts from
     // the first part's weighted partial)
-    const float* pother =
-        p.part_o + ((static_cast<size_t>(other) * 2 + other_slot) * kRows + r) * kD + 64 * k;
+    // partials are stored chunk-major (float4 chunk c of row r at index c * 128 + r), so that a
+    // warp's 32 rows of one chunk are 512 contiguous bytes
+    const float4* pother = reinterpret_cast<const float4*>(p.part_o) +
+                           (static_cast<size_t>(other) * 2 + other_slot) * kPartChunks * kRows +
+                           static_cast<size_t>(16 * k) * kRows + r;
     float o[2][32];
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
@@ -991,7 +994,7 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
       if (second) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(pother + ch * 32) + q);
+          const float4 v = __ldcg(pother + static_cast<size_t>(8 * ch + q) * kRows);
           o[ch][4 * q] = v.x * w2;
           o[ch][4 * q + 1] = v.y * w2;
           o[ch][4 * q + 2] = v.z * w2;
@@ -1052,12 +1055,15 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
         st_shared_v4(srow + 16 * (q ^ m), w[q][0], w[q][1], w[q][2], w[q][3]);
       fence_proxy_async_smem();  // visible to the bulk copy (async proxy)
     } else {
-      float* po = p.part_o + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r) * kD + 64 * k;
+      // chunk-major (see above): each store instruction of a warp writes 512 contiguous bytes
+      float4* po = reinterpret_cast<float4*>(p.part_o) +
+                   (static_cast<size_t>(blockIdx.x) * 2 + slot) * kPartChunks * kRows +
+                   static_cast<size_t>(16 * k) * kRows + r;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(po + ch * 32 + 4 * q) =
+          po[static_cast<size_t>(8 * ch + q) * kRows] =
               make_float4(o[ch][4 * q], o[ch][4 * q + 1], o[ch][4 * q + 2], o[ch][4 * q + 3]);
       if (k == 0) p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = lse_row;
       if (fused) __threadfence();  // the partial is visible before the flag

@@ -23,6 +23,7 @@ constexpr int kMaxLayersPerLaunch = 64;
 // that their launches carry ~2 KB of parameters instead of ~19 KB.
 constexpr int kSmallCap = 8;
 constexpr int kScaleBlock = 128;  // FP8 scale granularity (rows)
+constexpr int kPartChunks = kD / 4;  // float4 chunks per row of a partial output
 
 // Bytes of one staged operand tile in the 128-byte-swizzled K-major layout: two 64-column
 // halves ("atoms"), each [rows][128 bytes]; inside every 8-row group of 1024 bytes the 16-byte
@@ -51,7 +52,8 @@ enum : uint32_t {
 //   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
 //   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; e4m3
 //                                 high and low codes)
-//   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised)
+//   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised), per slot chunk-major:
+//                                     float4 chunk c (columns 4c .. 4c+3) of row r at c * 128 + r
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
 struct WsLayout {
   size_t sync_off, qscale_off, svref_off, q_off, part_o_off, part_lse_off, total;

@@ -7,30 +7,33 @@
 //   M = max_s lse_s,   w_s = 2^(lse_s - M) / sum_t 2^(lse_t - M),   out = sum_s w_s O_s,
 // written as bf16 to out[layer][2g + r/64][r%64][:] (folded row r of kv head g).
 //
-// One warp per folded row; lane j owns columns [4j, 4j+4). Parts are taken kBatch at a time
-// (8, or 24 when a unit has more than 8 parts): every lane requests the batch's lse values
-// (broadcast loads) together with its float4s, so a row costs one round trip to L2 per batch,
-// and the running max and weight sum are carried across batches (a unit has at most as many
-// parts as there are CTAs: a single layer spread over every SM has ~20, one batch of 24).
+// Partials are stored chunk-major (float4 chunk c of row r at c * 128 + r). A CTA of 128
+// threads takes one split unit and one chunk (4 output columns): thread r owns row r, so that
+// every load instruction of a warp reads 512 contiguous bytes. Parts are taken kBatch at a time
+// (8, or 24 when a unit has more than 8), each thread requesting the batch's lse values and
+// chunks together (indices past the last part are clamped to it and weighted 0), so that a row
+// costs one round trip to L2 per batch; the running max and weight sum are carried across
+// batches (a unit has at most as many parts as there are CTAs: a single layer spread over every
+// SM has ~20, one batch of 24).
 #include "internal.cuh"
 #include "ptx.cuh"
 
 namespace ea {
 
-constexpr int kMergeWarps = 4;  // rows per CTA
+constexpr int kMergeThreads = kRows;  // one thread per folded row
 
 template <int CAP, int kBatch>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ MergeParams<CAP> p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams<CAP> p) {
   // Launched programmatically after the attention kernel: let the next kernel in the stream set
   // up, then wait until every partial of the attention grid is written and visible.
   pdl_launch_dependents();
   pdl_wait_primary();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x / (kRows / kMergeWarps);
-  const int r = (blockIdx.x % (kRows / kMergeWarps)) * kMergeWarps + warp;
+  const int split = blockIdx.x / kPartChunks;
+  const int c = blockIdx.x % kPartChunks;  // the chunk (columns 4c .. 4c + 3) of this CTA
+  const int r = threadIdx.x;
   if (split >= p.n_split) return;
   const SplitUnit su = p.unit[split];
-  const int u = su.u, c0 = su.c0, nparts = su.nparts;
+  const int u = su.u, nparts = su.nparts;
 
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -39,16 +42,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
     float4 o[kBatch];
 #pragma unroll
     for (int e = 0; e < kBatch; ++e) {
-      if (q0 + e < nparts) {
-        const int q = q0 + e;
-        const size_t pr = (static_cast<size_t>(c0 + q) * 2 + (q == 0 ? su.slot0 : 0)) * kRows + r;
-        lse[e] = __ldcg(p.part_lse + pr);
-        o[e] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * kD) + lane);
-      } else {
-        lse[e] = -INFINITY;
-        o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      const int q = min(q0 + e, nparts - 1);
+      // part q's slot: 2 (c0 + q), except the first part's, which is 2 c0 + slot0
+      const size_t sl = static_cast<size_t>(su.c0 + q) * 2 + (q == 0 ? su.slot0 : 0);
+      lse[e] = __ldcg(p.part_lse + sl * kRows + r);
+      o[e] = __ldcg(reinterpret_cast<const float4*>(p.part_o) + (sl * kPartChunks + c) * kRows + r);
     }
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e)
+      if (q0 + e >= nparts) lse[e] = -INFINITY;  // padding: weight 0
     float mb = lse[0];
 #pragma unroll
     for (int e = 1; e < kBatch; ++e) mb = fmaxf(mb, lse[e]);
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
     acc.w *= alpha;
 #pragma unroll
     for (int e = 0; e < kBatch; ++e) {
-      const float w = ex2_approx(lse[e] - Mn);  // 0 for the padding entries
+      const float w = ex2_approx(lse[e] - Mn);
       L += w;
       acc.x = fmaf(w, o[e].x, acc.x);
       acc.y = fmaf(w, o[e].y, acc.y);
@@ -71,22 +73,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
     M = Mn;
   }
   const float invL = 1.0f / L;
-  acc.x *= invL;
-  acc.y *= invL;
-  acc.z *= invL;
-  acc.w *= invL;
-  __nv_bfloat16* orow = p.out[u / kHkv] + (static_cast<size_t>(u % kHkv) * kRows + r) * kD;
+  // folded row r of kv head g is row r % 64 of q head 2g + r / 64
+  __nv_bfloat16* orow = p.out[u / kHkv] + (static_cast<size_t>(u % kHkv) * kRows + r) * kD + 4 * c;
   uint2 v;
-  v.x = pack_bf16x2(acc.x, acc.y);
-  v.y = pack_bf16x2(acc.z, acc.w);
-  *reinterpret_cast<uint2*>(orow + 4 * lane) = v;
+  v.x = pack_bf16x2(acc.x * invL, acc.y * invL);
+  v.y = pack_bf16x2(acc.z * invL, acc.w * invL);
+  *reinterpret_cast<uint2*>(orow) = v;
 }
 
 // Host-side launcher (the kernel template is instantiated and launched in this file).
 template <int CAP>
 cudaError_t launch_merge_kernel(const MergeParams<CAP>& mp, cudaLaunchConfig_t cfg) {
-  cfg.gridDim = dim3(mp.n_split * (kRows / kMergeWarps));
-  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.gridDim = dim3(mp.n_split * kPartChunks);
+  cfg.blockDim = dim3(kMergeThreads);
   int max_parts = 0;
   for (int i = 0; i < mp.n_split; ++i) max_parts = mp.unit[i].nparts > max_parts ? mp.unit[i].nparts : max_parts;
   return max_parts <= 8 ? cudaLaunchKernelEx(&cfg, merge_kernel<CAP, 8>, mp)
