@@ -48,10 +48,6 @@ namespace attn {
 constexpr int kThreads = 384;
 constexpr int kPrepThreads = 64;  // bf16: warps 10 and 11
 constexpr int kSoftmaxThreads = 256;
-// bf16: the producer warp and the prep warps start their memory traffic only once the softmax
-// threads have issued the loads of the first segment's raw q (named barrier 3), so that those
-// loads are not queued behind the K/V ring fill
-constexpr uint32_t kBarQFirst = 3, kBarQFirstThreads = kSoftmaxThreads + 32 + kPrepThreads;
 
 // Shared-memory layout of one CTA. bf16 cache: a K or V tile is 128 rows x 256 bytes, stored as
 // two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom;
@@ -110,8 +106,11 @@ struct Seg {
 // Next segment of a CTA's tile range, in range order: t is the next tile, end the range end.
 __device__ __forceinline__ bool next_seg(long long& t, long long end, int T, Seg& s) {
   if (t >= end) return false;
-  s.u = static_cast<int>(t / T);
-  s.j0 = static_cast<int>(t - static_cast<long long>(s.u) * T);
+  // tile indices stay below 2^31 (at most 64 layers x 8 heads x (Smax/128 + 1) tiles), so the
+  // division is a 32-bit one
+  const int ti = static_cast<int>(t);
+  s.u = ti / T;
+  s.j0 = ti - s.u * T;
   const long long j1 = s.j0 + (end - t);
   s.j1 = static_cast<int>(j1 < T ? j1 : T);
   t += s.j1 - s.j0;
@@ -288,10 +287,7 @@ template <class PP>
 __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
   long long t = cx.start;
   Seg s;
-  if (!next_seg(t, cx.end, p.T, s)) {
-    bar_arrive(kBarQFirst, kBarQFirstThreads);
-    return;
-  }
+  if (!next_seg(t, cx.end, p.T, s)) return;
   const int oc = threadIdx.x >> 3, i = threadIdx.x & 7;
   const int dl = 8 * i, dh = 64 + 8 * i;
   const int l = s.u / kHkv, g = s.u % kHkv;
@@ -319,7 +315,6 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
       kv[tt][1][1] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dh);
     }
   }
-  bar_arrive(kBarQFirst, kBarQFirstThreads);  // the loads are issued: the K/V stream may start
   float gl[8], gh[8];
   unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gl);
   unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dh), gh);
@@ -1144,14 +1139,12 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     if constexpr (!F8) first_q_prep(p, cx);
     softmax_warps<F8>(p, cx);
   } else if (warp == 8) {
-    if constexpr (!F8) bar_sync(kBarQFirst, kBarQFirstThreads);
     if (lane == 0) producer<F8>(p, cx);
   } else if (warp == 9) {
     if (lane == 0) mma_issuer<F8>(p, cx);
   } else if constexpr (F8) {
     if (warp == 10 && lane == 0) q_loader<F8>(p, cx);
   } else {
-    bar_sync(kBarQFirst, kBarQFirstThreads);
     prep_warps(p, cx);
   }
 
