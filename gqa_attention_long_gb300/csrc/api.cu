@@ -207,7 +207,7 @@ namespace {
 
 // Bytes that expert_attn_workspace_init zeroes: everything before the first region that the
 // kernels fully rewrite on every call.
-constexpr size_t kInitBytes = ws_layout(kMaxLayersPerLaunch, 1).qscale_off;
+constexpr size_t kInitBytes = ws_layout(kMaxLayersPerLaunch, 1, true).qscale_off;
 
 // RoPE inverse frequencies theta^(-2j/128) = 5e6^(-j/64), j < 64, as fp32 (hi, lo) pairs.
 void rope_inv_freq(float* hi, float* lo) {
@@ -257,7 +257,7 @@ int launch_prologue_t(const ea_layer_args* a, int n, int S, int Smax, int rope_d
     d.q_rope = static_cast<__nv_bfloat16*>(a[l].q_rope);
   }
   rope_inv_freq(pp.inv_hi, pp.inv_lo);
-  pp.q_ws = ws + wl.q_off;
+  pp.q_ws = fp8 ? ws + wl.q_off : nullptr;  // bf16: Q is prepared inside the attention kernel
   pp.q_scale = reinterpret_cast<float*>(ws + wl.qscale_off);
   pp.sv_ref = reinterpret_cast<float*>(ws + wl.svref_off);
   pp.unit_sync = reinterpret_cast<uint32_t*>(ws + wl.sync_off);
@@ -337,7 +337,7 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
   ap.S = S;
   ap.Smax = Smax;
   ap.W = static_cast<long long>(n) * kHkv * ap.T;
-  ap.q_ws = ws + wl.q_off;
+  ap.q_ws = fp8 ? ws + wl.q_off : nullptr;
   ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
   ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
   ap.q_scale = reinterpret_cast<const float*>(ws + wl.qscale_off);
@@ -406,7 +406,7 @@ int run_layers(const ea_layer_args* a, int n_layers, int S, int Smax, int rope_d
   DeviceInfo di;
   if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
   const int per = n_layers < kMaxLayersPerLaunch ? n_layers : kMaxLayersPerLaunch;
-  const WsLayout wl = ws_layout(per, di.sm_count);
+  const WsLayout wl = ws_layout(per, di.sm_count, kv_dtype == EA_KV_FP8_E4M3);
   if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -430,7 +430,7 @@ size_t expert_attn_workspace_size(int n_layers, int Smax, int kv_dtype) {
   DeviceInfo di;
   if (!device_info(&dev, &di)) return 0;
   const int per = n_layers < kMaxLayersPerLaunch ? n_layers : kMaxLayersPerLaunch;
-  return ws_layout(per, di.sm_count).total;
+  return ws_layout(per, di.sm_count, kv_dtype == EA_KV_FP8_E4M3).total;
 }
 
 int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream) {
@@ -451,7 +451,7 @@ int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta
   int dev;
   DeviceInfo di;
   if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
-  const WsLayout wl = ws_layout(1, di.sm_count);
+  const WsLayout wl = ws_layout(1, di.sm_count, kv_dtype == EA_KV_FP8_E4M3);
   if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
   return launch_prologue(a, 1, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3,
                          static_cast<uint8_t*>(workspace), wl, di.sm_count,
@@ -552,7 +552,7 @@ const char* expert_attn_status_string(int status) {
 namespace {
 
 constexpr size_t noalloc_bytes() {
-  return ws_layout(EA_NOALLOC_MAX_LAYERS, EA_NOALLOC_MAX_CTAS).total;
+  return ws_layout(EA_NOALLOC_MAX_LAYERS, EA_NOALLOC_MAX_CTAS, true).total;
 }
 static_assert(noalloc_bytes() == EA_NOALLOC_SCRATCH_BYTES, "scratch size in the header is stale");
 
@@ -587,7 +587,7 @@ extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_lay
   if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
   DeviceInfo capped = di;
   if (capped.sm_count > EA_NOALLOC_MAX_CTAS) capped.sm_count = EA_NOALLOC_MAX_CTAS;
-  const WsLayout wl = ws_layout(n_layers, capped.sm_count);
+  const WsLayout wl = ws_layout(n_layers, capped.sm_count, kv_dtype == EA_KV_FP8_E4M3);
   if (wl.total > EA_NOALLOC_SCRATCH_BYTES) return EA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
   if (ws == nullptr) return EA_ERR_CUDA;

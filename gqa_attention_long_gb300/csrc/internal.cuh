@@ -50,8 +50,9 @@ enum : uint32_t {
 //                                   in-kernel merge of two-part units (zero between calls)
 //   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
 //   svref   n_layers * 8 fp32          FP8 only: per-unit reference V scale (max over its tiles)
-//   q       n_layers * 8 * 32 KB  roped Q per (layer, kv head), swizzled K-major (bf16; e4m3
-//                                 high and low codes)
+//   q       n_layers * 8 * 32 KB  e4m3 only: roped Q per (layer, kv head) as high and low e4m3
+//                                 codes, swizzled K-major (a bf16 call prepares Q in the
+//                                 attention kernel's shared memory and has no such region)
 //   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised), per slot chunk-major:
 //                                     float4 chunk c (columns 4c .. 4c+3) of row r at c * 128 + r
 //   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
@@ -59,7 +60,7 @@ struct WsLayout {
   size_t sync_off, qscale_off, svref_off, q_off, part_o_off, part_lse_off, total;
 };
 
-constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
+constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas, bool fp8) {
   WsLayout w{};
   size_t off = 1024;
   w.sync_off = off;
@@ -70,7 +71,7 @@ constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas) {
   w.svref_off = off;
   off += ((static_cast<size_t>(n_layers_per_launch) * kHkv * sizeof(float)) + 1023) & ~static_cast<size_t>(1023);
   w.q_off = off;
-  off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
+  if (fp8) off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
   w.part_o_off = off;
   off += static_cast<size_t>(max_ctas) * 2 * kRows * kD * sizeof(float);
   w.part_lse_off = off;
@@ -98,7 +99,7 @@ struct PrologueParams {
   PrologueLayer layer[CAP];
   float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
   float inv_lo[kD / 2];
-  uint8_t* q_ws;
+  uint8_t* q_ws;   // FP8: staged roped Q codes (bf16: null, nothing staged)
   float* q_scale;  // FP8: [unit][128] scale of each e4m3 Q row
   float* sv_ref;   // FP8: [unit] reference V scale
   uint32_t* unit_sync;  // [unit][2]: zeroed here for the attention kernel's in-kernel merge
@@ -125,7 +126,7 @@ struct AttnParams {
   __nv_bfloat16* out[CAP];
   const float* ks[CAP];      // FP8: block scales [8][Smax/128 + 1] (else null)
   const float* vs[CAP];
-  const uint8_t* q_ws;
+  const uint8_t* q_ws;  // FP8: the prologue's staged Q codes (bf16: null)
   float* part_o;
   float* part_lse;
   const float* q_scale;  // FP8: [unit][128]

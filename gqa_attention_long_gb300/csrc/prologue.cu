@@ -1,6 +1,8 @@
-// prologue.cu — K1: fused per-head RMSNorm + HF rotate_half RoPE of the 64 expert tokens, the
-// own-row write into the cache tail, and the staging of the roped Q (and a swizzled copy of the
-// own K/V rows) in the workspace in the shared-memory layout the attention kernel consumes.
+// prologue.cu — K1: fused per-head RMSNorm + HF rotate_half RoPE of the 64 expert tokens and
+// the own-row write into the cache tail; for an e4m3 cache also the staging of the roped Q (high
+// and low codes, per-row scale) in the workspace in the shared-memory layout the attention
+// kernel consumes. With a bf16 cache the attention kernel does this work itself; this kernel
+// then serves only the stand-alone prologue entry point (cache tail and optional roped q).
 //
 // alpamayo_tt/expert.py, TTExpert.layer (rms_norm of q and k with the q_norm / k_norm gains,
 // rotary_embedding_hf, typecast to the cache dtype, fill_cache at row Smax-64) and
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
       cur_l = l;
     }
     const uint8_t* src = psm + (k % kPRing) * kPUnitBytes;
-    uint8_t* qdst = p.q_ws + static_cast<size_t>(u) * kQTileBytes;
+    uint8_t* qdst = F8 ? p.q_ws + static_cast<size_t>(u) * kQTileBytes : nullptr;
     float krl[TPO][8], krh[TPO][8], vrl[TPO][8], vrh[TPO][8];  // FP8: kept for the heads' scales
     float kmax = 0.f, vmax = 0.f;
 #pragma unroll
@@ -210,9 +212,6 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
           *reinterpret_cast<uint2*>(qdst + swz8_off(r, i + 8)) = hi;
           *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i + 8)) = lo;
           if (i == 0) p.q_scale[static_cast<size_t>(u) * kRows + r] = sq;
-        } else {
-          *reinterpret_cast<uint4*>(qdst + swz_off(r, i, kQTileBytes / 2)) = ql;
-          *reinterpret_cast<uint4*>(qdst + swz_off(r, i + 8, kQTileBytes / 2)) = qh;
         }
         if (L.q_rope != nullptr) {
           __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;

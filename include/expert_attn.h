@@ -76,8 +76,9 @@ typedef struct {
   void* q_rope;   /* optional, may be NULL */
 } ea_layer_args;
 
-/* Bytes of device workspace needed by a call over n_layers layers on the current device
- * (0 if no suitable device is present). The workspace must be 256-byte aligned and, before
+/* Bytes of device workspace needed by a call over n_layers layers of the given cache dtype on
+ * the current device (0 if no suitable device is present; an e4m3 workspace also serves bf16
+ * calls). The workspace must be 256-byte aligned and, before
  * its first use, cleared with expert_attn_workspace_init. */
 size_t expert_attn_workspace_size(int n_layers, int Smax, int kv_dtype);
 
@@ -88,8 +89,9 @@ int expert_attn_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t str
 
 /* Steps 1 + 2 only (alpamayo_tt/expert.py, TTExpert.layer: q/k rms_norm, rotary_embedding_hf,
  * fill_cache): norm and rope q and k of one layer, write the own k/v rows into the cache tail
- * (FP8: quantised with their own scale slot), and stage the roped q in the workspace (and in
- * a->q_rope when it is not NULL). Requires 0 <= S <= Smax-64 and |S + rope_delta| + 64 < 2^24. */
+ * (FP8: quantised with their own scale slot, and the roped q staged in the workspace as e4m3
+ * codes), and write the roped q to a->q_rope when it is not NULL. Requires 0 <= S <= Smax-64
+ * and |S + rope_delta| + 64 < 2^24. */
 int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 

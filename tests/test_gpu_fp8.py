@@ -116,3 +116,25 @@ def test_fp8_sixteen_layers_split_units():
         check_out(Ls[l], oracle_fp8(xs[l]), f"layer {l}")
     for L in Ls:
         assert torch.isfinite(L.out.float()).all()
+
+
+def test_workspace_size_by_dtype():
+    """Only an e4m3 call stages the roped Q codes in the workspace (32 KB per unit); a bf16 call
+    prepares Q in the attention kernel's shared memory, and a bf16-sized workspace is refused
+    for an e4m3 call before anything is launched."""
+    b = ea.expert_attn_workspace_size(64, 8192, ea.EA_KV_BF16)
+    f = ea.expert_attn_workspace_size(64, 8192, ea.EA_KV_FP8_E4M3)
+    assert f - b == 64 * 8 * 32768
+    S, Smax = 256, 512
+    x = layer_inputs(config_seed(3, 7), S, Smax)
+    codes_k, sk = quantize_on_gpu(x.k_cache, S, Smax)
+    codes_v, sv = quantize_on_gpu(x.v_cache, S, Smax)
+    d = torch.device("cuda")
+    L = ea.LayerBuffers(q_raw=x.q_raw.to(d), k_raw=x.k_raw.to(d), v_raw=x.v_raw.to(d),
+                        q_gamma=x.q_gamma.to(d), k_gamma=x.k_gamma.to(d), k_cache=codes_k,
+                        v_cache=codes_v, k_scale=sk, v_scale=sv,
+                        out=torch.empty(16, 64, 128, dtype=torch.bfloat16, device=d))
+    ws = ea.alloc_workspace(1, Smax, ea.EA_KV_BF16)
+    with pytest.raises(ea.ExpertAttnError) as e:
+        ea.expert_attn_layer(L, S, Smax, 0, ea.EA_KV_FP8_E4M3, ws)
+    assert e.value.rc == 4
