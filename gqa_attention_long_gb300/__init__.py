@@ -11,4 +11,6 @@ from ._lib import (  # noqa: F401
     expert_attn_set_splits,
     expert_attn_status_string, expert_attn_workspace_init, expert_attn_workspace_size,
     kernels_per_call, lib, make_args, split_parts, split_units,
+    alloc_decoder_layer_workspace, expert_decoder_layer, expert_decoder_layer_workspace_size,
+    expert_linear64, expert_linear64_workspace_size,
 )

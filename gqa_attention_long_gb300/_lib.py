@@ -27,6 +27,13 @@ class EaLayerArgs(ctypes.Structure):
         "k_scale", "v_scale", "out", "q_rope")]
 
 
+class EaDecoderLayerArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("x_out", ctypes.c_void_p), ("hidden", ctypes.c_int),
+                ("inter", ctypes.c_int)] + [(n, ctypes.c_void_p) for n in (
+                    "ln1", "wqkv", "q_norm", "k_norm", "wo", "ln2", "w1", "w3", "w2",
+                    "k_cache", "v_cache", "q_rope")]
+
+
 _lib_handle = None
 
 
@@ -51,6 +58,10 @@ def lib() -> ctypes.CDLL:
             "expert_attn_read_status": (I, [V, V, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_uint32)]),
             "expert_attn_status_string": (ctypes.c_char_p, [I]),
             "expert_attn_selftest_wait_timeout": (I, [I, V, S, V]),
+            "expert_decoder_layer_workspace_size": (S, [I, I]),
+            "expert_decoder_layer": (I, [ctypes.POINTER(EaDecoderLayerArgs), I, I, I, V, S, V]),
+            "expert_linear64_workspace_size": (S, [I, I]),
+            "expert_linear64": (I, [V, V, V, I, I, V, S, V]),
         }
         for name, (res, args) in sig.items():
             f = getattr(h, name)
@@ -268,3 +279,60 @@ def expert_attn_read_status(ws: torch.Tensor, stream=None) -> tuple[int, int]:
     _check("expert_attn_read_status", lib().expert_attn_read_status(
         _ptr(ws, "workspace", torch.uint8), _stream(stream), ctypes.byref(st), ctypes.byref(bits)))
     return st.value, bits.value
+
+
+# ----------------------------------------------------------------- whole decoder layer
+def expert_decoder_layer_workspace_size(hidden: int, inter: int) -> int:
+    return int(lib().expert_decoder_layer_workspace_size(int(hidden), int(inter)))
+
+
+def alloc_decoder_layer_workspace(hidden: int, inter: int, device="cuda") -> torch.Tensor:
+    """A cleared workspace for expert_decoder_layer (torch-allocated)."""
+    n = expert_decoder_layer_workspace_size(hidden, inter)
+    if n == 0:
+        raise RuntimeError("expert_decoder_layer_workspace_size returned 0 (bad widths or no sm_103 GPU)")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    expert_attn_workspace_init(ws)
+    return ws
+
+
+def expert_decoder_layer(x: torch.Tensor, x_out: torch.Tensor, w, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, S: int, Smax: int, rope_delta: int,
+                         ws: torch.Tensor, q_rope: torch.Tensor | None = None, stream=None) -> None:
+    """One decoder layer (include/expert_attn.h): ``w`` has the bf16 tensors ln1, wqkv, q_norm,
+    k_norm, wo, ln2, w1, w3, w2 ([out_features, in_features] for the projections)."""
+    bf = torch.bfloat16
+    hidden, inter = x.shape[-1], w.w1.shape[0]
+    a = EaDecoderLayerArgs()
+    a.x = _ptr(x, "x", bf, 64 * hidden)
+    a.x_out = _ptr(x_out, "x_out", bf, 64 * hidden)
+    a.hidden, a.inter = int(hidden), int(inter)
+    a.ln1 = _ptr(w.ln1, "ln1", bf, hidden)
+    a.wqkv = _ptr(w.wqkv, "wqkv", bf, 4096 * hidden)
+    a.q_norm = _ptr(w.q_norm, "q_norm", bf, 128)
+    a.k_norm = _ptr(w.k_norm, "k_norm", bf, 128)
+    a.wo = _ptr(w.wo, "wo", bf, hidden * 2048)
+    a.ln2 = _ptr(w.ln2, "ln2", bf, hidden)
+    a.w1 = _ptr(w.w1, "w1", bf, inter * hidden)
+    a.w3 = _ptr(w.w3, "w3", bf, inter * hidden)
+    a.w2 = _ptr(w.w2, "w2", bf, hidden * inter)
+    a.k_cache = _ptr(k_cache, "k_cache", bf, 8 * Smax * 128)
+    a.v_cache = _ptr(v_cache, "v_cache", bf, 8 * Smax * 128)
+    a.q_rope = _ptr(q_rope, "q_rope", bf, 16 * 64 * 128)
+    p, n = _ws(ws)
+    _check("expert_decoder_layer", lib().expert_decoder_layer(ctypes.byref(a), S, Smax, rope_delta, p, n,
+                                                              _stream(stream)))
+
+
+def expert_linear64_workspace_size(K: int, N: int) -> int:
+    return int(lib().expert_linear64_workspace_size(int(K), int(N)))
+
+
+def expert_linear64(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """y[64][N] = x[64][K] w^T (bf16, fp32 accumulation) on the tensor cores."""
+    bf = torch.bfloat16
+    N, K = w.shape
+    p, n = _ws(ws)
+    _check("expert_linear64", lib().expert_linear64(_ptr(x, "x", bf, 64 * K), _ptr(w, "w", bf, N * K),
+                                                    _ptr(y, "y", bf, 64 * N), int(K), int(N), p, n,
+                                                    _stream(stream)))

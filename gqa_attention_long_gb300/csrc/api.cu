@@ -600,3 +600,341 @@ extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_lay
   return launch_chunk(layers, n_layers, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3, ws, wl,
                       capped, st, nullptr);
 }
+
+// ------------------------------------------------------------------ whole decoder layer
+// Host side of expert_decoder_layer and expert_linear64: tensor maps of the projections'
+// operands (cached), split-K planning, the layer workspace, and the launches (all chained with
+// programmatic dependent launch).
+namespace ea {
+cudaError_t linear_set_attributes();
+cudaError_t launch_linear(const LinearParams& lp, int tiles, int splits, cudaLaunchConfig_t cfg);
+cudaError_t launch_residual_norm(const float* part, int splits, const __nv_bfloat16* x, int width,
+                                 __nv_bfloat16* y_out, const __nv_bfloat16* gamma,
+                                 __nv_bfloat16* h_out, cudaLaunchConfig_t cfg);
+cudaError_t launch_qkv_heads(const float* part, int splits, __nv_bfloat16* q, __nv_bfloat16* k,
+                             __nv_bfloat16* v, cudaLaunchConfig_t cfg);
+cudaError_t launch_swiglu(const float* part, int splits, int inter, __nv_bfloat16* gu,
+                          cudaLaunchConfig_t cfg);
+cudaError_t launch_split_sum_bf16(const float* part, int splits, int N, __nv_bfloat16* y,
+                                  cudaLaunchConfig_t cfg);
+}  // namespace ea
+
+namespace {
+
+struct TmapKey {
+  const void* ptr;
+  int rank;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  bool operator==(const TmapKey& o) const { return std::memcmp(this, &o, sizeof(TmapKey)) == 0; }
+};
+struct TmapKeyHash {
+  size_t operator()(const TmapKey& k) const {
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+    size_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(TmapKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+    return h;
+  }
+};
+std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
+
+// bf16 tiled map with 128-byte swizzle (boxes are 64 channels = 128 bytes wide).
+bool bf16_map(const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box, CUtensorMap* out) {
+  TmapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.ptr = ptr;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides[i];
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_tmaps.find(key);
+    if (it != g_tmaps.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr),
+         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_tmaps.size() > 16384) g_tmaps.clear();
+  g_tmaps[key] = m;
+  *out = m;
+  return true;
+}
+
+// Weights [rows][K] (row-major): 2-D {K, rows}, box {64, 128}.
+bool weight_map(const void* w, int K, int rows, CUtensorMap* out) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  return bf16_map(w, 2, dims, strides, box, out);
+}
+
+// Row-major activations [64][K]: 4-D {64, K/64, 64, 1}, box {64, 1, 64, 1}; k-step kk at
+// (0, kk, 0, 0).
+bool rows_map(const void* x, int K, CUtensorMap* out) {
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K / 64), kTok, 1};
+  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(K) * 2 * kTok};
+  const cuuint32_t box[4] = {64, 1, kTok, 1};
+  return bf16_map(x, 4, dims, strides, box, out);
+}
+
+// The attention output [16][64][128] read as the [64][2048] input of wo (feature 128 h + d):
+// 4-D {64 channels, 2 halves, 64 tokens, 16 heads}, box {64, 1, 64, 1}; k-step kk at
+// (0, kk % 2, 0, kk / 2).
+bool heads_map(const void* a, CUtensorMap* out) {
+  const cuuint64_t dims[4] = {64, 2, kTok, kHq};
+  const cuuint64_t strides[3] = {128, kD * 2, static_cast<cuuint64_t>(kTok) * kD * 2};
+  const cuuint32_t box[4] = {64, 1, kTok, 1};
+  return bf16_map(a, 4, dims, strides, box, out);
+}
+
+// Split count of a projection: about two CTAs per SM (two fit), at least two k-steps per CTA
+// where the k-steps allow it, and no empty split.
+void plan_splits(int tiles, int ksteps, int sm_count, int* splits, int* kps) {
+  int s = (2 * sm_count) / tiles;
+  if (s > ksteps / 2) s = ksteps / 2;
+  if (s < 1) s = 1;
+  *kps = (ksteps + s - 1) / s;
+  *splits = (ksteps + *kps - 1) / *kps;
+}
+
+size_t part_floats(int N, int K, int sm_count) {
+  int splits, kps;
+  plan_splits(N / 128, K / 64, sm_count, &splits, &kps);
+  return static_cast<size_t>(splits) * kTok * N;
+}
+
+size_t align_kb(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
+
+struct LayerWs {
+  size_t attn_ws, h, q, k, v, attn, x1, h2, gu, part, total;
+};
+
+// Layer workspace: the attention's own workspace first (its status word, at offset 0, is
+// the one every kernel of the layer reports to), then the layer's activations and the
+// projections' partial sums.
+LayerWs layer_ws_layout(int hidden, int inter, int sm_count) {
+  LayerWs w{};
+  size_t off = 0;
+  w.attn_ws = off;
+  off += align_kb(ws_layout(1, sm_count, false).total);
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_kb(bytes);
+    return o;
+  };
+  w.h = take(static_cast<size_t>(kTok) * hidden * 2);
+  w.q = take(static_cast<size_t>(kHq) * kTok * kD * 2);
+  w.k = take(static_cast<size_t>(kHkv) * kTok * kD * 2);
+  w.v = take(static_cast<size_t>(kHkv) * kTok * kD * 2);
+  w.attn = take(static_cast<size_t>(kHq) * kTok * kD * 2);
+  w.x1 = take(static_cast<size_t>(kTok) * hidden * 2);
+  w.h2 = take(static_cast<size_t>(kTok) * hidden * 2);
+  w.gu = take(static_cast<size_t>(kTok) * inter * 2);
+  size_t pf = part_floats((kHq + 2 * kHkv) * kD, hidden, sm_count);
+  const size_t candidates[3] = {part_floats(hidden, kHq * kD, sm_count),
+                                part_floats(2 * inter, hidden, sm_count),
+                                part_floats(hidden, inter, sm_count)};
+  for (size_t c : candidates) pf = c > pf ? c : pf;
+  w.part = take(pf * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+bool layer_dims_ok(int hidden, int inter) {
+  return hidden >= 128 && hidden <= kMaxHidden && hidden % 128 == 0 && inter >= 128 &&
+         inter <= kMaxInter && inter % 128 == 0;
+}
+
+// One projection: part = X W^T (two weights side by side when w1 != nullptr).
+int run_linear(const CUtensorMap& xmap, int c1, const void* w0, int rows0, const void* w1, int rows1,
+               int K, float* part, uint32_t* status, int sm_count, cudaStream_t st, int* splits_out) {
+  static_assert(sizeof(LinearParams) < 4096, "linear parameter block");
+  LinearParams lp;
+  std::memset(&lp, 0, sizeof(lp));
+  if (!weight_map(w0, K, rows0, &lp.wmap[0])) return EA_ERR_CUDA;
+  if (w1 != nullptr && !weight_map(w1, K, rows1, &lp.wmap[1])) return EA_ERR_CUDA;
+  lp.xmap = xmap;
+  lp.part = part;
+  lp.status = status;
+  lp.N = rows0 + (w1 != nullptr ? rows1 : 0);
+  lp.tiles0 = rows0 / 128;
+  lp.ksteps = K / 64;
+  lp.c1 = c1;
+  int splits, kps;
+  plan_splits(lp.N / 128, lp.ksteps, sm_count, &splits, &kps);
+  lp.kps = kps;
+  cudaLaunchAttribute attr[1];
+  if (launch_linear(lp, lp.N / 128, splits, launch_config(st, attr, true)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  *splits_out = splits;
+  return EA_OK;
+}
+
+bool linear_attrs_ready() {
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [] {
+    ok = linear_set_attributes() == cudaSuccess;
+    cudaGetLastError();
+  });
+  return ok;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t expert_decoder_layer_workspace_size(int hidden, int inter) {
+  if (!layer_dims_ok(hidden, inter)) return 0;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return 0;
+  return layer_ws_layout(hidden, inter, di.sm_count).total;
+}
+
+int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int rope_delta,
+                         void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  if (a == nullptr || workspace == nullptr) return EA_ERR_INVALID_ARG;
+  if (!layer_dims_ok(a->hidden, a->inter)) return EA_ERR_INVALID_ARG;
+  const void* req[] = {a->x, a->x_out, a->ln1, a->wqkv, a->q_norm, a->k_norm, a->wo, a->ln2,
+                       a->w1, a->w3, a->w2, a->k_cache, a->v_cache};
+  for (const void* p : req) {
+    if (p == nullptr) return EA_ERR_INVALID_ARG;
+    if (!aligned16(p)) return EA_ERR_MISALIGNED;
+  }
+  if (a->x == a->x_out) return EA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EA_ERR_MISALIGNED;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di) || !linear_attrs_ready()) return EA_ERR_UNSUPPORTED;
+  const int H = a->hidden, I = a->inter;
+  const LayerWs wl = layer_ws_layout(H, I, di.sm_count);
+  if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+  float* part = reinterpret_cast<float*>(ws + wl.part);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + wl.attn_ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a->x);
+  cudaLaunchAttribute attr[1];
+  int splits = 1;
+
+  // the attention step's arguments (validated like any expert_attn_layer call)
+  ea_layer_args la;
+  std::memset(&la, 0, sizeof(la));
+  la.q_raw = bf(wl.q);
+  la.k_raw = bf(wl.k);
+  la.v_raw = bf(wl.v);
+  la.q_gamma = a->q_norm;
+  la.k_gamma = a->k_norm;
+  la.k_cache = a->k_cache;
+  la.v_cache = a->v_cache;
+  la.out = bf(wl.attn);
+  la.q_rope = a->q_rope;
+  int rc = validate(&la, 1, S, Smax, rope_delta, EA_KV_BF16, ws + wl.attn_ws, true);
+  if (rc != EA_OK) return rc;
+
+  CUtensorMap xm_h, xm_attn, xm_h2, xm_gu;
+  if (!rows_map(bf(wl.h), H, &xm_h) || !heads_map(bf(wl.attn), &xm_attn) ||
+      !rows_map(bf(wl.h2), H, &xm_h2) || !rows_map(bf(wl.gu), I, &xm_gu))
+    return EA_ERR_CUDA;
+  // h = rms_norm(x, ln1)
+  if (launch_residual_norm(nullptr, 0, x, H, nullptr, static_cast<const __nv_bfloat16*>(a->ln1),
+                           bf(wl.h), launch_config(st, attr, true)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  // q, k, v = heads of h wqkv^T
+  rc = run_linear(xm_h, H / 64, a->wqkv, (kHq + 2 * kHkv) * kD, nullptr, 0, H, part, status,
+                  di.sm_count, st, &splits);
+  if (rc != EA_OK) return rc;
+  if (launch_qkv_heads(part, splits, bf(wl.q), bf(wl.k), bf(wl.v), launch_config(st, attr, true)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  // attention (q/k norm, RoPE, own rows into the cache tail, split-KV attention, merge)
+  rc = launch_chunk(&la, 1, S, Smax, rope_delta, false, ws + wl.attn_ws, ws_layout(1, di.sm_count, false),
+                    di, st, nullptr);
+  if (rc != EA_OK) return rc;
+  // x1 = x + concat_heads(attn) wo^T; h2 = rms_norm(x1, ln2)
+  rc = run_linear(xm_attn, 2, a->wo, H, nullptr, 0, kHq * kD, part, status, di.sm_count, st, &splits);
+  if (rc != EA_OK) return rc;
+  if (launch_residual_norm(part, splits, x, H, bf(wl.x1), static_cast<const __nv_bfloat16*>(a->ln2),
+                           bf(wl.h2), launch_config(st, attr, true)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  // gu = silu(h2 w1^T) * (h2 w3^T)
+  rc = run_linear(xm_h2, H / 64, a->w1, I, a->w3, I, H, part, status, di.sm_count, st, &splits);
+  if (rc != EA_OK) return rc;
+  if (launch_swiglu(part, splits, I, bf(wl.gu), launch_config(st, attr, true)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  // x_out = x1 + gu w2^T
+  rc = run_linear(xm_gu, I / 64, a->w2, H, nullptr, 0, I, part, status, di.sm_count, st, &splits);
+  if (rc != EA_OK) return rc;
+  if (launch_residual_norm(part, splits, bf(wl.x1), H, static_cast<__nv_bfloat16*>(a->x_out), nullptr,
+                           nullptr, launch_config(st, attr, true)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return EA_OK;
+}
+
+size_t expert_linear64_workspace_size(int K, int N) {
+  if (K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0) return 0;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return 0;
+  return 1024 + align_kb(part_floats(N, K, di.sm_count) * sizeof(float));
+}
+
+int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* workspace,
+                    size_t ws_bytes, ea_stream_t stream) {
+  if (x == nullptr || w == nullptr || y == nullptr || workspace == nullptr) return EA_ERR_INVALID_ARG;
+  if (K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0 || K > (1 << 20) || N > (1 << 20))
+    return EA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return EA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EA_ERR_MISALIGNED;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di) || !linear_attrs_ready()) return EA_ERR_UNSUPPORTED;
+  if (ws_bytes < 1024 + align_kb(part_floats(N, K, di.sm_count) * sizeof(float))) return EA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* part = reinterpret_cast<float*>(ws + 1024);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap xm;
+  if (!rows_map(x, K, &xm)) return EA_ERR_CUDA;
+  int splits = 1;
+  int rc = run_linear(xm, K / 64, w, N, nullptr, 0, K, part, status, di.sm_count, st, &splits);
+  if (rc != EA_OK) return rc;
+  cudaLaunchAttribute attr[1];
+  if (launch_split_sum_bf16(part, splits, N, static_cast<__nv_bfloat16*>(y), launch_config(st, attr, true)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return EA_OK;
+}
+
+}  // extern "C"

@@ -42,6 +42,7 @@ enum : uint32_t {
   kErrPrologueWait = 1u << 4,
   kErrMergeWait = 1u << 5,
   kErrSelftestWait = 1u << 6,
+  kErrLinearWait = 1u << 7,
 };
 
 // ------------------------------------------------------------------------- workspace layout
@@ -140,6 +141,28 @@ struct AttnParams {
   int ncol;            // FP8: scale columns per kv head, Smax/128 + 1 (the last one: own rows)
   int fused_merge;     // every split unit has two parts: the second one merges in-kernel
   float scale_log2;    // log2(e) / sqrt(128)
+};
+
+// ------------------------------------------------------------ decoder-layer projections
+constexpr int kMaxHidden = 8192;   // widest residual stream the finishing kernels take
+constexpr int kMaxInter = 32768;
+
+// One projection Y[t][n] = sum_k X[t][k] W[n][k] for the 64 tokens (linear.cu). The weights of
+// tiles [0, tiles0) come from wmap[0], the rest from wmap[1] (two projections of the same input
+// side by side: the gate and up projections of the MLP). Each weight map is 2-D {K, rows} with
+// a {64, 128} box; the activation map is 4-D {64, c1, 64, c3} with a {64, 1, 64, 1} box, k-step
+// kk at coordinates (0, kk % c1, 0, kk / c1) (row-major X: c1 = K / 64, c3 = 1; the attention
+// output [16][64][128]: c1 = 2 halves of a head, c3 = 16 heads).
+struct LinearParams {
+  CUtensorMap wmap[2];
+  CUtensorMap xmap;
+  float* part;       // [splits][64][N] fp32 partial sums
+  uint32_t* status;  // workspace status word
+  int N;             // output features (all tiles), a multiple of 128
+  int tiles0;
+  int ksteps;        // K / 64
+  int kps;           // k-steps per split
+  int c1;
 };
 
 // Units split across CTAs, merged by the LSE merge kernel: at most one per CTA boundary.

@@ -133,3 +133,64 @@ def layer_inputs_on_device(seed: int, S: int, Smax: int, device, hidden_fill: fl
                     r(HKV, Smax, D).to(bf), r(HKV, Smax, D).to(bf), int(S), int(Smax))
     fill_hidden(x.k_cache, x.v_cache, S, Smax, hidden_fill, seed)
     return x
+
+
+# ------------------------------------------------------------------- whole decoder layer
+# The expert's trained weights are not available, so the layer is exercised with synthetic
+# ones of the model's shapes (alpamayo_tt/EXPERT_NOTES.md, "Matmul program configs": hidden
+# 1536, wqkv 1536 -> 4096, wo 2048 -> 1536, w1 / w3 1536 -> 6144, w2 6144 -> 1536). Each weight
+# is stored [out_features, in_features] and drawn N(0, 1 / in_features), so that activations
+# stay of order one through the layer; norm gains are 1 + 0.1 N(0, 1); the residual stream
+# x ~ N(0, 1).
+HIDDEN, INTER, QKV_DIM, Q_DIM = 1536, 6144, 4096, 2048
+
+
+@dataclass
+class ExpertLayerWeights:
+    ln1: torch.Tensor     # bf16 [hidden]
+    wqkv: torch.Tensor    # bf16 [4096, hidden]: q (16 x 128), k (8 x 128), v (8 x 128) features
+    q_norm: torch.Tensor  # bf16 [128]
+    k_norm: torch.Tensor  # bf16 [128]
+    wo: torch.Tensor      # bf16 [hidden, 2048]
+    ln2: torch.Tensor     # bf16 [hidden]
+    w1: torch.Tensor      # bf16 [inter, hidden] (gate)
+    w3: torch.Tensor      # bf16 [inter, hidden] (up)
+    w2: torch.Tensor      # bf16 [hidden, inter] (down)
+
+
+def expert_layer_weights(seed: int, hidden: int = HIDDEN, inter: int = INTER) -> ExpertLayerWeights:
+    """One layer's synthetic weights, bf16 on the CPU (numpy PCG64, as :func:`layer_inputs`)."""
+    rng = np.random.Generator(np.random.PCG64(int(seed) + 104729))
+    n = rng.standard_normal
+    return ExpertLayerWeights(
+        ln1=_bf16(1.0 + 0.1 * n(hidden)),
+        wqkv=_bf16(n((QKV_DIM, hidden)) / np.sqrt(hidden)),
+        q_norm=_bf16(1.0 + 0.1 * n(D)), k_norm=_bf16(1.0 + 0.1 * n(D)),
+        wo=_bf16(n((hidden, Q_DIM)) / np.sqrt(Q_DIM)),
+        ln2=_bf16(1.0 + 0.1 * n(hidden)),
+        w1=_bf16(n((inter, hidden)) / np.sqrt(hidden)),
+        w3=_bf16(n((inter, hidden)) / np.sqrt(hidden)),
+        w2=_bf16(n((hidden, inter)) / np.sqrt(inter)))
+
+
+def expert_layer_weights_on_device(seed: int, device, hidden: int = HIDDEN,
+                                   inter: int = INTER) -> ExpertLayerWeights:
+    """Same distributions drawn on ``device`` with a seeded generator of that device."""
+    g = torch.Generator(device=device).manual_seed(int(seed) + 104729)
+    bf = torch.bfloat16
+    r = lambda *shape: torch.randn(*shape, generator=g, device=device)  # noqa: E731
+    return ExpertLayerWeights(
+        ln1=(1.0 + 0.1 * r(hidden)).to(bf),
+        wqkv=(r(QKV_DIM, hidden) / hidden ** 0.5).to(bf),
+        q_norm=(1.0 + 0.1 * r(D)).to(bf), k_norm=(1.0 + 0.1 * r(D)).to(bf),
+        wo=(r(hidden, Q_DIM) / Q_DIM ** 0.5).to(bf),
+        ln2=(1.0 + 0.1 * r(hidden)).to(bf),
+        w1=(r(inter, hidden) / hidden ** 0.5).to(bf),
+        w3=(r(inter, hidden) / hidden ** 0.5).to(bf),
+        w2=(r(hidden, inter) / inter ** 0.5).to(bf))
+
+
+def residual_stream(seed: int, hidden: int = HIDDEN) -> torch.Tensor:
+    """The layer input x [64, hidden] ~ N(0, 1), bf16 on the CPU."""
+    rng = np.random.Generator(np.random.PCG64(int(seed) + 15485863))
+    return _bf16(rng.standard_normal((T, hidden)))

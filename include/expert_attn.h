@@ -172,6 +172,56 @@ int expert_attn_selftest_wait_timeout(int limit_us, void* workspace, size_t ws_b
 int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                int rope_delta, int kv_dtype, ea_stream_t stream);
 
+/* ------------------------------------------------------------------ whole decoder layer
+ * One decoder layer of the expert around the attention above (alpamayo_tt/expert.py,
+ * TTExpert.layer):
+ *   h  = rms_norm(x, ln1)                       (per token over the hidden channels, eps 1e-6)
+ *   q, k, v = heads of h wqkv^T                  (wqkv rows: q features 128 h + d of the 16 heads,
+ *                                                then k, then v of the 8 KV heads)
+ *   a  = the attention above (q/k norms, RoPE, own rows into the cache tail, masked GQA)
+ *   x1 = x + concat_heads(a) wo^T                (token row = the 16 heads side by side)
+ *   x_out = x1 + (silu(h2 w1^T) * (h2 w3^T)) w2^T,  h2 = rms_norm(x1, ln2)
+ * Every weight is bf16 row-major [out_features][in_features] (y = x W^T); activations between
+ * the steps are kept in bf16 and products accumulate in fp32. Widths: hidden and inter are
+ * multiples of 128 with hidden <= 8192 and inter <= 32768 (the expert: 1536 and 6144). The
+ * cache is bf16 [8][Smax][128] with the same rules as expert_attn_layer (rows [Smax-64, Smax)
+ * are written). All pointers are device pointers, 16-byte aligned. */
+typedef struct {
+  const void* x;      /* bf16 [64][hidden] layer input (residual stream) */
+  void* x_out;        /* bf16 [64][hidden] layer output; must not be x */
+  int hidden, inter;
+  const void* ln1;    /* bf16 [hidden] */
+  const void* wqkv;   /* bf16 [4096][hidden] */
+  const void* q_norm; /* bf16 [128] */
+  const void* k_norm; /* bf16 [128] */
+  const void* wo;     /* bf16 [hidden][2048] */
+  const void* ln2;    /* bf16 [hidden] */
+  const void* w1;     /* bf16 [inter][hidden] (gate) */
+  const void* w3;     /* bf16 [inter][hidden] (up) */
+  const void* w2;     /* bf16 [hidden][inter] (down) */
+  void* k_cache;      /* bf16 [8][Smax][128] */
+  void* v_cache;
+  void* q_rope;       /* optional bf16 [16][64][128]: the normalised, roped q (NULL to skip) */
+} ea_decoder_layer_args;
+
+/* Bytes of workspace for expert_decoder_layer on the current device (0 for invalid widths or
+ * no suitable device). The workspace must be 256-byte aligned and cleared once with
+ * expert_attn_workspace_init; expert_attn_read_status reads its status word. */
+size_t expert_decoder_layer_workspace_size(int hidden, int inter);
+
+/* One decoder layer (see above): ten kernels on the stream (the RMSNorms, four projections on
+ * the tensor cores with their finishing kernels, and the attention kernel). */
+int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int rope_delta,
+                         void* workspace, size_t ws_bytes, ea_stream_t stream);
+
+/* One projection of the 64 tokens on the tensor cores: y[64][N] = x[64][K] W^T in bf16 with fp32
+ * accumulation (W bf16 [N][K]); K a multiple of 64, N a multiple of 128, device pointers
+ * 16-byte aligned; the workspace (size from expert_linear64_workspace_size, 256-byte aligned,
+ * cleared once with expert_attn_workspace_init) holds the status word and the partial sums. */
+size_t expert_linear64_workspace_size(int K, int N);
+int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* workspace,
+                    size_t ws_bytes, ea_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

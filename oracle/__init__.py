@@ -12,9 +12,13 @@ expert_attention : the per-layer attention of the flow-matching action expert
 fp8_e4m3         : the OCP E4M3 ("e4m3fn") code table, a round-to-nearest-even
                    saturating encoder, and the per-(kv head, 128-row block)
                    cache quantiser used by the FP8 cache variant.
+decoder_layer    : the whole decoder layer around that attention (RMSNorm, fused
+                   qkv projection, head split, attention, head concat, wo, residual,
+                   RMSNorm, SwiGLU MLP, residual), for synthetic weights.
 
-Every function is pinned by ``tests/test_oracle_pins.py`` against closed forms,
-invariants, brute force on tiny inputs and independent library routines.
+Every function is pinned by ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_layer_pins.py`` against closed forms, invariants, brute force on tiny
+inputs and independent library routines.
 """
 from .expert_attention import (  # noqa: F401
     D, EPS, HQ, HKV, MASK_MIN, REP, T, THETA,
@@ -24,4 +28,8 @@ from .expert_attention import (  # noqa: F401
 from .fp8_e4m3 import (  # noqa: F401
     E4M3_MAX, decode_e4m3, dequantize_cache, e4m3_magnitudes, encode_e4m3_rne_sat,
     quantize_cache_blocks, quantize_tail_rows,
+)
+from .decoder_layer import (  # noqa: F401
+    HIDDEN, INTER, KV_DIM, Q_DIM, QKV_DIM, concat_heads, expert_layer, linear, silu,
+    split_qkv_heads, swiglu_mlp,
 )

@@ -24,13 +24,14 @@ def h():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(expert_attn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(expert_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("expert_attn_prologue", "expert_attn_layer", "expert_attn_layers",
-              "expert_attn_workspace_size", "expert_attn_status_string"):
+              "expert_attn_workspace_size", "expert_attn_status_string", "expert_decoder_layer",
+              "expert_decoder_layer_workspace_size", "expert_linear64"):
         assert n in names
 
 
@@ -99,3 +100,43 @@ def test_selftest_rejects_bad_arguments_without_gpu(h):
     assert h.expert_attn_selftest_wait_timeout(1000, ws, 16, None) == _lib.EA_ERR_INVALID_ARG
     assert h.expert_attn_selftest_wait_timeout(1000, ctypes.c_void_p(0x10010), 1 << 20, None) == \
         _lib.EA_ERR_MISALIGNED
+
+
+def _layer_args(**over):
+    a = _lib.EaDecoderLayerArgs()
+    for n, t in _lib.EaDecoderLayerArgs._fields_:
+        if t is ctypes.c_void_p:
+            setattr(a, n, 0x10000)
+    a.x_out = 0x20000
+    a.q_rope = None
+    a.hidden, a.inter = 1536, 6144
+    for k, v in over.items():
+        setattr(a, k, v)
+    return ctypes.byref(a)
+
+
+def test_decoder_layer_rejects_bad_arguments_without_gpu(h):
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 30
+    assert h.expert_decoder_layer(None, 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(), 10, 512, 0, None, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(hidden=1500), 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(inter=64), 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(hidden=16384), 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(w2=None), 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(wo=0x10008), 10, 512, 0, ws, big, None) == _lib.EA_ERR_MISALIGNED
+    assert h.expert_decoder_layer(_layer_args(x_out=0x10000), 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_decoder_layer(_layer_args(), 10, 512, 0, ctypes.c_void_p(0x100080), big, None) == \
+        _lib.EA_ERR_MISALIGNED
+    assert h.expert_decoder_layer_workspace_size(1500, 6144) == 0
+
+
+def test_linear64_rejects_bad_arguments_without_gpu(h):
+    ws = ctypes.c_void_p(0x100000)
+    p = ctypes.c_void_p(0x10000)
+    big = 1 << 30
+    assert h.expert_linear64(None, p, p, 64, 128, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert h.expert_linear64(p, p, p, 96, 128, ws, big, None) == _lib.EA_ERR_INVALID_ARG   # K % 64
+    assert h.expert_linear64(p, p, p, 64, 192, ws, big, None) == _lib.EA_ERR_INVALID_ARG   # N % 128
+    assert h.expert_linear64(ctypes.c_void_p(0x10004), p, p, 64, 128, ws, big, None) == _lib.EA_ERR_MISALIGNED
+    assert h.expert_linear64_workspace_size(96, 128) == 0

@@ -1,0 +1,98 @@
+"""GPU parity of the whole decoder layer and of its tensor-core projection (through the C ABI)
+against the fp64 CPU oracle.
+
+Projection bar (expert_linear64): every output within one bf16 step of the exact product plus
+the fp32 accumulation bound K * 2^-24 * sum_k |x_k w_k|.
+Layer bar (expert_decoder_layer): the output x2 within relative L2 6e-3 and max-abs 6e-2 of the
+oracle. Derivation: an emulation of the device's arithmetic (bf16 storage of h, q/k/v, the
+attention output, x1, h2, silu(gate)*up and x2; fp32 products) against the fp64 oracle gives
+relative L2 2.9e-3 and max-abs 2.3e-2 at the model's widths (|x2| reaches 5, where one bf16
+step is 0.03); the bar is about twice that.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_long_gb300 as ea
+import oracle
+from gqa_attention_long_gb300.inputs import expert_layer_weights, layer_inputs, residual_stream
+from tests._gpu_util import bf16_ulp, check_status, f64
+
+pytestmark = pytest.mark.gpu
+
+LAYER_REL_L2 = 6e-3
+LAYER_MAX_ABS = 6e-2
+
+
+@pytest.mark.parametrize("K,N", [(64, 128), (448, 384), (1536, 4096), (2048, 1536), (6144, 1536),
+                                 (1536, 12288)])
+def test_linear64_matches_exact_product(K, N):
+    rng = np.random.Generator(np.random.PCG64(K * 7 + N))
+    x = torch.from_numpy(rng.standard_normal((64, K)).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32)).to(torch.bfloat16)
+    d = torch.device("cuda")
+    y = torch.full((64, N), float("nan"), dtype=torch.bfloat16, device=d)
+    ws = torch.empty(ea.expert_linear64_workspace_size(K, N), dtype=torch.uint8, device=d)
+    ea.expert_attn_workspace_init(ws)
+    ea.expert_linear64(x.to(d), w.to(d), y, ws)
+    torch.cuda.synchronize()
+    check_status(ws)
+    xf, wf = f64(x), f64(w)
+    ref = xf @ wf.T
+    bound = bf16_ulp(ref) + K * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf).T)
+    err = np.abs(f64(y) - ref)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3f}"
+
+
+def _layer_on_device(x_in, w, lay):
+    d = torch.device("cuda")
+    wd = type(w)(**{k: v.to(d) for k, v in w.__dict__.items()})
+    return (x_in.to(d), wd, lay.k_cache.to(d), lay.v_cache.to(d))
+
+
+def run_layer(seed, S, Smax, hidden=1536, inter=6144, rope_delta=0, want_q_rope=False):
+    lay = layer_inputs(seed, S, Smax)
+    w = expert_layer_weights(seed, hidden=hidden, inter=inter)
+    xs = residual_stream(seed, hidden=hidden)
+    x, wd, kc, vc = _layer_on_device(xs, w, lay)
+    out = torch.full_like(x, float("nan"))
+    q_rope = torch.zeros(16, 64, 128, dtype=torch.bfloat16, device=x.device) if want_q_rope else None
+    ws = ea.alloc_decoder_layer_workspace(hidden, inter)
+    ea.expert_decoder_layer(x, out, wd, kc, vc, S, Smax, rope_delta, ws, q_rope=q_rope)
+    torch.cuda.synchronize()
+    check_status(ws)
+    r = oracle.expert_layer(f64(xs), {k: f64(v) for k, v in w.__dict__.items()}, f64(lay.k_cache),
+                            f64(lay.v_cache), S, Smax, rope_delta)
+    return out, r, kc, q_rope, (x, wd, kc, vc, ws)
+
+
+def assert_layer_close(got, ref, what="x2"):
+    assert np.all(np.isfinite(got)), "non-finite output"
+    mx = float(np.max(np.abs(got - ref)))
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert mx <= LAYER_MAX_ABS and rel <= LAYER_REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rel:.3e}"
+
+
+@pytest.mark.parametrize("S,Smax", [(256, 512), (4700, 8192)])
+def test_decoder_layer_matches_oracle(S, Smax):
+    out, r, _, _, _ = run_layer(11, S, Smax)
+    assert_layer_close(f64(out), r["x2"], f"S={S}")
+
+
+def test_decoder_layer_small_widths_and_rope_delta():
+    out, r, kc, q_rope, _ = run_layer(12, 1000, 1152, hidden=256, inter=384, rope_delta=-9, want_q_rope=True)
+    assert_layer_close(f64(out), r["x2"])
+    # the roped q and the own K rows derive from bf16 projection outputs, so they are compared
+    # in relative L2 (a few bf16 steps)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)  # noqa: E731
+    assert rel(f64(q_rope), r["q_rope"]) < 1e-2
+    assert rel(f64(kc[:, 1152 - 64:]), r["k_store"]) < 1e-2
+
+
+def test_decoder_layer_repeatable_bitwise():
+    out, _, _, _, (x, wd, kc, vc, ws) = run_layer(13, 700, 1024, hidden=512, inter=1024)
+    again = torch.full_like(out, float("nan"))
+    ea.expert_decoder_layer(x, again, wd, kc, vc, 700, 1024, 0, ws)
+    torch.cuda.synchronize()
+    check_status(ws)
+    assert torch.equal(out, again)

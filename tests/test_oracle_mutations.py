@@ -78,3 +78,59 @@ def test_unpatched_pins_pass():
     for _, _, pin in MUTATIONS:
         pin()
     assert math.isfinite(1.0)
+
+
+# ------------------------------------------------------------------ whole-layer oracle
+import oracle.decoder_layer as el  # noqa: E402
+from tests import test_oracle_layer_pins as lpins  # noqa: E402
+
+
+def _silu_wrong(x):
+    x = np.asarray(x, np.float64)
+    return x / (1.0 + np.exp(x))                              # planted: sigmoid(-x)
+
+
+def _split_kv_swapped(qkv):
+    q, k, v = _split_reference(qkv)
+    return q, v, k                                            # planted: k and v swapped
+
+
+def _split_reference(qkv):
+    q = qkv[:, :2048].reshape(64, 16, 128).transpose(1, 0, 2)
+    k = qkv[:, 2048:3072].reshape(64, 8, 128).transpose(1, 0, 2)
+    v = qkv[:, 3072:].reshape(64, 8, 128).transpose(1, 0, 2)
+    return q, k, v
+
+
+def _concat_no_transpose(a):
+    return np.asarray(a, np.float64).reshape(64, 2048)       # planted: heads not interleaved per token
+
+
+def _layer_missing_residual(x, w, k_cache, v_cache, S, Smax, rope_delta):
+    r = _original_layer(x, w, k_cache, v_cache, S, Smax, rope_delta)
+    r["x2"] = r["x2"] - r["x1"]                               # planted: second residual dropped
+    return r
+
+
+_original_layer = el.expert_layer
+
+LAYER_MUTATIONS = [
+    ("silu", _silu_wrong, lpins.test_matches_torch_composition),
+    ("split_qkv_heads", _split_kv_swapped, lpins.test_kv_split_order),
+    ("concat_heads", _concat_no_transpose, lpins.test_matches_torch_composition),
+    ("expert_layer", _layer_missing_residual, lpins.test_zero_output_projections_leave_the_residual_stream),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", LAYER_MUTATIONS, ids=[m[0] for m in LAYER_MUTATIONS])
+def test_layer_pin_catches_planted_mistake(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(el, name, bad)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_unpatched_layer_pins_pass():
+    for _, _, pin in LAYER_MUTATIONS:
+        pin()
