@@ -38,6 +38,15 @@ def algo_bytes_per_layer(S: int, b: int = 2) -> int:
     return 2 * HKV * S * D * b + 2 * (2 * HKV * T * D * b) + (HQ + 2 * HKV) * T * D * 2 + HQ * T * D * 2
 
 
+def layer_bytes(S: int, hidden: int = 1536, inter: int = 6144) -> int:
+    """Algorithmic HBM bytes of one whole decoder layer: its bf16 weights (wqkv, wo, w1, w3, w2
+    and the norm gains), the live cache K/V rows, the own K/V rows written and read back, and
+    the residual stream read and written (the activations between the steps are intermediates)."""
+    weights = 2 * (4096 * hidden + hidden * 2048 + 3 * inter * hidden + 2 * hidden + 2 * D)
+    cache = 2 * HKV * S * D * 2 + 2 * (2 * HKV * T * D * 2)
+    return weights + cache + 2 * (2 * T * hidden)
+
+
 def algo_bytes_per_layer_fp8(S: int) -> int:
     """As algo_bytes_per_layer for an e4m3 cache (1-byte K/V codes; block scales negligible)."""
     return 2 * HKV * S * D + 2 * (2 * HKV * T * D) + (HQ + 2 * HKV) * T * D * 2 + HQ * T * D * 2
@@ -407,6 +416,55 @@ def main():
                  "us_per_layer": msc * 1e3 / n, "ms_per_chain": msc,
                  "launches_per_layer": launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count)}
 
+    # ---- the whole decoder layer with synthetic weights (survey NEXT row 2): 8 distinct layers
+    # chained (layer i+1's input is layer i's output), one expert_decoder_layer call each,
+    # replayed as a CUDA graph; the weights (75.5 MB per layer) and caches of the 8 layers exceed
+    # L2, so every replay streams them from HBM
+    dlayer = None
+    if not args.no_extras and n >= 8:
+        from gqa_attention_long_gb300.inputs import expert_layer_weights_on_device
+        H, I, NL = 1536, 6144, 8
+        Wl = [expert_layer_weights_on_device(config_seed(5, l), dev) for l in range(NL)]
+        g5 = torch.Generator(device=dev).manual_seed(config_seed(5, 99))
+        xb = [torch.randn(T, H, generator=g5, device=dev).to(torch.bfloat16) for _ in range(NL + 1)]
+        wsl = ea.alloc_decoder_layer_workspace(H, I)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+
+        def layer_chain():
+            for l in range(NL):
+                ea.expert_decoder_layer(xb[l], xb[l + 1], Wl[l], xs[l].k_cache, xs[l].v_cache, S, Smax, 0,
+                                        wsl, stream=side)
+        with torch.cuda.stream(side):
+            layer_chain()  # warm-up outside the capture (tensor maps, attributes)
+        torch.cuda.synchronize()
+        graph_l = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_l, stream=side):
+            layer_chain()
+        for _ in range(args.warmup):
+            graph_l.replay()
+        torch.cuda.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(side)
+        with torch.cuda.stream(side):
+            for _ in range(args.steps):
+                graph_l.replay()
+        d1.record(side)
+        torch.cuda.synchronize()
+        stl, bitsl = ea.expert_attn_read_status(wsl)
+        if stl != 0:
+            raise RuntimeError(f"decoder layer status bits {bitsl:#x}")
+        msl = d0.elapsed_time(d1) / args.steps
+        lb = layer_bytes(S, H, I)
+        dlayer = {"workload": f"{NL} chained decoder layers (hidden {H}, inter {I}, synthetic bf16 weights "
+                              f"75.5 MB per layer), S={S}, Smax={Smax}, bf16 cache, one expert_decoder_layer call "
+                              f"each, replayed as a CUDA graph",
+                  "us_per_layer": msl * 1e3 / NL, "bytes_per_layer": lb,
+                  "hbm_gbs": lb * NL / (msl * 1e-3) / 1e9,
+                  "roofline_frac": lb * NL / (msl * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "launches_per_layer": 10}
+        del Wl, wsl
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         smp = oracle_sample(S, Smax, 8, 10.0)
@@ -435,6 +493,7 @@ def main():
             "fp8_step": fp8,
             "single_layer": single,
             "sequential_chain": chain,
+            "decoder_layer": dlayer,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

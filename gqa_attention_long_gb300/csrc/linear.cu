@@ -69,8 +69,6 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
-  // The activations are written by the previous kernel in the stream.
-  pdl_wait_primary();
 
   if (warp == 4) {
     if (lane == 0) {
@@ -78,14 +76,27 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       const uint64_t pol_x = l2_policy_evict_last();   // activations: read by every CTA
       const CUtensorMap* wm = &p.wmap[tile < p.tiles0 ? 0 : 1];
       const int row0 = (tile < p.tiles0 ? tile : tile - p.tiles0) * 128;
+      // The weights do not depend on the previous kernel in the stream (no kernel of this
+      // library writes them): their first ring stages are loaded, and the rest of this CTA's
+      // weight slice prefetched into L2, while that kernel may still run. The activations
+      // are its output: they are loaded only after griddepcontrol.wait.
+      const int pre = nk < kStages ? nk : kStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(full(i), kStage);
+        tma_load_2d(sbase + i * kStage, wm, full(i), (k0 + i) * 64, row0, pol_w);
+      }
+      for (int i = pre; i < nk; ++i) tma_prefetch_2d(wm, (k0 + i) * 64, row0);
+      pdl_wait_primary();
+      for (int i = 0; i < pre; ++i) {
+        const int kk = k0 + i;
+        tma_load_4d(sbase + i * kStage + kWTile, &p.xmap, full(i), 0, kk % p.c1, 0, kk / p.c1, pol_x);
+      }
       bool ok = true;
-      int i = 0;
+      int i = pre;
       for (; i < nk; ++i) {
         const int s = i % kStages;
-        if (i >= kStages) {
-          ok = bounded_wait(empty(s), ((i / kStages) - 1) & 1, abort_flag, p.status, kErrLinearWait);
-          if (!ok) break;
-        }
+        ok = bounded_wait(empty(s), ((i / kStages) - 1) & 1, abort_flag, p.status, kErrLinearWait);
+        if (!ok) break;
         const int kk = k0 + i;
         const uint32_t dst = sbase + s * kStage;
         mbar_expect_tx(full(s), kStage);
@@ -121,7 +132,9 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
   } else {
     // epilogue: thread r of warps 0-3 owns TMEM lane r = weight row 128 tile + r; its 64 columns
     // are the 64 tokens. part[split][t][n]: for a fixed token a warp's stores are 128
-    // contiguous bytes.
+    // contiguous bytes. (The partial buffer may still be read by the previous kernel in the
+    // stream until griddepcontrol.wait returns.)
+    pdl_wait_primary();
     const bool ok = bounded_wait(done, 0, abort_flag, p.status, kErrLinearWait);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
@@ -145,15 +158,26 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
 }
 
 // ----------------------------------------------------------------------- finishing kernels
-// Sum over the K splits of part[s][t][n .. n+3] (fp32, 16-byte aligned).
+// Sum over the K splits of part[s][t][n .. n+3] (fp32, 16-byte aligned), eight splits' loads
+// in flight at a time (the adds in split order).
 __device__ __forceinline__ float4 split_sum4(const float* part, int splits, int N, int t, int n) {
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < splits; ++s) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(part + (static_cast<size_t>(s) * kTok + t) * N + n));
-    a.x += v.x;
-    a.y += v.y;
-    a.z += v.z;
-    a.w += v.w;
+  const size_t stride = static_cast<size_t>(kTok) * N;
+  const float* p0 = part + static_cast<size_t>(t) * N + n;
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)  // unconditional loads (index clamped), so all eight are in flight
+      v[e] = __ldcg(reinterpret_cast<const float4*>(p0 + min(s0 + e, splits - 1) * stride));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (s0 + e < splits) {
+        a.x += v[e].x;
+        a.y += v[e].y;
+        a.z += v[e].z;
+        a.w += v[e].w;
+      }
+    }
   }
   return a;
 }
@@ -164,14 +188,14 @@ __device__ __forceinline__ float bf16_val(float x) { return __bfloat162float(__f
 // to y_out (if given); then, if gamma is given, h = gamma * y / sqrt(mean(y^2) + eps) over the
 // row's `width` channels, rounded to bf16 and stored to h_out. The layer's first RMSNorm
 // (no part), the wo finish (part, residual, norm) and the w2 finish (part, residual) use it.
-__global__ void __launch_bounds__(256) residual_norm_kernel(const float* part, int splits,
+__global__ void __launch_bounds__(384) residual_norm_kernel(const float* part, int splits,
                                                            const __nv_bfloat16* x, int width,
                                                            __nv_bfloat16* y_out,
                                                            const __nv_bfloat16* gamma,
                                                            __nv_bfloat16* h_out) {
   pdl_launch_dependents();
   pdl_wait_primary();
-  __shared__ float red[8];
+  __shared__ float red[32];
   __shared__ float row_y[kMaxHidden];
   const int t = blockIdx.x;
   float ss = 0.f;
@@ -290,7 +314,7 @@ cudaError_t launch_residual_norm(const float* part, int splits, const __nv_bfloa
                                  __nv_bfloat16* y_out, const __nv_bfloat16* gamma,
                                  __nv_bfloat16* h_out, cudaLaunchConfig_t cfg) {
   cfg.gridDim = dim3(kTok);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(384);  // one float4 of a 1536-wide row per thread
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, residual_norm_kernel, part, splits, x, width, y_out, gamma, h_out);
 }

@@ -185,7 +185,10 @@ int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S,
  * the steps are kept in bf16 and products accumulate in fp32. Widths: hidden and inter are
  * multiples of 128 with hidden <= 8192 and inter <= 32768 (the expert: 1536 and 6144). The
  * cache is bf16 [8][Smax][128] with the same rules as expert_attn_layer (rows [Smax-64, Smax)
- * are written). All pointers are device pointers, 16-byte aligned. */
+ * are written). All pointers are device pointers, 16-byte aligned. The projections start
+ * streaming their weights before the preceding kernel on the stream has finished when that
+ * kernel allows programmatic dependent launch (the library's own kernels do, ordinary
+ * launches do not), so weights must not be produced by such a kernel. */
 typedef struct {
   const void* x;      /* bf16 [64][hidden] layer input (residual stream) */
   void* x_out;        /* bf16 [64][hidden] layer output; must not be x */
