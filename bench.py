@@ -462,7 +462,7 @@ def main():
                   "us_per_layer": msl * 1e3 / NL, "bytes_per_layer": lb,
                   "hbm_gbs": lb * NL / (msl * 1e-3) / 1e9,
                   "roofline_frac": lb * NL / (msl * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                  "launches_per_layer": 10}
+                  "launches_per_layer": 8 if launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1 else 7}
         del Wl, wsl
 
     cpu = None

@@ -608,15 +608,8 @@ extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_lay
 namespace ea {
 cudaError_t linear_set_attributes();
 cudaError_t launch_linear(const LinearParams& lp, int tiles, int splits, cudaLaunchConfig_t cfg);
-cudaError_t launch_residual_norm(const float* part, int splits, const __nv_bfloat16* x, int width,
-                                 __nv_bfloat16* y_out, const __nv_bfloat16* gamma,
+cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, int width, const __nv_bfloat16* gamma,
                                  __nv_bfloat16* h_out, cudaLaunchConfig_t cfg);
-cudaError_t launch_qkv_heads(const float* part, int splits, __nv_bfloat16* q, __nv_bfloat16* k,
-                             __nv_bfloat16* v, cudaLaunchConfig_t cfg);
-cudaError_t launch_swiglu(const float* part, int splits, int inter, __nv_bfloat16* gu,
-                          cudaLaunchConfig_t cfg);
-cudaError_t launch_split_sum_bf16(const float* part, int splits, int N, __nv_bfloat16* y,
-                                  cudaLaunchConfig_t cfg);
 }  // namespace ea
 
 namespace {
@@ -675,11 +668,11 @@ bool bf16_map(const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_
   return true;
 }
 
-// Weights [rows][K] (row-major): 2-D {K, rows}, box {64, 128}.
-bool weight_map(const void* w, int K, int rows, CUtensorMap* out) {
+// Weights [rows][K] (row-major): 2-D {K, rows}, box {64, box_rows}.
+bool weight_map(const void* w, int K, int rows, int box_rows, CUtensorMap* out) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   return bf16_map(w, 2, dims, strides, box, out);
 }
 
@@ -702,31 +695,27 @@ bool heads_map(const void* a, CUtensorMap* out) {
   return bf16_map(a, 4, dims, strides, box, out);
 }
 
-// Split count of a projection: about two CTAs per SM (two fit), at least two k-steps per CTA
-// where the k-steps allow it, and no empty split.
+// Split count of a projection (the cluster size of a tile): about two CTAs per SM (two fit), at
+// least two k-steps per CTA where the k-steps allow it, at most 16 (the largest cluster), and no
+// empty split.
+constexpr int kMaxLinearCluster = 16;
 void plan_splits(int tiles, int ksteps, int sm_count, int* splits, int* kps) {
   int s = (2 * sm_count) / tiles;
   if (s > ksteps / 2) s = ksteps / 2;
+  if (s > kMaxLinearCluster) s = kMaxLinearCluster;
   if (s < 1) s = 1;
   *kps = (ksteps + s - 1) / s;
   *splits = (ksteps + *kps - 1) / *kps;
 }
 
-size_t part_floats(int N, int K, int sm_count) {
-  int splits, kps;
-  plan_splits(N / 128, K / 64, sm_count, &splits, &kps);
-  return static_cast<size_t>(splits) * kTok * N;
-}
-
 size_t align_kb(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 struct LayerWs {
-  size_t attn_ws, h, q, k, v, attn, x1, h2, gu, part, total;
+  size_t attn_ws, h, q, k, v, attn, x1, h2, gu, total;
 };
 
 // Layer workspace: the attention's own workspace first (its status word, at offset 0, is
-// the one every kernel of the layer reports to), then the layer's activations and the
-// projections' partial sums.
+// the one every kernel of the layer reports to), then the layer's bf16 activations.
 LayerWs layer_ws_layout(int hidden, int inter, int sm_count) {
   LayerWs w{};
   size_t off = 0;
@@ -745,12 +734,6 @@ LayerWs layer_ws_layout(int hidden, int inter, int sm_count) {
   w.x1 = take(static_cast<size_t>(kTok) * hidden * 2);
   w.h2 = take(static_cast<size_t>(kTok) * hidden * 2);
   w.gu = take(static_cast<size_t>(kTok) * inter * 2);
-  size_t pf = part_floats((kHq + 2 * kHkv) * kD, hidden, sm_count);
-  const size_t candidates[3] = {part_floats(hidden, kHq * kD, sm_count),
-                                part_floats(2 * inter, hidden, sm_count),
-                                part_floats(hidden, inter, sm_count)};
-  for (size_t c : candidates) pf = c > pf ? c : pf;
-  w.part = take(pf * sizeof(float));
   w.total = off;
   return w;
 }
@@ -760,30 +743,37 @@ bool layer_dims_ok(int hidden, int inter) {
          inter <= kMaxInter && inter % 128 == 0;
 }
 
-// One projection: part = X W^T (two weights side by side when w1 != nullptr).
-int run_linear(const CUtensorMap& xmap, int c1, const void* w0, int rows0, const void* w1, int rows1,
-               int K, float* part, uint32_t* status, int sm_count, cudaStream_t st, int* splits_out) {
+// One projection with its epilogue (LinearParams). w1 != nullptr: the gate/up pair of SwiGLU
+// (tiles of 64 features of both), else tiles of 128 output features.
+int run_linear(const CUtensorMap& xmap, int c1, const void* w0, const void* w1, int N, int K, int mode,
+               const __nv_bfloat16* res, __nv_bfloat16* y, __nv_bfloat16* q, __nv_bfloat16* k,
+               __nv_bfloat16* v, uint32_t* status, int sm_count, cudaStream_t st) {
   static_assert(sizeof(LinearParams) < 4096, "linear parameter block");
   LinearParams lp;
   std::memset(&lp, 0, sizeof(lp));
-  if (!weight_map(w0, K, rows0, &lp.wmap[0])) return EA_ERR_CUDA;
-  if (w1 != nullptr && !weight_map(w1, K, rows1, &lp.wmap[1])) return EA_ERR_CUDA;
+  const bool pair = w1 != nullptr;
+  if (!weight_map(w0, K, N, pair ? 64 : 128, &lp.wmap[0])) return EA_ERR_CUDA;
+  if (pair && !weight_map(w1, K, N, 64, &lp.wmap[1])) return EA_ERR_CUDA;
   lp.xmap = xmap;
-  lp.part = part;
   lp.status = status;
-  lp.N = rows0 + (w1 != nullptr ? rows1 : 0);
-  lp.tiles0 = rows0 / 128;
+  lp.res = res;
+  lp.y = y;
+  lp.q = q;
+  lp.k = k;
+  lp.v = v;
+  lp.N = N;
   lp.ksteps = K / 64;
   lp.c1 = c1;
+  lp.mode = mode;
+  const int tiles = pair ? N / 64 : N / 128;
   int splits, kps;
-  plan_splits(lp.N / 128, lp.ksteps, sm_count, &splits, &kps);
+  plan_splits(tiles, lp.ksteps, sm_count, &splits, &kps);
   lp.kps = kps;
-  cudaLaunchAttribute attr[1];
-  if (launch_linear(lp, lp.N / 128, splits, launch_config(st, attr, true)) != cudaSuccess) {
+  cudaLaunchAttribute attr[2];  // PDL, and the cluster shape added by the launcher
+  if (launch_linear(lp, tiles, splits, launch_config(st, attr, true)) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
-  *splits_out = splits;
   return EA_OK;
 }
 
@@ -829,12 +819,10 @@ int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int ro
   if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
-  float* part = reinterpret_cast<float*>(ws + wl.part);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + wl.attn_ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a->x);
   cudaLaunchAttribute attr[1];
-  int splits = 1;
 
   // the attention step's arguments (validated like any expert_attn_layer call)
   ea_layer_args la;
@@ -856,56 +844,41 @@ int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int ro
       !rows_map(bf(wl.h2), H, &xm_h2) || !rows_map(bf(wl.gu), I, &xm_gu))
     return EA_ERR_CUDA;
   // h = rms_norm(x, ln1)
-  if (launch_residual_norm(nullptr, 0, x, H, nullptr, static_cast<const __nv_bfloat16*>(a->ln1),
-                           bf(wl.h), launch_config(st, attr, true)) != cudaSuccess) {
+  if (launch_rms_norm_rows(x, H, static_cast<const __nv_bfloat16*>(a->ln1), bf(wl.h),
+                           launch_config(st, attr, true)) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
   // q, k, v = heads of h wqkv^T
-  rc = run_linear(xm_h, H / 64, a->wqkv, (kHq + 2 * kHkv) * kD, nullptr, 0, H, part, status,
-                  di.sm_count, st, &splits);
+  rc = run_linear(xm_h, H / 64, a->wqkv, nullptr, (kHq + 2 * kHkv) * kD, H, kLinQkvHeads, nullptr,
+                  nullptr, bf(wl.q), bf(wl.k), bf(wl.v), status, di.sm_count, st);
   if (rc != EA_OK) return rc;
-  if (launch_qkv_heads(part, splits, bf(wl.q), bf(wl.k), bf(wl.v), launch_config(st, attr, true)) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
   // attention (q/k norm, RoPE, own rows into the cache tail, split-KV attention, merge)
   rc = launch_chunk(&la, 1, S, Smax, rope_delta, false, ws + wl.attn_ws, ws_layout(1, di.sm_count, false),
                     di, st, nullptr);
   if (rc != EA_OK) return rc;
-  // x1 = x + concat_heads(attn) wo^T; h2 = rms_norm(x1, ln2)
-  rc = run_linear(xm_attn, 2, a->wo, H, nullptr, 0, kHq * kD, part, status, di.sm_count, st, &splits);
+  // x1 = x + concat_heads(attn) wo^T
+  rc = run_linear(xm_attn, 2, a->wo, nullptr, H, kHq * kD, kLinResidual, x, bf(wl.x1), nullptr, nullptr,
+                  nullptr, status, di.sm_count, st);
   if (rc != EA_OK) return rc;
-  if (launch_residual_norm(part, splits, x, H, bf(wl.x1), static_cast<const __nv_bfloat16*>(a->ln2),
-                           bf(wl.h2), launch_config(st, attr, true)) != cudaSuccess) {
+  // h2 = rms_norm(x1, ln2)
+  if (launch_rms_norm_rows(bf(wl.x1), H, static_cast<const __nv_bfloat16*>(a->ln2), bf(wl.h2),
+                           launch_config(st, attr, true)) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
   // gu = silu(h2 w1^T) * (h2 w3^T)
-  rc = run_linear(xm_h2, H / 64, a->w1, I, a->w3, I, H, part, status, di.sm_count, st, &splits);
+  rc = run_linear(xm_h2, H / 64, a->w1, a->w3, I, H, kLinSwiglu, nullptr, bf(wl.gu), nullptr, nullptr,
+                  nullptr, status, di.sm_count, st);
   if (rc != EA_OK) return rc;
-  if (launch_swiglu(part, splits, I, bf(wl.gu), launch_config(st, attr, true)) != cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
   // x_out = x1 + gu w2^T
-  rc = run_linear(xm_gu, I / 64, a->w2, H, nullptr, 0, I, part, status, di.sm_count, st, &splits);
-  if (rc != EA_OK) return rc;
-  if (launch_residual_norm(part, splits, bf(wl.x1), H, static_cast<__nv_bfloat16*>(a->x_out), nullptr,
-                           nullptr, launch_config(st, attr, true)) != cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
-  return EA_OK;
+  return run_linear(xm_gu, I / 64, a->w2, nullptr, H, I, kLinResidual, bf(wl.x1),
+                    static_cast<__nv_bfloat16*>(a->x_out), nullptr, nullptr, nullptr, status, di.sm_count, st);
 }
 
 size_t expert_linear64_workspace_size(int K, int N) {
   if (K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0) return 0;
-  int dev;
-  DeviceInfo di;
-  if (!device_info(&dev, &di)) return 0;
-  return 1024 + align_kb(part_floats(N, K, di.sm_count) * sizeof(float));
+  return 1024;  // the status word (partial sums stay in the clusters' shared memory)
 }
 
 int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* workspace,
@@ -915,26 +888,15 @@ int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* w
     return EA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return EA_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EA_ERR_MISALIGNED;
+  if (ws_bytes < 1024) return EA_ERR_WORKSPACE;
   int dev;
   DeviceInfo di;
   if (!device_info(&dev, &di) || !linear_attrs_ready()) return EA_ERR_UNSUPPORTED;
-  if (ws_bytes < 1024 + align_kb(part_floats(N, K, di.sm_count) * sizeof(float))) return EA_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  float* part = reinterpret_cast<float*>(ws + 1024);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   CUtensorMap xm;
   if (!rows_map(x, K, &xm)) return EA_ERR_CUDA;
-  int splits = 1;
-  int rc = run_linear(xm, K / 64, w, N, nullptr, 0, K, part, status, di.sm_count, st, &splits);
-  if (rc != EA_OK) return rc;
-  cudaLaunchAttribute attr[1];
-  if (launch_split_sum_bf16(part, splits, N, static_cast<__nv_bfloat16*>(y), launch_config(st, attr, true)) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
-  return EA_OK;
+  return run_linear(xm, K / 64, w, nullptr, N, K, kLinPlain, nullptr, static_cast<__nv_bfloat16*>(y),
+                    nullptr, nullptr, nullptr, static_cast<uint32_t*>(workspace), di.sm_count,
+                    static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -147,22 +147,28 @@ struct AttnParams {
 constexpr int kMaxHidden = 8192;   // widest residual stream the finishing kernels take
 constexpr int kMaxInter = 32768;
 
-// One projection Y[t][n] = sum_k X[t][k] W[n][k] for the 64 tokens (linear.cu). The weights of
-// tiles [0, tiles0) come from wmap[0], the rest from wmap[1] (two projections of the same input
-// side by side: the gate and up projections of the MLP). Each weight map is 2-D {K, rows} with
-// a {64, 128} box; the activation map is 4-D {64, c1, 64, c3} with a {64, 1, 64, 1} box, k-step
-// kk at coordinates (0, kk % c1, 0, kk / c1) (row-major X: c1 = K / 64, c3 = 1; the attention
-// output [16][64][128]: c1 = 2 halves of a head, c3 = 16 heads).
+// One projection Y[t][n] = sum_k X[t][k] W[n][k] for the 64 tokens (linear.cu), with the
+// epilogue `mode`. Each weight map is 2-D {K, rows} with a {64, 128} box ({64, 64} for the
+// gate/up pair of kLinSwiglu, whose tile i takes rows [64 i, 64 i + 64) of wmap[0] and of
+// wmap[1]); the activation map is 4-D {64, c1, 64, c3} with a {64, 1, 64, 1} box, k-step kk at
+// coordinates (0, kk % c1, 0, kk / c1) (row-major X: c1 = K / 64, c3 = 1; the attention output
+// [16][64][128]: c1 = 2 halves of a head, c3 = 16 heads).
+enum : int { kLinPlain = 0, kLinResidual = 1, kLinQkvHeads = 2, kLinSwiglu = 3 };
+
 struct LinearParams {
   CUtensorMap wmap[2];
   CUtensorMap xmap;
-  float* part;       // [splits][64][N] fp32 partial sums
-  uint32_t* status;  // workspace status word
-  int N;             // output features (all tiles), a multiple of 128
-  int tiles0;
-  int ksteps;        // K / 64
-  int kps;           // k-steps per split
+  uint32_t* status;          // workspace status word
+  const __nv_bfloat16* res;  // kLinResidual: residual input [64][N]
+  __nv_bfloat16* y;          // kLinPlain, kLinResidual, kLinSwiglu: output [64][N]
+  __nv_bfloat16* q;          // kLinQkvHeads: [16][64][128], k and v [8][64][128]
+  __nv_bfloat16* k;
+  __nv_bfloat16* v;
+  int N;                     // output features (kLinSwiglu: of the gate projection alone)
+  int ksteps;                // K / 64
+  int kps;                   // k-steps per split (the splits of a tile form one cluster)
   int c1;
+  int mode;
 };
 
 // Units split across CTAs, merged by the LSE merge kernel: at most one per CTA boundary.

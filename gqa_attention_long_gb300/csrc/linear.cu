@@ -1,6 +1,6 @@
 // linear.cu — the projections of the expert's decoder layer for its 64 tokens (Y = X W^T with
 // weights stored [out_features, in_features]) on the sm_103a tensor cores, and the small
-// kernels that finish the layer around them: RMSNorm, head split, residual adds, SwiGLU.
+// RMSNorm of the layer's residual stream.
 //
 // alpamayo_tt/expert.py, TTExpert.layer: rms_norm(x, ln1); the fused wqkv projection and
 // nlp_create_qkv_heads; after the attention, nlp_concat_heads, wo and the residual add;
@@ -11,9 +11,11 @@
 // X[t][k]: 128 weight rows form the M = 128 operand A and the 64 tokens the N = 64 operand B of
 // tcgen05.mma (kind::f16, bf16 in, fp32 accumulator in 64 TMEM columns). To spread the weights
 // over every SM the K dimension is split: CTA (tile, split) streams weight rows [128 tile,
-// 128 tile + 128) over its range of 64-channel k-steps, and writes its fp32 partial
-// D[t][n] into part[split][t][n]; a finishing kernel sums the splits and applies the layer's
-// epilogue. Two CTAs fit on an SM (96 KB ring, 64 TMEM columns each).
+// 128 tile + 128) over its range of 64-channel k-steps. The splits of a tile form one thread-
+// block cluster, which sums its fp32 partials through distributed shared memory and writes
+// the projection's output with its epilogue (head split, residual add, SwiGLU) applied, so no
+// partial sum travels through global memory. Two CTAs fit on an SM (96 KB ring, 64 TMEM
+// columns each).
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -30,8 +32,51 @@ constexpr uint32_t SM_TMEM = SM_BAR + (2 * kStages + 1) * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;   // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 64;
+constexpr int kMaxCluster = 16;                         // K splits of one tile = one cluster
+static_assert(kTok * 128 * 4 <= kStages * kStage, "the fp32 tile fits in the drained ring");
 }  // namespace lin
 
+// Sum over the cluster's S CTAs (in rank order) of the float4 at shared address `addr` of each,
+// four 16-byte remote loads in flight at a time.
+__device__ __forceinline__ float4 cluster_sum4(uint32_t addr, uint32_t S) {
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t p0 = 0; p0 < S; p0 += 4) {
+    float4 v[4];
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) v[e] = ld_shared_cluster_v4(mapa_shared(addr, min(p0 + e, S - 1)));
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) {
+      if (p0 + e < S) {
+        a.x += v[e].x;
+        a.y += v[e].y;
+        a.z += v[e].z;
+        a.w += v[e].w;
+      }
+    }
+  }
+  return a;
+}
+
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+  uint2 o;
+  o.x = pack_bf16x2(a, b);
+  o.y = pack_bf16x2(c, d);
+  return o;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g * __frcp_rn(1.0f + expf(-g)) * u; }
+
+// One projection tile: CTA (tile, split) of a cluster of the tile's S splits. Its MMAs leave the
+// split's fp32 partial D[row][token] in TMEM; the epilogue warps move it into the (drained)
+// ring as [token][row]; after a cluster barrier every CTA sums, for its share of the tile, the
+// S partials read from the cluster's shared memory (in split order, so the result does not
+// depend on timing), and applies the projection's epilogue:
+//   kLinPlain     y[t][n] = sum                      (y row-major [64][N])
+//   kLinResidual  y[t][n] = res[t][n] + sum          (rounded once, to bf16)
+//   kLinQkvHeads  tile h = features [128 h, 128 h + 128): q head h (h < 16), k head h - 16
+//                 (h < 24) or v head h - 24, written head-major [head][t][d]
+//   kLinSwiglu    the tile's rows are 64 gate rows (wmap[0]) then the same 64 up rows
+//                 (wmap[1]); y[t][64 tile + j] = silu(gate_j) * up_j
 __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_constant__ LinearParams p) {
   using namespace lin;
   extern __shared__ uint8_t smem_raw[];
@@ -45,6 +90,7 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_ABORT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
+  const bool pair = p.mode == kLinSwiglu;
   const int k0 = split * p.kps;
   const int nk = min(p.kps, p.ksteps - k0);  // >= 1 by the host's choice of the split count
 
@@ -62,7 +108,8 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
     tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
-    prefetch_tensormap(&p.wmap[tile < p.tiles0 ? 0 : 1]);
+    prefetch_tensormap(&p.wmap[0]);
+    if (pair) prefetch_tensormap(&p.wmap[1]);
     prefetch_tensormap(&p.xmap);
   }
   tc_fence_before();
@@ -74,8 +121,12 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();  // weights: read once
       const uint64_t pol_x = l2_policy_evict_last();   // activations: read by every CTA
-      const CUtensorMap* wm = &p.wmap[tile < p.tiles0 ? 0 : 1];
-      const int row0 = (tile < p.tiles0 ? tile : tile - p.tiles0) * 128;
+      const int row0 = tile * (pair ? 64 : 128);
+      auto load_w = [&](int s, int kk) {  // one stage's weight rows (two 64-row boxes for a pair)
+        const uint32_t dst = sbase + s * kStage;
+        tma_load_2d(dst, &p.wmap[0], full(s), kk * 64, row0, pol_w);
+        if (pair) tma_load_2d(dst + kWTile / 2, &p.wmap[1], full(s), kk * 64, row0, pol_w);
+      };
       // The weights do not depend on the previous kernel in the stream (no kernel of this
       // library writes them): their first ring stages are loaded, and the rest of this CTA's
       // weight slice prefetched into L2, while that kernel may still run. The activations
@@ -83,9 +134,12 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       const int pre = nk < kStages ? nk : kStages;
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(full(i), kStage);
-        tma_load_2d(sbase + i * kStage, wm, full(i), (k0 + i) * 64, row0, pol_w);
+        load_w(i, k0 + i);
       }
-      for (int i = pre; i < nk; ++i) tma_prefetch_2d(wm, (k0 + i) * 64, row0);
+      for (int i = pre; i < nk; ++i) {
+        tma_prefetch_2d(&p.wmap[0], (k0 + i) * 64, row0);
+        if (pair) tma_prefetch_2d(&p.wmap[1], (k0 + i) * 64, row0);
+      }
       pdl_wait_primary();
       for (int i = 0; i < pre; ++i) {
         const int kk = k0 + i;
@@ -98,13 +152,12 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
         ok = bounded_wait(empty(s), ((i / kStages) - 1) & 1, abort_flag, p.status, kErrLinearWait);
         if (!ok) break;
         const int kk = k0 + i;
-        const uint32_t dst = sbase + s * kStage;
         mbar_expect_tx(full(s), kStage);
-        tma_load_2d(dst, wm, full(s), kk * 64, row0, pol_w);
-        tma_load_4d(dst + kWTile, &p.xmap, full(s), 0, kk % p.c1, 0, kk / p.c1, pol_x);
+        load_w(s, kk);
+        tma_load_4d(sbase + s * kStage + kWTile, &p.xmap, full(s), 0, kk % p.c1, 0, kk / p.c1, pol_x);
       }
       pdl_launch_dependents();
-      if (!ok) {  // let the copies already issued land before the CTA gives its shared memory back
+      if (!ok) {  // let the copies already issued land before the ring is reused or released
         for (int j = (i > kStages ? i - kStages : 0); j < i; ++j)
           if (!drain_wait(full(j % kStages), (j / kStages) & 1)) atomicOr(p.status, kErrDrain);
       }
@@ -130,16 +183,12 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       if (!drain_wait(done, 0)) atomicOr(p.status, kErrDrain);
     }
   } else {
-    // epilogue: thread r of warps 0-3 owns TMEM lane r = weight row 128 tile + r; its 64 columns
-    // are the 64 tokens. part[split][t][n]: for a fixed token a warp's stores are 128
-    // contiguous bytes. (The partial buffer may still be read by the previous kernel in the
-    // stream until griddepcontrol.wait returns.)
-    pdl_wait_primary();
+    // thread r of warps 0-3 owns TMEM lane r (tile row r); its 64 columns are the 64 tokens.
+    // The split's partial goes to shared memory as [token][row] (conflict-free stores).
     const bool ok = bounded_wait(done, 0, abort_flag, p.status, kErrLinearWait);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int r = warp * 32 + lane;
-      float* dst = p.part + static_cast<size_t>(split) * kTok * p.N + static_cast<size_t>(tile) * 128 + r;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t v[32];
@@ -147,82 +196,73 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
         tmem_wait_ld();
         reg_fence32(v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(32 * h + e) * p.N] = __uint_as_float(v[e]);
+        for (int e = 0; e < 32; ++e)
+          st_shared_f32(sbase + static_cast<uint32_t>((32 * h + e) * 128 + r) * 4u, __uint_as_float(v[e]));
       }
     }
   }
+  // every CTA of the cluster has its partial in shared memory
+  cluster_sync();
+  if (warp < 4) {
+    // outputs are written, and the residual read, only after the previous kernel has finished
+    pdl_wait_primary();
+    const uint32_t S = gridDim.y, q = cluster_ctarank();
+    const int i = threadIdx.x;
+    const int per_t = pair ? 16 : 32;  // float4 items per token: (gate) rows of the tile / 4
+    const int n_items = kTok * per_t;
+    for (int item = static_cast<int>(q) * 128 + i; item < n_items; item += static_cast<int>(S) * 128) {
+      const int t = item / per_t, c = 4 * (item % per_t);  // token, first row of the float4
+      const float4 a = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + c) * 4u, S);
+      if (p.mode == kLinSwiglu) {
+        const float4 u = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + 64 + c) * 4u, S);
+        *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(t) * p.N + tile * 64 + c) =
+            pack_bf16x4(silu_mul(a.x, u.x), silu_mul(a.y, u.y), silu_mul(a.z, u.z), silu_mul(a.w, u.w));
+      } else if (p.mode == kLinQkvHeads) {
+        __nv_bfloat16* dst = tile < kHq ? p.q + static_cast<size_t>(tile) * kTok * kD
+                             : tile < kHq + kHkv ? p.k + static_cast<size_t>(tile - kHq) * kTok * kD
+                                                 : p.v + static_cast<size_t>(tile - kHq - kHkv) * kTok * kD;
+        *reinterpret_cast<uint2*>(dst + static_cast<size_t>(t) * kD + c) = pack_bf16x4(a.x, a.y, a.z, a.w);
+      } else {
+        const size_t o = static_cast<size_t>(t) * p.N + tile * 128 + c;
+        float4 b = a;
+        if (p.mode == kLinResidual) {
+          const uint2 rv = *reinterpret_cast<const uint2*>(p.res + o);
+          b.x += __uint_as_float(rv.x << 16);
+          b.y += __uint_as_float(rv.x & 0xFFFF0000u);
+          b.z += __uint_as_float(rv.y << 16);
+          b.w += __uint_as_float(rv.y & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint2*>(p.y + o) = pack_bf16x4(b.x, b.y, b.z, b.w);
+      }
+    }
+  }
+  // no CTA leaves (or reuses its shared memory) while a peer may still read it
+  cluster_sync();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ----------------------------------------------------------------------- finishing kernels
-// Sum over the K splits of part[s][t][n .. n+3] (fp32, 16-byte aligned), eight splits' loads
-// in flight at a time (the adds in split order).
-__device__ __forceinline__ float4 split_sum4(const float* part, int splits, int N, int t, int n) {
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  const size_t stride = static_cast<size_t>(kTok) * N;
-  const float* p0 = part + static_cast<size_t>(t) * N + n;
-  for (int s0 = 0; s0 < splits; s0 += 8) {
-    float4 v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)  // unconditional loads (index clamped), so all eight are in flight
-      v[e] = __ldcg(reinterpret_cast<const float4*>(p0 + min(s0 + e, splits - 1) * stride));
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (s0 + e < splits) {
-        a.x += v[e].x;
-        a.y += v[e].y;
-        a.z += v[e].z;
-        a.w += v[e].w;
-      }
-    }
-  }
-  return a;
-}
-
-__device__ __forceinline__ float bf16_val(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
-// One CTA per token row: y = x (+ the split sum of part, if given), rounded to bf16 and stored
-// to y_out (if given); then, if gamma is given, h = gamma * y / sqrt(mean(y^2) + eps) over the
-// row's `width` channels, rounded to bf16 and stored to h_out. The layer's first RMSNorm
-// (no part), the wo finish (part, residual, norm) and the w2 finish (part, residual) use it.
-__global__ void __launch_bounds__(384) residual_norm_kernel(const float* part, int splits,
-                                                           const __nv_bfloat16* x, int width,
-                                                           __nv_bfloat16* y_out,
+// ----------------------------------------------------------------------------- RMSNorm rows
+// One CTA per token row: h = gamma * x / sqrt(mean(x^2) + eps) over the row's `width` channels,
+// rounded to bf16 (the layer's two RMSNorms; x is the bf16 residual stream).
+__global__ void __launch_bounds__(384) rms_norm_rows_kernel(const __nv_bfloat16* x, int width,
                                                            const __nv_bfloat16* gamma,
                                                            __nv_bfloat16* h_out) {
   pdl_launch_dependents();
   pdl_wait_primary();
   __shared__ float red[32];
-  __shared__ float row_y[kMaxHidden];
   const int t = blockIdx.x;
+  const __nv_bfloat16* row = x + static_cast<size_t>(t) * width;
   float ss = 0.f;
   for (int n = 4 * threadIdx.x; n < width; n += 4 * blockDim.x) {
-    const uint2 xv = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * width + n);
-    float y[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
-                  __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
-    if (part != nullptr) {
-      const float4 a = split_sum4(part, splits, width, t, n);
-      y[0] = bf16_val(y[0] + a.x);
-      y[1] = bf16_val(y[1] + a.y);
-      y[2] = bf16_val(y[2] + a.z);
-      y[3] = bf16_val(y[3] + a.w);
-    }
-    if (y_out != nullptr) {
-      uint2 o;
-      o.x = pack_bf16x2(y[0], y[1]);
-      o.y = pack_bf16x2(y[2], y[3]);
-      *reinterpret_cast<uint2*>(y_out + static_cast<size_t>(t) * width + n) = o;
-    }
+    const uint2 xv = *reinterpret_cast<const uint2*>(row + n);
+    const float y[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
+                        __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      row_y[n + e] = y[e];
-      ss = fmaf(y[e], y[e], ss);
-    }
+    for (int e = 0; e < 4; ++e) ss = fmaf(y[e], y[e], ss);
   }
-  if (gamma == nullptr) return;
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -231,119 +271,46 @@ __global__ void __launch_bounds__(384) residual_norm_kernel(const float* part, i
   for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += red[w];
   const float rs = rsqrtf(tot / static_cast<float>(width) + 1e-6f);
   for (int n = 4 * threadIdx.x; n < width; n += 4 * blockDim.x) {
+    const uint2 xv = *reinterpret_cast<const uint2*>(row + n);
     const uint2 gv = *reinterpret_cast<const uint2*>(gamma + n);
+    const float y[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
+                        __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
     const float g[4] = {__uint_as_float(gv.x << 16), __uint_as_float(gv.x & 0xFFFF0000u),
                         __uint_as_float(gv.y << 16), __uint_as_float(gv.y & 0xFFFF0000u)};
-    uint2 o;
-    o.x = pack_bf16x2(g[0] * (row_y[n] * rs), g[1] * (row_y[n + 1] * rs));
-    o.y = pack_bf16x2(g[2] * (row_y[n + 2] * rs), g[3] * (row_y[n + 3] * rs));
-    *reinterpret_cast<uint2*>(h_out + static_cast<size_t>(t) * width + n) = o;
+    *reinterpret_cast<uint2*>(h_out + static_cast<size_t>(t) * width + n) =
+        pack_bf16x4(g[0] * (y[0] * rs), g[1] * (y[1] * rs), g[2] * (y[2] * rs), g[3] * (y[3] * rs));
   }
-}
-
-// The fused projection's split sums -> bf16 q [16][64][128], k and v [8][64][128]: feature
-// 128 h + d of the q (k, v) block is channel d of head h (nlp_create_qkv_heads).
-__global__ void __launch_bounds__(256) qkv_heads_kernel(const float* part, int splits,
-                                                       __nv_bfloat16* q, __nv_bfloat16* k,
-                                                       __nv_bfloat16* v) {
-  pdl_launch_dependents();
-  pdl_wait_primary();
-  constexpr int kN = (kHq + 2 * kHkv) * kD;  // 4096
-  const int t = blockIdx.y;
-  const int n = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (n >= kN) return;
-  const float4 a = split_sum4(part, splits, kN, t, n);
-  uint2 o;
-  o.x = pack_bf16x2(a.x, a.y);
-  o.y = pack_bf16x2(a.z, a.w);
-  const int head = n / kD, d = n % kD;
-  __nv_bfloat16* dst = head < kHq ? q + (static_cast<size_t>(head) * kTok + t) * kD
-                       : head < kHq + kHkv ? k + (static_cast<size_t>(head - kHq) * kTok + t) * kD
-                                           : v + (static_cast<size_t>(head - kHq - kHkv) * kTok + t) * kD;
-  *reinterpret_cast<uint2*>(dst + d) = o;
-}
-
-// SwiGLU: gu[t][j] = silu(gate) * up, where gate and up are the split sums of features j and
-// inter + j (the gate projection w1 fills the first `inter` features of the GEMM, the up
-// projection w3 the rest); silu(g) = g / (1 + e^-g).
-__global__ void __launch_bounds__(256) swiglu_kernel(const float* part, int splits, int inter,
-                                                    __nv_bfloat16* gu) {
-  pdl_launch_dependents();
-  pdl_wait_primary();
-  const int t = blockIdx.y;
-  const int j = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (j >= inter) return;
-  const float4 g = split_sum4(part, splits, 2 * inter, t, j);
-  const float4 u = split_sum4(part, splits, 2 * inter, t, inter + j);
-  auto sw = [](float a, float b) { return a * __frcp_rn(1.0f + expf(-a)) * b; };
-  uint2 o;
-  o.x = pack_bf16x2(sw(g.x, u.x), sw(g.y, u.y));
-  o.y = pack_bf16x2(sw(g.z, u.z), sw(g.w, u.w));
-  *reinterpret_cast<uint2*>(gu + static_cast<size_t>(t) * inter + j) = o;
-}
-
-// Plain projection output: y[t][n] = bf16(split sum of part[.][t][n]), y row-major [64][N].
-__global__ void __launch_bounds__(256) split_sum_bf16_kernel(const float* part, int splits, int N,
-                                                            __nv_bfloat16* y) {
-  pdl_launch_dependents();
-  pdl_wait_primary();
-  const int t = blockIdx.y;
-  const int n = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (n >= N) return;
-  const float4 a = split_sum4(part, splits, N, t, n);
-  uint2 o;
-  o.x = pack_bf16x2(a.x, a.y);
-  o.y = pack_bf16x2(a.z, a.w);
-  *reinterpret_cast<uint2*>(y + static_cast<size_t>(t) * N + n) = o;
 }
 
 // ------------------------------------------------------------------------------ launchers
 cudaError_t linear_set_attributes() {
-  return cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(lin::kSmemBytes));
+  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(lin::kSmemBytes));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
+// grid (tiles, splits) in clusters of (1, splits); cfg carries the PDL attribute in attrs[0] and
+// has room for the cluster attribute in attrs[1]
 cudaError_t launch_linear(const LinearParams& lp, int tiles, int splits, cudaLaunchConfig_t cfg) {
   cfg.gridDim = dim3(tiles, splits);
   cfg.blockDim = dim3(lin::kThreads);
   cfg.dynamicSmemBytes = lin::kSmemBytes;
+  cudaLaunchAttribute* attr = cfg.attrs;
+  attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+  attr[cfg.numAttrs].val.clusterDim.x = 1;
+  attr[cfg.numAttrs].val.clusterDim.y = static_cast<unsigned>(splits);
+  attr[cfg.numAttrs].val.clusterDim.z = 1;
+  cfg.numAttrs += 1;
   return cudaLaunchKernelEx(&cfg, linear_kernel, lp);
 }
 
-cudaError_t launch_residual_norm(const float* part, int splits, const __nv_bfloat16* x, int width,
-                                 __nv_bfloat16* y_out, const __nv_bfloat16* gamma,
+cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, int width, const __nv_bfloat16* gamma,
                                  __nv_bfloat16* h_out, cudaLaunchConfig_t cfg) {
   cfg.gridDim = dim3(kTok);
   cfg.blockDim = dim3(384);  // one float4 of a 1536-wide row per thread
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, residual_norm_kernel, part, splits, x, width, y_out, gamma, h_out);
+  return cudaLaunchKernelEx(&cfg, rms_norm_rows_kernel, x, width, gamma, h_out);
 }
 
-cudaError_t launch_qkv_heads(const float* part, int splits, __nv_bfloat16* q, __nv_bfloat16* k,
-                             __nv_bfloat16* v, cudaLaunchConfig_t cfg) {
-  constexpr int kN = (kHq + 2 * kHkv) * kD;
-  cfg.gridDim = dim3(kN / 4 / 256, kTok);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, qkv_heads_kernel, part, splits, q, k, v);
-}
-
-cudaError_t launch_swiglu(const float* part, int splits, int inter, __nv_bfloat16* gu,
-                          cudaLaunchConfig_t cfg) {
-  cfg.gridDim = dim3((inter / 4 + 255) / 256, kTok);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, swiglu_kernel, part, splits, inter, gu);
-}
-
-}  // namespace ea
-
-namespace ea {
-cudaError_t launch_split_sum_bf16(const float* part, int splits, int N, __nv_bfloat16* y,
-                                  cudaLaunchConfig_t cfg) {
-  cfg.gridDim = dim3((N / 4 + 255) / 256, kTok);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, split_sum_bf16_kernel, part, splits, N, y);
-}
 }  // namespace ea

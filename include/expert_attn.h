@@ -212,15 +212,16 @@ typedef struct {
  * expert_attn_workspace_init; expert_attn_read_status reads its status word. */
 size_t expert_decoder_layer_workspace_size(int hidden, int inter);
 
-/* One decoder layer (see above): ten kernels on the stream (the RMSNorms, four projections on
- * the tensor cores with their finishing kernels, and the attention kernel). */
+/* One decoder layer (see above): the two RMSNorm kernels, four projections on the tensor cores
+ * (each also applies its epilogue: head split, residual add or SwiGLU), and the attention
+ * kernel (followed by its merge kernel when a unit is split over more than two CTAs). */
 int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int rope_delta,
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* One projection of the 64 tokens on the tensor cores: y[64][N] = x[64][K] W^T in bf16 with fp32
  * accumulation (W bf16 [N][K]); K a multiple of 64, N a multiple of 128, device pointers
  * 16-byte aligned; the workspace (size from expert_linear64_workspace_size, 256-byte aligned,
- * cleared once with expert_attn_workspace_init) holds the status word and the partial sums. */
+ * cleared once with expert_attn_workspace_init) holds the status word. */
 size_t expert_linear64_workspace_size(int K, int N);
 int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* workspace,
                     size_t ws_bytes, ea_stream_t stream);
