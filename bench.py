@@ -299,28 +299,54 @@ def main():
     traffic = attention_traffic(S, Smax, n)
     merge_launched = launches_per_call(n, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1
 
-    # ---- end to end through the C ABI with host buffers: H2D of q/k/v, call, D2H of out
+    # ---- end to end through the C ABI with host buffers: every step copies its raw q/k/v in from
+    # pinned host memory, runs the step and copies its outputs back. Two device buffer sets and
+    # three streams (host->device copy, compute, device->host copy) let consecutive steps
+    # overlap, as a serving loop would; events keep a buffer set from being refilled before the
+    # step that reads it, and its outputs from being overwritten before they are copied out.
     h_act = act.cpu().pin_memory()
-    h_out = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
+    h_out = [torch.empty(outs.shape, dtype=outs.dtype).pin_memory() for _ in range(2)]
+    act_b = [act, torch.empty_like(act)]
+    outs_b = [outs, torch.empty_like(outs)]
+    Ls_b = [Ls, [ea.LayerBuffers(q_raw=act_b[1][l, :HQ], k_raw=act_b[1][l, HQ:HQ + HKV],
+                                 v_raw=act_b[1][l, HQ + HKV:], q_gamma=x.q_gamma, k_gamma=x.k_gamma,
+                                 k_cache=x.k_cache, v_cache=x.v_cache, out=outs_b[1][l])
+                 for l, x in enumerate(xs)]]
+    arr_b = [arr, ea.make_args(Ls_b[1], Smax, ea.EA_KV_BF16)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
 
-    def e2e_step():
-        act.copy_(h_act, non_blocking=True)
-        step()
-        h_out.copy_(outs, non_blocking=True)
+    def e2e_steps(k_steps):
+        for i in range(k_steps):
+            b = i % 2
+            if i >= 2:  # buffer set b is free once step i-2 has computed from it
+                s_in.wait_event(ev["comp"][b])
+            with torch.cuda.stream(s_in):
+                act_b[b].copy_(h_act, non_blocking=True)
+            ev["in"][b].record(s_in)
+            stream.wait_event(ev["in"][b])
+            if i >= 2:  # its outputs of step i-2 have been copied out
+                stream.wait_event(ev["out"][b])
+            ea.expert_attn_layers(Ls_b[b], S, Smax, 0, ea.EA_KV_BF16, ws, stream, _arr=arr_b[b])
+            ev["comp"][b].record(stream)
+            s_out.wait_event(ev["comp"][b])
+            with torch.cuda.stream(s_out):
+                h_out[b].copy_(outs_b[b], non_blocking=True)
+            ev["out"][b].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    e2e_steps(4)
     torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    s_in.wait_stream(stream)
+    e2e_steps(args.steps)
+    stream.wait_stream(s_out)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
     h2d = h_act.numel() * h_act.element_size()
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
 
     # ---- FP8 (e4m3) cache variant of the same step: caches quantised on the device by the library
     fp8 = None
@@ -487,7 +513,9 @@ def main():
             "kernels_ms": {"attention": k2, "merge": k3 if merge_launched else None},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_ms * 1e3 / (n * world), "unit": "us/layer", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "pipelining": "two device buffer sets; host->device copy, step and device->host "
+                                  "copy on three streams, consecutive steps overlapping"},
             "gpu_launches": args.steps * launches_per_call(n, S, torch.cuda.get_device_properties(dev).multi_processor_count),
             "cpu_baseline": cpu,
             "fp8_step": fp8,
