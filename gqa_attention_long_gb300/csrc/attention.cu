@@ -11,8 +11,10 @@
 // 64-row tile of own rows) are laid out unit-major and cut into one contiguous range per CTA
 // (grid = number of SMs, one CTA per SM). A CTA walks its range as "segments" (the part of one
 // unit inside the range). A segment that covers a whole unit writes the bf16 output directly;
-// a partial one writes a normalised fp32 partial plus its log2-sum-exp per row, which the
-// log-sum-exp merge kernel (merge.cu) combines once this grid has finished.
+// a partial one writes a normalised fp32 partial plus its log2-sum-exp per row. When every
+// split unit has two parts, the part that finishes second merges the first one's partial into
+// its own output here; otherwise the log-sum-exp merge kernel (merge.cu) combines the partials
+// once this grid has finished.
 //
 // Two key streams per CTA: the CTA's tiles alternate between stream 0 (even tile count) and
 // stream 1 (odd), each with its own TMEM score buffer, its own TMEM accumulator and its own
@@ -24,8 +26,10 @@
 // Warp roles (384 threads):
 //   warps 0-3, 4-7  softmax of stream 0, 1: thread r of a warpgroup owns folded row r (= TMEM
 //              lane r); online softmax in fp32 with lazy rescaling of its TMEM accumulator; P
-//              written back to TMEM as bf16 (e4m3) over the scores it came from, and read from
-//              there by the PV MMA
+//              written back to TMEM as bf16 (f16 for an e4m3 cache) over the scores it came
+//              from, and read from there by the PV MMA. With a bf16 cache these 256 threads
+//              first prepare the CTA's first Q (and its unit's own rows, if that segment holds
+//              them).
 //   warp 8     K/V producer: one thread issues 3-D TMA loads of the K/V tiles (cache rows, and the
 //              unit's own rows from the cache tail) into the ring
 //   warp 9     MMA: one thread issues tcgen05.mma (S = Q K^T from shared memory into the score
@@ -36,7 +40,8 @@
 //              never waits for it; for the segment holding the own-row tile, the roped K and the V
 //              rows into the cache tail. e4m3: one thread of warp 10 bulk-copies the Q codes that
 //              the prologue kernel staged.
-// Shared memory: Q x2 (64 KB), K/V ring (160 KB), barriers, a 1 KB row-statistics exchange.
+// Shared memory: Q x2 (64 KB), K/V ring (bf16: 5 x 32 KB; e4m3: 6 x 16 KB plus two 32 KB f16
+// copies of V), barriers, a 1.5 KB row-statistics exchange.
 // TMEM: 512 columns (two 128-column score/P buffers, two 128-column fp32 accumulators).
 #include "internal.cuh"
 #include "ptx.cuh"

@@ -144,7 +144,7 @@ struct AttnParams {
 };
 
 // ------------------------------------------------------------ decoder-layer projections
-constexpr int kMaxHidden = 8192;   // widest residual stream the finishing kernels take
+constexpr int kMaxHidden = 8192;   // widest residual stream of the decoder layer
 constexpr int kMaxInter = 32768;
 
 // One projection Y[t][n] = sum_k X[t][k] W[n][k] for the 64 tokens (linear.cu), with the

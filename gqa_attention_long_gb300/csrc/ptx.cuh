@@ -165,11 +165,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
 __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t a) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -231,10 +226,6 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
 // Named barrier `id` over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-// Arrival on named barrier `id` without waiting for the other threads.
-__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 // Orders this thread's generic-proxy global writes before later async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -316,15 +307,6 @@ __device__ __forceinline__ void umma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uin
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -385,14 +367,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -438,32 +412,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-// Four fp32 values -> four e4m3 codes (RNE, satfinite) in one 32-bit word, lowest byte first.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a), "f"(b));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(c), "f"(d));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-// Four fp32 values p -> e4m3 codes hi = e4m3(p) and lo = e4m3(p - value(hi)) (residual formed in
-// f16), four per 32-bit word each. hi + lo represents p to about 7 significant bits.
-__device__ __forceinline__ void pack_e4m3x4_hilo(float a, float b, float c, float d, uint32_t& hi,
-                                                 uint32_t& lo) {
-  uint16_t h0, h1, l0, l1;
-  uint32_t hv0, hv1, pv0, pv1, r0, r1;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(h0) : "f"(a), "f"(b));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(h1) : "f"(c), "f"(d));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hv0) : "h"(h0));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hv1) : "h"(h1));
-  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(pv0) : "f"(a), "f"(b));
-  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(pv1) : "f"(c), "f"(d));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r0) : "r"(pv0), "r"(hv0));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r1) : "r"(pv1), "r"(hv1));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l0) : "r"(r0));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l1) : "r"(r1));
-  hi = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-  lo = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
 }
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
