@@ -25,7 +25,7 @@ LAYER_MAX_ABS = 6e-2
 
 
 @pytest.mark.parametrize("K,N", [(64, 128), (448, 384), (1536, 4096), (2048, 1536), (6144, 1536),
-                                 (1536, 12288)])
+                                 (1536, 12288), (6144, 128)])
 def test_linear64_matches_exact_product(K, N):
     rng = np.random.Generator(np.random.PCG64(K * 7 + N))
     x = torch.from_numpy(rng.standard_normal((64, K)).astype(np.float32)).to(torch.bfloat16)
@@ -96,3 +96,32 @@ def test_decoder_layer_repeatable_bitwise():
     torch.cuda.synchronize()
     check_status(ws)
     assert torch.equal(out, again)
+
+
+def test_decoder_layer_without_cache_rows():
+    """S = 0: the tokens attend only to their own rows."""
+    out, r, _, _, _ = run_layer(14, 0, 128, hidden=256, inter=256)
+    assert_layer_close(f64(out), r["x2"], "S=0")
+
+
+def test_two_chained_layers():
+    """Layer 2 reads layer 1's output as its residual stream; the oracle runs layer 2 on the
+    bf16 values the GPU's layer 1 produced (each layer within the bar)."""
+    S, Smax, hidden, inter = 300, 512, 512, 768
+    d = torch.device("cuda")
+    lays = [layer_inputs(20 + i, S, Smax) for i in range(2)]
+    ws_ = [expert_layer_weights(20 + i, hidden=hidden, inter=inter) for i in range(2)]
+    x0 = residual_stream(20, hidden=hidden)
+    xs = [x0.to(d), torch.empty(64, hidden, dtype=torch.bfloat16, device=d),
+          torch.empty(64, hidden, dtype=torch.bfloat16, device=d)]
+    caches = [(lay.k_cache.to(d), lay.v_cache.to(d)) for lay in lays]
+    wdev = [type(w)(**{k: v.to(d) for k, v in w.__dict__.items()}) for w in ws_]
+    ws = ea.alloc_decoder_layer_workspace(hidden, inter)
+    for i in range(2):
+        ea.expert_decoder_layer(xs[i], xs[i + 1], wdev[i], caches[i][0], caches[i][1], S, Smax, 0, ws)
+    torch.cuda.synchronize()
+    check_status(ws)
+    for i in range(2):
+        r = oracle.expert_layer(f64(xs[i]), {k: f64(v) for k, v in ws_[i].__dict__.items()},
+                                f64(lays[i].k_cache), f64(lays[i].v_cache), S, Smax, 0)
+        assert_layer_close(f64(xs[i + 1]), r["x2"], f"layer {i}")
