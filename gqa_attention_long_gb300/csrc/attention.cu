@@ -557,11 +557,14 @@ __device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------------------------ MMA
-// Issue order per segment: QK(0), then for i >= 1: QK(i), PV(i-1); finally PV(nt-1). Tile n of
-// the CTA (counted over all its segments) belongs to stream n & 1: QK(n) writes that stream's
-// score buffer, PV(n) accumulates into that stream's accumulator. QK(n) is issued only after
-// PV(n-2), the previous MMA that read the same buffer, has completed; so a completed S(n)
-// also tells the softmax that every earlier PV of its stream is done.
+// Per segment, step i (0 <= i <= nt) has up to two MMAs to issue: QK(i) (if i < nt) and PV(i-1)
+// (if i > 0). Tile n of the CTA (counted over all its segments) belongs to stream n & 1: QK(n)
+// writes that stream's score buffer, PV(n) accumulates into that stream's accumulator. QK(n) is
+// issued only after PV(n-2), the previous MMA that read the same buffer, has completed; so a
+// completed S(n) also tells the softmax that every earlier PV of its stream is done. The two MMAs
+// of a step belong to different streams (different TMEM buffers, ring slots and barriers), so
+// whichever has its inputs first is issued first: PV(i-1) does not wait behind QK(i), whose
+// inputs (K(i), and the completion of PV(i-2)) may arrive later than P(i-1).
 template <bool F8, class PP>
 __device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
   EA_LAYOUT_ALIASES;
@@ -582,81 +585,107 @@ __device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
     tc_fence_after();
     const uint32_t qaddr = cx.sbase + SM_Q + qb * kQB;
     const int nt = s.j1 - s.j0;
+    // Inputs of QK(i): K(i) in its ring slot; PV(n_qk - 2) complete, since QK(n) overwrites the
+    // score buffer whose first columns hold P(n-2), the A operand of PV(n-2) (even and odd PVs
+    // complete on separate barriers; this thread observes every PV completion in order).
+    auto qk_ready = [&](int i) -> bool {
+      const uint32_t pos = ring + 2 * i;
+      if (!mbar_test_wait(cx.bar(B_KVFULL + pos % kRing), (pos / kRing) & 1)) return false;
+      return n_qk < 2 || mbar_test_wait(cx.bar(B_ODONE + ((n_qk - 2) & 1)), ((n_qk - 2) >> 1) & 1);
+    };
+    auto issue_qk = [&](int i) {
+      const int j = s.j0 + i;
+      const uint32_t slot = (ring + 2 * i) % kRing;
+      tc_fence_after();
+      const uint32_t kaddr = cx.sbase + SM_RING + slot * kSlotBytes;
+      const uint32_t d = cx.tmem + TM_S + (n_qk & 1) * 128;
+      const uint32_t idesc = j < p.n_main ? kIdescQK128 : kIdescQK64;
+      if constexpr (F8) {
+        // 4 steps of 32 channels within the 128-byte atom, for the high Q codes and then the
+        // low ones (same scale), both accumulating into S
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_f8_ss(d, sw128_desc(qaddr + (kk >> 2) * kQTileBytesF8 + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(kaddr + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 8 steps of 16 channels; 4 per 64-channel atom
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_f16_ss(d, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024),
+                      idesc, kk > 0);
+        }
+      }
+      umma_commit(cx.bar(B_SFULL + (n_qk & 1)));
+      umma_commit(cx.bar(B_KVEMPTY + slot));
+      if (i == nt - 1) umma_commit(cx.bar(B_QEMPTY + qb));
+      ++n_qk;
+    };
+    // Inputs of PV(ii): the softmax warpgroup's P(ii) (P of even and odd tiles arrive on separate
+    // barriers); bf16: V(ii) in its ring slot (e4m3: the stream's widened copy, written before the
+    // warpgroup arrived on PFULL); for the first PV of a segment, which overwrites both
+    // accumulators' previous contents, the softmax warpgroups' release of the previous segment's
+    // accumulators (OFREE completes once per segment).
+    auto pv_ready = [&](int ii) -> bool {
+      if (ii == 0 && seg > 0 && !mbar_test_wait(cx.bar(B_OFREE), (seg - 1) & 1)) return false;
+      if (!mbar_test_wait(cx.bar(B_PFULL + (n_pv & 1)), (n_pv >> 1) & 1)) return false;
+      if constexpr (!F8) {
+        const uint32_t pos = ring + 2 * ii + 1;
+        if (!mbar_test_wait(cx.bar(B_KVFULL + pos % kRing), (pos / kRing) & 1)) return false;
+      }
+      return true;
+    };
+    auto issue_pv = [&](int ii) {
+      const int j = s.j0 + ii;
+      const uint32_t slot = (ring + 2 * ii + 1) % kRing;
+      tc_fence_after();
+      const uint32_t vaddr = F8 ? cx.sbase + SM_V16 + (n_pv & 1) * 32768u
+                                : cx.sbase + SM_RING + slot * kSlotBytes;
+      // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together),
+      // as 16-bit pairs: a K step of 16 keys spans 8 TMEM columns
+      const uint32_t pcol = cx.tmem + TM_S + (n_pv & 1) * 128;
+      // the first PV of each stream in a segment (segment tiles 0 and 1) starts a fresh sum
+      const uint32_t ocol = cx.tmem + TM_O + (n_pv & 1) * 128;
+      const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
+      for (int kk = 0; kk < nk; ++kk)        // V: 16 key rows of 128 bytes per step and atom
+        umma_f16_ts(ocol, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024), kIdescPV,
+                    (ii > 1 || kk > 0));
+      // even and odd PVs complete on separate barriers: a waiter that knows PV k-2 is done
+      // can then always tell PV k's completion from an older phase
+      umma_commit(cx.bar(B_ODONE + (n_pv & 1)));
+      if constexpr (!F8) umma_commit(cx.bar(B_KVEMPTY + slot));
+      ++n_pv;
+    };
     for (int i = 0; i <= nt && ok; ++i) {
-      if (i < nt) {
-        const int j = s.j0 + i;
-        const uint32_t pos = ring + 2 * i, slot = pos % kRing;
-        ok = bounded_wait(cx.bar(B_KVFULL + slot), (pos / kRing) & 1, cx.abort_flag, cx.status,
-                          kErrMmaWait);
-        // QK(n) overwrites the score buffer whose first columns hold P(n-2), the A operand of
-        // PV(n-2): wait until that MMA has completed (even/odd PVs complete on separate
-        // barriers; this thread observes every PV completion in order).
-        if (ok && n_qk >= 2)
-          ok = bounded_wait(cx.bar(B_ODONE + ((n_qk - 2) & 1)), ((n_qk - 2) >> 1) & 1,
-                            cx.abort_flag, cx.status, kErrMmaWait);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kaddr = cx.sbase + SM_RING + slot * kSlotBytes;
-        const uint32_t d = cx.tmem + TM_S + (n_qk & 1) * 128;
-        const uint32_t idesc = j < p.n_main ? kIdescQK128 : kIdescQK64;
-        if constexpr (F8) {
-          // 4 steps of 32 channels within the 128-byte atom, for the high Q codes and then the
-          // low ones (same scale), both accumulating into S
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f8_ss(d, sw128_desc(qaddr + (kk >> 2) * kQTileBytesF8 + (kk & 3) * 32, 16, 1024),
-                       sw128_desc(kaddr + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 8 steps of 16 channels; 4 per 64-channel atom
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_f16_ss(d, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024),
-                        idesc, kk > 0);
+      bool qk_todo = i < nt, pv_todo = i > 0;
+      uint64_t t0 = 0;
+      for (uint32_t it = 0; qk_todo || pv_todo; ++it) {
+        bool moved = false;
+        if (qk_todo && qk_ready(i)) {
+          issue_qk(i);
+          qk_todo = false;
+          moved = true;
+        }
+        if (pv_todo && pv_ready(i - 1)) {
+          issue_pv(i - 1);
+          pv_todo = false;
+          moved = true;
+        }
+        if (moved) continue;
+        // bounded like every other wait: the CTA's abort flag, a time limit and a poll limit
+        if ((it & 63u) == 0) {
+          if (*cx.abort_flag) {
+            ok = false;
+            break;
+          }
+          const uint64_t now = globaltimer_ns();
+          if (t0 == 0) t0 = now;
+          if (now - t0 > kWaitLimitNs || it >= 0x7fffffc0u) {
+            *cx.abort_flag = 1u;
+            atomicOr(cx.status, kErrMmaWait);
+            ok = false;
+            break;
           }
         }
-        umma_commit(cx.bar(B_SFULL + (n_qk & 1)));
-        umma_commit(cx.bar(B_KVEMPTY + slot));
-        if (i == nt - 1) umma_commit(cx.bar(B_QEMPTY + qb));
-        ++n_qk;
-      }
-      if (i > 0) {
-        const int ii = i - 1, j = s.j0 + ii;
-        // the first PV of a segment overwrites both accumulators' previous contents: wait until
-        // the softmax warpgroups have read the previous segment's (OFREE completes once per
-        // segment)
-        if (ii == 0 && seg > 0) {
-          ok = bounded_wait(cx.bar(B_OFREE), (seg - 1) & 1, cx.abort_flag, cx.status, kErrMmaWait);
-          if (!ok) break;
-        }
-        // P of even and odd tiles (streams 0 and 1) arrive on separate barriers, each from its
-        // own softmax warpgroup
-        ok = bounded_wait(cx.bar(B_PFULL + (n_pv & 1)), (n_pv >> 1) & 1, cx.abort_flag, cx.status,
-                          kErrMmaWait);
-        if (!ok) break;
-        const uint32_t pos = ring + 2 * ii + 1, slot = pos % kRing;
-        // bf16: V is read from its ring slot; e4m3: from the stream's widened copy, written by
-        // the softmax warpgroup before it arrived on PFULL (which also released the slot)
-        if constexpr (!F8)
-          ok = bounded_wait(cx.bar(B_KVFULL + slot), (pos / kRing) & 1, cx.abort_flag, cx.status,
-                            kErrMmaWait);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vaddr = F8 ? cx.sbase + SM_V16 + (n_pv & 1) * 32768u
-                                  : cx.sbase + SM_RING + slot * kSlotBytes;
-        // P(ii) sits in TMEM, in the score buffer of QK(ii) (PV and QK counts advance together),
-        // as 16-bit pairs: a K step of 16 keys spans 8 TMEM columns
-        const uint32_t pcol = cx.tmem + TM_S + (n_pv & 1) * 128;
-        // the first PV of each stream in a segment (segment tiles 0 and 1) starts a fresh sum
-        const uint32_t ocol = cx.tmem + TM_O + (n_pv & 1) * 128;
-        const int nk = j < p.n_main ? 8 : 4;  // 16 keys per step; the own-row tile has 64 keys
-        for (int kk = 0; kk < nk; ++kk)        // V: 16 key rows of 128 bytes per step and atom
-          umma_f16_ts(ocol, pcol + kk * 8, sw128_desc(vaddr + kk * 16 * 128, kAtom, 1024), kIdescPV,
-                      (ii > 1 || kk > 0));
-        // even and odd PVs complete on separate barriers: a waiter that knows PV k-2 is done
-        // can then always tell PV k's completion from an older phase
-        umma_commit(cx.bar(B_ODONE + (n_pv & 1)));
-        if constexpr (!F8) umma_commit(cx.bar(B_KVEMPTY + slot));
-        ++n_pv;
       }
     }
     ring += 2 * nt;
