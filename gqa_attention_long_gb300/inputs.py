@@ -194,3 +194,79 @@ def residual_stream(seed: int, hidden: int = HIDDEN) -> torch.Tensor:
     """The layer input x [64, hidden] ~ N(0, 1), bf16 on the CPU."""
     rng = np.random.Generator(np.random.PCG64(int(seed) + 15485863))
     return _bf16(rng.standard_normal((T, hidden)))
+
+
+# ------------------------------------------------------------------- text-model decode step
+# One decode step of the VLM text model over the same per-layer cache layout (alpamayo_tt/text.py,
+# TTText._layer_decode): 64 query heads and 8 KV heads of width 128 for the single new token;
+# the cache rows [0, pos) are valid and the step writes row pos.
+HQ_TEXT = 64
+
+
+@dataclass
+class DecodeInputs:
+    q_raw: torch.Tensor    # bf16 [64, 128]
+    k_raw: torch.Tensor    # bf16 [8, 128]
+    v_raw: torch.Tensor    # bf16 [8, 128]
+    q_gamma: torch.Tensor  # bf16 [128]
+    k_gamma: torch.Tensor  # bf16 [128]
+    k_cache: torch.Tensor  # bf16 [8, Smax, 128]
+    v_cache: torch.Tensor  # bf16 [8, Smax, 128]
+    pos: int
+    Smax: int
+
+
+def decode_inputs(seed: int, pos: int, Smax: int, later_fill: float | str = 7.0) -> DecodeInputs:
+    """One layer's decode-step inputs, all bf16 on the CPU (numpy PCG64, as layer_inputs).
+
+    raw q/k/v and cache K/V ~ N(0, 1); gains 1 + 0.1 N(0, 1). Rows [pos, Smax) of both caches
+    (the new token's row and the rows after it, not yet written by the text model) are set by
+    ``later_fill``: a number, ``"garbage"``, ``"nan"`` or ``"inf"``.
+    """
+    assert 0 <= pos < Smax
+    rng = np.random.Generator(np.random.PCG64(int(seed)))
+    q_raw = _bf16(rng.standard_normal((HQ_TEXT, D)))
+    k_raw = _bf16(rng.standard_normal((HKV, D)))
+    v_raw = _bf16(rng.standard_normal((HKV, D)))
+    q_gamma = _bf16(1.0 + 0.1 * rng.standard_normal(D))
+    k_gamma = _bf16(1.0 + 0.1 * rng.standard_normal(D))
+    k_cache = _bf16(rng.standard_normal((HKV, Smax, D)))
+    v_cache = _bf16(rng.standard_normal((HKV, Smax, D)))
+    _fill_rows(k_cache, v_cache, pos, Smax, later_fill, seed)
+    return DecodeInputs(q_raw, k_raw, v_raw, q_gamma, k_gamma, k_cache, v_cache, int(pos), int(Smax))
+
+
+def decode_inputs_on_device(seed: int, pos: int, Smax: int, device) -> DecodeInputs:
+    """Same distributions as :func:`decode_inputs`, drawn on ``device`` (full-size workloads)."""
+    assert 0 <= pos < Smax
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    bf = torch.bfloat16
+    r = lambda *shape: torch.randn(*shape, generator=g, device=device)  # noqa: E731
+    x = DecodeInputs(r(HQ_TEXT, D).to(bf), r(HKV, D).to(bf), r(HKV, D).to(bf),
+                     (1.0 + 0.1 * r(D)).to(bf), (1.0 + 0.1 * r(D)).to(bf),
+                     r(HKV, Smax, D).to(bf), r(HKV, Smax, D).to(bf), int(pos), int(Smax))
+    _fill_rows(x.k_cache, x.v_cache, pos, Smax, 7.0, seed)
+    return x
+
+
+def _fill_rows(k_cache: torch.Tensor, v_cache: torch.Tensor, lo: int, hi: int,
+               fill: float | str, seed: int) -> None:
+    """Overwrite rows [lo, hi) of both caches in place (a number, garbage, NaN or Inf)."""
+    if hi <= lo:
+        return
+    if isinstance(fill, str):
+        if fill == "garbage":
+            rng = np.random.Generator(np.random.PCG64(int(seed) + 7919))
+            for c in (k_cache, v_cache):
+                c[:, lo:hi] = _bf16(1e4 * rng.standard_normal((c.shape[0], hi - lo, c.shape[2]))).to(c.device)
+        elif fill == "nan":
+            k_cache[:, lo:hi] = float("nan")
+            v_cache[:, lo:hi] = float("nan")
+        elif fill == "inf":
+            k_cache[:, lo:hi] = float("inf")
+            v_cache[:, lo:hi] = float("-inf")
+        else:
+            raise ValueError(fill)
+    else:
+        k_cache[:, lo:hi] = float(fill)
+        v_cache[:, lo:hi] = float(fill)

@@ -15,10 +15,13 @@ fp8_e4m3         : the OCP E4M3 ("e4m3fn") code table, a round-to-nearest-even
 decoder_layer    : the whole decoder layer around that attention (RMSNorm, fused
                    qkv projection, head split, attention, head concat, wo, residual,
                    RMSNorm, SwiGLU MLP, residual), for synthetic weights.
+decode_attention : the text model's single-token decode attention over the same caches
+                   (64 query heads / 8 KV heads, norm and RoPE at pos + rope_delta, the
+                   new row written at pos, attention over rows 0..pos).
 
-Every function is pinned by ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_layer_pins.py`` against closed forms, invariants, brute force on tiny
-inputs and independent library routines.
+Every function is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_oracle_layer_pins.py`` and ``tests/test_oracle_decode_pins.py`` against closed
+forms, invariants, brute force on tiny inputs and independent library routines.
 """
 from .expert_attention import (  # noqa: F401
     D, EPS, HQ, HKV, MASK_MIN, REP, T, THETA,
@@ -32,4 +35,7 @@ from .fp8_e4m3 import (  # noqa: F401
 from .decoder_layer import (  # noqa: F401
     HIDDEN, INTER, KV_DIM, Q_DIM, QKV_DIM, concat_heads, expert_layer, linear, silu,
     split_qkv_heads, swiglu_mlp,
+)
+from .decode_attention import (  # noqa: F401
+    HKV_TEXT, HQ_TEXT, REP_TEXT, decode_attend, decode_prologue, text_decode_attention,
 )

@@ -134,3 +134,57 @@ def test_layer_pin_catches_planted_mistake(monkeypatch, name, bad, pin):
 def test_unpatched_layer_pins_pass():
     for _, _, pin in LAYER_MUTATIONS:
         pin()
+
+
+# ------------------------------------------------------------- text-model decode oracle
+import oracle.decode_attention as da  # noqa: E402
+from tests import test_oracle_decode_pins as dpins  # noqa: E402
+
+
+def _decode_attend_wrong_group(q, k_cache, v_cache, pos):
+    out = np.empty((64, 128))
+    for h in range(64):
+        g = h % 8                                             # planted: wrong GQA map
+        s = (np.asarray(k_cache[g, :pos + 1], np.float64) @ q[h]) / math.sqrt(128)
+        w = np.exp(s - s.max())
+        out[h] = (w @ np.asarray(v_cache[g, :pos + 1], np.float64)) / w.sum()
+    return out
+
+
+def _decode_attend_exclusive(q, k_cache, v_cache, pos):
+    out = np.empty((64, 128))
+    n = max(pos, 1)                                           # planted: cur_pos exclusive
+    for h in range(64):
+        g = h // 8
+        s = (np.asarray(k_cache[g, :n], np.float64) @ q[h]) / math.sqrt(128)
+        w = np.exp(s - s.max())
+        out[h] = (w @ np.asarray(v_cache[g, :n], np.float64)) / w.sum()
+    return out
+
+
+def _decode_prologue_no_delta(q_raw, k_raw, v_raw, q_gamma, k_gamma, pos, rope_delta):
+    return _original_decode_prologue(q_raw, k_raw, v_raw, q_gamma, k_gamma, pos, 0)  # planted
+
+
+_original_decode_prologue = da.decode_prologue
+
+DECODE_MUTATIONS = [
+    ("decode_attend", _decode_attend_wrong_group, dpins.test_decode_gqa_group_mapping),
+    ("decode_attend", _decode_attend_exclusive, dpins.test_decode_attends_to_its_own_new_row),
+    ("decode_prologue", _decode_prologue_no_delta, dpins.test_decode_positions_are_pos_plus_delta),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", DECODE_MUTATIONS,
+                         ids=["gqa_map", "exclusive_cur_pos", "no_rope_delta"])
+def test_decode_pin_catches_planted_mistake(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(da, name, bad)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_unpatched_decode_pins_pass():
+    for _, _, pin in DECODE_MUTATIONS:
+        pin()
