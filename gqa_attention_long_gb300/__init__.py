@@ -13,4 +13,6 @@ from ._lib import (  # noqa: F401
     kernels_per_call, lib, make_args, split_parts, split_units,
     alloc_decoder_layer_workspace, expert_decoder_layer, expert_decoder_layer_workspace_size,
     expert_linear64, expert_linear64_workspace_size,
+    DecodeBuffers, alloc_decode_workspace, make_decode_args, text_decode_attention,
+    text_decode_workspace_init, text_decode_workspace_size,
 )

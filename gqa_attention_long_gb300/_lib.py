@@ -34,6 +34,11 @@ class EaDecoderLayerArgs(ctypes.Structure):
                     "k_cache", "v_cache", "q_rope")]
 
 
+class EaDecodeArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "q_raw", "k_raw", "v_raw", "q_gamma", "k_gamma", "k_cache", "v_cache", "out")]
+
+
 _lib_handle = None
 
 
@@ -62,6 +67,9 @@ def lib() -> ctypes.CDLL:
             "expert_decoder_layer": (I, [ctypes.POINTER(EaDecoderLayerArgs), I, I, I, V, S, V]),
             "expert_linear64_workspace_size": (S, [I, I]),
             "expert_linear64": (I, [V, V, V, I, I, V, S, V]),
+            "text_decode_workspace_size": (S, [I]),
+            "text_decode_workspace_init": (I, [V, S, V]),
+            "text_decode_attention": (I, [ctypes.POINTER(EaDecodeArgs), I, I, I, I, V, S, V]),
         }
         for name, (res, args) in sig.items():
             f = getattr(h, name)
@@ -336,3 +344,60 @@ def expert_linear64(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, ws: torch
     _check("expert_linear64", lib().expert_linear64(_ptr(x, "x", bf, 64 * K), _ptr(w, "w", bf, N * K),
                                                     _ptr(y, "y", bf, 64 * N), int(K), int(N), p, n,
                                                     _stream(stream)))
+
+
+# --------------------------------------------------------------- text-model decode attention
+@dataclass
+class DecodeBuffers:
+    """One layer's device tensors for text_decode_attention (include/expert_attn.h)."""
+    q_raw: torch.Tensor    # bf16 [64, 128]
+    k_raw: torch.Tensor    # bf16 [8, 128]
+    v_raw: torch.Tensor    # bf16 [8, 128]
+    q_gamma: torch.Tensor  # bf16 [128]
+    k_gamma: torch.Tensor  # bf16 [128]
+    k_cache: torch.Tensor  # bf16 [8, Smax, 128]
+    v_cache: torch.Tensor
+    out: torch.Tensor      # bf16 [64, 128]
+
+
+def make_decode_args(layers: list[DecodeBuffers], Smax: int):
+    arr = (EaDecodeArgs * len(layers))()
+    bf = torch.bfloat16
+    for i, L in enumerate(layers):
+        a = arr[i]
+        a.q_raw = _ptr(L.q_raw, "q_raw", bf, 64 * 128)
+        a.k_raw = _ptr(L.k_raw, "k_raw", bf, 8 * 128)
+        a.v_raw = _ptr(L.v_raw, "v_raw", bf, 8 * 128)
+        a.q_gamma = _ptr(L.q_gamma, "q_gamma", bf, 128)
+        a.k_gamma = _ptr(L.k_gamma, "k_gamma", bf, 128)
+        a.k_cache = _ptr(L.k_cache, "k_cache", bf, 8 * Smax * 128)
+        a.v_cache = _ptr(L.v_cache, "v_cache", bf, 8 * Smax * 128)
+        a.out = _ptr(L.out, "out", bf, 64 * 128)
+    return arr
+
+
+def text_decode_workspace_size(n_layers: int) -> int:
+    return int(lib().text_decode_workspace_size(int(n_layers)))
+
+
+def text_decode_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    p, n = _ws(ws)
+    _check("text_decode_workspace_init", lib().text_decode_workspace_init(p, n, _stream(stream)))
+
+
+def alloc_decode_workspace(n_layers: int, device="cuda") -> torch.Tensor:
+    """A cleared workspace for text_decode_attention (torch-allocated)."""
+    n = text_decode_workspace_size(n_layers)
+    if n == 0:
+        raise RuntimeError("text_decode_workspace_size returned 0: no sm_103 GPU available")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    text_decode_workspace_init(ws)
+    return ws
+
+
+def text_decode_attention(layers: list[DecodeBuffers], pos: int, Smax: int, rope_delta: int,
+                          ws: torch.Tensor, stream=None, _arr=None) -> None:
+    arr = _arr if _arr is not None else make_decode_args(layers, Smax)
+    p, n = _ws(ws)
+    _check("text_decode_attention", lib().text_decode_attention(arr, len(arr), int(pos), int(Smax),
+                                                                int(rope_delta), p, n, _stream(stream)))

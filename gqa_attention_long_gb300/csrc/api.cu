@@ -900,3 +900,146 @@ int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* w
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ text-model decode attention
+// Host side of text_decode_attention: validation, the cache tensor maps (shared with the expert
+// path's cache), the tile partition and one launch of the decode kernel per chunk of <= 64
+// layers (programmatic dependent launch).
+namespace ea {
+cudaError_t decode_set_attributes();
+template <int CAP>
+cudaError_t launch_decode_kernel(const DecodeParams<CAP>& dp, cudaLaunchConfig_t cfg);
+}  // namespace ea
+
+namespace {
+
+bool decode_attrs_ready() {
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [] {
+    ok = decode_set_attributes() == cudaSuccess;
+    cudaGetLastError();
+  });
+  return ok;
+}
+
+int validate_decode(const ea_decode_args* a, int n_layers, int pos, int Smax, int rope_delta,
+                    const void* ws) {
+  if (a == nullptr || n_layers < 1 || ws == nullptr) return EA_ERR_INVALID_ARG;
+  if (Smax < kKeyTile || Smax % kTok != 0 || Smax > (1 << 22)) return EA_ERR_INVALID_ARG;
+  if (pos < 0 || pos >= Smax) return EA_ERR_INVALID_ARG;
+  const long long p0 = static_cast<long long>(pos) + rope_delta;
+  if (p0 <= -(1LL << 24) || p0 >= (1LL << 24)) return EA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return EA_ERR_MISALIGNED;
+  for (int l = 0; l < n_layers; ++l) {
+    const ea_decode_args& x = a[l];
+    const void* req[] = {x.q_raw, x.k_raw, x.v_raw, x.q_gamma, x.k_gamma, x.k_cache, x.v_cache, x.out};
+    for (const void* p : req) {
+      if (p == nullptr) return EA_ERR_INVALID_ARG;
+      if (!aligned16(p)) return EA_ERR_MISALIGNED;
+    }
+  }
+  return EA_OK;
+}
+
+template <int CAP>
+struct DecodeBlock {
+  DecodeParams<CAP> dp;
+  std::mutex mu;
+};
+template <int CAP>
+DecodeBlock<CAP>& decode_block() {
+  static DecodeBlock<CAP> b;
+  return b;
+}
+
+template <int CAP>
+int launch_decode_t(const ea_decode_args* a, int n, int pos, int Smax, int rope_delta, uint8_t* ws,
+                    const DecodeWs& wl, int sm_count, cudaStream_t st) {
+  DecodeBlock<CAP>& b = decode_block<CAP>();
+  std::lock_guard<std::mutex> lk(b.mu);
+  DecodeParams<CAP>& dp = b.dp;
+  std::memset(&dp, 0, sizeof(dp));
+  for (int l = 0; l < n; ++l) {
+    if (!cache_map(a[l].k_cache, 0, Smax, false, &dp.kmap[l]) ||
+        !cache_map(a[l].v_cache, 0, Smax, false, &dp.vmap[l]))
+      return EA_ERR_CUDA;
+    dp.q_raw[l] = static_cast<const __nv_bfloat16*>(a[l].q_raw);
+    dp.k_raw[l] = static_cast<const __nv_bfloat16*>(a[l].k_raw);
+    dp.v_raw[l] = static_cast<const __nv_bfloat16*>(a[l].v_raw);
+    dp.q_gamma[l] = static_cast<const __nv_bfloat16*>(a[l].q_gamma);
+    dp.k_gamma[l] = static_cast<const __nv_bfloat16*>(a[l].k_gamma);
+    dp.kc[l] = static_cast<__nv_bfloat16*>(a[l].k_cache);
+    dp.vc[l] = static_cast<__nv_bfloat16*>(a[l].v_cache);
+    dp.out[l] = static_cast<__nv_bfloat16*>(a[l].out);
+  }
+  rope_inv_freq(dp.inv_hi, dp.inv_lo);
+  dp.T = (pos + 1 + kKeyTile - 1) / kKeyTile;
+  dp.W = static_cast<long long>(n) * kHkv * dp.T;
+  dp.pos = pos;
+  dp.rope_pos = pos + rope_delta;
+  dp.Smax = Smax;
+  dp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+  dp.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
+  dp.part_ml = reinterpret_cast<float*>(ws + wl.part_ml_off);
+  dp.unit_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
+  dp.status = reinterpret_cast<uint32_t*>(ws);
+  const int n_ctas = static_cast<long long>(sm_count) < dp.W ? sm_count : static_cast<int>(dp.W);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(st, attr, true);
+  cfg.gridDim = dim3(n_ctas);
+  if (launch_decode_kernel<CAP>(dp, cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return EA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t text_decode_workspace_size(int n_layers) {
+  if (n_layers < 1) return 0;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return 0;
+  const int per = n_layers < kDecodeMaxLayers ? n_layers : kDecodeMaxLayers;
+  return decode_ws_layout(per, di.sm_count).total;
+}
+
+int text_decode_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < 1024) return EA_ERR_INVALID_ARG;
+  // the status word and the per-unit arrival counts of up to 64 layers per launch
+  const size_t init = decode_ws_layout(kDecodeMaxLayers, 1).part_o_off;
+  const size_t n = ws_bytes < init ? ws_bytes : init;
+  if (cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return EA_ERR_CUDA;
+  }
+  return EA_OK;
+}
+
+int text_decode_attention(const ea_decode_args* layers, int n_layers, int pos, int Smax,
+                          int rope_delta, void* workspace, size_t ws_bytes, ea_stream_t stream) {
+  int rc = validate_decode(layers, n_layers, pos, Smax, rope_delta, workspace);
+  if (rc != EA_OK) return rc;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di) || !decode_attrs_ready()) return EA_ERR_UNSUPPORTED;
+  const int per = n_layers < kDecodeMaxLayers ? n_layers : kDecodeMaxLayers;
+  const DecodeWs wl = decode_ws_layout(per, di.sm_count);
+  if (ws_bytes < wl.total) return EA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (int l0 = 0; l0 < n_layers; l0 += per) {
+    const int n = n_layers - l0 < per ? n_layers - l0 : per;
+    rc = n <= kSmallCap ? launch_decode_t<kSmallCap>(layers + l0, n, pos, Smax, rope_delta, ws, wl, di.sm_count, st)
+                        : launch_decode_t<kDecodeMaxLayers>(layers + l0, n, pos, Smax, rope_delta, ws, wl,
+                                                            di.sm_count, st);
+    if (rc != EA_OK) return rc;
+  }
+  return EA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,470 @@
+// decode.cu — split-KV single-token decode attention of the VLM text model on sm_103a.
+//
+// What it computes (alpamayo_tt/text.py, TTText._layer_decode and TTText._decode_inputs_host):
+// per layer, for the decode token's 64 query heads and 8 KV heads (query head h reads KV head
+// h / 8),
+//   1. q and k rows RMS-normalised with the q_norm / k_norm gains (eps 1e-6) and rotated with
+//      the HF rotate_half RoPE (theta 5e6) at position pos + rope_delta;
+//   2. the roped k and the raw v written into row pos of the layer's K and V caches
+//      (paged_update_cache);
+//   3. softmax(q K[g, 0..pos]^T / sqrt(128)) V[g, 0..pos] for every query head
+//      (scaled_dot_product_attention_decode with cur_pos = pos).
+//
+// Work decomposition: a unit is one (layer, kv head): its 8 query heads against keys [0, pos],
+// cut into tiles of 128 keys. The tiles of all units, unit-major, are cut into one contiguous
+// range per CTA (one CTA per SM); a CTA walks its range as segments (the part of one unit in
+// it). Per tile, on the tensor cores (one issuing thread):
+//   S^T  = K Q^T    M = 128 keys (TMEM lanes), N = 16 (the 8 query heads and 8 zero rows),
+//                   K = 128 channels; A = the K tile (TMA, 128-byte swizzle, K-major), B = the
+//                   unit's roped q rows in shared memory;
+//   O^T += V^T P^T  M = 128 channels (TMEM lanes), N = 16, K = 128 keys; A = the same V tile
+//                   read MN-major, B = P (bf16) written by the softmax threads.
+// Between the two, the 128 compute threads (thread = key = TMEM lane) form the exact online
+// softmax per head: the tile's max and sum over keys by warp shuffles and a 4-warp exchange.
+// Keys after pos (the end of the last tile) get score -inf and zeroed V rows, so rows the text
+// model has not written yet (any content, NaN included) cannot leak. The tensor cores see the
+// GQA group's 8 heads as the N dimension; at ~8 flop per cache byte the kernel is bound by HBM,
+// and the tensor cores keep the per-key arithmetic (2 x 8 x 128 FMAs) off the issue slots.
+//
+// The CTA whose segment holds the unit's last tile also writes the new k and v rows into cache
+// row pos, and its producer loads that tile only after they are out. A unit cut over several
+// CTAs is merged by the part that finishes last (a per-unit arrival count): it combines every
+// part's unnormalised output with weights 2^(m_p - M) and writes the bf16 result; no CTA ever
+// waits for another.
+//
+// Warp roles (160 threads): warps 0-3 compute (prologue, MMA issue by thread 0, softmax,
+// epilogue); warp 4 lane 0 issues the TMA loads of the K and V tiles into a 3-stage ring.
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "rope.cuh"
+
+namespace ea {
+namespace dec {
+
+constexpr int kThreads = 160;
+constexpr int kCompute = 128;
+constexpr int kStages = 3;
+constexpr uint32_t kAtomBytes = 16384;          // one 64-channel half of a 128-row tile
+constexpr uint32_t kTileBytes = 2 * kAtomBytes;  // a K or a V tile
+constexpr uint32_t kStageBytes = 2 * kTileBytes;
+constexpr uint32_t kOpAtom = 2048;  // one 64-element half of a 16-row operand (Q or P)
+// Shared memory (offsets from the 1024-byte-aligned base)
+constexpr uint32_t SM_RING = 0;
+constexpr uint32_t SM_QT = SM_RING + kStages * kStageBytes;  // 16 rows x 128 channels bf16
+constexpr uint32_t SM_PT = SM_QT + 2 * kOpAtom;              // 16 rows x 128 keys bf16
+constexpr uint32_t SM_RED = SM_PT + 2 * kOpAtom;             // [2][4 warps][8 heads] fp32
+constexpr uint32_t SM_BAR = SM_RED + 2 * 4 * kRepText * 4;
+constexpr int B_FULL = 0, B_EMPTY = kStages, B_SDONE = 2 * kStages, B_ODONE = B_SDONE + 1,
+              B_TAIL = B_ODONE + 1, B_DRAIN = B_TAIL + 1, kNumBars = B_DRAIN + 1;
+constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
+constexpr uint32_t SM_ABORT = SM_TMEM + 4;
+constexpr uint32_t SM_MERGE = SM_ABORT + 4;
+constexpr uint32_t kSmemBytes = SM_MERGE + 4 + 1024;  // + slack to align the base
+static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
+constexpr uint32_t kTmemCols = 32;  // S^T in columns [0, 16), O^T in [16, 32)
+constexpr uint32_t TM_S = 0, TM_O = 16;
+
+struct Seg {
+  int u, j0, j1;  // unit and its key-tile range [j0, j1)
+};
+
+// Next segment of a CTA's tile range [t, end): unit u = t / T (tile indices stay below 2^31).
+__device__ __forceinline__ bool next_seg(long long& t, long long end, int T, Seg& s) {
+  if (t >= end) return false;
+  const int ti = static_cast<int>(t);
+  s.u = ti / T;
+  s.j0 = ti - s.u * T;
+  const long long j1 = s.j0 + (end - t);
+  s.j1 = static_cast<int>(j1 < T ? j1 : T);
+  t += s.j1 - s.j0;
+  return true;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+
+// ------------------------------------------------------------------------------ producer
+template <int CAP>
+__device__ __noinline__ void producer(const DecodeParams<CAP>& p, uint32_t sbase, long long start,
+                                      long long end, volatile uint32_t* abort_flag) {
+  const uint64_t pol = l2_policy_evict_first();  // every cache tile is read once
+  const uint32_t bar0 = sbase + SM_BAR;
+  uint32_t n = 0, n_tail = 0;
+  bool ok = true;
+  long long t = start;
+  Seg s;
+  while (ok && next_seg(t, end, p.T, s)) {
+    const int l = s.u / kHkv, g = s.u % kHkv;
+    for (int j = s.j0; j < s.j1 && ok; ++j) {
+      if (j == p.T - 1) {
+        // the unit's last tile holds row pos, written by this CTA's compute warps
+        ok = bounded_wait(bar0 + 8 * B_TAIL, n_tail & 1, abort_flag, p.status, kErrDecodeWait);
+        if (!ok) break;
+        fence_proxy_async_global();
+        ++n_tail;
+      }
+      const uint32_t slot = n % kStages, round = n / kStages;
+      if (round > 0) {
+        ok = bounded_wait(bar0 + 8 * (B_EMPTY + slot), (round - 1) & 1, abort_flag, p.status,
+                          kErrDecodeWait);
+        if (!ok) break;
+      }
+      const uint32_t fb = bar0 + 8 * (B_FULL + slot);
+      const uint32_t dst = sbase + SM_RING + slot * kStageBytes;
+      mbar_expect_tx(fb, kStageBytes);
+      const int row0 = j * kKeyTile;  // rows past Smax arrive zero-filled
+      tma_load_3d(dst, &p.kmap[l], fb, 0, row0, g, pol);
+      tma_load_3d(dst + kAtomBytes, &p.kmap[l], fb, 64, row0, g, pol);
+      tma_load_3d(dst + kTileBytes, &p.vmap[l], fb, 0, row0, g, pol);
+      tma_load_3d(dst + kTileBytes + kAtomBytes, &p.vmap[l], fb, 64, row0, g, pol);
+      ++n;
+    }
+  }
+  if (!ok) {  // let every copy already issued land before the CTA gives its shared memory back
+    for (uint32_t k = 0; k < static_cast<uint32_t>(kStages) && k < n; ++k) {
+      const uint32_t q = n - 1 - k;
+      if (!drain_wait(bar0 + 8 * (B_FULL + q % kStages), (q / kStages) & 1)) atomicOr(p.status, kErrDrain);
+    }
+  }
+}
+
+// --------------------------------------------------------------------------- compute warps
+// Prologue of a segment: the roped q rows of the unit's 8 heads into QT rows 0-7 (warps 0-1,
+// octet o = head o: lane i holds channels [8i, 8i+8) and their RoPE partners [64+8i, 64+8i+8)),
+// and, for the segment holding the unit's last tile, the new k row (normed, roped, bf16) and v
+// row into cache row pos (warp 2: its four octets compute the same row, octet 0 stores it).
+template <int CAP>
+__device__ __forceinline__ void segment_prologue(const DecodeParams<CAP>& p, uint32_t sbase, int l,
+                                                 int g, bool last, int tid) {
+  const int w = tid >> 5;
+  if (w > 2 || (w == 2 && !last)) return;
+  const int i = tid & 7;
+  const int dl = 8 * i, dh = 64 + 8 * i;
+  float cs[8], sn[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_pos, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[e], sn[e]);
+  float xl[8], xh[8], gl[8], gh[8], yl[8], yh[8];
+  if (w < 2) {
+    const int h = tid >> 3;  // 0..7
+    const __nv_bfloat16* row = p.q_raw[l] + static_cast<size_t>(kRepText * g + h) * kD;
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dl), xl);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dh), xh);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gl);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dh), gh);
+    norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
+    const uint4 ql = pack8(yl, false), qh = pack8(yh, false);
+    const uint32_t qt = sbase + SM_QT;
+    st_shared_v4(qt + swz_off(h, i, kOpAtom), ql.x, ql.y, ql.z, ql.w);
+    st_shared_v4(qt + swz_off(h, i + 8, kOpAtom), qh.x, qh.y, qh.z, qh.w);
+  } else {
+    const __nv_bfloat16* krow = p.k_raw[l] + static_cast<size_t>(g) * kD;
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl), xl);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh), xh);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gl);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gh);
+    norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
+    if (tid < 64 + 8) {
+      const size_t ro = (static_cast<size_t>(g) * p.Smax + p.pos) * kD;
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = pack8(yl, false);
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = pack8(yh, false);
+      const __nv_bfloat16* vrow = p.v_raw[l] + static_cast<size_t>(g) * kD;
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = *reinterpret_cast<const uint4*>(vrow + dl);
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = *reinterpret_cast<const uint4*>(vrow + dh);
+      fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
+    }
+  }
+}
+
+template <int CAP>
+__device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase, uint8_t* smem,
+                                     uint32_t tmem, long long start, long long end,
+                                     volatile uint32_t* abort_flag) {
+  const int tid = threadIdx.x;  // key row (score phase) or channel (output phase) = TMEM lane
+  const int warp = tid >> 5;
+  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t bar0 = sbase + SM_BAR;
+  float* red = reinterpret_cast<float*>(smem + SM_RED);  // [2][4][8]
+  volatile uint32_t* merge_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_MERGE);
+  // S^T: A = K tile (K-major), B = QT (K-major); O^T: A = V tile (MN-major), B = PT (K-major)
+  constexpr uint32_t kIdescS = umma_idesc_f16(128, 16, true, false, false);
+  constexpr uint32_t kIdescO = umma_idesc_f16(128, 16, true, true, false);
+  const uint32_t qt = sbase + SM_QT, pt = sbase + SM_PT;
+  auto wait = [&](int b, uint32_t parity) -> bool {
+    return bounded_wait(bar0 + 8 * b, parity, abort_flag, p.status, kErrDecodeWait);
+  };
+  uint32_t n = 0;  // tiles of this CTA so far
+  bool ok = true, first_seg = true;
+  long long t = start;
+  Seg s;
+  while (ok && next_seg(t, end, p.T, s)) {
+    const int l = s.u / kHkv, g = s.u % kHkv;
+    const bool last = s.j1 == p.T;
+    segment_prologue(p, sbase, l, g, last, tid);
+    fence_proxy_async_smem();  // QT is read by the tensor core (async proxy)
+    bar_sync(1, kCompute);
+    if (last && tid == 0) mbar_arrive(bar0 + 8 * B_TAIL);
+    float m[kRepText], lsum[kRepText];
+#pragma unroll
+    for (int h = 0; h < kRepText; ++h) {
+      m[h] = -INFINITY;
+      lsum[h] = 0.f;
+    }
+    for (int j = s.j0; j < s.j1; ++j, ++n) {
+      const uint32_t slot = n % kStages;
+      const uint32_t kaddr = sbase + SM_RING + slot * kStageBytes, vaddr = kaddr + kTileBytes;
+      bool okt = wait(B_FULL + slot, (n / kStages) & 1);
+      if (tid == 0 && okt) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // 16 channels per step; 4 steps per 64-channel half
+          umma_f16_ss(tmem + TM_S,
+                      sw128_desc(kaddr + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
+                      sw128_desc(qt + (kk >> 2) * kOpAtom + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0);
+        umma_commit(bar0 + 8 * B_SDONE);
+      }
+      // S(n) complete; also PV(n-1), issued before QK(n), so P and the accumulator are free
+      okt = okt && wait(B_SDONE, n & 1);
+      okt = __all_sync(0xffffffffu, okt);
+      const int key = j * kKeyTile + tid;
+      const bool live = key <= p.pos;
+      float x[kRepText];
+      if (okt) {
+        tc_fence_after();
+        uint32_t sv[8];
+        tmem_ld8(tmem + lane_addr + TM_S, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kRepText; ++h) x[h] = live ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
+        if (!live) {  // a row the text model has not written (or past Smax): zero its V row
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            st_shared_v4(vaddr + tid * 128 + 16 * c, 0u, 0u, 0u, 0u);
+            st_shared_v4(vaddr + kAtomBytes + tid * 128 + 16 * c, 0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < kRepText; ++h) {
+          const float mx = warp_max(x[h]);
+          if ((tid & 31) == 0) red[warp * kRepText + h] = mx;
+        }
+      }
+      if (!bar_sync_and(1, kCompute, okt)) {
+        ok = false;
+        break;
+      }
+      float alpha[kRepText], pr[kRepText];
+      bool resc = false;
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h) {
+        const float tm = fmaxf(fmaxf(red[h], red[kRepText + h]), fmaxf(red[2 * kRepText + h], red[3 * kRepText + h]));
+        const float mn = fmaxf(m[h], tm);  // every tile has a live key, so mn is finite
+        alpha[h] = ex2_approx(m[h] - mn);  // 0 on the segment's first tile
+        resc |= alpha[h] != 1.0f;
+        m[h] = mn;
+        pr[h] = ex2_approx(x[h] - mn);
+      }
+      // P^T (B operand, K-major): row h = head, column = key; 16-byte chunk c of row h at
+      // chunk c ^ (h % 8) of the key's 64-key half
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h) {
+        const uint32_t a = pt + (tid >> 6) * kOpAtom + h * 128 +
+                           ((((tid & 63) >> 3) ^ (h & 7)) << 4) + (tid & 7) * 2;
+        st_shared_u16(a, __bfloat16_as_ushort(__float2bfloat16_rn(pr[h])));
+      }
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h) {
+        const float sm = warp_sum(pr[h]);
+        if ((tid & 31) == 0) red[4 * kRepText + warp * kRepText + h] = sm;
+      }
+      bar_sync(1, kCompute);
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h)
+        lsum[h] = lsum[h] * alpha[h] + ((red[4 * kRepText + h] + red[5 * kRepText + h]) +
+                                        (red[6 * kRepText + h] + red[7 * kRepText + h]));
+      if (j > s.j0 && resc) {  // bring the accumulator (tiles before this one) to the new max
+        uint32_t ov[8];
+        tmem_ld8(tmem + lane_addr + TM_O, ov);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kRepText; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+        tmem_st8(tmem + lane_addr + TM_O, ov);
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();  // P^T and zeroed V rows are read by the tensor core
+      tc_fence_before();
+      bar_sync(1, kCompute);
+      if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // 16 keys per step
+          umma_f16_ss(tmem + TM_O, sw128_desc(vaddr + kk * 16 * 128, kAtomBytes, 1024),
+                      sw128_desc(pt + (kk >> 2) * kOpAtom + (kk & 3) * 32, 16, 1024), kIdescO,
+                      (j > s.j0 || kk > 0));
+        umma_commit(bar0 + 8 * (B_EMPTY + slot));  // K and V of this stage are consumed
+        umma_commit(bar0 + 8 * B_ODONE);
+      }
+    }
+    if (!ok) break;
+    // ---- segment end: the last PV (ODONE completes once per tile; PV(n-2) is known complete
+    // since S(n-1) was, so the phase of PV(n-1) is unambiguous)
+    bool oke = wait(B_ODONE, (n - 1) & 1);
+    oke = __all_sync(0xffffffffu, oke);
+    uint32_t ov[8];
+    if (oke) {
+      tc_fence_after();
+      tmem_ld8(tmem + lane_addr + TM_O, ov);  // O^T row = channel tid, column = head
+      tmem_wait_ld();
+    }
+    tc_fence_before();
+    if (!bar_sync_and(1, kCompute, oke)) {
+      ok = false;
+      break;
+    }
+    const bool full = s.j0 == 0 && s.j1 == p.T;
+    if (full) {
+      __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g) * kD + tid;
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h) o[h * kD] = __float2bfloat16_rn(__uint_as_float(ov[h]) / lsum[h]);
+    } else {
+      // partial: unnormalised output with its (max, sum) per head, then the arrival count; the
+      // part that arrives last merges every part of the unit
+      const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
+      const size_t ps = static_cast<size_t>(blockIdx.x) * 2 + slot;
+      float* po = p.part_o + ps * kRepText * kD + tid;
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h) po[h * kD] = __uint_as_float(ov[h]);
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h)
+        if (tid == h) {
+          p.part_ml[(ps * kRepText + h) * 2] = m[h];
+          p.part_ml[(ps * kRepText + h) * 2 + 1] = lsum[h];
+        }
+      __threadfence();
+      bar_sync(1, kCompute);
+      const long long u0 = static_cast<long long>(s.u) * p.T;
+      const int c0 = cta_of_tile(u0, p.W, gridDim.x), c1 = cta_of_tile(u0 + p.T - 1, p.W, gridDim.x);
+      if (tid == 0) *merge_flag = atomicAdd(p.unit_cnt + s.u, 1u) == static_cast<uint32_t>(c1 - c0) ? 1u : 0u;
+      bar_sync(1, kCompute);
+      if (*merge_flag) {
+        __threadfence();
+        float M[kRepText], L[kRepText], acc[kRepText];
+#pragma unroll
+        for (int h = 0; h < kRepText; ++h) {
+          M[h] = -INFINITY;
+          L[h] = 0.f;
+          acc[h] = 0.f;
+        }
+        for (int c = c0; c <= c1; ++c) {
+          const size_t cs = static_cast<size_t>(c) * 2 + (cta_tile_start(c, p.W, gridDim.x) >= u0 ? 0 : 1);
+#pragma unroll
+          for (int h = 0; h < kRepText; ++h) M[h] = fmaxf(M[h], __ldcg(p.part_ml + (cs * kRepText + h) * 2));
+        }
+        for (int c = c0; c <= c1; ++c) {
+          const size_t cs = static_cast<size_t>(c) * 2 + (cta_tile_start(c, p.W, gridDim.x) >= u0 ? 0 : 1);
+#pragma unroll
+          for (int h = 0; h < kRepText; ++h) {
+            const float wgt = ex2_approx(__ldcg(p.part_ml + (cs * kRepText + h) * 2) - M[h]);
+            L[h] = fmaf(__ldcg(p.part_ml + (cs * kRepText + h) * 2 + 1), wgt, L[h]);
+            acc[h] = fmaf(__ldcg(p.part_o + (cs * kRepText + h) * kD + tid), wgt, acc[h]);
+          }
+        }
+        __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g) * kD + tid;
+#pragma unroll
+        for (int h = 0; h < kRepText; ++h) o[h * kD] = __float2bfloat16_rn(acc[h] / L[h]);
+        if (tid == 0) p.unit_cnt[s.u] = 0u;  // every part has arrived: ready for the next call
+      }
+      bar_sync(1, kCompute);  // the merge flag is read before the next segment overwrites it
+    }
+    first_seg = false;
+  }
+  // Every MMA issued must be complete before TMEM is released.
+  if (tid == 0) {
+    umma_commit(bar0 + 8 * B_DRAIN);
+    if (!drain_wait(bar0 + 8 * B_DRAIN, 0)) atomicOr(p.status, kErrDrain);
+  }
+}
+
+}  // namespace dec
+
+template <int CAP>
+__global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(const __grid_constant__ DecodeParams<CAP> p) {
+  using namespace dec;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + SM_BAR;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_ABORT);
+  const long long start = cta_tile_start(blockIdx.x, p.W, gridDim.x);
+  const long long end = cta_tile_start(blockIdx.x + 1, p.W, gridDim.x);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kStages; ++b) {
+      mbar_init(bar0 + 8 * (B_FULL + b), 1);
+      mbar_init(bar0 + 8 * (B_EMPTY + b), 1);
+    }
+    mbar_init(bar0 + 8 * B_SDONE, 1);
+    mbar_init(bar0 + 8 * B_ODONE, 1);
+    mbar_init(bar0 + 8 * B_TAIL, 1);
+    mbar_init(bar0 + 8 * B_DRAIN, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  // rows 8-15 of the Q and P operands are the zero padding of N = 16
+  for (int i = threadIdx.x; i < 2 * 2 * 64; i += kThreads) {
+    const uint32_t op = (i >> 7) ? SM_PT : SM_QT;
+    const uint32_t off = op + ((i >> 6) & 1) * kOpAtom + 1024 + (i & 63) * 16;
+    st_shared_v4(sbase + off, 0u, 0u, 0u, 0u);
+  }
+  if (warp == 0) {
+    tmem_alloc(sbase + SM_TMEM, kTmemCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  // everything below reads what earlier kernels in the stream wrote (inputs, caches)
+  pdl_wait_primary();
+  if (warp < 4) {
+    compute(p, sbase, smem, tmem, start, end, abort_flag);
+  } else if ((threadIdx.x & 31) == 0) {
+    prefetch_tensormap(&p.kmap[0]);
+    producer(p, sbase, start, end, abort_flag);
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t decode_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(decode_attention_kernel<kSmallCap>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dec::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_attention_kernel<kDecodeMaxLayers>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dec::kSmemBytes));
+  return e;
+}
+
+template <int CAP>
+cudaError_t launch_decode_kernel(const DecodeParams<CAP>& dp, cudaLaunchConfig_t cfg) {
+  cfg.blockDim = dim3(dec::kThreads);
+  cfg.dynamicSmemBytes = dec::kSmemBytes;
+  return cudaLaunchKernelEx(&cfg, decode_attention_kernel<CAP>, dp);
+}
+template cudaError_t launch_decode_kernel<kSmallCap>(const DecodeParams<kSmallCap>&, cudaLaunchConfig_t);
+template cudaError_t launch_decode_kernel<kDecodeMaxLayers>(const DecodeParams<kDecodeMaxLayers>&,
+                                                            cudaLaunchConfig_t);
+
+}  // namespace ea

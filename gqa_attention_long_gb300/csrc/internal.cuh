@@ -43,6 +43,7 @@ enum : uint32_t {
   kErrMergeWait = 1u << 5,
   kErrSelftestWait = 1u << 6,
   kErrLinearWait = 1u << 7,
+  kErrDecodeWait = 1u << 8,
 };
 
 // ------------------------------------------------------------------------- workspace layout
@@ -142,6 +143,57 @@ struct AttnParams {
   int fused_merge;     // every split unit has two parts: the second one merges in-kernel
   float scale_log2;    // log2(e) / sqrt(128)
 };
+
+// ------------------------------------------------------------ text-model decode attention
+// One decode step of the VLM text model (alpamayo_tt/text.py, TTText._layer_decode): 64 query
+// heads, 8 KV heads; query head h reads KV head h / 8. A unit is one (layer, kv head): its 8
+// query heads against cache rows [0, pos], cut into key tiles of 128 rows.
+constexpr int kHqText = 64;
+constexpr int kRepText = kHqText / kHkv;  // query heads per KV head
+constexpr int kDecodeMaxLayers = 64;
+
+template <int CAP>
+struct DecodeParams {
+  CUtensorMap kmap[CAP];  // all Smax rows of K: dims {128, Smax, 8}, box {64, 128, 1}, 128B swizzle
+  CUtensorMap vmap[CAP];
+  const __nv_bfloat16* q_raw[CAP];  // [64][128]
+  const __nv_bfloat16* k_raw[CAP];  // [8][128]
+  const __nv_bfloat16* v_raw[CAP];  // [8][128]
+  const __nv_bfloat16* q_gamma[CAP];
+  const __nv_bfloat16* k_gamma[CAP];
+  __nv_bfloat16* kc[CAP];  // caches [8][Smax][128]; the kernel writes row pos
+  __nv_bfloat16* vc[CAP];
+  __nv_bfloat16* out[CAP];  // [64][128]
+  float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
+  float inv_lo[kD / 2];
+  float* part_o;         // [n_ctas][2 slots][8 heads][128] unnormalised partial outputs
+  float* part_ml;        // [n_ctas][2 slots][8 heads][2]: running max (log2 units) and sum
+  uint32_t* unit_cnt;    // [unit]: parts that have written their partial (zero between calls)
+  uint32_t* status;
+  long long W;           // total key tiles = n_layers * 8 * T
+  int T;                 // key tiles per unit: ceil((pos + 1) / 128)
+  int pos, rope_pos;     // the token's cache row, and its RoPE position pos + rope_delta
+  int Smax;              // cache rows per head
+  float scale_log2;      // log2(e) / sqrt(128)
+};
+
+// Decode workspace: [0, 1024) status word; unit counters n_layers * 8 uint32 (1 KB aligned);
+// partial outputs and statistics for at most max_ctas CTAs.
+struct DecodeWs {
+  size_t cnt_off, part_o_off, part_ml_off, total;
+};
+constexpr DecodeWs decode_ws_layout(int n_layers, int max_ctas) {
+  DecodeWs w{};
+  size_t off = 1024;
+  w.cnt_off = off;
+  off += ((static_cast<size_t>(n_layers) * kHkv * sizeof(uint32_t)) + 1023) & ~static_cast<size_t>(1023);
+  w.part_o_off = off;
+  off += static_cast<size_t>(max_ctas) * 2 * kRepText * kD * sizeof(float);
+  w.part_ml_off = off;
+  off += static_cast<size_t>(max_ctas) * 2 * kRepText * 2 * sizeof(float);
+  w.total = (off + 1023) & ~static_cast<size_t>(1023);
+  return w;
+}
 
 // ------------------------------------------------------------ decoder-layer projections
 constexpr int kMaxHidden = 8192;   // widest residual stream of the decoder layer

@@ -226,6 +226,52 @@ size_t expert_linear64_workspace_size(int K, int N);
 int expert_linear64(const void* x, const void* w, void* y, int K, int N, void* workspace,
                     size_t ws_bytes, ea_stream_t stream);
 
+/* ------------------------------------------------------------ text-model decode attention
+ * One decode step of the VLM text model over the same per-layer caches (alpamayo_tt/text.py,
+ * TTText._layer_decode, with the cos/sin of TTText._decode_inputs_host): for the new token at
+ * cache row pos, with 64 query heads and 8 KV heads of width 128 (query head h reads KV head
+ * h / 8),
+ *   1. RMS-normalise every q and k head row with the q_norm / k_norm gains (eps 1e-6) and rotate
+ *      it with the HF rotate_half RoPE, theta 5e6, at position pos + rope_delta (the text
+ *      model's multimodal RoPE with its three position ids equal);
+ *   2. write the roped k (rounded to bf16) and the raw v into row pos of the layer's K and V
+ *      caches (paged_update_cache);
+ *   3. out[h] = softmax(q_h K[h/8, 0..pos]^T / sqrt(128)) V[h/8, 0..pos]
+ *      (scaled_dot_product_attention_decode with cur_pos = pos: the new row is included).
+ * Rows after pos are never read (their content, NaN included, does not matter) and only row pos
+ * is written. Layouts: q_raw bf16 [64][128], k_raw and v_raw bf16 [8][128], gains bf16 [128],
+ * caches bf16 [8][Smax][128] row-major per head (the layout of ea_layer_args), out bf16
+ * [64][128]. All pointers are device pointers, 16-byte aligned; 0 <= pos < Smax, Smax a
+ * multiple of 64 and >= 128. Ownership, asynchrony and errors as for expert_attn_layers. */
+typedef struct {
+  const void* q_raw;
+  const void* k_raw;
+  const void* v_raw;
+  const void* q_gamma;
+  const void* k_gamma;
+  void* k_cache;
+  void* v_cache;
+  void* out;
+} ea_decode_args;
+
+/* Bytes of workspace for text_decode_attention over n_layers layers per call on the current
+ * device (0 if no suitable device is present). */
+size_t text_decode_workspace_size(int n_layers);
+
+/* Zeroes the status word and the per-unit arrival counts (cudaMemsetAsync on `stream`). Call
+ * once before the first use of a workspace; the kernel leaves the counts zero after every
+ * call that completes, and after a call that reported EA_ERR_TIMEOUT the workspace must be
+ * cleared again. The status word is read with expert_attn_read_status. */
+int text_decode_workspace_init(void* workspace, size_t ws_bytes, ea_stream_t stream);
+
+/* The decode step of n_layers independent layers (an array of n_layers ea_decode_args in host
+ * memory) at the same pos and rope_delta, one kernel launch per 64 layers: every layer's keys
+ * are cut into 128-row tiles that are spread over all SMs; a layer's KV head split over several
+ * CTAs is merged by the part that finishes last. The workspace (256-byte aligned, size from
+ * text_decode_workspace_size, cleared once) must not be shared by calls that overlap. */
+int text_decode_attention(const ea_decode_args* layers, int n_layers, int pos, int Smax,
+                          int rope_delta, void* workspace, size_t ws_bytes, ea_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

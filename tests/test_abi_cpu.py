@@ -24,14 +24,15 @@ def h():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(expert_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**((?:expert|text)_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("expert_attn_prologue", "expert_attn_layer", "expert_attn_layers",
               "expert_attn_workspace_size", "expert_attn_status_string", "expert_decoder_layer",
-              "expert_decoder_layer_workspace_size", "expert_linear64"):
+              "expert_decoder_layer_workspace_size", "expert_linear64", "text_decode_attention",
+              "text_decode_workspace_size", "text_decode_workspace_init"):
         assert n in names
 
 
@@ -140,3 +141,30 @@ def test_linear64_rejects_bad_arguments_without_gpu(h):
     assert h.expert_linear64(p, p, p, 64, 192, ws, big, None) == _lib.EA_ERR_INVALID_ARG   # N % 128
     assert h.expert_linear64(ctypes.c_void_p(0x10004), p, p, 64, 128, ws, big, None) == _lib.EA_ERR_MISALIGNED
     assert h.expert_linear64_workspace_size(96, 128) == 0
+
+
+def _decode_args(**over):
+    a = _lib.EaDecodeArgs()
+    for name, _ in _lib.EaDecodeArgs._fields_:
+        setattr(a, name, over.get(name, 0x10000))
+    return a
+
+
+def test_decode_rejects_bad_arguments_without_gpu(h):
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 30
+    f = h.text_decode_attention
+    one = ctypes.byref(_decode_args())
+    assert f(None, 1, 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(one, 0, 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG       # no layers
+    assert f(one, 1, -1, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG       # pos < 0
+    assert f(one, 1, 512, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG      # pos >= Smax
+    assert f(one, 1, 10, 500, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG       # Smax % 64
+    assert f(one, 1, 10, 512, 1 << 25, ws, big, None) == _lib.EA_ERR_INVALID_ARG  # position range
+    assert f(one, 1, 10, 512, 0, None, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(one, 1, 10, 512, 0, ctypes.c_void_p(0x100080), big, None) == _lib.EA_ERR_MISALIGNED
+    assert f(ctypes.byref(_decode_args(out=None)), 1, 10, 512, 0, ws, big, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(ctypes.byref(_decode_args(k_cache=0x10008)), 1, 10, 512, 0, ws, big, None) == \
+        _lib.EA_ERR_MISALIGNED
+    assert h.text_decode_workspace_size(0) == 0
+    assert h.text_decode_workspace_init(None, 4096, None) == _lib.EA_ERR_INVALID_ARG
