@@ -59,6 +59,12 @@ def launches_per_call(n_layers: int, S: int, sm_count: int, kv_dtype: int = 0) -
     return kernels_per_call(n_layers, S, sm_count, kv_dtype)
 
 
+def decode_bytes_per_layer(pos: int) -> int:
+    """Algorithmic HBM bytes of one text-model decode step of one layer: cache K/V rows 0..pos
+    read (row pos after it is written), the new k/v row written, raw q/k/v read, output written."""
+    return 2 * HKV * (pos + 1) * D * 2 + 2 * HKV * D * 2 + (64 + 2 * HKV) * D * 2 + 64 * D * 2
+
+
 def flops_per_layer(S: int) -> int:
     return 4 * (2 * T) * D * (S + T) * HKV
 
@@ -491,6 +497,56 @@ def main():
                   "launches_per_layer": 8 if launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1 else 7}
         del Wl, wsl
 
+    # ---- the text model's single-token decode attention (survey NEXT row 3) over the same caches:
+    # the decode token at row pos = S of every layer's cache (the expert never reads that row).
+    # All 64 layers in one call (throughput), and one layer per call rotating over 8 layers
+    # (the latency of one layer of a decode step)
+    tdec = None
+    if not args.no_extras:
+        g6 = torch.Generator(device=dev).manual_seed(config_seed(6, 0))
+        rb = lambda *shape: torch.randn(*shape, generator=g6, device=dev).to(torch.bfloat16)  # noqa: E731
+        Ld = [ea.DecodeBuffers(q_raw=rb(64, D), k_raw=rb(HKV, D), v_raw=rb(HKV, D), q_gamma=x.q_gamma,
+                               k_gamma=x.k_gamma, k_cache=x.k_cache, v_cache=x.v_cache,
+                               out=torch.empty(64, D, dtype=torch.bfloat16, device=dev)) for x in xs]
+        wsd = ea.alloc_decode_workspace(n)
+        arrd = ea.make_decode_args(Ld, Smax)
+        for _ in range(args.warmup):
+            ea.text_decode_attention(Ld, S, Smax, 0, wsd, stream, _arr=arrd)
+        torch.cuda.synchronize()
+        t0d, t1d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0d.record(stream)
+        for _ in range(args.steps):
+            ea.text_decode_attention(Ld, S, Smax, 0, wsd, stream, _arr=arrd)
+        t1d.record(stream)
+        torch.cuda.synchronize()
+        msd = t0d.elapsed_time(t1d) / args.steps
+        ws1d = ea.alloc_decode_workspace(1)
+        arr1 = [ea.make_decode_args([Ld[l]], Smax) for l in range(8)]
+        for l in range(8):
+            ea.text_decode_attention([Ld[l]], S, Smax, 0, ws1d, stream, _arr=arr1[l])
+        torch.cuda.synchronize()
+        reps = 8 * max(4, args.steps // 2)
+        t2d, t3d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t2d.record(stream)
+        for k in range(reps):
+            ea.text_decode_attention([Ld[k % 8]], S, Smax, 0, ws1d, stream, _arr=arr1[k % 8])
+        t3d.record(stream)
+        torch.cuda.synchronize()
+        us1d = t2d.elapsed_time(t3d) * 1e3 / reps
+        for w_ in (wsd, ws1d):
+            std, bitsd = ea.expert_attn_read_status(w_)
+            if std != 0:
+                raise RuntimeError(f"decode kernel status bits {bitsd:#x}")
+        bd = decode_bytes_per_layer(S)
+        tdec = {"workload": f"text-model decode attention, 64 q heads / 8 kv heads, pos={S}, Smax={Smax}, "
+                            f"bf16 cache; {n} layers per call, and one layer per call over 8 layers",
+                "us_per_layer": msd * 1e3 / n, "bytes_per_layer": bd,
+                "hbm_gbs": bd * n / (msd * 1e-3) / 1e9,
+                "roofline_frac": bd * n / (msd * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "one_layer_per_call_us": us1d, "one_layer_hbm_gbs": bd / (us1d * 1e-6) / 1e9,
+                "launches_per_call": 1}
+        del Ld, wsd, ws1d
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         smp = oracle_sample(S, Smax, 8, 10.0)
@@ -522,6 +578,7 @@ def main():
             "single_layer": single,
             "sequential_chain": chain,
             "decoder_layer": dlayer,
+            "text_decode": tdec,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

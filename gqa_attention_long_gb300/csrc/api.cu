@@ -209,13 +209,20 @@ namespace {
 // kernels fully rewrite on every call.
 constexpr size_t kInitBytes = ws_layout(kMaxLayersPerLaunch, 1, true).qscale_off;
 
-// RoPE inverse frequencies theta^(-2j/128) = 5e6^(-j/64), j < 64, as fp32 (hi, lo) pairs.
+// RoPE inverse frequencies theta^(-2j/128) = 5e6^(-j/64), j < 64, as fp32 (hi, lo) pairs
+// (computed once per process).
 void rope_inv_freq(float* hi, float* lo) {
-  for (int j = 0; j < kD / 2; ++j) {
-    const double inv = std::pow(5.0e6, -static_cast<double>(j) / (kD / 2));
-    hi[j] = static_cast<float>(inv);
-    lo[j] = static_cast<float>(inv - static_cast<double>(hi[j]));
-  }
+  static float t_hi[kD / 2], t_lo[kD / 2];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (int j = 0; j < kD / 2; ++j) {
+      const double inv = std::pow(5.0e6, -static_cast<double>(j) / (kD / 2));
+      t_hi[j] = static_cast<float>(inv);
+      t_lo[j] = static_cast<float>(inv - static_cast<double>(t_hi[j]));
+    }
+  });
+  std::memcpy(hi, t_hi, sizeof(t_hi));
+  std::memcpy(lo, t_lo, sizeof(t_lo));
 }
 
 int n_ctas_for(long long W, int sm_count) {
@@ -984,7 +991,9 @@ int launch_decode_t(const ea_decode_args* a, int n, int pos, int Smax, int rope_
   dp.part_ml = reinterpret_cast<float*>(ws + wl.part_ml_off);
   dp.unit_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
   dp.status = reinterpret_cast<uint32_t*>(ws);
-  const int n_ctas = static_cast<long long>(sm_count) < dp.W ? sm_count : static_cast<int>(dp.W);
+  // one CTA per SM (at most 160: the merge stages at most that many parts in shared memory)
+  int n_ctas = sm_count < 160 ? sm_count : 160;
+  if (static_cast<long long>(n_ctas) > dp.W) n_ctas = static_cast<int>(dp.W);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(st, attr, true);
   cfg.gridDim = dim3(n_ctas);

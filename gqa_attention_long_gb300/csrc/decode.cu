@@ -59,7 +59,9 @@ constexpr int B_FULL = 0, B_EMPTY = kStages, B_SDONE = 2 * kStages, B_ODONE = B_
 constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t SM_MERGE = SM_ABORT + 4;
-constexpr uint32_t kSmemBytes = SM_MERGE + 4 + 1024;  // + slack to align the base
+constexpr int kMaxParts = 160;  // parts of one unit (at most one per CTA; the grid is <= 160)
+constexpr uint32_t SM_PARTML = (SM_MERGE + 4 + 15) & ~15u;  // [part][head] (max, sum) of a merge
+constexpr uint32_t kSmemBytes = SM_PARTML + kMaxParts * kRepText * 8 + 1024;  // + base alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
 constexpr uint32_t kTmemCols = 32;  // S^T in columns [0, 16), O^T in [16, 32)
 constexpr uint32_t TM_S = 0, TM_O = 16;
@@ -355,6 +357,17 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       bar_sync(1, kCompute);
       if (*merge_flag) {
         __threadfence();
+        // every part's (max, sum) into shared memory with one round of independent loads; the
+        // first part's partial may sit in its CTA's second slot, every other part's in its first
+        const int np = c1 - c0 + 1;
+        const int slot0 = cta_tile_start(c0, p.W, gridDim.x) >= u0 ? 0 : 1;
+        float2* sml = reinterpret_cast<float2*>(smem + SM_PARTML);  // [part][head]
+        for (int i = tid; i < np * kRepText; i += kCompute) {
+          const int c = c0 + i / kRepText;
+          const size_t cs = static_cast<size_t>(c) * 2 + (c == c0 ? slot0 : 0);
+          sml[i] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + cs * kRepText + i % kRepText);
+        }
+        bar_sync(1, kCompute);
         float M[kRepText], L[kRepText], acc[kRepText];
 #pragma unroll
         for (int h = 0; h < kRepText; ++h) {
@@ -362,18 +375,30 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
           L[h] = 0.f;
           acc[h] = 0.f;
         }
-        for (int c = c0; c <= c1; ++c) {
-          const size_t cs = static_cast<size_t>(c) * 2 + (cta_tile_start(c, p.W, gridDim.x) >= u0 ? 0 : 1);
+        for (int c = 0; c < np; ++c)
 #pragma unroll
-          for (int h = 0; h < kRepText; ++h) M[h] = fmaxf(M[h], __ldcg(p.part_ml + (cs * kRepText + h) * 2));
-        }
-        for (int c = c0; c <= c1; ++c) {
-          const size_t cs = static_cast<size_t>(c) * 2 + (cta_tile_start(c, p.W, gridDim.x) >= u0 ? 0 : 1);
+          for (int h = 0; h < kRepText; ++h) M[h] = fmaxf(M[h], sml[c * kRepText + h].x);
+        // the parts' outputs, eight parts per batch of independent loads (past the last part the
+        // index is clamped and the weight is 0)
+        for (int cb = 0; cb < np; cb += 8) {
+          float v[8][kRepText];
 #pragma unroll
-          for (int h = 0; h < kRepText; ++h) {
-            const float wgt = ex2_approx(__ldcg(p.part_ml + (cs * kRepText + h) * 2) - M[h]);
-            L[h] = fmaf(__ldcg(p.part_ml + (cs * kRepText + h) * 2 + 1), wgt, L[h]);
-            acc[h] = fmaf(__ldcg(p.part_o + (cs * kRepText + h) * kD + tid), wgt, acc[h]);
+          for (int b = 0; b < 8; ++b) {
+            const int c = cb + b < np ? cb + b : np - 1;
+            const size_t cs = static_cast<size_t>(c0 + c) * 2 + (c == 0 ? slot0 : 0);
+#pragma unroll
+            for (int h = 0; h < kRepText; ++h) v[b][h] = __ldcg(p.part_o + (cs * kRepText + h) * kD + tid);
+          }
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (cb + b >= np) break;
+#pragma unroll
+            for (int h = 0; h < kRepText; ++h) {
+              const float2 ml = sml[(cb + b) * kRepText + h];
+              const float wgt = ex2_approx(ml.x - M[h]);
+              L[h] = fmaf(ml.y, wgt, L[h]);
+              acc[h] = fmaf(v[b][h], wgt, acc[h]);
+            }
           }
         }
         __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g) * kD + tid;
