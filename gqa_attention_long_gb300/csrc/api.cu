@@ -991,12 +991,24 @@ int launch_decode_t(const ea_decode_args* a, int n, int pos, int Smax, int rope_
   dp.part_ml = reinterpret_cast<float*>(ws + wl.part_ml_off);
   dp.unit_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt_off);
   dp.status = reinterpret_cast<uint32_t*>(ws);
-  // one CTA per SM (at most 160: the merge stages at most that many parts in shared memory)
-  int n_ctas = sm_count < 160 ? sm_count : 160;
-  if (static_cast<long long>(n_ctas) > dp.W) n_ctas = static_cast<int>(dp.W);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(st, attr, true);
-  cfg.gridDim = dim3(n_ctas);
+  if (n == 1 && dp.T >= 2 && dp.T <= 8) {
+    // one layer over a short cache: a cluster of T CTAs (one per key tile) per kv head,
+    // merged through distributed shared memory
+    dp.cluster = dp.T;
+    cfg.gridDim = dim3(kHkv * dp.cluster);
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(dp.cluster);
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    ++cfg.numAttrs;
+  } else {
+    // one CTA per SM (at most 160: the merge stages at most that many parts in shared memory)
+    int n_ctas = sm_count < 160 ? sm_count : 160;
+    if (static_cast<long long>(n_ctas) > dp.W) n_ctas = static_cast<int>(dp.W);
+    cfg.gridDim = dim3(n_ctas);
+  }
   if (launch_decode_kernel<CAP>(dp, cfg) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;

@@ -30,7 +30,15 @@
 // row pos, and its producer loads that tile only after they are out. A unit cut over several
 // CTAs is merged by the part that finishes last (a per-unit arrival count): it combines every
 // part's unnormalised output with weights 2^(m_p - M) and writes the bf16 result; no CTA ever
-// waits for another.
+// waits for another. A single-layer call over a short cache (2 to 8 key tiles per unit: the
+// decode step of one layer, pos < 1024) runs instead as one thread-block cluster per unit with
+// one CTA per tile: the parts leave their partials in shared memory and, after a cluster
+// barrier, the CTAs combine the unit's outputs from the cluster's shared memory, so no partial
+// travels through global memory. (For longer caches the grid-wide split is faster: clusters of
+// 16 CTAs that each hold a whole SM wait for a whole free GPC, which a preceding kernel's tail
+// delays.)
+// Before waiting for the preceding kernel, the producer asks L2 for the CTA's first tiles (a
+// prefetch only: what the preceding kernel writes still wins).
 //
 // Warp roles (160 threads): warps 0-3 compute (prologue, MMA issue by thread 0, softmax,
 // epilogue); warp 4 lane 0 issues the TMA loads of the K and V tiles into a 3-stage ring.
@@ -61,7 +69,11 @@ constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t SM_MERGE = SM_ABORT + 4;
 constexpr int kMaxParts = 160;  // parts of one unit (at most one per CTA; the grid is <= 160)
 constexpr uint32_t SM_PARTML = (SM_MERGE + 4 + 15) & ~15u;  // [part][head] (max, sum) of a merge
-constexpr uint32_t kSmemBytes = SM_PARTML + kMaxParts * kRepText * 8 + 1024;  // + base alignment
+// cluster mode: this CTA's partial, read by the cluster's other CTAs: O [8 heads][128] fp32, then
+// (max, sum) per head
+constexpr uint32_t SM_CPART = SM_PARTML + kMaxParts * kRepText * 8;
+constexpr uint32_t SM_CPART_ML = SM_CPART + kRepText * kD * 4;
+constexpr uint32_t kSmemBytes = SM_CPART_ML + kRepText * 8 + 1024;  // + base alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
 constexpr uint32_t kTmemCols = 32;  // S^T in columns [0, 16), O^T in [16, 32)
 constexpr uint32_t TM_S = 0, TM_O = 16;
@@ -202,6 +214,8 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
   auto wait = [&](int b, uint32_t parity) -> bool {
     return bounded_wait(bar0 + 8 * b, parity, abort_flag, p.status, kErrDecodeWait);
   };
+  if (p.cluster && tid < kRepText)  // an empty partial, for a CTA without tiles (or that gave up)
+    reinterpret_cast<float2*>(smem + SM_CPART_ML)[tid] = make_float2(-INFINITY, 0.f);
   uint32_t n = 0;  // tiles of this CTA so far
   bool ok = true, first_seg = true;
   long long t = start;
@@ -331,7 +345,16 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       break;
     }
     const bool full = s.j0 == 0 && s.j1 == p.T;
-    if (full) {
+    if (p.cluster) {
+      // cluster mode: the partial stays in this CTA's shared memory for the cluster's merge
+      float* cpo = reinterpret_cast<float*>(smem + SM_CPART) + tid;
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h) cpo[h * kD] = __uint_as_float(ov[h]);
+      float2* cml = reinterpret_cast<float2*>(smem + SM_CPART_ML);
+#pragma unroll
+      for (int h = 0; h < kRepText; ++h)
+        if (tid == h) cml[h] = make_float2(m[h], lsum[h]);
+    } else if (full) {
       __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g) * kD + tid;
 #pragma unroll
       for (int h = 0; h < kRepText; ++h) o[h * kD] = __float2bfloat16_rn(__uint_as_float(ov[h]) / lsum[h]);
@@ -428,8 +451,15 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + SM_BAR;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_ABORT);
-  const long long start = cta_tile_start(blockIdx.x, p.W, gridDim.x);
-  const long long end = cta_tile_start(blockIdx.x + 1, p.W, gridDim.x);
+  long long start, end;
+  if (p.cluster) {  // one cluster per unit, rank r: tiles [r T / CS, (r + 1) T / CS) of it
+    const long long u = blockIdx.x / p.cluster, r = blockIdx.x % p.cluster;
+    start = u * p.T + r * p.T / p.cluster;
+    end = u * p.T + (r + 1) * p.T / p.cluster;
+  } else {
+    start = cta_tile_start(blockIdx.x, p.W, gridDim.x);
+    end = cta_tile_start(blockIdx.x + 1, p.W, gridDim.x);
+  }
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int b = 0; b < kStages; ++b) {
@@ -458,6 +488,18 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
+  if (warp == 4 && (threadIdx.x & 31) == 0) {
+    // the first tiles of this CTA's range into L2 while the preceding kernel finishes (a hint:
+    // the TMA loads below run after the wait and read whatever that kernel wrote)
+    for (long long x = start; x < end && x < start + kStages; ++x) {
+      const int u = static_cast<int>(x / p.T), j = static_cast<int>(x - static_cast<long long>(u) * p.T);
+      const int l = u / kHkv, g = u % kHkv;
+      const int rows = p.Smax - j * kKeyTile < kKeyTile ? p.Smax - j * kKeyTile : kKeyTile;
+      const size_t off = (static_cast<size_t>(g) * p.Smax + static_cast<size_t>(j) * kKeyTile) * kD;
+      prefetch_l2_bulk(p.kc[l] + off, static_cast<uint32_t>(rows) * kD * 2);
+      prefetch_l2_bulk(p.vc[l] + off, static_cast<uint32_t>(rows) * kD * 2);
+    }
+  }
   // everything below reads what earlier kernels in the stream wrote (inputs, caches)
   pdl_wait_primary();
   if (warp < 4) {
@@ -470,6 +512,50 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.cluster) {
+    // every CTA of the cluster has its partial (or an empty one) in shared memory. The cluster's
+    // CS (2..8) CTAs share the unit's 1024 outputs (head h, channel c at index 128 h + c):
+    // rank r combines indices r, r + CS, ..., each from the CS parts, with every remote load
+    // of a thread issued before the first is used. Every thread of every CTA reaches both
+    // cluster barriers exactly once.
+    cluster_sync();
+    const uint32_t cs = static_cast<uint32_t>(p.cluster), r = cluster_ctarank();
+    float2* lml = reinterpret_cast<float2*>(smem + SM_PARTML);  // the parts' (max, sum) [part][head]
+    if (threadIdx.x < cs * kRepText)
+      lml[threadIdx.x] = ld_shared_cluster_v2(
+          mapa_shared(sbase + SM_CPART_ML + (threadIdx.x % kRepText) * 8, threadIdx.x / kRepText));
+    __syncthreads();
+    if (threadIdx.x < kCompute) {
+      const int u = blockIdx.x / p.cluster, l = u / kHkv, g = u % kHkv;
+      float ov[4][16];  // output jj of this thread (index r + CS (tid + 128 jj)), part k
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint32_t idx = r + cs * (threadIdx.x + 128u * jj);
+#pragma unroll
+        for (uint32_t k = 0; k < 16; ++k)
+          if (idx < kRepText * kD && k < cs) ov[jj][k] = ld_shared_cluster_f32(mapa_shared(sbase + SM_CPART + idx * 4, k));
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint32_t idx = r + cs * (threadIdx.x + 128u * jj);
+        if (idx >= kRepText * kD) continue;
+        const uint32_t h = idx >> 7;
+        float M = -INFINITY, L = 0.f, acc = 0.f;
+#pragma unroll
+        for (uint32_t k = 0; k < 16; ++k)
+          if (k < cs) M = fmaxf(M, lml[k * kRepText + h].x);
+#pragma unroll
+        for (uint32_t k = 0; k < 16; ++k)
+          if (k < cs && lml[k * kRepText + h].x != -INFINITY) {  // parts without tiles add nothing
+            const float wgt = ex2_approx(lml[k * kRepText + h].x - M);
+            L = fmaf(lml[k * kRepText + h].y, wgt, L);
+            acc = fmaf(ov[jj][k], wgt, acc);
+          }
+        p.out[l][static_cast<size_t>(kRepText * g) * kD + idx] = __float2bfloat16_rn(acc / L);
+      }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
+  }
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -479,6 +565,8 @@ cudaError_t decode_set_attributes() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_attention_kernel<kDecodeMaxLayers>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dec::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_attention_kernel<kSmallCap>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 

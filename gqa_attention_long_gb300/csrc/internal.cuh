@@ -174,6 +174,9 @@ struct DecodeParams {
   int T;                 // key tiles per unit: ceil((pos + 1) / 128)
   int pos, rope_pos;     // the token's cache row, and its RoPE position pos + rope_delta
   int Smax;              // cache rows per head
+  int cluster;           // 0: tiles of all units over all CTAs, split units merged through global
+                         // memory; else the cluster size: one cluster per unit, merged through
+                         // distributed shared memory
   float scale_log2;      // log2(e) / sqrt(128)
 };
 

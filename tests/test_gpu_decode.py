@@ -113,21 +113,26 @@ def decode_inputs_copy(x):
                         c(x.k_cache), c(x.v_cache), x.pos, x.Smax)
 
 
-def test_decode_repeated_calls_are_bitwise_equal_and_leave_counts_zero():
-    # The split heads are merged by whichever part arrives last; the result must not depend on
-    # that order, and each call must leave the per-unit counts at zero for the next one.
-    x = decode_inputs(840, 3000, 4096)
-    L = to_dev(x)
-    ws = ea.alloc_decode_workspace(1)
+@pytest.mark.parametrize("n_layers,pos", [(1, 900), (1, 3000), (2, 3000)])
+def test_decode_repeated_calls_are_bitwise_equal_and_leave_counts_zero(n_layers, pos):
+    # One layer over up to 8 key tiles runs as one cluster per kv head (partials combined in
+    # distributed shared memory); longer caches and several layers spread many parts per kv
+    # head over the grid, merged by whichever part arrives last. No result may depend on
+    # timing, and every call must leave the per-unit counts at zero for the next one.
+    xs = [decode_inputs(840 + l, pos, 4096) for l in range(n_layers)]
+    Ls = [to_dev(x) for x in xs]
+    ws = ea.alloc_decode_workspace(n_layers)
     outs = []
     for _ in range(3):
-        L.k_cache.copy_(x.k_cache.cuda())
-        L.v_cache.copy_(x.v_cache.cuda())
-        ea.text_decode_attention([L], x.pos, x.Smax, 0, ws)
+        for x, L in zip(xs, Ls):
+            L.k_cache.copy_(x.k_cache.cuda())
+            L.v_cache.copy_(x.v_cache.cuda())
+        ea.text_decode_attention(Ls, xs[0].pos, xs[0].Smax, 0, ws)
         torch.cuda.synchronize()
         check_status(ws)
-        outs.append(L.out.clone())
-    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
-    assert_close(f64(outs[0]), oracle_step(x)["out"])
+        outs.append([L.out.clone() for L in Ls])
+    for l in range(n_layers):
+        assert torch.equal(outs[0][l], outs[1][l]) and torch.equal(outs[0][l], outs[2][l])
+        assert_close(f64(outs[0][l]), oracle_step(xs[l])["out"], f"layer {l}")
     n_cnt = 1024  # the per-unit counts follow the 1 KB status block
     assert int(ws[1024:1024 + n_cnt].count_nonzero()) == 0
