@@ -136,3 +136,44 @@ def test_decode_repeated_calls_are_bitwise_equal_and_leave_counts_zero(n_layers,
         assert_close(f64(outs[0][l]), oracle_step(xs[l])["out"], f"layer {l}")
     n_cnt = 1024  # the per-unit counts follow the 1 KB status block
     assert int(ws[1024:1024 + n_cnt].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("n_layers", [1, 2])
+def test_decode_cache_length_not_a_multiple_of_128(n_layers):
+    # Smax = 576: the last 128-row tile of pos = 575 reaches past the cache; TMA fills those rows
+    # with zeros and the softmax masks them (one layer: a 5-CTA cluster per head; two layers:
+    # the grid-wide split)
+    xs = [decode_inputs(860 + l, 575, 576) for l in range(n_layers)]
+    Ls, _ = run(xs, rope_delta=-500)
+    for l, (x, L) in enumerate(zip(xs, Ls)):
+        assert_close(f64(L.out), oracle_step(x, rope_delta=-500)["out"], f"layer {l}")
+
+
+def test_decode_and_expert_share_one_cache():
+    # The two workloads of the pages on one layer's cache: the text model decodes the token at
+    # row S (writing that row), then the expert attends to the S + 1 rows before its own tail
+    # rows, the decoded row included. Each step is checked against the oracle on the cache state
+    # the oracle itself predicts.
+    from gqa_attention_long_gb300.inputs import layer_inputs
+    from tests._gpu_util import oracle_layer, to_dev as expert_to_dev
+    S, Smax = 300, 512
+    xe = layer_inputs(870, S + 1, Smax)           # expert inputs; its cache is the shared one
+    xd = decode_inputs(871, S, Smax)
+    xd.k_cache, xd.v_cache = xe.k_cache.clone(), xe.v_cache.clone()
+    Le = expert_to_dev(xe)
+    Ld = to_dev(xd)
+    Ld.k_cache, Ld.v_cache = Le.k_cache, Le.v_cache  # the same device buffers
+    wsd = ea.alloc_decode_workspace(1)
+    ea.text_decode_attention([Ld], S, Smax, 0, wsd)
+    torch.cuda.synchronize()
+    check_status(wsd)
+    rd = oracle_step(xd)
+    assert_close(f64(Ld.out), rd["out"], "decode step")
+    # the cache as the oracle predicts it after the decode step: row S holds the stored new row
+    xe.k_cache[:, S] = torch.from_numpy(rd["k_store"]).to(torch.bfloat16)
+    xe.v_cache[:, S] = torch.from_numpy(rd["v_store"]).to(torch.bfloat16)
+    wse = ea.alloc_workspace(1, Smax)
+    ea.expert_attn_layer(Le, S + 1, Smax, 0, ea.EA_KV_BF16, wse)
+    torch.cuda.synchronize()
+    check_status(wse)
+    assert_close(f64(Le.out), oracle_layer(xe)["out"], "expert layer after the decode step")
