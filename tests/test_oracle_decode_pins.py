@@ -7,7 +7,9 @@ step must have (rows after pos unread; KV head g feeds exactly query heads 8g..8
 row is attended to). A plausible mistake (a wrong GQA map, an exclusive cur_pos, a dropped
 rope_delta) fails one of them; ``tests/test_oracle_mutations.py`` plants those mistakes.
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -155,3 +157,14 @@ def test_decode_positions_are_pos_plus_delta():
                                f64(x.k_gamma), 7, -7)
     n = f64(x.k_raw) * f64(x.k_gamma) / np.sqrt((f64(x.k_raw) ** 2).mean(-1, keepdims=True) + 1e-6)
     assert np.max(np.abs(z[1] - n)) < 1e-13
+
+
+def test_stored_decode_samples_unchanged():
+    # Written by tests/golden/make_golden.py, which calls only the oracle.
+    path = os.path.join(os.path.dirname(__file__), "golden", "decode_samples.json")
+    g = json.load(open(path))
+    for case in g["cases"]:
+        x = decode_inputs(case["seed"], case["pos"], case["Smax"])
+        out = run(x, rope_delta=case["rope_delta"])["out"]
+        idx = np.array(case["idx"])
+        assert np.allclose(out[idx[:, 0], idx[:, 1]], np.array(case["val"]), rtol=0, atol=1e-12)
