@@ -40,8 +40,11 @@
 // Before waiting for the preceding kernel, the producer asks L2 for the CTA's first tiles (a
 // prefetch only: what the preceding kernel writes still wins).
 //
-// Warp roles (160 threads): warps 0-3 compute (prologue, MMA issue by thread 0, softmax,
-// epilogue); warp 4 lane 0 issues the TMA loads of the K and V tiles into a 3-stage ring.
+// Warp roles (192 threads): warps 0-3 compute (prologue, softmax, epilogue); warp 4 lane 0 issues
+// the TMA loads of the K and V tiles into a 3-stage ring; warp 5 lane 0 issues the MMAs. S and P
+// are double-buffered, so QK(n) is issued as soon as the softmax of tile n-2 has released its
+// score buffer: it runs while the softmax of tile n-1 does, and the compute warps go from one
+// tile's softmax to the next without waiting for the tensor core.
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -49,7 +52,7 @@
 namespace ea {
 namespace dec {
 
-constexpr int kThreads = 160;
+constexpr int kThreads = 192;
 constexpr int kCompute = 128;
 constexpr int kStages = 3;
 constexpr uint32_t kAtomBytes = 16384;          // one 64-channel half of a 128-row tile
@@ -59,11 +62,15 @@ constexpr uint32_t kOpAtom = 2048;  // one 64-element half of a 16-row operand (
 // Shared memory (offsets from the 1024-byte-aligned base)
 constexpr uint32_t SM_RING = 0;
 constexpr uint32_t SM_QT = SM_RING + kStages * kStageBytes;  // 16 rows x 128 channels bf16
-constexpr uint32_t SM_PT = SM_QT + 2 * kOpAtom;              // 16 rows x 128 keys bf16
-constexpr uint32_t SM_RED = SM_PT + 2 * kOpAtom;             // [2][4 warps][8 heads] fp32
+constexpr uint32_t SM_PT = SM_QT + 2 * kOpAtom;              // 2 x (16 rows x 128 keys bf16)
+constexpr uint32_t kPtBytes = 2 * kOpAtom;
+constexpr uint32_t SM_RED = SM_PT + 2 * kPtBytes;            // [2][4 warps][8 heads] fp32
 constexpr uint32_t SM_BAR = SM_RED + 2 * 4 * kRepText * 4;
-constexpr int B_FULL = 0, B_EMPTY = kStages, B_SDONE = 2 * kStages, B_ODONE = B_SDONE + 1,
-              B_TAIL = B_ODONE + 1, B_DRAIN = B_TAIL + 1, kNumBars = B_DRAIN + 1;
+// SDONE, PFULL, ODONE: one barrier per parity of the tile count (tile n uses S and P buffer n % 2);
+// QFULL and OFREE complete once per segment
+constexpr int B_FULL = 0, B_EMPTY = kStages, B_SDONE = 2 * kStages, B_PFULL = B_SDONE + 2,
+              B_ODONE = B_PFULL + 2, B_QFULL = B_ODONE + 2, B_OFREE = B_QFULL + 1,
+              B_TAIL = B_OFREE + 1, B_DRAIN = B_TAIL + 1, kNumBars = B_DRAIN + 1;
 constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t SM_MERGE = SM_ABORT + 4;
@@ -75,8 +82,8 @@ constexpr uint32_t SM_CPART = SM_PARTML + kMaxParts * kRepText * 8;
 constexpr uint32_t SM_CPART_ML = SM_CPART + kRepText * kD * 4;
 constexpr uint32_t kSmemBytes = SM_CPART_ML + kRepText * 8 + 1024;  // + base alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103 CTA");
-constexpr uint32_t kTmemCols = 32;  // S^T in columns [0, 16), O^T in [16, 32)
-constexpr uint32_t TM_S = 0, TM_O = 16;
+constexpr uint32_t kTmemCols = 64;  // S^T of even / odd tiles in [0, 16) / [16, 32), O^T in [32, 48)
+constexpr uint32_t TM_S = 0, TM_O = 32;
 
 struct Seg {
   int u, j0, j1;  // unit and its key-tile range [j0, j1)
@@ -197,6 +204,108 @@ __device__ __forceinline__ void segment_prologue(const DecodeParams<CAP>& p, uin
   }
 }
 
+// ----------------------------------------------------------------------------- MMA issuer
+// Per segment, step i issues QK(i) and PV(i-1), in whichever order their inputs arrive. QK(n) needs
+// its tile in the ring and score buffer n % 2 released by the softmax of tile n-2 (its PFULL). PV(n)
+// needs P(n) (PFULL of tile n); the segment's first PV, which starts a fresh accumulator, also
+// needs the previous segment's epilogue to have read it (OFREE completes once per segment). A PV
+// whose P is ready is not held behind a tile still in flight, so its ring stage is released as
+// early as the softmax allows.
+template <int CAP>
+__device__ __noinline__ void mma_issuer(const DecodeParams<CAP>& p, uint32_t sbase, uint32_t tmem,
+                                        long long start, long long end, volatile uint32_t* abort_flag) {
+  const uint32_t bar0 = sbase + SM_BAR;
+  // S^T: A = K tile (K-major), B = QT (K-major); O^T: A = V tile (MN-major), B = PT (K-major)
+  constexpr uint32_t kIdescS = umma_idesc_f16(128, 16, true, false, false);
+  constexpr uint32_t kIdescO = umma_idesc_f16(128, 16, true, true, false);
+  const uint32_t qt = sbase + SM_QT, pt = sbase + SM_PT;
+  auto bar = [&](int b) { return bar0 + 8 * b; };
+  uint32_t n = 0;  // tiles of this CTA before the current segment
+  int sg = 0;
+  bool ok = true;
+  long long t = start;
+  Seg s;
+  while (ok && next_seg(t, end, p.T, s)) {
+    // this segment's q rows are in QT (the previous segment's QKs were all observed complete by
+    // the compute warps before they rewrote it)
+    ok = bounded_wait(bar(B_QFULL), sg & 1, abort_flag, p.status, kErrDecodeWait);
+    if (!ok) break;
+    const int nt = s.j1 - s.j0;
+    auto qk_ready = [&](int i) -> bool {
+      const uint32_t nn = n + i;
+      if (!mbar_test_wait(bar(B_FULL + nn % kStages), (nn / kStages) & 1)) return false;
+      return nn < 2 || mbar_test_wait(bar(B_PFULL + (nn & 1)), ((nn - 2) >> 1) & 1);
+    };
+    auto issue_qk = [&](int i) {
+      const uint32_t nn = n + i;
+      const uint32_t ka = sbase + SM_RING + (nn % kStages) * kStageBytes;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // 16 channels per step; 4 steps per 64-channel half
+        umma_f16_ss(tmem + TM_S + (nn & 1) * 16,
+                    sw128_desc(ka + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
+                    sw128_desc(qt + (kk >> 2) * kOpAtom + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0);
+      umma_commit(bar(B_SDONE + (nn & 1)));
+    };
+    auto pv_ready = [&](int ii) -> bool {
+      const uint32_t nn = n + ii;
+      if (ii == 0 && sg > 0 && !mbar_test_wait(bar(B_OFREE), (sg - 1) & 1)) return false;
+      return mbar_test_wait(bar(B_PFULL + (nn & 1)), (nn >> 1) & 1);
+    };
+    auto issue_pv = [&](int ii) {
+      const uint32_t nn = n + ii, slot = nn % kStages;
+      const uint32_t va = sbase + SM_RING + slot * kStageBytes + kTileBytes;
+      const uint32_t ptb = pt + (nn & 1) * kPtBytes;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // 16 keys per step
+        umma_f16_ss(tmem + TM_O, sw128_desc(va + kk * 16 * 128, kAtomBytes, 1024),
+                    sw128_desc(ptb + (kk >> 2) * kOpAtom + (kk & 3) * 32, 16, 1024), kIdescO,
+                    (ii > 0 || kk > 0));
+      umma_commit(bar(B_EMPTY + slot));  // K and V of this stage are consumed
+      umma_commit(bar(B_ODONE + (nn & 1)));
+    };
+    for (int i = 0; i <= nt && ok; ++i) {
+      bool qk_todo = i < nt, pv_todo = i > 0;
+      uint64_t t0 = 0;
+      for (uint32_t it = 0; qk_todo || pv_todo; ++it) {
+        bool moved = false;
+        if (qk_todo && qk_ready(i)) {
+          issue_qk(i);
+          qk_todo = false;
+          moved = true;
+        }
+        if (pv_todo && pv_ready(i - 1)) {
+          issue_pv(i - 1);
+          pv_todo = false;
+          moved = true;
+        }
+        if (moved) continue;
+        // bounded like every other wait: the CTA's abort flag, a time limit and a poll limit
+        if ((it & 63u) == 0) {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          const uint64_t now = globaltimer_ns();
+          if (t0 == 0) t0 = now;
+          if (now - t0 > kWaitLimitNs || it >= 0x7fffffc0u) {
+            *abort_flag = 1u;
+            atomicOr(p.status, kErrDecodeWait);
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    n += nt;
+    ++sg;
+  }
+  // Every MMA issued must be complete before TMEM is released.
+  umma_commit(bar(B_DRAIN));
+  if (!drain_wait(bar(B_DRAIN), 0)) atomicOr(p.status, kErrDrain);
+}
+
 template <int CAP>
 __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase, uint8_t* smem,
                                      uint32_t tmem, long long start, long long end,
@@ -207,10 +316,7 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
   const uint32_t bar0 = sbase + SM_BAR;
   float* red = reinterpret_cast<float*>(smem + SM_RED);  // [2][4][8]
   volatile uint32_t* merge_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_MERGE);
-  // S^T: A = K tile (K-major), B = QT (K-major); O^T: A = V tile (MN-major), B = PT (K-major)
-  constexpr uint32_t kIdescS = umma_idesc_f16(128, 16, true, false, false);
-  constexpr uint32_t kIdescO = umma_idesc_f16(128, 16, true, true, false);
-  const uint32_t qt = sbase + SM_QT, pt = sbase + SM_PT;
+  const uint32_t pt = sbase + SM_PT;
   auto wait = [&](int b, uint32_t parity) -> bool {
     return bounded_wait(bar0 + 8 * b, parity, abort_flag, p.status, kErrDecodeWait);
   };
@@ -226,7 +332,10 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
     segment_prologue(p, sbase, l, g, last, tid);
     fence_proxy_async_smem();  // QT is read by the tensor core (async proxy)
     bar_sync(1, kCompute);
-    if (last && tid == 0) mbar_arrive(bar0 + 8 * B_TAIL);
+    if (tid == 0) {
+      if (last) mbar_arrive(bar0 + 8 * B_TAIL);
+      mbar_arrive(bar0 + 8 * B_QFULL);
+    }
     float m[kRepText], lsum[kRepText];
 #pragma unroll
     for (int h = 0; h < kRepText; ++h) {
@@ -236,26 +345,21 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
     for (int j = s.j0; j < s.j1; ++j, ++n) {
       const uint32_t slot = n % kStages;
       const uint32_t kaddr = sbase + SM_RING + slot * kStageBytes, vaddr = kaddr + kTileBytes;
+      // the tile has landed (its V rows of keys after pos are zeroed below), S(n) is complete, and
+      // P buffer n % 2 is free: PV(n-2), its last reader, has completed (this warpgroup waits for
+      // every PV of a parity in turn, so the phase is unambiguous)
       bool okt = wait(B_FULL + slot, (n / kStages) & 1);
-      if (tid == 0 && okt) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 channels per step; 4 steps per 64-channel half
-          umma_f16_ss(tmem + TM_S,
-                      sw128_desc(kaddr + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024),
-                      sw128_desc(qt + (kk >> 2) * kOpAtom + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0);
-        umma_commit(bar0 + 8 * B_SDONE);
-      }
-      // S(n) complete; also PV(n-1), issued before QK(n), so P and the accumulator are free
-      okt = okt && wait(B_SDONE, n & 1);
+      okt = okt && wait(B_SDONE + (n & 1), (n >> 1) & 1);
+      if (n >= 2) okt = okt && wait(B_ODONE + (n & 1), ((n - 2) >> 1) & 1);
       okt = __all_sync(0xffffffffu, okt);
+      const uint32_t ptb = pt + (n & 1) * kPtBytes;
       const int key = j * kKeyTile + tid;
       const bool live = key <= p.pos;
       float x[kRepText];
       if (okt) {
         tc_fence_after();
         uint32_t sv[8];
-        tmem_ld8(tmem + lane_addr + TM_S, sv);
+        tmem_ld8(tmem + lane_addr + TM_S + (n & 1) * 16, sv);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < kRepText; ++h) x[h] = live ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
@@ -291,7 +395,7 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       // chunk c ^ (h % 8) of the key's 64-key half
 #pragma unroll
       for (int h = 0; h < kRepText; ++h) {
-        const uint32_t a = pt + (tid >> 6) * kOpAtom + h * 128 +
+        const uint32_t a = ptb + (tid >> 6) * kOpAtom + h * 128 +
                            ((((tid & 63) >> 3) ^ (h & 7)) << 4) + (tid & 7) * 2;
         st_shared_u16(a, __bfloat16_as_ushort(__float2bfloat16_rn(pr[h])));
       }
@@ -305,33 +409,34 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       for (int h = 0; h < kRepText; ++h)
         lsum[h] = lsum[h] * alpha[h] + ((red[4 * kRepText + h] + red[5 * kRepText + h]) +
                                         (red[6 * kRepText + h] + red[7 * kRepText + h]));
-      if (j > s.j0 && resc) {  // bring the accumulator (tiles before this one) to the new max
-        uint32_t ov[8];
-        tmem_ld8(tmem + lane_addr + TM_O, ov);
-        tmem_wait_ld();
+      bool okr = true;
+      if (j > s.j0 && resc) {
+        // bring the accumulator (the segment's tiles before this one) to the new max, once PV(n-1)
+        // has completed (PV(n-3) was waited for at tile n-1)
+        okr = __all_sync(0xffffffffu, wait(B_ODONE + ((n - 1) & 1), ((n - 1) >> 1) & 1));
+        if (okr) {
+          tc_fence_after();
+          uint32_t ov[8];
+          tmem_ld8(tmem + lane_addr + TM_O, ov);
+          tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < kRepText; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-        tmem_st8(tmem + lane_addr + TM_O, ov);
-        tmem_wait_st();
+          for (int h = 0; h < kRepText; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+          tmem_st8(tmem + lane_addr + TM_O, ov);
+          tmem_wait_st();
+        }
       }
       fence_proxy_async_smem();  // P^T and zeroed V rows are read by the tensor core
       tc_fence_before();
-      bar_sync(1, kCompute);
-      if (tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 keys per step
-          umma_f16_ss(tmem + TM_O, sw128_desc(vaddr + kk * 16 * 128, kAtomBytes, 1024),
-                      sw128_desc(pt + (kk >> 2) * kOpAtom + (kk & 3) * 32, 16, 1024), kIdescO,
-                      (j > s.j0 || kk > 0));
-        umma_commit(bar0 + 8 * (B_EMPTY + slot));  // K and V of this stage are consumed
-        umma_commit(bar0 + 8 * B_ODONE);
+      if (!bar_sync_and(1, kCompute, okr)) {
+        ok = false;
+        break;
       }
+      if (tid == 0) mbar_arrive(bar0 + 8 * (B_PFULL + (n & 1)));  // P(n) out, S(n) read
     }
     if (!ok) break;
-    // ---- segment end: the last PV (ODONE completes once per tile; PV(n-2) is known complete
-    // since S(n-1) was, so the phase of PV(n-1) is unambiguous)
-    bool oke = wait(B_ODONE, (n - 1) & 1);
+    // ---- segment end: the last PV, PV(n-1), and with it every earlier MMA (PV(n-3), the
+    // previous phase of its barrier, was waited for at tile n-1; PV(n+1) is not issued)
+    bool oke = wait(B_ODONE + ((n - 1) & 1), ((n - 1) >> 1) & 1);
     oke = __all_sync(0xffffffffu, oke);
     uint32_t ov[8];
     if (oke) {
@@ -344,6 +449,7 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       ok = false;
       break;
     }
+    if (tid == 0) mbar_arrive(bar0 + 8 * B_OFREE);  // the accumulator is read
     const bool full = s.j0 == 0 && s.j1 == p.T;
     if (p.cluster) {
       // cluster mode: the partial stays in this CTA's shared memory for the cluster's merge
@@ -433,11 +539,6 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
     }
     first_seg = false;
   }
-  // Every MMA issued must be complete before TMEM is released.
-  if (tid == 0) {
-    umma_commit(bar0 + 8 * B_DRAIN);
-    if (!drain_wait(bar0 + 8 * B_DRAIN, 0)) atomicOr(p.status, kErrDrain);
-  }
 }
 
 }  // namespace dec
@@ -466,16 +567,21 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
       mbar_init(bar0 + 8 * (B_FULL + b), 1);
       mbar_init(bar0 + 8 * (B_EMPTY + b), 1);
     }
-    mbar_init(bar0 + 8 * B_SDONE, 1);
-    mbar_init(bar0 + 8 * B_ODONE, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar0 + 8 * (B_SDONE + b), 1);
+      mbar_init(bar0 + 8 * (B_PFULL + b), 1);
+      mbar_init(bar0 + 8 * (B_ODONE + b), 1);
+    }
+    mbar_init(bar0 + 8 * B_QFULL, 1);
+    mbar_init(bar0 + 8 * B_OFREE, 1);
     mbar_init(bar0 + 8 * B_TAIL, 1);
     mbar_init(bar0 + 8 * B_DRAIN, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  // rows 8-15 of the Q and P operands are the zero padding of N = 16
-  for (int i = threadIdx.x; i < 2 * 2 * 64; i += kThreads) {
-    const uint32_t op = (i >> 7) ? SM_PT : SM_QT;
+  // rows 8-15 of the Q operand and of both P operands are the zero padding of N = 16
+  for (int i = threadIdx.x; i < 3 * 2 * 64; i += kThreads) {
+    const uint32_t op = SM_QT + (i >> 7) * 2 * kOpAtom;  // QT, PT[0], PT[1] are contiguous
     const uint32_t off = op + ((i >> 6) & 1) * kOpAtom + 1024 + (i & 63) * 16;
     st_shared_v4(sbase + off, 0u, 0u, 0u, 0u);
   }
@@ -504,9 +610,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   pdl_wait_primary();
   if (warp < 4) {
     compute(p, sbase, smem, tmem, start, end, abort_flag);
-  } else if ((threadIdx.x & 31) == 0) {
+  } else if (warp == 4 && (threadIdx.x & 31) == 0) {
     prefetch_tensormap(&p.kmap[0]);
     producer(p, sbase, start, end, abort_flag);
+  } else if (warp == 5 && (threadIdx.x & 31) == 0) {
+    mma_issuer(p, sbase, tmem, start, end, abort_flag);
   }
   pdl_launch_dependents();
   tc_fence_before();
