@@ -75,6 +75,7 @@ constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t SM_MERGE = SM_ABORT + 4;
 constexpr int kMaxParts = 160;  // parts of one unit (at most one per CTA; the grid is <= 160)
+constexpr int kMergeBatch = 10;  // parts per round of loads in the last arriver's merge
 constexpr uint32_t SM_PARTML = (SM_MERGE + 4 + 15) & ~15u;  // [part][head] (max, sum) of a merge
 // cluster mode: this CTA's partial, read by the cluster's other CTAs: O [8 heads][128] fp32, then
 // (max, sum) per head
@@ -486,53 +487,67 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       bar_sync(1, kCompute);
       if (*merge_flag) {
         __threadfence();
-        // every part's (max, sum) into shared memory with one round of independent loads; the
-        // first part's partial may sit in its CTA's second slot, every other part's in its first
+        // One pass over the parts with a running max, kMergeBatch parts per round of independent
+        // 16-byte loads. Thread tid owns heads 2q and 2q + 1 (q = tid / 32) at channels
+        // 4 (tid % 32) .. + 3: per part two float4 of the partial output and one float4 holding
+        // both heads' (max, sum). The first part's partial may sit in its CTA's second slot,
+        // every other part's in its first. Every part has a live key (each tile of a unit holds
+        // a row <= pos), so its max is finite.
         const int np = c1 - c0 + 1;
         const int slot0 = cta_tile_start(c0, p.W, gridDim.x) >= u0 ? 0 : 1;
-        float2* sml = reinterpret_cast<float2*>(smem + SM_PARTML);  // [part][head]
-        for (int i = tid; i < np * kRepText; i += kCompute) {
-          const int c = c0 + i / kRepText;
-          const size_t cs = static_cast<size_t>(c) * 2 + (c == c0 ? slot0 : 0);
-          sml[i] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + cs * kRepText + i % kRepText);
-        }
-        bar_sync(1, kCompute);
-        float M[kRepText], L[kRepText], acc[kRepText];
+        const int hq = 2 * (tid >> 5), c4 = 4 * (tid & 31);
+        float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f};
+        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        for (int cb = 0; cb < np; cb += kMergeBatch) {
+          float4 v[kMergeBatch][2], ml[kMergeBatch];
 #pragma unroll
-        for (int h = 0; h < kRepText; ++h) {
-          M[h] = -INFINITY;
-          L[h] = 0.f;
-          acc[h] = 0.f;
-        }
-        for (int c = 0; c < np; ++c)
-#pragma unroll
-          for (int h = 0; h < kRepText; ++h) M[h] = fmaxf(M[h], sml[c * kRepText + h].x);
-        // the parts' outputs, eight parts per batch of independent loads (past the last part the
-        // index is clamped and the weight is 0)
-        for (int cb = 0; cb < np; cb += 8) {
-          float v[8][kRepText];
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            const int c = cb + b < np ? cb + b : np - 1;
+          for (int b = 0; b < kMergeBatch; ++b) {
+            const int c = cb + b < np ? cb + b : np - 1;  // past the last part: a repeat, unused
             const size_t cs = static_cast<size_t>(c0 + c) * 2 + (c == 0 ? slot0 : 0);
 #pragma unroll
-            for (int h = 0; h < kRepText; ++h) v[b][h] = __ldcg(p.part_o + (cs * kRepText + h) * kD + tid);
+            for (int e = 0; e < 2; ++e)
+              v[b][e] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (cs * kRepText + hq + e) * kD + c4));
+            ml[b] = __ldcg(reinterpret_cast<const float4*>(p.part_ml + (cs * kRepText + hq) * 2));
           }
+          const int nb = np - cb < kMergeBatch ? np - cb : kMergeBatch;
+          float Mn[2] = {M[0], M[1]};
 #pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            if (cb + b >= np) break;
-#pragma unroll
-            for (int h = 0; h < kRepText; ++h) {
-              const float2 ml = sml[(cb + b) * kRepText + h];
-              const float wgt = ex2_approx(ml.x - M[h]);
-              L[h] = fmaf(ml.y, wgt, L[h]);
-              acc[h] = fmaf(v[b][h], wgt, acc[h]);
+          for (int b = 0; b < kMergeBatch; ++b)
+            if (b < nb) {
+              Mn[0] = fmaxf(Mn[0], ml[b].x);
+              Mn[1] = fmaxf(Mn[1], ml[b].z);
             }
-          }
-        }
-        __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g) * kD + tid;
 #pragma unroll
-        for (int h = 0; h < kRepText; ++h) o[h * kD] = __float2bfloat16_rn(acc[h] / L[h]);
+          for (int e = 0; e < 2; ++e) {  // earlier parts to the new running max (0 on the first round)
+            const float sc = ex2_approx(M[e] - Mn[e]);
+            L[e] *= sc;
+            acc[e].x *= sc;
+            acc[e].y *= sc;
+            acc[e].z *= sc;
+            acc[e].w *= sc;
+            M[e] = Mn[e];
+          }
+#pragma unroll
+          for (int b = 0; b < kMergeBatch; ++b)
+            if (b < nb) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float wgt = ex2_approx((e ? ml[b].z : ml[b].x) - M[e]);
+                L[e] = fmaf(e ? ml[b].w : ml[b].y, wgt, L[e]);
+                acc[e].x = fmaf(v[b][e].x, wgt, acc[e].x);
+                acc[e].y = fmaf(v[b][e].y, wgt, acc[e].y);
+                acc[e].z = fmaf(v[b][e].z, wgt, acc[e].z);
+                acc[e].w = fmaf(v[b][e].w, wgt, acc[e].w);
+              }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float inv = 1.0f / L[e];
+          __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g + hq + e) * kD + c4;
+          *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[e].x * inv, acc[e].y * inv),
+                                                    pack_bf16x2(acc[e].z * inv, acc[e].w * inv));
+        }
         if (tid == 0) p.unit_cnt[s.u] = 0u;  // every part has arrived: ready for the next call
       }
       bar_sync(1, kCompute);  // the merge flag is read before the next segment overwrites it
