@@ -76,6 +76,7 @@ constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t SM_MERGE = SM_ABORT + 4;
 constexpr int kMaxParts = 160;  // parts of one unit (at most one per CTA; the grid is <= 160)
 constexpr int kMergeBatch = 10;  // parts per round of loads in the last arriver's merge
+constexpr uint32_t kMaxCluster = 8;  // cluster mode: CTAs per unit (the host launches 2..8)
 constexpr uint32_t SM_PARTML = (SM_MERGE + 4 + 15) & ~15u;  // [part][head] (max, sum) of a merge
 // cluster mode: this CTA's partial, read by the cluster's other CTAs: O [8 heads][128] fp32, then
 // (max, sum) per head
@@ -637,10 +638,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   tc_fence_after();
   if (p.cluster) {
     // every CTA of the cluster has its partial (or an empty one) in shared memory. The cluster's
-    // CS (2..8) CTAs share the unit's 1024 outputs (head h, channel c at index 128 h + c):
-    // rank r combines indices r, r + CS, ..., each from the CS parts, with every remote load
-    // of a thread issued before the first is used. Every thread of every CTA reaches both
-    // cluster barriers exactly once.
+    // CS (2..8) CTAs share the unit's 256 output chunks (head h, channels 4 c .. 4 c + 3, chunk
+    // 32 h + c): rank r takes chunks [r Q, r Q + Q), Q = ceil(256 / CS), one per thread, each
+    // read as one 16-byte load from every part (consecutive threads, consecutive chunks). Every
+    // thread of every CTA reaches both cluster barriers exactly once.
     cluster_sync();
     const uint32_t cs = static_cast<uint32_t>(p.cluster), r = cluster_ctarank();
     float2* lml = reinterpret_cast<float2*>(smem + SM_PARTML);  // the parts' (max, sum) [part][head]
@@ -648,34 +649,32 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
       lml[threadIdx.x] = ld_shared_cluster_v2(
           mapa_shared(sbase + SM_CPART_ML + (threadIdx.x % kRepText) * 8, threadIdx.x / kRepText));
     __syncthreads();
-    if (threadIdx.x < kCompute) {
+    const uint32_t q = (256u + cs - 1) / cs, chunk = r * q + threadIdx.x;
+    if (threadIdx.x < q && chunk < 256u) {
       const int u = blockIdx.x / p.cluster, l = u / kHkv, g = u % kHkv;
-      float ov[4][16];  // output jj of this thread (index r + CS (tid + 128 jj)), part k
+      const uint32_t h = chunk >> 5;
+      float4 ov[kMaxCluster];  // the chunk in part k
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint32_t idx = r + cs * (threadIdx.x + 128u * jj);
+      for (uint32_t k = 0; k < kMaxCluster; ++k)
+        if (k < cs) ov[k] = ld_shared_cluster_v4(mapa_shared(sbase + SM_CPART + chunk * 16, k));
+      float M = -INFINITY, L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (uint32_t k = 0; k < 16; ++k)
-          if (idx < kRepText * kD && k < cs) ov[jj][k] = ld_shared_cluster_f32(mapa_shared(sbase + SM_CPART + idx * 4, k));
-      }
+      for (uint32_t k = 0; k < kMaxCluster; ++k)
+        if (k < cs) M = fmaxf(M, lml[k * kRepText + h].x);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint32_t idx = r + cs * (threadIdx.x + 128u * jj);
-        if (idx >= kRepText * kD) continue;
-        const uint32_t h = idx >> 7;
-        float M = -INFINITY, L = 0.f, acc = 0.f;
-#pragma unroll
-        for (uint32_t k = 0; k < 16; ++k)
-          if (k < cs) M = fmaxf(M, lml[k * kRepText + h].x);
-#pragma unroll
-        for (uint32_t k = 0; k < 16; ++k)
-          if (k < cs && lml[k * kRepText + h].x != -INFINITY) {  // parts without tiles add nothing
-            const float wgt = ex2_approx(lml[k * kRepText + h].x - M);
-            L = fmaf(lml[k * kRepText + h].y, wgt, L);
-            acc = fmaf(ov[jj][k], wgt, acc);
-          }
-        p.out[l][static_cast<size_t>(kRepText * g) * kD + idx] = __float2bfloat16_rn(acc / L);
-      }
+      for (uint32_t k = 0; k < kMaxCluster; ++k)
+        if (k < cs && lml[k * kRepText + h].x != -INFINITY) {  // parts without tiles add nothing
+          const float wgt = ex2_approx(lml[k * kRepText + h].x - M);
+          L = fmaf(lml[k * kRepText + h].y, wgt, L);
+          acc.x = fmaf(ov[k].x, wgt, acc.x);
+          acc.y = fmaf(ov[k].y, wgt, acc.y);
+          acc.z = fmaf(ov[k].z, wgt, acc.z);
+          acc.w = fmaf(ov[k].w, wgt, acc.w);
+        }
+      const float inv = 1.0f / L;
+      *reinterpret_cast<uint2*>(p.out[l] + static_cast<size_t>(kRepText * g) * kD + 4 * chunk) =
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }
