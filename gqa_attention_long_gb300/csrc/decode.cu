@@ -13,7 +13,7 @@
 // Work decomposition: a unit is one (layer, kv head): its 8 query heads against keys [0, pos],
 // cut into tiles of 128 keys. The tiles of all units, unit-major, are cut into one contiguous
 // range per CTA (one CTA per SM); a CTA walks its range as segments (the part of one unit in
-// it). Per tile, on the tensor cores (one issuing thread):
+// it). Per tile, on the tensor cores (issued by the MMA warp):
 //   S^T  = K Q^T    M = 128 keys (TMEM lanes), N = 16 (the 8 query heads and 8 zero rows),
 //                   K = 128 channels; A = the K tile (TMA, 128-byte swizzle, K-major), B = the
 //                   unit's roped q rows in shared memory;
