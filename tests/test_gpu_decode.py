@@ -177,3 +177,48 @@ def test_decode_and_expert_share_one_cache():
     torch.cuda.synchronize()
     check_status(wse)
     assert_close(f64(Le.out), oracle_layer(xe)["out"], "expert layer after the decode step")
+
+
+def _parts_per_unit(n_layers: int, pos: int, n_sm: int):
+    """Parts of each unit under the grid-wide split (the host's plan: T tiles of 128 keys per
+    unit, units laid out layer-major, tile c W / G .. of CTA c), or None in cluster mode."""
+    T = (pos + 1 + 127) // 128
+    if n_layers == 1 and 2 <= T <= 8:
+        return None
+    W = n_layers * 8 * T
+    G = min(n_sm, 160, W)
+
+    def cta_of(x):
+        c = x * G // W
+        while c + 1 < G and (c + 1) * W // G <= x:
+            c += 1
+        while c > 0 and c * W // G > x:
+            c -= 1
+        return c
+
+    return [cta_of(u * T + T - 1) - cta_of(u * T) + 1 for u in range(n_layers * 8)]
+
+
+@pytest.mark.parametrize("want", [9, 10, 11, 19])
+def test_decode_merge_batch_boundaries(want):
+    # The last arriver of a split unit reads ten parts per round of loads: a unit of exactly
+    # 9, 10, 11 or 19 parts (19 = the most on 152 SMs: 8 units over 152 CTAs) ends its first
+    # round early, on its last part, with one part left over, or two rounds in.
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    found = None
+    for n_layers in (1, 2, 3, 4):
+        for pos in range(1024, 8192, 37):
+            parts = _parts_per_unit(n_layers, pos, n_sm)
+            if parts is not None and want in parts:
+                found = (n_layers, pos)
+                break
+        if found:
+            break
+    if found is None:
+        pytest.skip(f"no layer count <= 4 and pos < 8192 gives a {want}-part unit on {n_sm} SMs")
+    n_layers, pos = found
+    xs = [decode_inputs(900 + 10 * want + l, pos, 8192) for l in range(n_layers)]
+    Ls, _ = run(xs, rope_delta=5)
+    for l, (x, L) in enumerate(zip(xs, Ls)):
+        assert_close(f64(L.out), oracle_step(x, rope_delta=5)["out"],
+                     f"{want}-part unit: n={n_layers}, pos={pos}, layer {l}")
