@@ -91,6 +91,13 @@ struct Seg {
   int u, j0, j1;  // unit and its key-tile range [j0, j1)
 };
 
+// atomicAdd at GPU scope with acquire-release semantics; returns the old value
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+
 // Next segment of a CTA's tile range [t, end): unit u = t / T (tile indices stay below 2^31).
 __device__ __forceinline__ bool next_seg(long long& t, long long end, int T, Seg& s) {
   if (t >= end) return false;
@@ -171,36 +178,39 @@ __device__ __forceinline__ void segment_prologue(const DecodeParams<CAP>& p, uin
   if (w > 2 || (w == 2 && !last)) return;
   const int i = tid & 7;
   const int dl = 8 * i, dh = 64 + 8 * i;
+  // the row's and the gain's global loads go out first; the rotation angles (kernel parameters
+  // only) are computed while they are in flight
+  const __nv_bfloat16* row = w < 2 ? p.q_raw[l] + static_cast<size_t>(kRepText * g + (tid >> 3)) * kD
+                                   : p.k_raw[l] + static_cast<size_t>(g) * kD;
+  const __nv_bfloat16* gam = w < 2 ? p.q_gamma[l] : p.k_gamma[l];
+  const uint4 rl = *reinterpret_cast<const uint4*>(row + dl), rh = *reinterpret_cast<const uint4*>(row + dh);
+  const uint4 ml = *reinterpret_cast<const uint4*>(gam + dl), mh = *reinterpret_cast<const uint4*>(gam + dh);
   float cs[8], sn[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_pos, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[e], sn[e]);
   float xl[8], xh[8], gl[8], gh[8], yl[8], yh[8];
+  unpack_bf16x8(rl, xl);
+  unpack_bf16x8(rh, xh);
+  unpack_bf16x8(ml, gl);
+  unpack_bf16x8(mh, gh);
   if (w < 2) {
     const int h = tid >> 3;  // 0..7
-    const __nv_bfloat16* row = p.q_raw[l] + static_cast<size_t>(kRepText * g + h) * kD;
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dl), xl);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dh), xh);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gl);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dh), gh);
     norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
     const uint4 ql = pack8(yl, false), qh = pack8(yh, false);
     const uint32_t qt = sbase + SM_QT;
     st_shared_v4(qt + swz_off(h, i, kOpAtom), ql.x, ql.y, ql.z, ql.w);
     st_shared_v4(qt + swz_off(h, i + 8, kOpAtom), qh.x, qh.y, qh.z, qh.w);
   } else {
-    const __nv_bfloat16* krow = p.k_raw[l] + static_cast<size_t>(g) * kD;
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl), xl);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh), xh);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gl);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gh);
+    // the v row's loads go out with the k row's (before any cache store)
+    const __nv_bfloat16* vrow = p.v_raw[l] + static_cast<size_t>(g) * kD;
+    const uint4 vl = *reinterpret_cast<const uint4*>(vrow + dl), vh = *reinterpret_cast<const uint4*>(vrow + dh);
     norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
     if (tid < 64 + 8) {
       const size_t ro = (static_cast<size_t>(g) * p.Smax + p.pos) * kD;
       *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = pack8(yl, false);
       *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = pack8(yh, false);
-      const __nv_bfloat16* vrow = p.v_raw[l] + static_cast<size_t>(g) * kD;
-      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = *reinterpret_cast<const uint4*>(vrow + dl);
-      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = *reinterpret_cast<const uint4*>(vrow + dh);
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = vl;
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = vh;
       fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
     }
   }
@@ -484,10 +494,14 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       bar_sync(1, kCompute);
       const long long u0 = static_cast<long long>(s.u) * p.T;
       const int c0 = cta_of_tile(u0, p.W, gridDim.x), c1 = cta_of_tile(u0 + p.T - 1, p.W, gridDim.x);
-      if (tid == 0) *merge_flag = atomicAdd(p.unit_cnt + s.u, 1u) == static_cast<uint32_t>(c1 - c0) ? 1u : 0u;
+      // the count is an acquire-release atomic: the release publishes this part (every thread's
+      // stores, fenced above and ordered before it by the barrier); for the last part the
+      // acquire orders the other parts' partials before its reads (the barrier below extends it
+      // to every thread)
+      if (tid == 0)
+        *merge_flag = atom_add_acq_rel_gpu(p.unit_cnt + s.u, 1u) == static_cast<uint32_t>(c1 - c0) ? 1u : 0u;
       bar_sync(1, kCompute);
       if (*merge_flag) {
-        __threadfence();
         // One pass over the parts with a running max, kMergeBatch parts per round of independent
         // 16-byte loads. Thread tid owns heads 2q and 2q + 1 (q = tid / 32) at channels
         // 4 (tid % 32) .. + 3: per part two float4 of the partial output and one float4 holding
