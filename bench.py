@@ -18,6 +18,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import torch
@@ -96,7 +97,8 @@ def load_peaks() -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / throttle sampling while the timed region runs. The raw samples go to a
+    CSV file in $EA_CLOCKS_DIR (default: the system temporary directory)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -104,7 +106,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        self.path = os.path.join(os.environ.get("EA_CLOCKS_DIR") or tempfile.gettempdir(),
+                                 f"clocks_gpu{index}.csv")
 
     def __enter__(self):
         try:
@@ -448,7 +451,7 @@ def main():
                  "us_per_layer": msc * 1e3 / n, "ms_per_chain": msc,
                  "launches_per_layer": launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count)}
 
-    # ---- the whole decoder layer with synthetic weights (survey NEXT row 2): 8 distinct layers
+    # ---- the whole decoder layer with synthetic weights: 8 distinct layers
     # chained (layer i+1's input is layer i's output), one expert_decoder_layer call each,
     # replayed as a CUDA graph; the weights (75.5 MB per layer) and caches of the 8 layers exceed
     # L2, so every replay streams them from HBM
@@ -497,7 +500,7 @@ def main():
                   "launches_per_layer": 8 if launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1 else 7}
         del Wl, wsl
 
-    # ---- the text model's single-token decode attention (survey NEXT row 3) over the same caches:
+    # ---- the text model's single-token decode attention over the same caches:
     # the decode token at row pos = S of every layer's cache (the expert never reads that row).
     # All 64 layers in one call (throughput), and one layer per call rotating over 8 layers
     # (the latency of one layer of a decode step)
