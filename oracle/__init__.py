@@ -12,6 +12,9 @@ expert_attention : the per-layer attention of the flow-matching action expert
 fp8_e4m3         : the OCP E4M3 ("e4m3fn") code table, a round-to-nearest-even
                    saturating encoder, and the per-(kv head, 128-row block)
                    cache quantiser used by the FP8 cache variant.
+mxfp4            : the OCP MX FP4 format: E2M1 codes, a round-to-nearest-even
+                   saturating encoder, and one power-of-two scale per 32 channels
+                   of a cache row (the 4-bit cache variant).
 decoder_layer    : the whole decoder layer around that attention (RMSNorm, fused
                    qkv projection, head split, attention, head concat, wo, residual,
                    RMSNorm, SwiGLU MLP, residual), for synthetic weights.
@@ -19,14 +22,19 @@ decode_attention : the text model's single-token decode attention over the same 
                    (64 query heads / 8 KV heads, norm and RoPE at pos + rope_delta, the
                    new row written at pos, attention over rows 0..pos).
 
-Every function is pinned by ``tests/test_oracle_pins.py``,
-``tests/test_oracle_layer_pins.py`` and ``tests/test_oracle_decode_pins.py`` against closed
+Every function is pinned by ``tests/test_oracle_pins.py``, ``tests/test_oracle_layer_pins.py``,
+``tests/test_oracle_decode_pins.py`` and ``tests/test_oracle_mxfp4_pins.py`` against closed
 forms, invariants, brute force on tiny inputs and independent library routines.
 """
 from .expert_attention import (  # noqa: F401
     D, EPS, HQ, HKV, MASK_MIN, REP, T, THETA,
     attention_concat, attention_tail_masked, bf16_round, expert_attention_layer,
-    expert_attention_layer_fp8, inv_freq, prologue, rms_norm, rope_angles, rope_rotate_half,
+    expert_attention_layer_fp8, expert_attention_layer_mxfp4, inv_freq, prologue, rms_norm,
+    rope_angles, rope_rotate_half,
+)
+from .mxfp4 import (  # noqa: F401
+    E2M1_MAX, MX_BLOCK, block_exponent, decode_e2m1, dequantize_rows, e2m1_magnitudes,
+    encode_e2m1_rne_sat, quantize_rows,
 )
 from .fp8_e4m3 import (  # noqa: F401
     E4M3_MAX, decode_e4m3, dequantize_cache, e4m3_magnitudes, encode_e4m3_rne_sat,

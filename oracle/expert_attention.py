@@ -210,3 +210,30 @@ def expert_attention_layer_fp8(q_raw, k_raw, v_raw, q_gamma, k_gamma,
     out = attention_concat(q, k_deq, v_deq, S, k_store, v_store)
     return {"q": q, "k": k, "k_tail_codes": kc, "v_tail_codes": vc, "k_tail_scale": ks,
             "v_tail_scale": vs, "k_store": k_store, "v_store": v_store, "out": out}
+
+
+def expert_attention_layer_mxfp4(q_raw, k_raw, v_raw, q_gamma, k_gamma,
+                                 k_codes, k_exps, v_codes, v_exps,
+                                 S: int, Smax: int, rope_delta: int) -> dict:
+    """One layer with an MXFP4 cache (E2M1 codes [8, Smax, 128] uint8 0..15, block exponents
+    [8, Smax, 4]: row r's channels [32 j, 32 j + 32) scaled by 2^exps[g, r, j]).
+
+    The own 64 rows are quantised on write like any row (each row has its own block scales):
+    k from the roped k in fp32, v from the raw bf16 v. Attention then runs in fp64 on the
+    dequantised values of cache rows [0, S) and of the own rows.
+    Returns ``q``, ``k``, ``k_tail_codes``, ``k_tail_exps``, ``v_tail_codes``,
+    ``v_tail_exps``, ``k_store``/``v_store`` (dequantised own rows) and ``out``.
+    """
+    from .mxfp4 import dequantize_rows, quantize_rows
+
+    assert 0 <= S <= Smax - T and Smax % 128 == 0
+    q, k, v = prologue(q_raw, k_raw, v_raw, q_gamma, k_gamma, S, rope_delta)
+    kc, ke = quantize_rows(k.astype(np.float32))
+    vc, ve = quantize_rows(v.astype(np.float32))
+    k_store = dequantize_rows(kc, ke)
+    v_store = dequantize_rows(vc, ve)
+    k_deq = dequantize_rows(np.asarray(k_codes)[:, :S], np.asarray(k_exps)[:, :S])
+    v_deq = dequantize_rows(np.asarray(v_codes)[:, :S], np.asarray(v_exps)[:, :S])
+    out = attention_concat(q, k_deq, v_deq, S, k_store, v_store)
+    return {"q": q, "k": k, "k_tail_codes": kc, "k_tail_exps": ke, "v_tail_codes": vc,
+            "v_tail_exps": ve, "k_store": k_store, "v_store": v_store, "out": out}

@@ -188,3 +188,73 @@ def test_decode_pin_catches_planted_mistake(monkeypatch, name, bad, pin):
 def test_unpatched_decode_pins_pass():
     for _, _, pin in DECODE_MUTATIONS:
         pin()
+
+
+# ------------------------------------------------------------------ MXFP4 cache format
+import oracle.mxfp4 as mx  # noqa: E402
+from tests import test_oracle_mxfp4_pins as mpins  # noqa: E402
+
+
+def _encode_ties_away(x):
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).astype(np.float64)
+    mags = mx.e2m1_magnitudes()
+    hi = np.minimum(np.searchsorted(mags, a, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    code = np.where(mags[hi] - a <= a - mags[lo], hi, lo)    # planted: ties away from zero
+    code = np.where(a >= 6.0, 7, np.where(a == 0.0, 0, code))
+    return (code | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+
+def _block_exponent_emax3(amax):
+    amax = float(amax)
+    if amax == 0.0:
+        return 0
+    return int(max(int(np.frexp(amax)[1]) - 1 - 3, -127))    # planted: emax 3 instead of 2
+
+
+def _magnitudes_bias2():
+    codes = np.arange(8)
+    e, m = codes >> 1, codes & 1
+    return np.where(e == 0, m * 0.25, (1.0 + m / 2.0) * np.exp2(e - 2.0))   # planted: bias 2
+
+
+def _quantize_whole_row(x):
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)                        # planted: one scale per row
+    exps = np.vectorize(mx.block_exponent, otypes=[np.int64])(amax).astype(np.int16)
+    codes = mx.encode_e2m1_rne_sat(x / np.exp2(exps.astype(np.float64)).astype(np.float32)[..., None])
+    return codes, np.repeat(exps[..., None], 4, axis=-1)
+
+
+def _layer_mxfp4_v_with_k_scales(q_raw, k_raw, v_raw, q_gamma, k_gamma, k_codes, k_exps, v_codes,
+                                 v_exps, S, Smax, rope_delta):
+    return _original_layer_mxfp4(q_raw, k_raw, v_raw, q_gamma, k_gamma, k_codes, k_exps, v_codes,
+                                 k_exps, S, Smax, rope_delta)   # planted: V read with K's scales
+
+
+_original_layer_mxfp4 = ea.expert_attention_layer_mxfp4
+
+MXFP4_MUTATIONS = [
+    (mx, "encode_e2m1_rne_sat", _encode_ties_away, mpins.test_ties_go_to_the_even_code),
+    (mx, "block_exponent", _block_exponent_emax3, mpins.test_block_exponent_puts_amax_in_4_to_8),
+    (mx, "e2m1_magnitudes", _magnitudes_bias2, mpins.test_e2m1_values_match_the_specification),
+    (mx, "quantize_rows", _quantize_whole_row, mpins.test_quantize_rows_error_bound_and_block_layout),
+    (ea, "expert_attention_layer_mxfp4", _layer_mxfp4_v_with_k_scales,
+     mpins.test_attention_equals_bf16_oracle_on_representable_cache),
+]
+
+
+@pytest.mark.parametrize("mod,name,bad,pin", MXFP4_MUTATIONS,
+                         ids=["ties_away", "emax3", "bias2", "row_scale", "v_with_k_scales"])
+def test_mxfp4_pin_catches_planted_mistake(monkeypatch, mod, name, bad, pin):
+    monkeypatch.setattr(mod, name, bad)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_unpatched_mxfp4_pins_pass():
+    for _, _, _, pin in MXFP4_MUTATIONS:
+        pin()
