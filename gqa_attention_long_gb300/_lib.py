@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "expert_attn_layers": (I, [P, I, I, I, I, I, V, S, V]),
             "expert_attn_layers_profiled": (I, [P, I, I, I, I, I, V, S, V, ctypes.POINTER(V)]),
             "expert_attn_quantize_cache": (I, [V, I, I, V, V, V]),
+            "expert_attn_quantize_cache_mxfp4": (I, [V, I, I, V, V, V]),
             "expert_attn_set_splits": (I, [I]),
             "expert_attn_read_status": (I, [V, V, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_uint32)]),
             "expert_attn_status_string": (ctypes.c_char_p, [I]),
@@ -219,6 +220,16 @@ def expert_attn_quantize_cache(src: torch.Tensor, n_rows: int, Smax: int, dst: t
         _ptr(src, "src", torch.bfloat16, 8 * Smax * 128), n_rows, Smax,
         _ptr(dst, "dst", (torch.uint8, torch.float8_e4m3fn), 8 * Smax * 128),
         _ptr(scales, "scales", torch.float32, 8 * (Smax // 128 + 1)), _stream(stream)))
+
+
+def expert_attn_quantize_cache_mxfp4(src: torch.Tensor, n_rows: int, Smax: int, codes: torch.Tensor,
+                                     scales: torch.Tensor, stream=None) -> None:
+    """MXFP4 cache producer: rows [0, n_rows) of a bf16 cache [8, Smax, 128] into packed E2M1
+    codes uint8 [8, Smax, 64] and block exponents uint8 [8, Smax, 4] (e + 127)."""
+    _check("expert_attn_quantize_cache_mxfp4", lib().expert_attn_quantize_cache_mxfp4(
+        _ptr(src, "src", torch.bfloat16, 8 * Smax * 128), n_rows, Smax,
+        _ptr(codes, "codes", torch.uint8, 8 * Smax * 64),
+        _ptr(scales, "scales", torch.uint8, 8 * Smax * 4), _stream(stream)))
 
 
 def split_units(n_layers: int, S: int, n_ctas: int) -> list[int]:

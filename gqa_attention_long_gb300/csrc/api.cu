@@ -26,6 +26,8 @@ template <int CAP>
 cudaError_t launch_attention_kernel(const AttnParams<CAP>& ap, bool f8, cudaLaunchConfig_t cfg);
 template <int CAP>
 cudaError_t launch_merge_kernel(const MergeParams<CAP>& mp, cudaLaunchConfig_t cfg);
+cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* src, uint8_t* codes, uint8_t* scales, int n_rows,
+                                  int Smax, cudaStream_t stream);
 __global__ void quantize_cache_kernel(const __nv_bfloat16* src, uint8_t* dst, float* scales,
                                       int n_rows, int Smax);
 }  // namespace ea
@@ -500,6 +502,22 @@ int expert_attn_quantize_cache(const void* src_bf16, int n_rows, int Smax, void*
       static_cast<const __nv_bfloat16*>(src_bf16), static_cast<uint8_t*>(dst_codes), scales, n_rows,
       Smax);
   return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+int expert_attn_quantize_cache_mxfp4(const void* src_bf16, int n_rows, int Smax, void* dst_codes,
+                                     void* dst_scales, ea_stream_t stream) {
+  if (src_bf16 == nullptr || dst_codes == nullptr || dst_scales == nullptr) return EA_ERR_INVALID_ARG;
+  if (Smax < 1 || Smax > (1 << 22) || n_rows < 0 || n_rows > Smax) return EA_ERR_INVALID_ARG;
+  if (!aligned16(src_bf16) || !aligned16(dst_codes)) return EA_ERR_MISALIGNED;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return EA_OK;
+  return launch_quantize_mxfp4(static_cast<const __nv_bfloat16*>(src_bf16), static_cast<uint8_t*>(dst_codes),
+                               static_cast<uint8_t*>(dst_scales), n_rows, Smax,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? EA_OK
+             : EA_ERR_CUDA;
 }
 
 int expert_attn_set_splits(int n_ctas_or_0_for_auto) {

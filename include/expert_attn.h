@@ -126,6 +126,18 @@ int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S
 int expert_attn_quantize_cache(const void* src_bf16, int n_rows, int Smax, void* dst_codes,
                                float* scales, ea_stream_t stream);
 
+/* 4-bit cache producer (OCP MX v1.0 MXFP4; the pages' lowest-precision cache is Tenstorrent
+ * block-float, which has no GPU counterpart): quantises rows [0, n_rows) of every kv head of a
+ * bf16 cache [8][Smax][128] into E2M1 codes with one power-of-two scale 2^e per 32 consecutive
+ * channels of a row, e = floor(log2(amax)) - 2 clamped to [-127, 127] (0 for an all-zero
+ * block); codes round to nearest, ties to the even code, saturating at +-6.
+ * dst_codes: uint8 [8][Smax][64], two codes per byte, the lower channel in the low nibble (bit 3
+ * of a code is the sign). dst_scales: uint8 [8][Smax][4], the biased exponent e + 127 of each
+ * block. Rows >= n_rows are not written. Requires 0 <= n_rows <= Smax <= 2^22; src_bf16 and
+ * dst_codes 16-byte aligned. Returns EA_ERR_INVALID_ARG / EA_ERR_MISALIGNED before any launch. */
+int expert_attn_quantize_cache_mxfp4(const void* src_bf16, int n_rows, int Smax, void* dst_codes,
+                                     void* dst_scales, ea_stream_t stream);
+
 /* Tuning knob: number of persistent attention CTAs (0 = one per SM, the default). Values above
  * the SM count are clamped. Process-wide. Returns the previous setting. */
 int expert_attn_set_splits(int n_ctas_or_0_for_auto);

@@ -168,3 +168,16 @@ def test_decode_rejects_bad_arguments_without_gpu(h):
         _lib.EA_ERR_MISALIGNED
     assert h.text_decode_workspace_size(0) == 0
     assert h.text_decode_workspace_init(None, 4096, None) == _lib.EA_ERR_INVALID_ARG
+
+
+def test_mxfp4_quantiser_rejects_bad_arguments_without_gpu(h):
+    p, c, s = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30001)
+    f = h.expert_attn_quantize_cache_mxfp4
+    assert f(None, 10, 512, c, s, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(p, 10, 512, None, s, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(p, 10, 512, c, None, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(p, -1, 512, c, s, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(p, 513, 512, c, s, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(p, 10, 0, c, s, None) == _lib.EA_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(0x10008), 10, 512, c, s, None) == _lib.EA_ERR_MISALIGNED
+    assert f(p, 10, 512, ctypes.c_void_p(0x20004), s, None) == _lib.EA_ERR_MISALIGNED
