@@ -1,5 +1,5 @@
 """Host-side pieces of bench.py that need no GPU: the clock sampler's parsing of nvidia-smi's
-CSV output (run against a stand-in nvidia-smi script on PATH) and its verdicts."""
+CSV output (run against a stand-in nvidia-smi script on PATH) and the throttle reasons it reports."""
 import os
 import stat
 import sys
