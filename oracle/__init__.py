@@ -22,9 +22,10 @@ decode_attention : the text model's single-token decode attention over the same 
                    (64 query heads / 8 KV heads, norm and RoPE at pos + rope_delta, the
                    new row written at pos, attention over rows 0..pos).
 
-Every function is pinned by ``tests/test_oracle_pins.py``, ``tests/test_oracle_layer_pins.py``,
-``tests/test_oracle_decode_pins.py`` and ``tests/test_oracle_mxfp4_pins.py`` against closed
-forms, invariants, brute force on tiny inputs and independent library routines.
+Every function is pinned by ``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8_pins.py``,
+``tests/test_oracle_layer_pins.py``, ``tests/test_oracle_decode_pins.py`` and
+``tests/test_oracle_mxfp4_pins.py`` against closed forms, invariants, brute force on tiny
+inputs and independent library routines.
 """
 from .expert_attention import (  # noqa: F401
     D, EPS, HQ, HKV, MASK_MIN, REP, T, THETA,

@@ -258,3 +258,63 @@ def test_mxfp4_pin_catches_planted_mistake(monkeypatch, mod, name, bad, pin):
 def test_unpatched_mxfp4_pins_pass():
     for _, _, _, pin in MXFP4_MUTATIONS:
         pin()
+
+
+# ------------------------------------------------------------ FP8 own rows (quantise on write)
+import oracle.fp8_e4m3 as f8  # noqa: E402
+from tests import test_oracle_fp8_pins as fpins  # noqa: E402
+
+_original_fp8_layer = ea.expert_attention_layer_fp8
+
+
+def _tail_rows_per_token_amax(x):
+    x = np.asarray(x, dtype=np.float32)
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty((x.shape[0],), dtype=np.float32)
+    for g in range(x.shape[0]):
+        sc_t = np.maximum(np.max(np.abs(x[g]), axis=-1), np.float32(1e-30)) / np.float32(448)
+        codes[g] = f8.encode_e4m3_rne_sat(x[g] / sc_t[:, None])   # planted: one amax per token
+        scales[g] = sc_t.max()
+    return codes, scales
+
+
+def _tail_rows_amax_over_all_heads(x):
+    x = np.asarray(x, dtype=np.float32)
+    sc = np.float32(np.max(np.abs(x)) / np.float32(448))           # planted: amax over all 8 heads
+    return f8.encode_e4m3_rne_sat(x / sc), np.full((x.shape[0],), sc, dtype=np.float32)
+
+
+def _fp8_layer_k_before_rope(q_raw, k_raw, v_raw, q_gamma, k_gamma, k_codes, k_scales, v_codes,
+                             v_scales, S, Smax, rope_delta):
+    r = _original_fp8_layer(q_raw, k_raw, v_raw, q_gamma, k_gamma, k_codes, k_scales, v_codes,
+                            v_scales, S, Smax, rope_delta)
+    kc, ks = f8.quantize_tail_rows(ea.rms_norm(k_raw, k_gamma).astype(np.float32))  # planted: no RoPE
+    r["k_tail_codes"], r["k_tail_scale"] = kc, ks
+    r["k_store"] = f8.decode_e4m3(kc) * ks.astype(np.float64)[:, None, None]
+    r["out"] = ea.attention_concat(r["q"], f8.dequantize_cache(k_codes, k_scales, S),
+                                   f8.dequantize_cache(v_codes, v_scales, S), S, r["k_store"], r["v_store"])
+    return r
+
+
+_FP8_CASE = fpins.CASES[0]
+FP8_MUTATIONS = [
+    (f8, "quantize_tail_rows", _tail_rows_per_token_amax, fpins.test_head_amax_encodes_to_448),
+    (f8, "quantize_tail_rows", _tail_rows_amax_over_all_heads, fpins.test_own_row_scale_is_head_amax_over_448),
+    (ea, "expert_attention_layer_fp8", _fp8_layer_k_before_rope,
+     fpins.test_own_rows_within_half_ulp_of_roped_k_and_raw_v),
+]
+
+
+@pytest.mark.parametrize("mod,name,bad,pin", FP8_MUTATIONS,
+                         ids=["per_token_amax", "amax_over_all_heads", "k_before_rope"])
+def test_fp8_own_row_pin_catches_planted_mistake(monkeypatch, mod, name, bad, pin):
+    monkeypatch.setattr(mod, name, bad)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises(AssertionError):
+        pin(*_FP8_CASE)
+
+
+def test_unpatched_fp8_own_row_pins_pass():
+    for _, _, _, pin in FP8_MUTATIONS:
+        pin(*_FP8_CASE)
