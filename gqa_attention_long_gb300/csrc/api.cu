@@ -617,13 +617,36 @@ extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_lay
   uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
   if (ws == nullptr) return EA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word and the in-kernel merge words start at 0
-  if (cudaMemsetAsync(ws, 0, wl.qscale_off, st) != cudaSuccess) {
+  // the in-kernel merge words start at 0; the status word (the first 4 bytes) is left alone, so
+  // that a timeout stays visible until expert_attn_noalloc_read_status reads and clears it
+  if (cudaMemsetAsync(ws + wl.sync_off, 0, wl.qscale_off - wl.sync_off, st) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }
   return launch_chunk(layers, n_layers, S, Smax, rope_delta, kv_dtype == EA_KV_FP8_E4M3, ws, wl,
                       capped, st, nullptr);
+}
+
+extern "C" int expert_attn_noalloc_read_status(ea_stream_t stream, int* status_out,
+                                               uint32_t* bits_out) {
+  if (status_out == nullptr) return EA_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo di;
+  if (!device_info(&dev, &di)) return EA_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
+  if (ws == nullptr) return EA_ERR_CUDA;
+  uint32_t bits = 0;
+  const int rc = expert_attn_read_status(ws, stream, status_out, &bits);
+  if (rc != EA_OK) return rc;
+  if (bits_out) *bits_out = bits;
+  if (bits != 0) {  // reported once: clear it for the calls that follow
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
+      cudaGetLastError();
+      return EA_ERR_CUDA;
+    }
+  }
+  return EA_OK;
 }
 
 // ------------------------------------------------------------------ whole decoder layer

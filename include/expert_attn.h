@@ -175,14 +175,25 @@ int expert_attn_selftest_wait_timeout(int limit_us, void* workspace, size_t ws_b
  * Set-up: the first call on a device looks up the array's device address on that device (which
  * must be current); make that first call before any stream capture.
  * Sharing: all calls in the process share the array and find the previous call's contents in
- * it; each call clears the status word itself. Calls that overlap on the GPU (for example on
- * two streams) race on the array and must be avoided. Timeouts of bounded waits are recorded
- * in the array's status word and are not reported by this call. */
+ * it; each call clears the words that must start at zero itself. Calls that overlap on the GPU
+ * (for example on two streams) race on the array and must be avoided.
+ * Errors: argument errors and failed launches are returned as by expert_attn_layers. A kernel
+ * that gives up a bounded wait records it in the array's status word, which stays set across
+ * later calls until expert_attn_noalloc_read_status reads it; the outputs of the call that
+ * timed out are undefined. */
 #define EA_NOALLOC_MAX_LAYERS 4
 #define EA_NOALLOC_MAX_CTAS 64
 #define EA_NOALLOC_SCRATCH_BYTES 9522176u /* 2 KB + 4 layers x 260 KB + 1 KB + 64 CTAs x 129 KB */
 int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                int rope_delta, int kv_dtype, ea_stream_t stream);
+
+/* Status of the calls above (no counterpart on the pages either): synchronises the stream and
+ * returns in *status_out EA_OK, or EA_ERR_TIMEOUT if a kernel of some expert_attn_layers_noalloc
+ * call on the current device gave up a bounded wait since the status was last read; the raw
+ * status bits go to *bits_out if not NULL. A set status is cleared by this read. Allocates
+ * nothing. Returns EA_ERR_INVALID_ARG for a null status_out, EA_ERR_UNSUPPORTED without an
+ * sm_103 device, EA_ERR_CUDA if the copy fails. */
+int expert_attn_noalloc_read_status(ea_stream_t stream, int* status_out, uint32_t* bits_out);
 
 /* ------------------------------------------------------------------ whole decoder layer
  * One decoder layer of the expert around the attention above (alpamayo_tt/expert.py,
