@@ -30,6 +30,7 @@ from gqa_attention_long_gb300._lib import kernels_per_call  # noqa: E402
 from gqa_attention_long_gb300.inputs import config_seed, layer_inputs, layer_inputs_on_device  # noqa: E402
 
 METRIC = "µs/layer & achieved HBM GB/s (% roofline), expert attention, S=4700 Smax=8192"
+CLOCK_WINDOW_S = 1.5
 HQ, HKV, D, T = 16, 8, 128, 64
 
 
@@ -97,9 +98,11 @@ def load_peaks() -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs. The raw samples go to a
-    CSV file in $EA_CLOCKS_DIR (default: the system temporary directory)."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling (every 50 ms) while the measured steps run. The raw
+    samples go to a CSV file in $EA_CLOCKS_DIR (default: the system temporary directory); the
+    summary keeps only the samples taken between two marks of the host clock (the window of
+    back-to-back steps around the timed region)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -114,7 +117,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -130,27 +133,45 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self) -> dict:
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def summary(self, t0: float | None = None, t1: float | None = None) -> dict:
+        """Median SM clock, highest max clock and active throttle reasons of the samples taken
+        in [t0, t1] (host time.time() marks; all samples when no marks are given)."""
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
+                continue
+            w = self._when(f[0])
+            if t0 is not None and (w is None or w < t0 or w > t1):
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if t0 is not None:
+            out["window_s"] = round(t1 - t0, 3)
+        return out
 
 
 def oracle_sample(S: int, Smax: int, n_layers: int, min_seconds: float) -> dict:
@@ -170,6 +191,21 @@ def oracle_sample(S: int, Smax: int, n_layers: int, min_seconds: float) -> dict:
             spent += time.perf_counter() - t0
             done += 1
     return {"us_per_layer": spent / done * 1e6, "layers": done, "seconds": spent}
+
+
+def time_calls(fn, warmup: int, reps: int, stream) -> float:
+    """Milliseconds per call of fn (launches on `stream`), CUDA events around reps back-to-back
+    calls after warmup untimed ones."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
 
 
 def dist_setup(n_gpus: int):
@@ -272,8 +308,16 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, device time with CUDA events on the launching stream
+    # ---- timed region: K steps, device time with CUDA events on the launching stream. The
+    # clocks are sampled over a window of at least CLOCK_WINDOW_S seconds of the same step run
+    # back to back (untimed), which ends with the timed steps themselves, so that the reported
+    # clock is the one the timed steps ran at even when they last only milliseconds.
     with ClockSampler(local) as clk:
+        t_win0 = time.time()
+        while time.time() - t_win0 < CLOCK_WINDOW_S:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -282,7 +326,10 @@ def main():
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        t_win1 = time.time()
         barrier(world)
+        time.sleep(0.1)  # let the sampler write its last line of the window
+    clocks = clk.summary(t_win0, t_win1)
     ms_total = max_over_ranks(e0.elapsed_time(e1), world)
     st, bits = ea.expert_attn_read_status(ws)
     if st != 0:
@@ -391,7 +438,66 @@ def main():
         fp8 = {"workload": f"{n}-layer step, S={S}, Smax={Smax}, e4m3 cache", "us_per_layer": ms8 * 1e3 / n,
                "ms_per_step": ms8, "step_hbm_gbs": b8 / (ms8 * 1e-3) / 1e9,
                "step_roofline_frac": b8 / (ms8 * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        if n >= 8:  # one layer per call (the e4m3 single-layer configuration), 8 layers rotated
+            ws81 = ea.alloc_workspace(1, Smax, ea.EA_KV_FP8_E4M3)
+            arr81 = [ea.make_args([L8[l]], Smax, ea.EA_KV_FP8_E4M3) for l in range(8)]
+            k81 = [0]
+
+            def one8():
+                ea.expert_attn_layers([L8[k81[0] % 8]], S, Smax, 0, ea.EA_KV_FP8_E4M3, ws81, stream,
+                                      _arr=arr81[k81[0] % 8])
+                k81[0] += 1
+            us81 = time_calls(one8, 8, 8 * max(4, args.steps // 2), stream) * 1e3
+            st81, bits81 = ea.expert_attn_read_status(ws81)
+            if st81 != 0:
+                raise RuntimeError(f"fp8 one-layer kernel status bits {bits81:#x}")
+            fp8["one_layer_per_call_us"] = us81
+            fp8["one_layer_hbm_gbs"] = algo_bytes_per_layer_fp8(S) / (us81 * 1e-6) / 1e9
+            del ws81
         del L8, ws8
+
+    # ---- the 64-layer step over the S sweep (S in {1024, 2048, 4700, 8128}, Smax 8192) and with
+    # the tighter cache (Smax 5120, S 4700): time should track S + 64, not Smax
+    sweep = tight = None
+    if not args.no_extras and n == 64 and Smax == 8192 and S <= 4700:
+        # rows [S, Smax - 64) of the caches above hold the hidden-row fill; for the larger S of the
+        # sweep they are live rows, so they get N(0, 1) values (still hidden at S = 4700)
+        g7 = torch.Generator(device=dev).manual_seed(config_seed(4, 999))
+        for x in xs:
+            for c in (x.k_cache, x.v_cache):
+                c[:, S:Smax - T].copy_(torch.randn(HKV, Smax - T - S, D, generator=g7, device=dev))
+        sweep = {}
+        for S_ in (1024, 2048, 4700, 8128):
+            ms_ = ms_step if S_ == S else time_calls(
+                lambda: ea.expert_attn_layers(Ls, S_, Smax, 0, ea.EA_KV_BF16, ws, stream, _arr=arr),
+                args.warmup, args.steps, stream)
+            b_ = algo_bytes_per_layer(S_) * n
+            sweep[f"S={S_}"] = {"us_per_layer": ms_ * 1e3 / n, "ms_per_step": ms_,
+                                "step_hbm_gbs": b_ / (ms_ * 1e-3) / 1e9,
+                                "step_roofline_frac": b_ / (ms_ * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                "roofline_us_per_step_at_8tbs": b_ / 8e12 * 1e6,
+                                "frac_of_8tbs_roofline": b_ / 8e12 / (ms_ * 1e-3)}
+        st_, bits_ = ea.expert_attn_read_status(ws)
+        if st_ != 0:
+            raise RuntimeError(f"sweep kernel status bits {bits_:#x}")
+        Smax2 = 5120
+        xs2 = [layer_inputs_on_device(config_seed(2, l), S, Smax2, dev) for l in range(n)]
+        Ls2 = [ea.LayerBuffers(q_raw=L.q_raw, k_raw=L.k_raw, v_raw=L.v_raw, q_gamma=x2.q_gamma,
+                               k_gamma=x2.k_gamma, k_cache=x2.k_cache, v_cache=x2.v_cache, out=L.out)
+               for L, x2 in zip(Ls, xs2)]
+        ws2 = ea.alloc_workspace(n, Smax2)
+        arr2 = ea.make_args(Ls2, Smax2, ea.EA_KV_BF16)
+        ms2 = time_calls(lambda: ea.expert_attn_layers(Ls2, S, Smax2, 0, ea.EA_KV_BF16, ws2, stream, _arr=arr2),
+                         args.warmup, args.steps, stream)
+        st2, bits2 = ea.expert_attn_read_status(ws2)
+        if st2 != 0:
+            raise RuntimeError(f"Smax 5120 kernel status bits {bits2:#x}")
+        b2 = algo_bytes_per_layer(S) * n
+        tight = {"workload": f"{n}-layer step, S={S}, Smax={Smax2}, bf16 cache", "us_per_layer": ms2 * 1e3 / n,
+                 "ms_per_step": ms2, "step_hbm_gbs": b2 / (ms2 * 1e-3) / 1e9,
+                 "step_roofline_frac": b2 / (ms2 * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                 "ratio_to_smax_8192": ms2 / ms_step}
+        del xs2, Ls2, ws2
 
     # ---- one layer per call (the pages' per-layer measurement), rotating over 8 distinct layers
     single = None
@@ -570,7 +676,7 @@ def main():
                          "kernel": "attention_kernel", "peak_src": peaks["src"],
                          "bytes_per_launch": k2_bytes, "ms_per_launch": k2},
             "kernels_ms": {"attention": k2, "merge": k3 if merge_launched else None},
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "e2e": {"value": e2e_ms * 1e3 / (n * world), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "pipelining": "two device buffer sets; host->device copy, step and device->host "
@@ -578,6 +684,8 @@ def main():
             "gpu_launches": args.steps * launches_per_call(n, S, torch.cuda.get_device_properties(dev).multi_processor_count),
             "cpu_baseline": cpu,
             "fp8_step": fp8,
+            "sweep_S": sweep,
+            "tight_cache": tight,
             "single_layer": single,
             "sequential_chain": chain,
             "decoder_layer": dlayer,
