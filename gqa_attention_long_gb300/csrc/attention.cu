@@ -671,6 +671,13 @@ __device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
           moved = true;
         }
         if (moved) continue;
+        // Nothing to issue: suspend on the barrier the next MMA most likely waits for, for at
+        // most ~0.3 us, then look at both again (a spinning thread takes issue slots from the
+        // softmax warps that share its SM sub-partition).
+        if (pv_todo)
+          mbar_try_wait_hint(cx.bar(B_PFULL + (n_pv & 1)), (n_pv >> 1) & 1, 300);
+        else if (n_qk >= 2)
+          mbar_try_wait_hint(cx.bar(B_ODONE + ((n_qk - 2) & 1)), ((n_qk - 2) >> 1) & 1, 300);
         // bounded like every other wait: the CTA's abort flag, a time limit and a poll limit
         if ((it & 63u) == 0) {
           if (*cx.abort_flag) {
@@ -714,6 +721,33 @@ __device__ __forceinline__ void rescale_O(uint32_t taddr, float alpha) {
     tmem_st32(taddr + ch * 32, o);
   }
   tmem_wait_st();
+}
+
+// The rare rescale of a running max move while a chunk's scores are live in registers: the
+// stream's accumulator O (128 columns) if it holds earlier tiles, and the current tile's P of
+// the earlier chunk (32 columns of 16-bit pairs) if there is one. Kept out of line, so that only
+// this path pays for the registers it needs.
+template <bool F8>
+__device__ __noinline__ void rescale_rare(uint32_t o_addr, uint32_t p_addr, float alpha, bool do_o, bool do_p) {
+  if (do_o) rescale_O(o_addr, alpha);
+  if (do_p) {
+    uint32_t q[32];
+    tmem_ld32(p_addr, q);
+    tmem_wait_ld();
+    reg_fence32(q);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      float2 f;
+      if constexpr (F8) {
+        f = __half22float2(*reinterpret_cast<const __half2*>(&q[e]));
+      } else {
+        f = make_float2(__uint_as_float(q[e] << 16), __uint_as_float(q[e] & 0xFFFF0000u));
+      }
+      q[e] = F8 ? pack_f16x2(f.x * alpha, f.y * alpha) : pack_bf16x2(f.x * alpha, f.y * alpha);
+    }
+    tmem_st32(p_addr, q);
+    tmem_wait_st();
+  }
 }
 
 template <bool F8, class PP>
@@ -807,9 +841,10 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
       tc_fence_after();
       const bool tail = j >= p.n_main;
       const uint32_t sa = cx.tmem + lane_addr + s_col;
-      // The score row is read in two passes of 64-column pairs (max, then exponentials), so
-      // that no more than 64 scores are live per thread: two softmax warpgroups share the
-      // register file. A cache tile has two pairs, the own-row tile (64 keys) one.
+      // The score row is read in chunks of 64 columns (a cache tile has two, the 64-key own-row
+      // tile one), each in one pass: its max, then its exponentials against the running max, so
+      // that no more than 64 scores are live per thread (two softmax warpgroups share the
+      // register file). The running max moves (lazily, see kLazy) when a chunk's max exceeds it.
       const int npair = tail ? 1 : 2;
       const int key0 = j * kKeyTile;
       const bool ragged = !tail && key0 + kKeyTile > p.S;  // keys >= S (hidden rows) are masked
@@ -827,20 +862,6 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
               if (key0 + 64 * pr + 32 * ch + e >= p.S) v[ch][e] = __float_as_uint(-INFINITY);
         }
       };
-      // row max with 8 independent accumulators (a single chain would serialise 128 fmax)
-      float mx8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
-#pragma unroll 1
-      for (int pr = 0; pr < npair; ++pr) {
-        uint32_t v[2][32];
-        load_pair(pr, v);
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
-      }
       // per-tile factors: scores in log2 units are s * ct; FP8 adds the block scales, and P is
       // stored as 2^(x - m) * (sv / svr) (exponent offset lgv) so that it carries the tile's V
       // scale relative to the unit's largest one (V itself stays as its e4m3 code values); the
@@ -853,44 +874,67 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
         lgv = __log2f(sv / svr);
         lmul = svr / sv;
       }
-      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * ct;
-      const bool need = (last_n < 0) || (mt > m_ref + kLazy);
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = fmaxf(m_ref, mt);
-        const float alpha = ex2_approx(m_ref - m_new);
-        // S(n) is complete, so PV(n-2) and every earlier PV of this stream are done: the
-        // accumulator is stable and holds this stream's tiles before n
-        if (last_n >= 0) rescale_O(cx.tmem + lane_addr + o_col, alpha);
-        lsum *= alpha;
-        m_ref = m_new;
-      }
-      const float neg = lgv - m_ref;
-      float ts8[8];  // row sum with 8 independent accumulators
+      float2 ts4[4];  // row sum of this tile with 4 independent pairs of accumulators
 #pragma unroll
-      for (int q = 0; q < 8; ++q) ts8[q] = 0.f;
-      // P(n) goes to TMEM over the columns of S(n). Pair pr's P lands in columns [32 pr,
-      // 32 pr + 32), which hold scores of pairs <= pr, already read. The buffer's previous P,
+      for (int q = 0; q < 4; ++q) ts4[q] = make_float2(0.f, 0.f);
+      const float2 ct2 = make_float2(ct, ct);
+      // P(n) goes to TMEM over the columns of S(n). Chunk pr's P lands in columns [32 pr,
+      // 32 pr + 32), which hold scores of chunks <= pr, already read. The buffer's previous P,
       // P(n-2), was consumed by PV(n-2), which completed before QK(n).
 #pragma unroll 1
       for (int pr = 0; pr < npair; ++pr) {
         uint32_t v[2][32];
         load_pair(pr, v);
-        // 16-bit pairs (bf16; f16 for an e4m3 cache, whose V is widened to f16): column c of
-        // the pair block holds keys 2c and 2c + 1
-        uint32_t pk[32];
+        // the chunk's max with 8 independent accumulators
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e]), ct, neg));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(v[ch][2 * e + 1]), ct, neg));
-            ts8[e & 7] += p0 + p1;
-            pk[16 * ch + e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          for (int e = 0; e < 32; e += 2)
+            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]));
+        const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * ct;
+        // a chunk 0 always holds a live key (key0 < S), so m_ref is finite after it
+        const bool need = (m_ref == -INFINITY) || (mc > m_ref + kLazy);
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m_ref, mc);
+          const float alpha = ex2_approx(m_ref - m_new);  // 0 for the segment's first chunk
+          // S(n) is complete, so PV(n-2) and every earlier PV of this stream are done: the
+          // accumulator is stable and holds this stream's tiles before n; this tile's P of the
+          // earlier chunk, already in TMEM columns [0, 32), moves too. The chunk's scores are
+          // not kept in registers across that (rare) step: they are read again from TMEM,
+          // where they stay until this chunk's P is written.
+          if (last_n >= 0 || pr > 0) {
+            rescale_rare<F8>(cx.tmem + lane_addr + o_col, pa_base, alpha, last_n >= 0, pr > 0);
+            load_pair(pr, v);
           }
-        tmem_st32(pa_base + 32 * pr, pk);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ts4[q] = make_float2(ts4[q].x * alpha, ts4[q].y * alpha);
+          lsum *= alpha;
+          m_ref = m_new;
+        }
+        const float neg = lgv - m_ref;
+        const float2 neg2 = make_float2(neg, neg);
+        // 16-bit pairs (bf16; f16 for an e4m3 cache, whose V is widened to f16): column c of
+        // the chunk's P block holds keys 2c and 2c + 1
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {  // 32 keys -> 16 TMEM columns at a time
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            // two keys per packed fma (x * ct + neg, one rounding each, as fmaf)
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(v[ch][2 * e]), __uint_as_float(v[ch][2 * e + 1])), ct2, neg2);
+            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            ts4[e & 3] = __fadd2_rn(ts4[e & 3], make_float2(p0, p1));
+            pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          }
+          tmem_st16(pa_base + 32 * pr + 16 * ch, pk);
+        }
       }
-      lsum += (((ts8[0] + ts8[1]) + (ts8[2] + ts8[3])) + ((ts8[4] + ts8[5]) + (ts8[6] + ts8[7]))) * lmul;
+      lsum += (((ts4[0].x + ts4[0].y) + (ts4[1].x + ts4[1].y)) + ((ts4[2].x + ts4[2].y) + (ts4[3].x + ts4[3].y))) * lmul;
       if constexpr (!F8) {
         if (ragged) {
           // the last cache tile: V rows of keys >= S (hidden rows, any content, NaN included)

@@ -230,3 +230,42 @@ def test_repeated_calls_leave_merge_words_zero():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     host = type(xs[5])(**{k: (v.cpu() if torch.is_tensor(v) else v) for k, v in xs[5].__dict__.items()})
     assert_close(f64(Ls[5].out), oracle_layer(host)["out"])
+
+
+def max_moving_inputs(seed, S=448, Smax=512):
+    """Cache keys that make the running row max move by more than the softmax's lazy-rescale
+    margin (8 in log2 units) inside a tile and across tiles, with moderate scores: rows
+    [0, 320) are zero (every score 0: tiles 0-1 and the first half of tile 2), rows [320, S)
+    are N(0, 2.8^2), whose largest score in a 64-key chunk is ~6.7 (9.7 in log2 units)."""
+    x = layer_inputs(seed, S, Smax)
+    j = torch.arange(Smax, dtype=torch.float32)
+    sc = torch.where(j < 320, torch.zeros_like(j), torch.full_like(j, 2.8))
+    x.k_cache = (x.k_cache.float() * sc[None, :, None]).to(torch.bfloat16)
+    return x
+
+
+def oracle_on_bf16_q(x, k_own=None, v_own=None, k_cache=None, v_cache=None):
+    """The oracle's attention with the oracle's own roped q rounded to bf16 (the precision the
+    tensor cores take it in): with peaked attention the rounding of q alone moves the output by
+    more than the bf16 bar, which this reference leaves out, so that the check is on the rest."""
+    import oracle
+    q, k, v = oracle.prologue(f64(x.q_raw), f64(x.k_raw), f64(x.v_raw), f64(x.q_gamma),
+                              f64(x.k_gamma), x.S, 0)
+    kc = f64(x.k_cache) if k_cache is None else k_cache
+    vc = f64(x.v_cache) if v_cache is None else v_cache
+    return oracle.attention_concat(oracle.bf16_round(q), kc, vc, x.S,
+                                   oracle.bf16_round(k) if k_own is None else k_own,
+                                   v if v_own is None else v_own)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_running_max_moves_inside_and_across_tiles(splits):
+    # the P already written for the first half of a tile and the accumulator of the earlier
+    # tiles are rescaled, in every split of the key range
+    x = max_moving_inputs(777)
+    prev = ea.expert_attn_set_splits(splits)
+    try:
+        L = run_layer(x)
+    finally:
+        ea.expert_attn_set_splits(prev)
+    assert_close(f64(L.out), oracle_on_bf16_q(x), f"running max moves, splits={splits}")

@@ -138,3 +138,20 @@ def test_workspace_size_by_dtype():
     with pytest.raises(ea.ExpertAttnError) as e:
         ea.expert_attn_layer(L, S, Smax, 0, ea.EA_KV_FP8_E4M3, ws)
     assert e.value.rc == 4
+
+
+
+def test_fp8_running_max_moves_inside_and_across_tiles():
+    # the bf16 test of the same name on an e4m3 cache (its P is rescaled as f16 pairs); the
+    # reference is the oracle on the dequantised cache with the bf16-rounded roped q
+    from tests.test_gpu_attention import max_moving_inputs, oracle_on_bf16_q
+    x = max_moving_inputs(778)
+    L = run_fp8_layers([x])[0]
+    r = oracle_fp8(x)
+    kc, ks = oracle.quantize_cache_blocks(f64(x.k_cache), x.S, x.Smax)
+    vc, vs = oracle.quantize_cache_blocks(f64(x.v_cache), x.S, x.Smax)
+    ref = oracle_on_bf16_q(x, r["k_store"], r["v_store"], oracle.dequantize_cache(kc, ks, x.S),
+                           oracle.dequantize_cache(vc, vs, x.S))
+    got = f64(L.out)
+    err = np.abs(got - ref).max()
+    assert np.all(np.isfinite(got)) and err <= TOL_FP8_MAX_ABS, f"max-abs {err:.3e}"
