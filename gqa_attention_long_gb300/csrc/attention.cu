@@ -28,18 +28,18 @@
 //              lane r); online softmax in fp32 with lazy rescaling of its TMEM accumulator; P
 //              written back to TMEM as bf16 (f16 for an e4m3 cache) over the scores it came
 //              from, and read from there by the PV MMA. With a bf16 cache these 256 threads
-//              first prepare the CTA's first Q (and its unit's own rows, if that segment holds
-//              them).
+//              first prepare the CTA's first segment: its unit's own rows (if it holds them) and
+//              its Q, with rotation angles computed before the kernel waits for the preceding one.
 //   warp 8     K/V producer: one thread issues 3-D TMA loads of the K/V tiles (cache rows, and the
 //              unit's own rows from the cache tail) into the ring
 //   warp 9     MMA: one thread issues tcgen05.mma (S = Q K^T from shared memory into the score
 //              buffer of the tile's stream; O += P V with P from TMEM and V from shared memory
 //              into the stream's accumulator) and tcgen05.commit to the barriers
-//   warps 10-11  bf16: Q and own-row prep (64 threads): per segment, RMSNorm + RoPE of the unit's
-//              raw q rows straight into one of two Q buffers, one segment ahead, so the K/V stream
-//              never waits for it; for the segment holding the own-row tile, the roped K and the V
-//              rows into the cache tail. e4m3: one thread of warp 10 bulk-copies the Q codes that
-//              the prologue kernel staged.
+//   warps 10-11  bf16: Q and own-row prep (64 threads): per later segment, RMSNorm + RoPE of the
+//              unit's raw q rows straight into one of two Q buffers, one segment ahead, so the
+//              K/V stream never waits for it; for a later segment holding the own-row tile, the
+//              roped K and the V rows into the cache tail. e4m3: one thread of warp 10 bulk-copies
+//              the Q codes that the prologue kernel staged.
 // Shared memory: Q x2 (64 KB), K/V ring (bf16: 5 x 32 KB; e4m3: 6 x 16 KB plus two 32 KB f16
 // copies of V), barriers, a 1.5 KB row-statistics exchange.
 // TMEM: 512 columns (two 128-column score/P buffers, two 128-column fp32 accumulators).
@@ -104,6 +104,8 @@ constexpr uint32_t TM_S = 0;    // score buffers of streams 0 and 1 at columns 0
 constexpr uint32_t TM_O = 256;  // accumulators of streams 0 and 1 at columns 256 and 384
 constexpr uint32_t kTmemCols = 512;
 
+constexpr uint32_t kAtomBytes = 16384u;  // one 64-channel half of a 16-bit operand tile
+
 struct Seg {
   int u, j0, j1;  // unit and its key-tile range [j0, j1)
 };
@@ -133,6 +135,16 @@ struct Ctx {
   __device__ __forceinline__ uint32_t bar(int i) const { return bar_base + 8u * i; }
 };
 
+// bf16: when the CTA's first segment holds its unit's own-row tile and that tile's K and V ring
+// positions fall in the ring's first round (the slots are still empty), the softmax threads
+// write the roped K rows and the V rows straight into those slots (and to the cache tail, for
+// the caller), and the producer skips both loads; otherwise the rows go through the cache tail
+// and the producer fetches them back by TMA once TAILRDY says they are written.
+template <class PP>
+__device__ __forceinline__ bool own_rows_direct(const PP& p, const Seg& first) {
+  return first.j1 == p.T && 2 * (first.j1 - 1 - first.j0) + 1 < Lay<false>::kRing;
+}
+
 // ------------------------------------------------------------------------------- producer
 template <bool F8, class PP>
 __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
@@ -143,9 +155,16 @@ __device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
   bool ok = true;
   long long t = cx.start;
   Seg s;
+  bool first = true;
   while (ok && next_seg(t, cx.end, p.T, s)) {
     const int l = s.u / kHkv, g = s.u % kHkv;
+    const bool direct = !F8 && first && own_rows_direct(p, s);
+    first = false;
     for (int j = s.j0; j < s.j1 && ok; ++j) {
+      if (direct && j >= p.n_main) {  // filled by the softmax threads
+        ring += 2;
+        continue;
+      }
       if (!F8 && j >= p.n_main) {
         // bf16 own-row tile: its rows are written into the cache tail by this CTA's prep warps
         ok = bounded_wait(cx.bar(B_TAILRDY + (n_own & 1)), (n_own >> 1) & 1, cx.abort_flag,
@@ -276,20 +295,35 @@ __device__ __forceinline__ void q_row_to_smem(uint32_t qbuf, int hh, int tok, in
   st_shared_v4(qbuf + swz_off(r, i + 8, kQTileBytes / 2), qh.x, qh.y, qh.z, qh.w);
 }
 
-// cos/sin of token tok at the eight frequencies [8i, 8i + 8).
+// cos/sin of token tok at the eight frequencies whose inverse frequencies are ih + il.
 template <class PP>
-__device__ __forceinline__ void token_cos_sin(const PP& p, int tok, int dl, float (&cs)[8],
-                                              float (&sn)[8]) {
+__device__ __forceinline__ void token_cos_sin(const PP& p, int tok, const float (&ih)[8], const float (&il)[8],
+                                              float (&cs)[8], float (&sn)[8]) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_base + tok, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[e], sn[e]);
+  for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_base + tok, ih[e], il[e], cs[e], sn[e]);
 }
 
-// The first segment's Q by the 256 softmax threads (32 octets, octet oc: tokens oc and oc + 32
-// of both heads), into Q buffer 0, and, when that segment holds its unit's own-row tile, the
-// unit's roped K rows and V rows into the cache tail; one thread then signals QFULL (and
-// TAILRDY). A CTA's first segment can be short, so that its own rows are needed early.
+// cos/sin of the two tokens (oc, oc + 32) whose rows a softmax thread prepares in the first
+// segment, at its eight frequencies [8i, 8i + 8). The positions depend only on the token index, S
+// and rope_delta, so this runs before the kernel waits for the preceding one.
 template <class PP>
-__device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
+__device__ __forceinline__ void first_angles(const PP& p, float (&cs)[2][8], float (&sn)[2][8]) {
+  const int oc = threadIdx.x >> 3, dl = 8 * (threadIdx.x & 7);
+  float ih[8], il[8];
+  load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
+  token_cos_sin(p, oc, ih, il, cs[0], sn[0]);
+  token_cos_sin(p, oc + 32, ih, il, cs[1], sn[1]);
+}
+
+// The first segment's rows by the 256 softmax threads (32 octets, octet oc: tokens oc and oc + 32,
+// whose rotation angles the threads already hold): the Q rows of both heads into Q buffer 0
+// (QFULL), then, when that segment holds its unit's own-row tile, the roped K rows and the V
+// rows into the cache tail and, when they fit the ring's first round (own_rows_direct), straight
+// into the two ring slots of that tile as well (KVFULL; no fetch back), else TAILRDY for the
+// producer to fetch them. A CTA's first segment can be short, so its own rows are needed early.
+template <class PP>
+__device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx, const float (&cs)[2][8],
+                                          const float (&sn)[2][8]) {
   long long t = cx.start;
   Seg s;
   if (!next_seg(t, cx.end, p.T, s)) return;
@@ -298,7 +332,7 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
   const int l = s.u / kHkv, g = s.u % kHkv;
   const bool own = s.j1 == p.T;
   const __nv_bfloat16* qsrc = p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD + oc * kD;
-  // both tokens' rows are requested at once (and the own k and v rows)
+  // every row of both tokens is requested at once
   uint4 raw[2][2][2];  // [token][head][lo, hi]
 #pragma unroll
   for (int tt = 0; tt < 2; ++tt)
@@ -327,24 +361,13 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
   // the optional roped q output is written by the CTA that holds the unit's own-row tile
   __nv_bfloat16* qr0 = own ? p.q_rope[l] : nullptr;
   if (qr0 != nullptr) qr0 += (static_cast<size_t>(2 * g) * kTok + oc) * kD;
-  // one token per pass (a short loop body, which stays in the instruction cache)
-#pragma unroll 1
-  for (int tt = 0; tt < 2; ++tt) {
-    uint4 cur[2][2];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      cur[hh][0] = raw[0][hh][0];
-      cur[hh][1] = raw[0][hh][1];
-      raw[0][hh][0] = raw[1][hh][0];
-      raw[0][hh][1] = raw[1][hh][1];
-    }
+  for (int tt = 0; tt < 2; ++tt) {
     const int tok = oc + 32 * tt;
-    float cs[8], sn[8];
-    token_cos_sin(p, tok, dl, cs, sn);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       uint4 ql, qh;
-      q_row_to_smem(qbuf, hh, tok, i, cur[hh][0], cur[hh][1], gl, gh, cs, sn, ql, qh);
+      q_row_to_smem(qbuf, hh, tok, i, raw[tt][hh][0], raw[tt][hh][1], gl, gh, cs[tt], sn[tt], ql, qh);
       if (qr0 != nullptr) {
         __nv_bfloat16* qr = qr0 + static_cast<size_t>(hh * kTok + 32 * tt) * kD;
         *reinterpret_cast<uint4*>(qr + dl) = ql;
@@ -355,37 +378,73 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx) {
   fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
   bar_sync(2, kSoftmaxThreads);
   if (threadIdx.x == 0) mbar_arrive(cx.bar(Lay<false>::B_QFULL));
-  if (own) {
-    // K rows: RMSNorm with the k_norm gain and RoPE; V rows as given; into cache rows
-    // Smax - 64 + t of head g
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gl);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gh);
-    const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
-#pragma unroll 1
-    for (int tt = 0; tt < 2; ++tt) {
-      uint4 cur[2][2];
+  if (!own) return;
+  // K rows: RMSNorm with the k_norm gain and RoPE; V rows as given; into cache rows Smax - 64 + t
+  // of head g, and (direct) into the own-row tile's K and V ring slots, row t in the swizzled
+  // layout the TMA would have produced (rows 64-127 of the slots are never read)
+  const bool direct = own_rows_direct(p, s);
+  const uint32_t n_tile = static_cast<uint32_t>(s.j1 - 1 - s.j0);  // CTA tile index of the own-row tile
+  const uint32_t kslot = cx.sbase + Lay<false>::SM_RING + (2 * n_tile) * Lay<false>::kSlot;
+  const uint32_t vslot = kslot + Lay<false>::kSlot;
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gl);
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gh);
+  const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        cur[h][0] = kv[0][h][0];
-        cur[h][1] = kv[0][h][1];
-        kv[0][h][0] = kv[1][h][0];
-        kv[0][h][1] = kv[1][h][1];
-      }
-      const int tok = oc + 32 * tt;
-      const size_t ro = tail + static_cast<size_t>(tok) * kD;
-      float cs[8], sn[8], xl[8], xh[8], yl[8], yh[8];
-      token_cos_sin(p, tok, dl, cs, sn);
-      unpack_bf16x8(cur[0][0], xl);
-      unpack_bf16x8(cur[0][1], xh);
-      norm_rope(xl, xh, gl, gh, cs, sn, yl, yh);
-      *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = pack8(yl, false);
-      *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = pack8(yh, false);
-      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = cur[1][0];
-      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = cur[1][1];
+  for (int tt = 0; tt < 2; ++tt) {
+    const int tok = oc + 32 * tt;
+    const size_t ro = tail + static_cast<size_t>(tok) * kD;
+    float xl[8], xh[8], yl[8], yh[8];
+    unpack_bf16x8(kv[tt][0][0], xl);
+    unpack_bf16x8(kv[tt][0][1], xh);
+    norm_rope(xl, xh, gl, gh, cs[tt], sn[tt], yl, yh);
+    const uint4 kl = pack8(yl, false), kh = pack8(yh, false);
+    *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = kl;
+    *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = kh;
+    *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = kv[tt][1][0];
+    *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = kv[tt][1][1];
+    if (direct) {
+      st_shared_v4(kslot + swz_off(tok, i, kAtomBytes), kl.x, kl.y, kl.z, kl.w);
+      st_shared_v4(kslot + swz_off(tok, i + 8, kAtomBytes), kh.x, kh.y, kh.z, kh.w);
+      const uint4 vl = kv[tt][1][0], vh = kv[tt][1][1];
+      st_shared_v4(vslot + swz_off(tok, i, kAtomBytes), vl.x, vl.y, vl.z, vl.w);
+      st_shared_v4(vslot + swz_off(tok, i + 8, kAtomBytes), vh.x, vh.y, vh.z, vh.w);
     }
+  }
+  if (direct) {
+    fence_proxy_async_smem();  // the slots are read by the tensor core (async proxy)
+    bar_sync(2, kSoftmaxThreads);
+    if (threadIdx.x == 0) {
+      mbar_arrive(cx.bar(Lay<false>::B_KVFULL + 2 * n_tile));
+      mbar_arrive(cx.bar(Lay<false>::B_KVFULL + 2 * n_tile + 1));
+    }
+  } else {
     fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
     bar_sync(2, kSoftmaxThreads);
     if (threadIdx.x == 0) mbar_arrive(cx.bar(Lay<false>::B_TAILRDY));
+  }
+}
+
+// Before the kernel waits for the preceding one (programmatic dependent launch), the producer
+// thread asks for the tensor maps of its first segment's layer and has L2 fetch that segment's
+// first cache tiles (at most kEarlyTiles; not the own-row tile, whose rows this kernel writes).
+// A prefetch reads nothing into the CTA, so a preceding kernel that writes those rows later
+// cannot make it wrong: the loads after the wait see the current rows.
+constexpr int kEarlyTiles = 3;
+template <bool F8, class PP>
+__device__ __noinline__ void early_prefetch(const PP& p, const Ctx& cx) {
+  long long t = cx.start;
+  Seg s;
+  if (!next_seg(t, cx.end, p.T, s)) return;
+  const int l = s.u / kHkv, g = s.u % kHkv;
+  prefetch_tensormap(&p.kmap[l]);
+  prefetch_tensormap(&p.vmap[l]);
+  for (int j = s.j0, k = 0; j < s.j1 && j < p.n_main && k < kEarlyTiles; ++j, ++k) {
+    tma_prefetch_3d(&p.kmap[l], 0, j * kKeyTile, g);
+    tma_prefetch_3d(&p.vmap[l], 0, j * kKeyTile, g);
+    if constexpr (!F8) {
+      tma_prefetch_3d(&p.kmap[l], 64, j * kKeyTile, g);
+      tma_prefetch_3d(&p.vmap[l], 64, j * kKeyTile, g);
+    }
   }
 }
 
@@ -402,6 +461,8 @@ __device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
   int hist_u[2] = {0, 0};  // units of the last two segments, by Q buffer
   int seg = 0, n_own = 0, cur_l = -1;
   float gql[8], gqh[8];
+  float ih[8], il[8];  // this thread's eight RoPE inverse frequencies, read once
+  load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
   bool ok = true;
   long long t = cx.start;
   Seg s;
@@ -478,7 +539,7 @@ __device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
           nx[kAhead - 1][hh][1] = *reinterpret_cast<const uint4*>(row + dh);
         }
         float cs[8], sn[8];
-        token_cos_sin(p, tok, dl, cs, sn);
+        token_cos_sin(p, tok, ih, il, cs, sn);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint4 ql, qh;
@@ -494,7 +555,7 @@ __device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
       bar_sync(1, kPrepThreads);
       if (px == 0) mbar_arrive(cx.bar(B_QFULL + qb));
     }
-    if (own && seg == 0) ++n_own;  // written by the softmax threads
+    if (own && seg == 0 && !own_rows_direct(p, s)) ++n_own;  // written by the softmax threads
     if (own && seg > 0) {
       // K rows: RMSNorm with the k_norm gain and RoPE; V rows: as given; both into cache rows
       // Smax - 64 + t of head g, which the producer then loads as the own-row tile
@@ -533,7 +594,7 @@ __device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
         nv[kAhead - 1][1] = *reinterpret_cast<const uint4*>(vsrc + rn + dh);
         const size_t ro = static_cast<size_t>(tok) * kD;
         float cs[8], sn[8], xl[8], xh[8], yl[8], yh[8];
-        token_cos_sin(p, tok, dl, cs, sn);
+        token_cos_sin(p, tok, ih, il, cs, sn);
         unpack_bf16x8(k0, xl);
         unpack_bf16x8(k1, xh);
         norm_rope(xl, xh, gkl, gkh, cs, sn, yl, yh);
@@ -1209,12 +1270,18 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + LY::SM_TMEM);
+  // Work that reads nothing a preceding kernel writes, done while it may still run.
+  float fcs[2][8], fsn[2][8];
+  if (warp == 8 && lane == 0) early_prefetch<F8>(p, cx);
+  if constexpr (!F8) {
+    if (warp < 8) first_angles(p, fcs, fsn);
+  }
   // Everything below reads what earlier kernels in the stream wrote (layer inputs, caches; e4m3:
   // the prologue's staged Q and own rows).
   pdl_wait_primary();
 
   if (warp < 8) {
-    if constexpr (!F8) first_q_prep(p, cx);
+    if constexpr (!F8) first_q_prep(p, cx, fcs, fsn);
     softmax_warps<F8>(p, cx);
   } else if (warp == 8) {
     if (lane == 0) producer<F8>(p, cx);

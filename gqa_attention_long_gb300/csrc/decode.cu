@@ -187,7 +187,10 @@ __device__ __forceinline__ void segment_prologue(const DecodeParams<CAP>& p, uin
   const uint4 ml = *reinterpret_cast<const uint4*>(gam + dl), mh = *reinterpret_cast<const uint4*>(gam + dh);
   float cs[8], sn[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_pos, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[e], sn[e]);
+  float ih[8], il[8];
+  load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rope_cos_sin(p.rope_pos, ih[e], il[e], cs[e], sn[e]);
   float xl[8], xh[8], gl[8], gh[8], yl[8], yh[8];
   unpack_bf16x8(rl, xl);
   unpack_bf16x8(rh, xh);

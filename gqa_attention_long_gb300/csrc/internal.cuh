@@ -99,8 +99,10 @@ struct PrologueLayer {
 template <int CAP>
 struct PrologueParams {
   PrologueLayer layer[CAP];
-  float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
-  float inv_lo[kD / 2];
+  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo (16-byte aligned: a thread
+  // reads its eight as two 16-byte vectors)
+  alignas(16) float inv_hi[kD / 2];
+  alignas(16) float inv_lo[kD / 2];
   uint8_t* q_ws;   // FP8: staged roped Q codes (bf16: null, nothing staged)
   float* q_scale;  // FP8: [unit][128] scale of each e4m3 Q row
   float* sv_ref;   // FP8: [unit] reference V scale
@@ -122,8 +124,10 @@ struct AttnParams {
   __nv_bfloat16* q_rope[CAP];  // optional
   __nv_bfloat16* kc[CAP];      // the caches, whose rows [Smax-64, Smax) the kernel writes
   __nv_bfloat16* vc[CAP];
-  float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
-  float inv_lo[kD / 2];
+  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo (16-byte aligned: a thread
+  // reads its eight as two 16-byte vectors)
+  alignas(16) float inv_hi[kD / 2];
+  alignas(16) float inv_lo[kD / 2];
   int rope_base;         // S + rope_delta: token t sits at position rope_base + t
   __nv_bfloat16* out[CAP];
   const float* ks[CAP];      // FP8: block scales [8][Smax/128 + 1] (else null)
@@ -164,8 +168,10 @@ struct DecodeParams {
   __nv_bfloat16* kc[CAP];  // caches [8][Smax][128]; the kernel writes row pos
   __nv_bfloat16* vc[CAP];
   __nv_bfloat16* out[CAP];  // [64][128]
-  float inv_hi[kD / 2];  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo
-  float inv_lo[kD / 2];
+  // RoPE inverse frequencies theta^(-j/64) as an fp32 pair hi + lo (16-byte aligned: a thread
+  // reads its eight as two 16-byte vectors)
+  alignas(16) float inv_hi[kD / 2];
+  alignas(16) float inv_lo[kD / 2];
   float* part_o;         // [n_ctas][2 slots][8 heads][128] unnormalised partial outputs
   float* part_ml;        // [n_ctas][2 slots][8 heads][2]: running max (log2 units) and sum
   uint32_t* unit_cnt;    // [unit]: parts that have written their partial (zero between calls)

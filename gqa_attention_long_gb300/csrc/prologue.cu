@@ -155,11 +155,13 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
 
   // cos/sin of this thread's tokens at its eight frequencies (the same in every unit)
   float cs[TPO][8], sn[TPO][8];
+  float ih[8], il[8];
+  load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
 #pragma unroll
   for (int tt = 0; tt < TPO; ++tt) {
     const int pos = t0 + oc + 32 * tt + p.rope_delta + p.S;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rope_cos_sin(pos, p.inv_hi[dl + e], p.inv_lo[dl + e], cs[tt][e], sn[tt][e]);
+    for (int e = 0; e < 8; ++e) rope_cos_sin(pos, ih[e], il[e], cs[tt][e], sn[tt][e]);
   }
 
   float gql[8], gqh[8], gkl[8], gkh[8];

@@ -222,6 +222,13 @@ __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int c0, int c1
                "r"(c0), "r"(c1)
                : "memory");
 }
+// Prefetch of one 3-D box of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 // 3-D tiled TMA load into shared memory, completing `bar`'s transaction count.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
                                             int c1, int c2, uint64_t policy) {

@@ -33,6 +33,17 @@ __device__ __forceinline__ void rope_cos_sin(int pos, float inv_hi, float inv_lo
   __sincosf(r, &s, &c);
 }
 
+// The eight inverse frequencies [dl, dl + 8) of the RoPE table (hi and lo parts), read as
+// 16-byte vectors (dl a multiple of 8). The lanes of a warp read different entries, so that one
+// vector read per four values keeps the table traffic low.
+__device__ __forceinline__ void load_inv8(const float* hi, const float* lo, int dl, float (&ih)[8],
+                                          float (&il)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(hi + dl), b = *reinterpret_cast<const float4*>(hi + dl + 4);
+  const float4 c = *reinterpret_cast<const float4*>(lo + dl), d = *reinterpret_cast<const float4*>(lo + dl + 4);
+  ih[0] = a.x; ih[1] = a.y; ih[2] = a.z; ih[3] = a.w; ih[4] = b.x; ih[5] = b.y; ih[6] = b.z; ih[7] = b.w;
+  il[0] = c.x; il[1] = c.y; il[2] = c.z; il[3] = c.w; il[4] = d.x; il[5] = d.y; il[6] = d.z; il[7] = d.w;
+}
+
 __device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&x)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
