@@ -254,6 +254,39 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_e4m3_step(args, ea, dev, rank: int, world: int) -> None:
+    """The step over e4m3 caches alone (caches quantised on the device by the library): warm-up,
+    then K timed steps; prints a short JSON line. A target for profilers, not the bench line."""
+    S, Smax, n = args.S, args.Smax, args.layers
+    ncol = Smax // 128 + 1
+    L8 = []
+    for l in range(n):
+        x = layer_inputs_on_device(config_seed(4, l) + 100000 * rank, S, Smax, dev)
+        kq = torch.empty(HKV, Smax, D, dtype=torch.uint8, device=dev)
+        vq = torch.empty(HKV, Smax, D, dtype=torch.uint8, device=dev)
+        ks = torch.empty(HKV, ncol, dtype=torch.float32, device=dev)
+        vs = torch.empty(HKV, ncol, dtype=torch.float32, device=dev)
+        ea.expert_attn_quantize_cache(x.k_cache, S, Smax, kq, ks)
+        ea.expert_attn_quantize_cache(x.v_cache, S, Smax, vq, vs)
+        L8.append(ea.LayerBuffers(q_raw=x.q_raw, k_raw=x.k_raw, v_raw=x.v_raw, q_gamma=x.q_gamma,
+                                  k_gamma=x.k_gamma, k_cache=kq, v_cache=vq, k_scale=ks, v_scale=vs,
+                                  out=torch.empty(HQ, T, D, dtype=torch.bfloat16, device=dev)))
+        del x
+    ws8 = ea.alloc_workspace(n, Smax, ea.EA_KV_FP8_E4M3)
+    arr8 = ea.make_args(L8, Smax, ea.EA_KV_FP8_E4M3)
+    ea.expert_attn_set_splits(args.splits)
+    stream = torch.cuda.current_stream()
+    ms = time_calls(lambda: ea.expert_attn_layers(L8, S, Smax, 0, ea.EA_KV_FP8_E4M3, ws8, stream, _arr=arr8),
+                    args.warmup, args.steps, stream)
+    st, bits = ea.expert_attn_read_status(ws8)
+    if st != 0:
+        raise RuntimeError(f"e4m3 kernel status bits {bits:#x}")
+    b8 = algo_bytes_per_layer_fp8(S) * n
+    if rank == 0:
+        print(json.dumps({"workload": f"{n}-layer step, S={S}, Smax={Smax}, e4m3 cache", "us_per_layer": ms * 1e3 / n,
+                          "ms_per_step": ms, "step_hbm_gbs": b8 / (ms * 1e-3) / 1e9}), flush=True)
+
+
 def workload_config(args) -> dict:
     return {"workload": f"{args.layers}-layer Euler step of expert attention, S={args.S}, Smax={args.Smax}, bf16 KV cache",
             "layers": args.layers, "S": args.S, "Smax": args.Smax, "q_heads": HQ, "kv_heads": HKV,
@@ -273,6 +306,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the FP8 and single-layer extras")
     ap.add_argument("--splits", type=int, default=0, help="attention CTAs (0 = one per SM)")
+    ap.add_argument("--kv", choices=["bf16", "e4m3"], default="bf16",
+                    help="e4m3: time only the step over e4m3 caches (a profiling target; no extras)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_setup(args.gpus)
@@ -284,6 +319,9 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     S, Smax, n = args.S, args.Smax, args.layers
+    if args.kv == "e4m3":
+        run_e4m3_step(args, ea, dev, rank, world)
+        return
     xs = [layer_inputs_on_device(config_seed(4, l) + 100000 * rank, S, Smax, dev) for l in range(n)]
     # the step's activations (raw q, k, v of every layer) and outputs live in one buffer each, so
     # that the end-to-end path moves them with one host->device and one device->host copy
