@@ -76,7 +76,8 @@ typedef struct {
   void* q_rope;   /* optional, may be NULL */
 } ea_layer_args;
 
-/* Bytes of device workspace needed by a call over n_layers layers of the given cache dtype on
+/* Utility (no counterpart on the pages). Bytes of device workspace needed by a call over
+ * n_layers layers of the given cache dtype on
  * the current device (0 if no suitable device is present; an e4m3 workspace also serves bf16
  * calls). The workspace must be 256-byte aligned and, before
  * its first use, cleared with expert_attn_workspace_init. */
@@ -138,8 +139,10 @@ int expert_attn_quantize_cache(const void* src_bf16, int n_rows, int Smax, void*
 int expert_attn_quantize_cache_mxfp4(const void* src_bf16, int n_rows, int Smax, void* dst_codes,
                                      void* dst_scales, ea_stream_t stream);
 
-/* Tuning knob: number of persistent attention CTAs (0 = one per SM, the default). Values above
- * the SM count are clamped. Process-wide. Returns the previous setting. */
+/* Utility (no counterpart on the pages). Tuning knob: number of persistent attention CTAs
+ * (0 = one per SM, the default). Values above the SM count are clamped. The setting is
+ * process-wide, not per stream or per thread: a call made on one thread changes the plan of
+ * calls launched afterwards from every thread. Returns the previous setting. */
 int expert_attn_set_splits(int n_ctas_or_0_for_auto);
 
 /* Synchronises the stream and returns the status recorded in the workspace by the kernels
@@ -147,7 +150,7 @@ int expert_attn_set_splits(int n_ctas_or_0_for_auto);
 int expert_attn_read_status(const void* workspace, ea_stream_t stream, int* status_out,
                             uint32_t* bits_out);
 
-/* A static string naming a status code. */
+/* Utility (no counterpart on the pages). A static string naming a status code. */
 const char* expert_attn_status_string(int status);
 
 /* Failure-detection self-test (the pages have no counterpart): launches one CTA on the stream
