@@ -186,7 +186,6 @@ __device__ __forceinline__ void segment_prologue(const DecodeParams<CAP>& p, uin
   const uint4 rl = *reinterpret_cast<const uint4*>(row + dl), rh = *reinterpret_cast<const uint4*>(row + dh);
   const uint4 ml = *reinterpret_cast<const uint4*>(gam + dl), mh = *reinterpret_cast<const uint4*>(gam + dh);
   float cs[8], sn[8];
-#pragma unroll
   float ih[8], il[8];
   load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
 #pragma unroll
