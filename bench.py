@@ -56,8 +56,8 @@ def algo_bytes_per_layer_fp8(S: int) -> int:
 
 def launches_per_call(n_layers: int, S: int, sm_count: int, kv_dtype: int = 0) -> int:
     """Kernels one expert_attn_layers call launches (the library's own plan, mirrored on the
-    host: bf16 attention kernel, plus the merge kernel when a split unit has more than two
-    parts; an e4m3 cache adds the prologue kernel)."""
+    host: the attention kernel per 64 layers, which merges its split units itself; an e4m3
+    cache adds the prologue kernel)."""
     return kernels_per_call(n_layers, S, sm_count, kv_dtype)
 
 
@@ -376,8 +376,8 @@ def main():
     us_layer = ms_step * 1e3 / (n * world)
 
     # ---- dominant kernel (attention) timed on its own with events between the kernels; with a
-    # bf16 cache it is the whole layer (no prologue kernel; no merge kernel when every split
-    # unit has two parts), so its algorithmic bytes are the layer's
+    # bf16 cache it is the whole layer (no prologue kernel, and it merges its split units
+    # itself), so its algorithmic bytes are the layer's
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for e in evs:  # torch creates the CUDA event on first record
         for x in e:
@@ -386,12 +386,10 @@ def main():
         ea.expert_attn_layers_profiled(Ls, S, Smax, 0, ea.EA_KV_BF16, ws, evs[i], stream, _arr=arr)
     torch.cuda.synchronize()
     k2 = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     peaks = load_peaks()
     k2_bytes = algo_bytes_per_layer(S) * n
     achieved = k2_bytes / (k2 * 1e-3) / 1e9
     traffic = attention_traffic(S, Smax, n)
-    merge_launched = launches_per_call(n, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1
 
     # ---- end to end through the C ABI with host buffers: every step copies its raw q/k/v in from
     # pinned host memory, runs the step and copies its outputs back. Two device buffer sets and
@@ -713,7 +711,7 @@ def main():
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "attention_kernel", "peak_src": peaks["src"],
                          "bytes_per_launch": k2_bytes, "ms_per_launch": k2},
-            "kernels_ms": {"attention": k2, "merge": k3 if merge_launched else None},
+            "kernels_ms": {"attention": k2},
             "clocks": clocks,
             "e2e": {"value": e2e_ms * 1e3 / (n * world), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,

@@ -234,7 +234,7 @@ def expert_attn_quantize_cache_mxfp4(src: torch.Tensor, n_rows: int, Smax: int, 
 
 def split_units(n_layers: int, S: int, n_ctas: int) -> list[int]:
     """Units (layer * 8 + kv head) whose key tiles the attention kernel's partition cuts between
-    CTAs, i.e. the units the merge kernel combines; the same plan the library makes for a chunk
+    CTAs, i.e. the units the attention kernel merges; the same plan the library makes for a chunk
     of n_layers (<= 64) layers on n_ctas persistent CTAs (capped by the number of key tiles).
     Host-side planning only (no GPU): used to count launches and by tests."""
     T = (S + 127) // 128 + 1
@@ -268,15 +268,11 @@ def split_parts(n_layers: int, S: int, n_ctas: int) -> list[tuple[int, int]]:
 
 def kernels_per_call(n_layers: int, S: int, n_ctas: int, kv_dtype: int = EA_KV_BF16) -> int:
     """Kernels one expert_attn_layers call launches: per chunk of 64 layers the prologue kernel
-    (e4m3 cache only; the bf16 attention kernel does its own prologue), the attention kernel and,
-    when a split unit has more than two parts, the merge kernel (two-part units are merged inside
-    the attention kernel)."""
+    (e4m3 cache only; the bf16 attention kernel does its own prologue) and the attention kernel,
+    which also merges the units that its CTA partition splits."""
     total = 0
     for l0 in range(0, n_layers, 64):
-        n = min(64, n_layers - l0)
-        parts = split_parts(n, S, n_ctas)
         total += (1 if kv_dtype == EA_KV_FP8_E4M3 else 0) + 1
-        total += 1 if parts and any(k != 2 for _, k in parts) else 0
     return total
 
 

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libexpert_attn.so")
-SOURCES = ["prologue.cu", "attention.cu", "merge.cu", "quantize.cu", "linear.cu", "decode.cu", "api.cu"]
+SOURCES = ["prologue.cu", "attention.cu", "quantize.cu", "linear.cu", "decode.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -1,8 +1,7 @@
 // api.cu — host side of libexpert_attn.so: argument validation, launch planning, TMA tensor-map
 // encoding (cached), workspace layout and the launches per chunk of layers (e4m3 cache: the
-// prologue kernel; the attention kernel, which does the bf16 prologue itself; the log-sum-exp
-// merge of the split units when the attention kernel does not merge them) chained with
-// programmatic dependent launch.
+// prologue kernel; the attention kernel, which does the bf16 prologue itself and merges the split
+// units), chained with programmatic dependent launch.
 // See include/expert_attn.h for the contract.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -24,8 +23,6 @@ cudaError_t prologue_set_attributes();
 cudaError_t attention_set_attributes();
 template <int CAP>
 cudaError_t launch_attention_kernel(const AttnParams<CAP>& ap, bool f8, cudaLaunchConfig_t cfg);
-template <int CAP>
-cudaError_t launch_merge_kernel(const MergeParams<CAP>& mp, cudaLaunchConfig_t cfg);
 cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* src, uint8_t* codes, uint8_t* scales, int n_rows,
                                   int Smax, cudaStream_t stream);
 __global__ void quantize_cache_kernel(const __nv_bfloat16* src, uint8_t* dst, float* scales,
@@ -292,12 +289,11 @@ int launch_prologue(const ea_layer_args* a, int n, int S, int Smax, int rope_del
                                                       st, pdl);
 }
 
-// Attention parameter blocks are large (~19 KB at full capacity): kept off the stack, one per
+// Attention parameter blocks are large (~25 KB at full capacity): kept off the stack, one per
 // capacity, guarded by their own mutex.
 template <int CAP>
 struct LaunchBlocks {
   AttnParams<CAP> ap;
-  MergeParams<CAP> mp;
   std::mutex mu;
 };
 template <int CAP>
@@ -358,17 +354,17 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
   const int n_ctas = n_ctas_for(ap.W, di.sm_count);
 
   // Units cut by a CTA boundary (each listed once, in order). When every one of them has two
-  // parts, the attention kernel merges them itself; otherwise K3 does.
-  MergeParams<CAP>& mp = lb.mp;
-  mp.n_split = 0;
+  // parts, the part that finishes second merges them inside the attention kernel; otherwise the
+  // whole grid merges them after a grid-wide arrival count (see the kernel).
+  ap.n_split = 0;
   bool all_two = true;
   for (int b = 1; b < n_ctas; ++b) {
     const long long tb = cta_tile_start(b, ap.W, n_ctas);
     if (tb % ap.T == 0) continue;
     const int u = static_cast<int>(tb / ap.T);
-    if (mp.n_split > 0 && mp.unit[mp.n_split - 1].u == u) continue;
+    if (ap.n_split > 0 && ap.split[ap.n_split - 1].u == u) continue;
     const long long first = static_cast<long long>(u) * ap.T;
-    SplitUnit& su = mp.unit[mp.n_split++];
+    SplitUnit& su = ap.split[ap.n_split++];
     su.u = u;
     su.c0 = static_cast<short>(cta_of_tile(first, ap.W, n_ctas));
     su.nparts = static_cast<short>(cta_of_tile(first + ap.T - 1, ap.W, n_ctas) - su.c0 + 1);
@@ -376,6 +372,8 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
     all_two = all_two && su.nparts == 2;
   }
   ap.fused_merge = all_two ? 1 : 0;
+  ap.grid_merge = ap.n_split > 0 && !all_two ? 1 : 0;
+  ap.grid_sync = reinterpret_cast<uint32_t*>(ws) + 1;  // words 1 and 2 of the status block
 
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(st, attr, pdl);
@@ -385,16 +383,6 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
     return EA_ERR_CUDA;
   }
   if (ev && ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return EA_ERR_CUDA;
-
-  if (mp.n_split > 0 && !ap.fused_merge) {
-    for (int l = 0; l < n; ++l) mp.out[l] = ap.out[l];
-    mp.part_o = ap.part_o;
-    mp.part_lse = ap.part_lse;
-    if (launch_merge_kernel<CAP>(mp, launch_config(st, attr, pdl)) != cudaSuccess) {
-      cudaGetLastError();
-      return EA_ERR_CUDA;
-    }
-  }
   if (ev && ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return EA_ERR_CUDA;
   return EA_OK;
 }
@@ -617,9 +605,10 @@ extern "C" int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_lay
   uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch(dev));
   if (ws == nullptr) return EA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the in-kernel merge words start at 0; the status word (the first 4 bytes) is left alone, so
-  // that a timeout stays visible until expert_attn_noalloc_read_status reads and clears it
-  if (cudaMemsetAsync(ws + wl.sync_off, 0, wl.qscale_off - wl.sync_off, st) != cudaSuccess) {
+  // the in-kernel merge words and the grid-merge counts start at 0; the status word (the first 4
+  // bytes) is left alone, so that a timeout stays visible until expert_attn_noalloc_read_status
+  // reads and clears it
+  if (cudaMemsetAsync(ws + sizeof(uint32_t), 0, wl.qscale_off - sizeof(uint32_t), st) != cudaSuccess) {
     cudaGetLastError();
     return EA_ERR_CUDA;
   }

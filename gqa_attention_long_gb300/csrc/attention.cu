@@ -44,6 +44,7 @@
 // copies of V), barriers, a 1.5 KB row-statistics exchange.
 // TMEM: 512 columns (two 128-column score/P buffers, two 128-column fp32 accumulators).
 #include "internal.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 #include "rope.cuh"
 
@@ -1218,6 +1219,57 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
   }
 }
 
+// ------------------------------------------------------------------------- grid-wide merge
+// Units cut into more than two parts (a single layer spread over every SM) are merged by the
+// grid itself once every CTA has written its partials: each CTA counts its arrival (after a
+// GPU-scope fence on its partial stores), one thread waits, bounded, until all CTAs have arrived,
+// and then the CTA merges its share of the split units' (unit, 4-column chunk) pairs, three
+// pairs at a time (128 threads, one per folded row, per pair). The grid has one CTA per SM at
+// most, so every CTA is resident or becomes so as soon as an earlier kernel frees its SM (a
+// kernel launched after this one cannot start before every CTA of this grid has started). The
+// last CTA to leave resets both counters.
+template <bool F8, class PP>
+__device__ __noinline__ void grid_merge(const PP& p, const Ctx& cx) {
+  EA_LAYOUT_ALIASES;
+  volatile uint32_t* go = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_ROLE);
+  __threadfence();  // this thread's partial stores, visible at GPU scope before the count
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(p.grid_sync, 1u);
+    const uint64_t t0 = globaltimer_ns();
+    bool ok = false;
+    for (uint32_t it = 0; it < 0x80000000u; ++it) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.grid_sync) : "memory");
+      if (v >= gridDim.x) {
+        ok = true;
+        break;
+      }
+      if ((it & 15u) == 15u && globaltimer_ns() - t0 > kWaitLimitNs) break;
+      __nanosleep(64);
+    }
+    if (!ok) atomicOr(p.status, kErrMergeWait);
+    __threadfence();
+    *go = ok ? 1u : 0u;
+  }
+  __syncthreads();
+  if (*go != 0u) {
+    const int P = p.n_split * kPartChunks;
+    const int c0 = static_cast<int>(static_cast<long long>(blockIdx.x) * P / gridDim.x);
+    const int c1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * P / gridDim.x);
+    for (int pi = c0 + static_cast<int>(threadIdx.x) / kRows; pi < c1; pi += kThreads / kRows) {
+      const SplitUnit su = p.split[pi / kPartChunks];
+      merge_row_chunk<24>(p.part_o, p.part_lse, su, pi % kPartChunks, threadIdx.x % kRows,
+                          p.out[su.u / kHkv]);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(p.grid_sync + 1, 1u) == gridDim.x - 1) {
+    p.grid_sync[0] = 0u;  // every CTA has passed the wait
+    p.grid_sync[1] = 0u;
+  }
+}
+
 }  // namespace attn
 
 // ------------------------------------------------------------------------------------ kernel
@@ -1297,6 +1349,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 9) tmem_dealloc(cx.tmem, kTmemCols);
+  if (p.grid_merge) grid_merge<F8>(p, cx);
 }
 
 // Host side: attributes and launch of the four instances (kept in this file, where the kernel

@@ -47,7 +47,8 @@ enum : uint32_t {
 };
 
 // ------------------------------------------------------------------------- workspace layout
-//   [0, 1024)                    status word (first 4 bytes), rest reserved
+//   [0, 1024)                    status word (bytes 0-3); grid-merge arrival and departure
+//                                 counts (bytes 4-11, zero between calls); rest reserved
 //   sync    n_layers * 8 * 2 uint32  per unit: arrival count and partial-ready flag of the
 //                                   in-kernel merge of two-part units (zero between calls)
 //   qscale  n_layers * 8 * 128 fp32    FP8 only: per-row scale of the e4m3 roped Q
@@ -111,6 +112,18 @@ struct PrologueParams {
   int n_layers, S, Smax, rope_delta, fp8;
 };
 
+// Units split across CTAs (at most one per CTA boundary), merged after the attention grid.
+constexpr int kMaxSplitUnits = 256;
+
+// One split unit: its parts are CTAs c0 .. c0 + nparts - 1; the partial of CTA c sits in slot
+// 2 c + 0, except the first CTA's, which sits in slot 2 c0 + slot0 (1 when the unit is that
+// CTA's last segment, its range having started in an earlier unit).
+struct SplitUnit {
+  int u;
+  short c0, nparts;
+  int slot0;
+};
+
 template <int CAP>
 struct AttnParams {
   CUtensorMap kmap[CAP];  // all Smax rows of K: dims {128, Smax, 8}, box {64 (e4m3: 128), 128, 1}
@@ -146,6 +159,13 @@ struct AttnParams {
   int ncol;            // FP8: scale columns per kv head, Smax/128 + 1 (the last one: own rows)
   int fused_merge;     // every split unit has two parts: the second one merges in-kernel
   float scale_log2;    // log2(e) / sqrt(128)
+  // Units of more than two parts (one layer spread over every SM) are merged by the whole grid
+  // after a grid-wide arrival count: grid_sync[0] counts arrivals, grid_sync[1] departures (both
+  // zero between calls: the last CTA to leave resets them).
+  uint32_t* grid_sync;
+  int grid_merge;      // 1 when some unit has more than two parts
+  int n_split;         // the split units, in order
+  SplitUnit split[kMaxSplitUnits];
 };
 
 // ------------------------------------------------------------ text-model decode attention
@@ -232,26 +252,6 @@ struct LinearParams {
   int mode;
 };
 
-// Units split across CTAs, merged by the LSE merge kernel: at most one per CTA boundary.
-constexpr int kMaxSplitUnits = 256;
-
-// One split unit: its parts are CTAs c0 .. c0 + nparts - 1; the partial of CTA c sits in slot
-// 2 c + 0, except the first CTA's, which sits in slot 2 c0 + slot0 (1 when the unit is that
-// CTA's last segment, its range having started in an earlier unit).
-struct SplitUnit {
-  int u;
-  short c0, nparts;
-  int slot0;
-};
-
-template <int CAP>
-struct MergeParams {
-  __nv_bfloat16* out[CAP];
-  const float* part_o;
-  const float* part_lse;
-  int n_split;
-  SplitUnit unit[kMaxSplitUnits];  // the split units, in order
-};
 
 // The key tiles of all (layer, kv head) units, in unit-major order, are cut into n_ctas
 // contiguous ranges; CTA c owns tiles [c*W/n, (c+1)*W/n).

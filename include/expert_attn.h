@@ -98,24 +98,25 @@ int expert_attn_prologue(const ea_layer_args* a, int S, int Smax, int rope_delta
 
 /* Steps 1-3 for one layer (the unit TTExpert.layer_fn can hand to a fused kernel): split-KV
  * attention on the tensor cores, whose kernel also does steps 1 and 2 for a bf16 cache (an e4m3
- * cache runs the prologue kernel first), then the log-sum-exp merge of the key ranges that were
- * split across SMs over more than two CTAs; writes a->out and, if not NULL, a->q_rope. */
+ * cache runs the prologue kernel first) and the log-sum-exp merge of the key ranges that it
+ * split across SMs; writes a->out and, if not NULL, a->q_rope. */
 int expert_attn_layer(const ea_layer_args* a, int S, int Smax, int rope_delta, int kv_dtype,
                       void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* Steps 1-3 for n_layers independent layers in one call (the 64 layers of one Euler step,
  * alpamayo_tt/expert.py, TTExpert._forward_dev), all with the same S, Smax and rope_delta.
  * layers is a HOST array of n_layers entries. Per 64 layers it launches the attention kernel,
- * after the prologue kernel for an e4m3 cache and before the merge kernel when some unit is
- * split over more than two CTAs (two-part units are merged inside the attention kernel). */
+ * after the prologue kernel for an e4m3 cache; the attention kernel merges the units it splits
+ * across CTAs itself (two-part units in the epilogue of the part that finishes second, units of
+ * more parts across the whole grid once every CTA has written its partials). */
 int expert_attn_layers(const ea_layer_args* layers, int n_layers, int S, int Smax, int rope_delta,
                        int kv_dtype, void* workspace, size_t ws_bytes, ea_stream_t stream);
 
 /* As expert_attn_layers, and records four cudaEvent_t (passed as void*, each may be NULL) on
  * the stream, around the first 64 layers: before the prologue kernel, before the attention
  * kernel (right after the first event for a bf16 cache, which has no prologue kernel), after
- * it, and after the merge kernel. Recording events between the kernels removes their launch
- * overlap; use it to time the kernels. */
+ * it, and a fourth right after the third (no kernel follows the attention kernel). Recording
+ * events between the kernels removes their launch overlap; use it to time the kernels. */
 int expert_attn_layers_profiled(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                 int rope_delta, int kv_dtype, void* workspace, size_t ws_bytes,
                                 ea_stream_t stream, void* const events[4]);
@@ -240,7 +241,7 @@ size_t expert_decoder_layer_workspace_size(int hidden, int inter);
 
 /* One decoder layer (see above): the two RMSNorm kernels, four projections on the tensor cores
  * (each also applies its epilogue: head split, residual add or SwiGLU), and the attention
- * kernel (followed by its merge kernel when a unit is split over more than two CTAs). */
+ * kernel. */
 int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int rope_delta,
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 

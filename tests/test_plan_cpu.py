@@ -1,6 +1,7 @@
 """Host-side launch planning (no GPU): the list of units that the attention kernel's partition
-cuts between CTAs, which the merge kernel combines, checked against a brute-force count of the
-CTAs whose tile range meets each unit."""
+cuts between CTAs, which the kernel merges (in the epilogue for two-part units, across the grid
+for more parts), checked against a brute-force count of the CTAs whose tile range meets each
+unit."""
 import random
 
 import pytest
@@ -41,7 +42,7 @@ def test_split_units_random():
 
 
 def test_single_layer_splits_every_unit():
-    # one layer over all 152 SMs: every (kv head) unit spans ~19 CTAs and needs the merge
+    # one layer over all 152 SMs: every (kv head) unit spans ~19 CTAs and needs the grid merge
     assert split_units(1, 4700, 152) == list(range(8))
 
 
@@ -53,11 +54,13 @@ def test_split_parts_random():
 
 
 def test_kernel_count():
-    # 64 layers at S=4700 on 152 SMs: every split unit has two parts (merged in the attention
-    # kernel), so a bf16 call is one kernel and an e4m3 call two (with the prologue)
+    # the attention kernel merges every split unit itself (two-part units in the epilogue, units
+    # of more parts across the grid), so a bf16 call is one kernel per 64 layers and an e4m3 call
+    # two (with the prologue)
     assert all(k == 2 for _, k in split_parts(64, 4700, 152))
     assert kernels_per_call(64, 4700, 152, EA_KV_BF16) == 1
     assert kernels_per_call(64, 4700, 152, EA_KV_FP8_E4M3) == 2
-    # one layer over 152 SMs: ~19 parts per unit, so the merge kernel runs
-    assert kernels_per_call(1, 4700, 152, EA_KV_BF16) == 2
+    assert all(k > 2 for _, k in split_parts(1, 4700, 152))
+    assert kernels_per_call(1, 4700, 152, EA_KV_BF16) == 1
+    assert kernels_per_call(1, 4700, 152, EA_KV_FP8_E4M3) == 2
     assert kernels_per_call(128, 4700, 152, EA_KV_BF16) == 2
