@@ -148,7 +148,7 @@ __device__ __forceinline__ bool own_rows_direct(const PP& p, const Seg& first) {
 
 // ------------------------------------------------------------------------------- producer
 template <bool F8, class PP>
-__device__ __noinline__ void producer(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void producer(const PP& p, const Ctx cx) {
   EA_LAYOUT_ALIASES;
   pdl_wait_primary();  // e4m3: roped Q and the cache's own rows are written by the prologue kernel
   const uint64_t pol_stream = l2_policy_evict_first();  // cache tiles are read exactly once
@@ -229,7 +229,7 @@ __device__ __forceinline__ bool drain_staged(const PP& p, const Ctx& cx, int sg,
 // One thread brings each segment's roped e4m3 Q (high and low codes, written by the prologue
 // kernel) into one of the two Q buffers, one segment ahead.
 template <bool F8, class PP>
-__device__ __noinline__ void q_loader(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void q_loader(const PP& p, const Ctx cx) {
   EA_LAYOUT_ALIASES;
   const uint64_t pol_keep = l2_policy_evict_last();
   int seg = 0;
@@ -323,7 +323,7 @@ __device__ __forceinline__ void first_angles(const PP& p, float (&cs)[2][8], flo
 // into the two ring slots of that tile as well (KVFULL; no fetch back), else TAILRDY for the
 // producer to fetch them. A CTA's first segment can be short, so its own rows are needed early.
 template <class PP>
-__device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx, const float (&cs)[2][8],
+__device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const float (&cs)[2][8],
                                           const float (&sn)[2][8]) {
   long long t = cx.start;
   Seg s;
@@ -344,6 +344,7 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx, const floa
       raw[tt][hh][1] = *reinterpret_cast<const uint4*>(row + dh);
     }
   uint4 kv[2][2][2];  // [token][k, v][lo, hi]
+  uint4 kg[2];        // k_norm gain, channels [8i, 8i + 8) and [64 + 8i, 64 + 8i + 8)
   const size_t unit_rows = static_cast<size_t>(g) * kTok * kD;
   if (own) {
 #pragma unroll
@@ -354,6 +355,8 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx, const floa
       kv[tt][1][0] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dl);
       kv[tt][1][1] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dh);
     }
+    kg[0] = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dl);
+    kg[1] = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dh);
   }
   float gl[8], gh[8];
   unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gl);
@@ -387,8 +390,8 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx, const floa
   const uint32_t n_tile = static_cast<uint32_t>(s.j1 - 1 - s.j0);  // CTA tile index of the own-row tile
   const uint32_t kslot = cx.sbase + Lay<false>::SM_RING + (2 * n_tile) * Lay<false>::kSlot;
   const uint32_t vslot = kslot + Lay<false>::kSlot;
-  unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dl), gl);
-  unpack_bf16x8(*reinterpret_cast<const uint4*>(p.k_gamma[l] + dh), gh);
+  unpack_bf16x8(kg[0], gl);
+  unpack_bf16x8(kg[1], gh);
   const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
 #pragma unroll
   for (int tt = 0; tt < 2; ++tt) {
@@ -425,14 +428,35 @@ __device__ __noinline__ void first_q_prep(const PP& p, const Ctx& cx, const floa
   }
 }
 
-// Before the kernel waits for the preceding one (programmatic dependent launch), the producer
-// thread asks for the tensor maps of its first segment's layer and has L2 fetch that segment's
-// first cache tiles (at most kEarlyTiles; not the own-row tile, whose rows this kernel writes).
-// A prefetch reads nothing into the CTA, so a preceding kernel that writes those rows later
-// cannot make it wrong: the loads after the wait see the current rows.
+// Before the kernel waits for the preceding one (programmatic dependent launch), one thread
+// asks for the tensor maps of its first segment's layer and has L2 fetch that segment's first
+// cache tiles (at most kEarlyTiles; not the own-row tile, whose rows this kernel writes). A
+// prefetch reads nothing into the CTA, so a preceding kernel that writes those rows later cannot
+// make it wrong: the loads after the wait see the current rows. The thread is not the producer,
+// which would otherwise reach its first load only once these requests are accepted.
 constexpr int kEarlyTiles = 3;
+
+// bf16, before the wait as well: L2 fetch of the layer inputs that the first segment's
+// preparation reads right after it, requested ahead of the cache tiles so that those loads do
+// not queue behind the tiles: the unit's q rows (both heads, 32 KB contiguous), the q gain and,
+// when the segment holds the unit's own-row tile, its raw k and v rows (16 KB each) and the k
+// gain. The preceding kernel may still be writing them; its writes land in L2 as well.
+template <class PP>
+__device__ __noinline__ void early_inputs(const PP& p, const Ctx cx) {
+  long long t = cx.start;
+  Seg s;
+  if (!next_seg(t, cx.end, p.T, s)) return;
+  const int l = s.u / kHkv, g = s.u % kHkv;
+  prefetch_l2_bulk(p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD, 2u * kTok * kD * 2u);
+  prefetch_l2_bulk(p.q_gamma[l], kD * 2u);
+  if (s.j1 == p.T) {
+    prefetch_l2_bulk(p.k_raw[l] + static_cast<size_t>(g) * kTok * kD, kTok * kD * 2u);
+    prefetch_l2_bulk(p.v_raw[l] + static_cast<size_t>(g) * kTok * kD, kTok * kD * 2u);
+    prefetch_l2_bulk(p.k_gamma[l], kD * 2u);
+  }
+}
 template <bool F8, class PP>
-__device__ __noinline__ void early_prefetch(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void early_prefetch(const PP& p, const Ctx cx) {
   long long t = cx.start;
   Seg s;
   if (!next_seg(t, cx.end, p.T, s)) return;
@@ -453,7 +477,7 @@ __device__ __noinline__ void early_prefetch(const PP& p, const Ctx& cx) {
 // one token, with the raw rows of the next kAhead tokens already requested.
 constexpr int kAhead = 1;
 template <class PP>
-__device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void prep_warps(const PP& p, const Ctx cx) {
   constexpr bool F8 = false;
   EA_LAYOUT_ALIASES;
   const int px = static_cast<int>(threadIdx.x) - (kThreads - kPrepThreads);
@@ -628,7 +652,7 @@ __device__ __noinline__ void prep_warps(const PP& p, const Ctx& cx) {
 // whichever has its inputs first is issued first: PV(i-1) does not wait behind QK(i), whose
 // inputs (K(i), and the completion of PV(i-2)) may arrive later than P(i-1).
 template <bool F8, class PP>
-__device__ __noinline__ void mma_issuer(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void mma_issuer(const PP& p, const Ctx cx) {
   EA_LAYOUT_ALIASES;
   // bf16: format code 1 (kind::f16); e4m3: format code 0 (kind::f8f6f4). V is MN-major.
   constexpr uint32_t kIdescQK128 = umma_idesc_f16(128, 128, !F8, false, false);
@@ -813,7 +837,7 @@ __device__ __noinline__ void rescale_rare(uint32_t o_addr, uint32_t p_addr, floa
 }
 
 template <bool F8, class PP>
-__device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void softmax_warps(const PP& p, const Ctx cx) {
   EA_LAYOUT_ALIASES;
   const int k = threadIdx.x >> 7;   // stream of this warpgroup
   const int r = threadIdx.x & 127;  // folded row = TMEM lane
@@ -1229,7 +1253,7 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx& cx) {
 // kernel launched after this one cannot start before every CTA of this grid has started). The
 // last CTA to leave resets both counters.
 template <bool F8, class PP>
-__device__ __noinline__ void grid_merge(const PP& p, const Ctx& cx) {
+__device__ __noinline__ void grid_merge(const PP& p, const Ctx cx) {
   EA_LAYOUT_ALIASES;
   volatile uint32_t* go = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_ROLE);
   __threadfence();  // this thread's partial stores, visible at GPU scope before the count
@@ -1324,7 +1348,10 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + LY::SM_TMEM);
   // Work that reads nothing a preceding kernel writes, done while it may still run.
   float fcs[2][8], fsn[2][8];
-  if (warp == 8 && lane == 0) early_prefetch<F8>(p, cx);
+  if (warp == 11 && lane == 0) {
+    if constexpr (!F8) early_inputs(p, cx);
+    early_prefetch<F8>(p, cx);
+  }
   if constexpr (!F8) {
     if (warp < 8) first_angles(p, fcs, fsn);
   }
