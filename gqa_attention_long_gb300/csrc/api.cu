@@ -343,7 +343,7 @@ int launch_chunk_t(const ea_layer_args* a, int n, int S, int Smax, int rope_delt
   ap.Smax = Smax;
   ap.W = static_cast<long long>(n) * kHkv * ap.T;
   ap.q_ws = fp8 ? ws + wl.q_off : nullptr;
-  ap.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
+  ap.part_o = reinterpret_cast<uint4*>(ws + wl.part_o_off);
   ap.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
   ap.q_scale = reinterpret_cast<const float*>(ws + wl.qscale_off);
   ap.sv_ref = reinterpret_cast<const float*>(ws + wl.svref_off);

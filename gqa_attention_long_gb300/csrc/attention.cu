@@ -1125,7 +1125,7 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx cx) {
       lse_row = M + log2f(L);
       if (second) {
         const float lse_o =
-            __ldcg(p.part_lse + (static_cast<size_t>(other) * 2 + other_slot) * kRows + r);
+            __ldcg(p.part_lse + (static_cast<size_t>(other) * 2 + other_slot) * 3 * kRows + r);
         const float M2 = fmaxf(lse_row, lse_o);
         const float ea = ex2_approx(lse_row - M2), eb = ex2_approx(lse_o - M2);
         const float rs = 1.0f / (ea + eb);
@@ -1141,23 +1141,27 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx cx) {
     tc_fence_after();
     // ---- this warpgroup's 64 columns of both accumulators, combined (a second part starts from
     // the first part's weighted partial)
-    // partials are stored chunk-major (float4 chunk c of row r at index c * 128 + r), so that a
-    // warp's 32 rows of one chunk are 512 contiguous bytes
-    const float4* pother = reinterpret_cast<const float4*>(p.part_o) +
-                           (static_cast<size_t>(other) * 2 + other_slot) * kPartChunks * kRows +
-                           static_cast<size_t>(16 * k) * kRows + r;
+    // partials are f16, stored chunk-major (16-byte chunk c of row r at index c * 128 + r), so
+    // that a warp's 32 rows of one chunk are 512 contiguous bytes; half row k of a partial is
+    // scaled by a power of two whose inverse sits beside the lse
+    const size_t oslot = static_cast<size_t>(other) * 2 + other_slot;
+    const uint4* pother = p.part_o + oslot * kPartChunks * kRows + static_cast<size_t>(8 * k) * kRows + r;
+    const float w2s = second ? w2 * __ldcg(p.part_lse + (oslot * 3 + 1 + k) * kRows + r) : 0.f;
     float o[2][32];
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       const uint32_t col = cx.tmem + lane_addr + TM_O + 64 * k + 32 * ch;
       if (second) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 v = __ldcg(pother + static_cast<size_t>(8 * ch + q) * kRows);
-          o[ch][4 * q] = v.x * w2;
-          o[ch][4 * q + 1] = v.y * w2;
-          o[ch][4 * q + 2] = v.z * w2;
-          o[ch][4 * q + 3] = v.w * w2;
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = __ldcg(pother + static_cast<size_t>(4 * ch + q) * kRows);
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float2 f = unpack_f16x2(wv[h]);
+            o[ch][8 * q + 2 * h] = f.x * w2s;
+            o[ch][8 * q + 2 * h + 1] = f.y * w2s;
+          }
         }
       } else {
 #pragma unroll
@@ -1214,17 +1218,33 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx cx) {
         st_shared_v4(srow + 16 * (q ^ m), w[q][0], w[q][1], w[q][2], w[q][3]);
       fence_proxy_async_smem();  // visible to the bulk copy (async proxy)
     } else {
-      // chunk-major (see above): each store instruction of a warp writes 512 contiguous bytes
-      float4* po = reinterpret_cast<float4*>(p.part_o) +
-                   (static_cast<size_t>(blockIdx.x) * 2 + slot) * kPartChunks * kRows +
-                   static_cast<size_t>(16 * k) * kRows + r;
+      // f16, chunk-major (see above): each store instruction of a warp writes 512 contiguous
+      // bytes. The half row is scaled by 2^(e - 127), e chosen from the exponent of its largest
+      // magnitude so that it lands in [2^14, 2^15) (f16 keeps 11 significant bits there and
+      // cannot overflow); a zero or tiny half row takes the largest scale, 2^126. The inverse,
+      // also a power of two, is stored beside the lse.
+      float mx = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          po[static_cast<size_t>(8 * ch + q) * kRows] =
-              make_float4(o[ch][4 * q], o[ch][4 * q + 1], o[ch][4 * q + 2], o[ch][4 * q + 3]);
-      if (k == 0) p.part_lse[(static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + r] = lse_row;
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(o[ch][e]));
+      const int ex = static_cast<int>(__float_as_uint(mx) >> 23) & 0xff;  // mx < 2^(ex - 126)
+      const int es = min(max(268 - ex, 1), 253);
+      const float sc = __uint_as_float(static_cast<uint32_t>(es) << 23);
+      const float isc = __uint_as_float(static_cast<uint32_t>(254 - es) << 23);
+      const size_t mslot = static_cast<size_t>(blockIdx.x) * 2 + slot;
+      uint4* po = p.part_o + mslot * kPartChunks * kRows + static_cast<size_t>(8 * k) * kRows + r;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float* x = &o[ch][8 * q];
+          po[static_cast<size_t>(4 * ch + q) * kRows] =
+              make_uint4(pack_f16x2(x[0] * sc, x[1] * sc), pack_f16x2(x[2] * sc, x[3] * sc),
+                         pack_f16x2(x[4] * sc, x[5] * sc), pack_f16x2(x[6] * sc, x[7] * sc));
+        }
+      p.part_lse[(mslot * 3 + 1 + k) * kRows + r] = isc;
+      if (k == 0) p.part_lse[mslot * 3 * kRows + r] = lse_row;
       if (fused) __threadfence();  // the partial is visible before the flag
     }
     if (leader) sflag[seg & 1] = staged ? 1u : 0u;
@@ -1247,7 +1267,7 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx cx) {
 // Units cut into more than two parts (a single layer spread over every SM) are merged by the
 // grid itself once every CTA has written its partials: each CTA counts its arrival (after a
 // GPU-scope fence on its partial stores), one thread waits, bounded, until all CTAs have arrived,
-// and then the CTA merges its share of the split units' (unit, 4-column chunk) pairs, three
+// and then the CTA merges its share of the split units' (unit, 8-column chunk) pairs, three
 // pairs at a time (128 threads, one per folded row, per pair). The grid has one CTA per SM at
 // most, so every CTA is resident or becomes so as soon as an earlier kernel frees its SM (a
 // kernel launched after this one cannot start before every CTA of this grid has started). The
@@ -1283,7 +1303,7 @@ __device__ __noinline__ void grid_merge(const PP& p, const Ctx cx) {
     const int c1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * P / gridDim.x);
     for (int pi = c0 + static_cast<int>(threadIdx.x) / kRows; pi < c1; pi += kThreads / kRows) {
       const SplitUnit su = p.split[pi / kPartChunks];
-      merge_row_chunk<24>(p.part_o, p.part_lse, su, pi % kPartChunks, threadIdx.x % kRows,
+      merge_row_chunk<20>(p.part_o, p.part_lse, su, pi % kPartChunks, threadIdx.x % kRows,
                           p.out[su.u / kHkv]);
     }
   }

@@ -23,7 +23,7 @@ constexpr int kMaxLayersPerLaunch = 64;
 // that their launches carry ~2 KB of parameters instead of ~19 KB.
 constexpr int kSmallCap = 8;
 constexpr int kScaleBlock = 128;  // FP8 scale granularity (rows)
-constexpr int kPartChunks = kD / 4;  // float4 chunks per row of a partial output
+constexpr int kPartChunks = kD / 8;  // 16-byte chunks (8 f16 columns) per row of a partial output
 
 // Bytes of one staged operand tile in the 128-byte-swizzled K-major layout: two 64-column
 // halves ("atoms"), each [rows][128 bytes]; inside every 8-row group of 1024 bytes the 16-byte
@@ -56,9 +56,12 @@ enum : uint32_t {
 //   q       n_layers * 8 * 32 KB  e4m3 only: roped Q per (layer, kv head) as high and low e4m3
 //                                 codes, swizzled K-major (a bf16 call prepares Q in the
 //                                 attention kernel's shared memory and has no such region)
-//   part_o  n_ctas * 2 * 128*128 fp32  split partial outputs (normalised), per slot chunk-major:
-//                                     float4 chunk c (columns 4c .. 4c+3) of row r at c * 128 + r
-//   part_lse n_ctas * 2 * 128 fp32     their log2-sum-exp (in units of log2-scaled scores)
+//   part_o  n_ctas * 2 * 128*128 f16   split partial outputs (normalised), per slot chunk-major:
+//                                     16-byte chunk c (columns 8c .. 8c+7) of row r at c * 128 + r;
+//                                     each half row (64 columns) is stored times a power of two
+//                                     that puts its largest magnitude in [2^14, 2^15)
+//   part_lse n_ctas * 2 * 3*128 fp32   per slot: the rows' log2-sum-exp (in units of log2-scaled
+//                                     scores), then per half row the inverse of that power of two
 struct WsLayout {
   size_t sync_off, qscale_off, svref_off, q_off, part_o_off, part_lse_off, total;
 };
@@ -76,9 +79,9 @@ constexpr WsLayout ws_layout(int n_layers_per_launch, int max_ctas, bool fp8) {
   w.q_off = off;
   if (fp8) off += static_cast<size_t>(n_layers_per_launch) * kHkv * kQTileBytes;
   w.part_o_off = off;
-  off += static_cast<size_t>(max_ctas) * 2 * kRows * kD * sizeof(float);
+  off += static_cast<size_t>(max_ctas) * 2 * kRows * kD * 2;
   w.part_lse_off = off;
-  off += static_cast<size_t>(max_ctas) * 2 * kRows * sizeof(float);
+  off += static_cast<size_t>(max_ctas) * 2 * 3 * kRows * sizeof(float);
   w.total = (off + 1023) & ~static_cast<size_t>(1023);
   return w;
 }
@@ -146,8 +149,8 @@ struct AttnParams {
   const float* ks[CAP];      // FP8: block scales [8][Smax/128 + 1] (else null)
   const float* vs[CAP];
   const uint8_t* q_ws;  // FP8: the prologue's staged Q codes (bf16: null)
-  float* part_o;
-  float* part_lse;
+  uint4* part_o;     // f16 partials, 16-byte chunks (see the workspace layout)
+  float* part_lse;   // per slot: lse[128], then the inverse scales of both half rows
   const float* q_scale;  // FP8: [unit][128]
   const float* sv_ref;   // FP8: [unit]
   uint32_t* unit_sync;   // [unit][2]: arrival count, partial-ready flag (in-kernel merge)

@@ -502,5 +502,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// The two f16 values of a packed pair (low half first), exactly, as fp32.
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+  __half2 v = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(v);
+}
 
 }  // namespace ea

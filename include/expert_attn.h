@@ -187,7 +187,7 @@ int expert_attn_selftest_wait_timeout(int limit_us, void* workspace, size_t ws_b
  * timed out are undefined. */
 #define EA_NOALLOC_MAX_LAYERS 4
 #define EA_NOALLOC_MAX_CTAS 64
-#define EA_NOALLOC_SCRATCH_BYTES 9522176u /* 2 KB + 4 layers x 260 KB + 1 KB + 64 CTAs x 129 KB */
+#define EA_NOALLOC_SCRATCH_BYTES 5458944u /* 2 KB + 4 layers x 260 KB + 1 KB + 64 CTAs x 67 KB */
 int expert_attn_layers_noalloc(const ea_layer_args* layers, int n_layers, int S, int Smax,
                                int rope_delta, int kv_dtype, ea_stream_t stream);
 
