@@ -54,6 +54,8 @@ namespace attn {
 constexpr int kThreads = 384;
 constexpr int kPrepThreads = 64;  // bf16: warps 10 and 11
 constexpr int kSoftmaxThreads = 256;
+// named barriers: 0 __syncthreads, 1 prep warps, 2 softmax warps, 3 stream 1's warpgroup (own rows)
+constexpr uint32_t kOwnRowsBar = 3;
 
 // Shared-memory layout of one CTA. bf16 cache: a K or V tile is 128 rows x 256 bytes, stored as
 // two 16 KB swizzle atoms (channels 0-63, 64-127). e4m3 cache: 128 rows x 128 bytes, one atom;
@@ -318,13 +320,16 @@ __device__ __forceinline__ void first_angles(const PP& p, float (&cs)[2][8], flo
 
 // The first segment's rows by the 256 softmax threads (32 octets, octet oc: tokens oc and oc + 32,
 // whose rotation angles the threads already hold): the Q rows of both heads into Q buffer 0
-// (QFULL), then, when that segment holds its unit's own-row tile, the roped K rows and the V
-// rows into the cache tail and, when they fit the ring's first round (own_rows_direct), straight
-// into the two ring slots of that tile as well (KVFULL; no fetch back), else TAILRDY for the
-// producer to fetch them. A CTA's first segment can be short, so its own rows are needed early.
+// (QFULL). When that segment holds its unit's own-row tile, stream 1's warpgroup then writes
+// the roped K rows and the V rows of all 64 tokens (its octet oc takes tokens oc - 16, oc,
+// oc + 16, oc + 32; it computes the angles of the two it did not hold) into the cache tail and,
+// when they fit the ring's first round (own_rows_direct), straight into the two ring slots of
+// that tile as well (KVFULL; no fetch back), else TAILRDY for the producer to fetch them.
+// Stream 0's warpgroup goes on to its first tile meanwhile: in a two-tile segment that is the
+// last cache tile, whose keys >= S it masks, so the CTA no longer waits for both tasks in turn.
 template <class PP>
 __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const float (&cs)[2][8],
-                                          const float (&sn)[2][8]) {
+                                             const float (&sn)[2][8]) {
   long long t = cx.start;
   Seg s;
   if (!next_seg(t, cx.end, p.T, s)) return;
@@ -332,6 +337,7 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
   const int dl = 8 * i, dh = 64 + 8 * i;
   const int l = s.u / kHkv, g = s.u % kHkv;
   const bool own = s.j1 == p.T;
+  const bool own_rows = own && threadIdx.x >= 128;  // stream 1's warpgroup
   const __nv_bfloat16* qsrc = p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD + oc * kD;
   // every row of both tokens is requested at once
   uint4 raw[2][2][2];  // [token][head][lo, hi]
@@ -343,21 +349,6 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
       raw[tt][hh][0] = *reinterpret_cast<const uint4*>(row + dl);
       raw[tt][hh][1] = *reinterpret_cast<const uint4*>(row + dh);
     }
-  uint4 kv[2][2][2];  // [token][k, v][lo, hi]
-  uint4 kg[2];        // k_norm gain, channels [8i, 8i + 8) and [64 + 8i, 64 + 8i + 8)
-  const size_t unit_rows = static_cast<size_t>(g) * kTok * kD;
-  if (own) {
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt) {
-      const size_t ro = unit_rows + static_cast<size_t>(oc + 32 * tt) * kD;
-      kv[tt][0][0] = *reinterpret_cast<const uint4*>(p.k_raw[l] + ro + dl);
-      kv[tt][0][1] = *reinterpret_cast<const uint4*>(p.k_raw[l] + ro + dh);
-      kv[tt][1][0] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dl);
-      kv[tt][1][1] = *reinterpret_cast<const uint4*>(p.v_raw[l] + ro + dh);
-    }
-    kg[0] = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dl);
-    kg[1] = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dh);
-  }
   float gl[8], gh[8];
   unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dl), gl);
   unpack_bf16x8(*reinterpret_cast<const uint4*>(p.q_gamma[l] + dh), gh);
@@ -382,49 +373,89 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
   fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
   bar_sync(2, kSoftmaxThreads);
   if (threadIdx.x == 0) mbar_arrive(cx.bar(Lay<false>::B_QFULL));
-  if (!own) return;
+  if (!own_rows) return;
   // K rows: RMSNorm with the k_norm gain and RoPE; V rows as given; into cache rows Smax - 64 + t
   // of head g, and (direct) into the own-row tile's K and V ring slots, row t in the swizzled
-  // layout the TMA would have produced (rows 64-127 of the slots are never read)
+  // layout the TMA would have produced (rows 64-127 of the slots are never read). The raw rows
+  // (in L2 since before the dependency wait) are requested at once, tokens oc - 16 + 16 m.
+  // angles of tokens oc - 16 and oc + 16 first (those of oc and oc + 32 are in cs, sn)
+  float xcs[2][8], xsn[2][8];
+  {
+    float ih[8], il[8];
+    load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
+    token_cos_sin(p, oc - 16, ih, il, xcs[0], xsn[0]);
+    token_cos_sin(p, oc + 16, ih, il, xcs[1], xsn[1]);
+  }
+  const size_t unit_rows = static_cast<size_t>(g) * kTok * kD;
+  const __nv_bfloat16* ksrc = p.k_raw[l] + unit_rows;
+  const __nv_bfloat16* vsrc = p.v_raw[l] + unit_rows;
+  uint4 kr[4][2];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const size_t ro = static_cast<size_t>(oc - 16 + 16 * m) * kD;
+    kr[m][0] = *reinterpret_cast<const uint4*>(ksrc + ro + dl);
+    kr[m][1] = *reinterpret_cast<const uint4*>(ksrc + ro + dh);
+  }
+  const uint4 kg0 = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dl);
+  const uint4 kg1 = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dh);
   const bool direct = own_rows_direct(p, s);
   const uint32_t n_tile = static_cast<uint32_t>(s.j1 - 1 - s.j0);  // CTA tile index of the own-row tile
   const uint32_t kslot = cx.sbase + Lay<false>::SM_RING + (2 * n_tile) * Lay<false>::kSlot;
   const uint32_t vslot = kslot + Lay<false>::kSlot;
-  unpack_bf16x8(kg[0], gl);
-  unpack_bf16x8(kg[1], gh);
+  unpack_bf16x8(kg0, gl);
+  unpack_bf16x8(kg1, gh);
   const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
 #pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
-    const int tok = oc + 32 * tt;
+  for (int m = 0; m < 4; ++m) {
+    const int tok = oc - 16 + 16 * m;
     const size_t ro = tail + static_cast<size_t>(tok) * kD;
-    float xl[8], xh[8], yl[8], yh[8];
-    unpack_bf16x8(kv[tt][0][0], xl);
-    unpack_bf16x8(kv[tt][0][1], xh);
-    norm_rope(xl, xh, gl, gh, cs[tt], sn[tt], yl, yh);
+    float xl[8], xh[8], yl[8], yh[8], c8[8], s8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {  // m is a compile-time index: these are register moves
+      c8[e] = (m & 1) ? cs[m >> 1][e] : xcs[m >> 1][e];
+      s8[e] = (m & 1) ? sn[m >> 1][e] : xsn[m >> 1][e];
+    }
+    unpack_bf16x8(kr[m][0], xl);
+    unpack_bf16x8(kr[m][1], xh);
+    norm_rope(xl, xh, gl, gh, c8, s8, yl, yh);
     const uint4 kl = pack8(yl, false), kh = pack8(yh, false);
     *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = kl;
     *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = kh;
-    *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = kv[tt][1][0];
-    *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = kv[tt][1][1];
     if (direct) {
       st_shared_v4(kslot + swz_off(tok, i, kAtomBytes), kl.x, kl.y, kl.z, kl.w);
       st_shared_v4(kslot + swz_off(tok, i + 8, kAtomBytes), kh.x, kh.y, kh.z, kh.w);
-      const uint4 vl = kv[tt][1][0], vh = kv[tt][1][1];
+    }
+  }
+  uint4 vr[4][2];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const size_t ro = static_cast<size_t>(oc - 16 + 16 * m) * kD;
+    vr[m][0] = *reinterpret_cast<const uint4*>(vsrc + ro + dl);
+    vr[m][1] = *reinterpret_cast<const uint4*>(vsrc + ro + dh);
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int tok = oc - 16 + 16 * m;
+    const size_t ro = tail + static_cast<size_t>(tok) * kD;
+    *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = vr[m][0];
+    *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = vr[m][1];
+    if (direct) {
+      const uint4 vl = vr[m][0], vh = vr[m][1];
       st_shared_v4(vslot + swz_off(tok, i, kAtomBytes), vl.x, vl.y, vl.z, vl.w);
       st_shared_v4(vslot + swz_off(tok, i + 8, kAtomBytes), vh.x, vh.y, vh.z, vh.w);
     }
   }
   if (direct) {
     fence_proxy_async_smem();  // the slots are read by the tensor core (async proxy)
-    bar_sync(2, kSoftmaxThreads);
-    if (threadIdx.x == 0) {
+    bar_sync(kOwnRowsBar, 128);
+    if (threadIdx.x == 128) {
       mbar_arrive(cx.bar(Lay<false>::B_KVFULL + 2 * n_tile));
       mbar_arrive(cx.bar(Lay<false>::B_KVFULL + 2 * n_tile + 1));
     }
   } else {
     fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
-    bar_sync(2, kSoftmaxThreads);
-    if (threadIdx.x == 0) mbar_arrive(cx.bar(Lay<false>::B_TAILRDY));
+    bar_sync(kOwnRowsBar, 128);
+    if (threadIdx.x == 128) mbar_arrive(cx.bar(Lay<false>::B_TAILRDY));
   }
 }
 
