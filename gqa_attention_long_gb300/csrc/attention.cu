@@ -77,7 +77,7 @@ struct Lay {
                        B_SFULL = 4 + 2 * kRing, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
                        B_X1 = B_ODONE + 2, B_X2 = B_X1 + 1, B_OFREE = B_X2 + 1,
                        B_STAGED = B_OFREE + 1, B_TAILRDY = B_STAGED + 2, B_DRAIN = B_TAILRDY + 2,
-                       kNumBars = B_DRAIN + 1;
+                       B_OWNRAW = B_DRAIN + 1, kNumBars = B_OWNRAW + 1;
   static constexpr uint32_t SM_XCH = SM_BAR + kNumBars * 8;  // three floats per folded row
   static constexpr uint32_t SM_ROLE = SM_XCH + kRows * 12;    // in-kernel merge role
   static constexpr uint32_t SM_SFLAG = SM_ROLE + 4;            // per Q buffer: output staged
@@ -309,13 +309,20 @@ __device__ __forceinline__ void token_cos_sin(const PP& p, int tok, const float 
 // cos/sin of the two tokens (oc, oc + 32) whose rows a softmax thread prepares in the first
 // segment, at its eight frequencies [8i, 8i + 8). The positions depend only on the token index, S
 // and rope_delta, so this runs before the kernel waits for the preceding one.
+// Stream 1's threads also take the angles of tokens oc - 16 and oc + 16 (xcs, xsn), which they
+// need for the own K rows when the first segment holds its unit's own-row tile.
 template <class PP>
-__device__ __forceinline__ void first_angles(const PP& p, float (&cs)[2][8], float (&sn)[2][8]) {
+__device__ __forceinline__ void first_angles(const PP& p, float (&cs)[2][8], float (&sn)[2][8],
+                                             float (&xcs)[2][8], float (&xsn)[2][8], bool own) {
   const int oc = threadIdx.x >> 3, dl = 8 * (threadIdx.x & 7);
   float ih[8], il[8];
   load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
   token_cos_sin(p, oc, ih, il, cs[0], sn[0]);
   token_cos_sin(p, oc + 32, ih, il, cs[1], sn[1]);
+  if (own && threadIdx.x >= 128) {
+    token_cos_sin(p, oc - 16, ih, il, xcs[0], xsn[0]);
+    token_cos_sin(p, oc + 16, ih, il, xcs[1], xsn[1]);
+  }
 }
 
 // The first segment's rows by the 256 softmax threads (32 octets, octet oc: tokens oc and oc + 32,
@@ -329,7 +336,8 @@ __device__ __forceinline__ void first_angles(const PP& p, float (&cs)[2][8], flo
 // last cache tile, whose keys >= S it masks, so the CTA no longer waits for both tasks in turn.
 template <class PP>
 __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const float (&cs)[2][8],
-                                             const float (&sn)[2][8]) {
+                                             const float (&sn)[2][8], const float (&xcs)[2][8],
+                                             const float (&xsn)[2][8]) {
   long long t = cx.start;
   Seg s;
   if (!next_seg(t, cx.end, p.T, s)) return;
@@ -338,6 +346,24 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
   const int l = s.u / kHkv, g = s.u % kHkv;
   const bool own = s.j1 == p.T;
   const bool own_rows = own && threadIdx.x >= 128;  // stream 1's warpgroup
+  const bool direct = own && own_rows_direct(p, s);
+  const uint32_t n_tile = static_cast<uint32_t>(s.j1 - 1 - s.j0);  // CTA tile index of the own-row tile
+  const uint32_t kslot = cx.sbase + Lay<false>::SM_RING + (2 * n_tile) * Lay<false>::kSlot;
+  const uint32_t vslot = kslot + Lay<false>::kSlot;
+  const size_t unit_rows = static_cast<size_t>(g) * kTok * kD;
+  if (direct && threadIdx.x == 128) {
+    // The raw own K and V rows (64 x 256 bytes each) by bulk copy into the rows of their ring
+    // slots that the 64-key tile never reads (rows 64-127 of each 64-channel atom): raw rows
+    // 0-31 into atom 0, rows 32-63 into atom 1, 8 KB each.
+    const uint32_t bar = cx.bar(Lay<false>::B_OWNRAW);
+    const uint64_t pol = l2_policy_evict_first();
+    mbar_expect_tx(bar, 4u * 8192u);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      bulk_load(kslot + h * kAtomBytes + 8192u, p.k_raw[l] + unit_rows + h * 32 * kD, 8192u, bar, pol);
+      bulk_load(vslot + h * kAtomBytes + 8192u, p.v_raw[l] + unit_rows + h * 32 * kD, 8192u, bar, pol);
+    }
+  }
   const __nv_bfloat16* qsrc = p.q_raw[l] + static_cast<size_t>(2 * g) * kTok * kD + oc * kD;
   // every row of both tokens is requested at once
   uint4 raw[2][2][2];  // [token][head][lo, hi]
@@ -378,33 +404,41 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
   // of head g, and (direct) into the own-row tile's K and V ring slots, row t in the swizzled
   // layout the TMA would have produced (rows 64-127 of the slots are never read). The raw rows
   // (in L2 since before the dependency wait) are requested at once, tokens oc - 16 + 16 m.
-  // angles of tokens oc - 16 and oc + 16 first (those of oc and oc + 32 are in cs, sn)
-  float xcs[2][8], xsn[2][8];
-  {
-    float ih[8], il[8];
-    load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
-    token_cos_sin(p, oc - 16, ih, il, xcs[0], xsn[0]);
-    token_cos_sin(p, oc + 16, ih, il, xcs[1], xsn[1]);
-  }
-  const size_t unit_rows = static_cast<size_t>(g) * kTok * kD;
+  // (the angles of tokens oc - 16 and oc + 16 were computed before the dependency wait, in
+  // xcs, xsn; those of oc and oc + 32 are in cs, sn)
   const __nv_bfloat16* ksrc = p.k_raw[l] + unit_rows;
   const __nv_bfloat16* vsrc = p.v_raw[l] + unit_rows;
-  uint4 kr[4][2];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const size_t ro = static_cast<size_t>(oc - 16 + 16 * m) * kD;
-    kr[m][0] = *reinterpret_cast<const uint4*>(ksrc + ro + dl);
-    kr[m][1] = *reinterpret_cast<const uint4*>(ksrc + ro + dh);
-  }
   const uint4 kg0 = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dl);
   const uint4 kg1 = *reinterpret_cast<const uint4*>(p.k_gamma[l] + dh);
-  const bool direct = own_rows_direct(p, s);
-  const uint32_t n_tile = static_cast<uint32_t>(s.j1 - 1 - s.j0);  // CTA tile index of the own-row tile
-  const uint32_t kslot = cx.sbase + Lay<false>::SM_RING + (2 * n_tile) * Lay<false>::kSlot;
-  const uint32_t vslot = kslot + Lay<false>::kSlot;
+  // raw row tok in shared memory (direct: where the bulk copies put it)
+  auto raw_row = [&](uint32_t slot, int tok) -> uint32_t {
+    return slot + static_cast<uint32_t>(tok >> 5) * kAtomBytes + 8192u + static_cast<uint32_t>(tok & 31) * 256u;
+  };
+  uint4 kr[4][2];
+  if (direct) {
+    if (!bounded_wait(cx.bar(Lay<false>::B_OWNRAW), 0, cx.abort_flag, cx.status, kErrSoftmaxWait)) {
+      // the copies land before the CTA can give its shared memory back
+      if (!drain_wait(cx.bar(Lay<false>::B_OWNRAW), 0)) atomicOr(cx.status, kErrDrain);
+      return;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t a = raw_row(kslot, oc - 16 + 16 * m);
+      kr[m][0] = ld_shared_v4(a + 16 * i);
+      kr[m][1] = ld_shared_v4(a + 128 + 16 * i);
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const size_t ro = static_cast<size_t>(oc - 16 + 16 * m) * kD;
+      kr[m][0] = *reinterpret_cast<const uint4*>(ksrc + ro + dl);
+      kr[m][1] = *reinterpret_cast<const uint4*>(ksrc + ro + dh);
+    }
+  }
   unpack_bf16x8(kg0, gl);
   unpack_bf16x8(kg1, gh);
   const size_t tail = (static_cast<size_t>(g) * p.Smax + (p.Smax - kTok)) * kD;
+  uint4 kst[4][2];  // the roped K rows, kept for the cache tail
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int tok = oc - 16 + 16 * m;
@@ -419,30 +453,40 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
     unpack_bf16x8(kr[m][1], xh);
     norm_rope(xl, xh, gl, gh, c8, s8, yl, yh);
     const uint4 kl = pack8(yl, false), kh = pack8(yh, false);
-    *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = kl;
-    *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = kh;
-    if (direct) {
+    kst[m][0] = kl;
+    kst[m][1] = kh;
+    if (direct) {  // the cache tail is written after the slots are handed to the MMA
       st_shared_v4(kslot + swz_off(tok, i, kAtomBytes), kl.x, kl.y, kl.z, kl.w);
       st_shared_v4(kslot + swz_off(tok, i + 8, kAtomBytes), kh.x, kh.y, kh.z, kh.w);
+    } else {
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = kl;
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = kh;
     }
   }
   uint4 vr[4][2];
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    const size_t ro = static_cast<size_t>(oc - 16 + 16 * m) * kD;
-    vr[m][0] = *reinterpret_cast<const uint4*>(vsrc + ro + dl);
-    vr[m][1] = *reinterpret_cast<const uint4*>(vsrc + ro + dh);
+    if (direct) {
+      const uint32_t a = raw_row(vslot, oc - 16 + 16 * m);
+      vr[m][0] = ld_shared_v4(a + 16 * i);
+      vr[m][1] = ld_shared_v4(a + 128 + 16 * i);
+    } else {
+      const size_t ro = static_cast<size_t>(oc - 16 + 16 * m) * kD;
+      vr[m][0] = *reinterpret_cast<const uint4*>(vsrc + ro + dl);
+      vr[m][1] = *reinterpret_cast<const uint4*>(vsrc + ro + dh);
+    }
   }
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int tok = oc - 16 + 16 * m;
-    const size_t ro = tail + static_cast<size_t>(tok) * kD;
-    *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = vr[m][0];
-    *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = vr[m][1];
     if (direct) {
       const uint4 vl = vr[m][0], vh = vr[m][1];
       st_shared_v4(vslot + swz_off(tok, i, kAtomBytes), vl.x, vl.y, vl.z, vl.w);
       st_shared_v4(vslot + swz_off(tok, i + 8, kAtomBytes), vh.x, vh.y, vh.z, vh.w);
+    } else {
+      const size_t ro = tail + static_cast<size_t>(tok) * kD;
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = vr[m][0];
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = vr[m][1];
     }
   }
   if (direct) {
@@ -451,6 +495,18 @@ __device__ __forceinline__ void first_q_prep(const PP& p, const Ctx& cx, const f
     if (threadIdx.x == 128) {
       mbar_arrive(cx.bar(Lay<false>::B_KVFULL + 2 * n_tile));
       mbar_arrive(cx.bar(Lay<false>::B_KVFULL + 2 * n_tile + 1));
+    }
+    // Then the cache tail, for the caller, from registers (global stores queue behind the
+    // cache stream in the memory system, so they stay off the path to the first MMA; the slots
+    // themselves may be refilled as soon as the MMA is done with them).
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int tok = oc - 16 + 16 * m;
+      const size_t ro = tail + static_cast<size_t>(tok) * kD;
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dl) = kst[m][0];
+      *reinterpret_cast<uint4*>(p.kc[l] + ro + dh) = kst[m][1];
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dl) = vr[m][0];
+      *reinterpret_cast<uint4*>(p.vc[l] + ro + dh) = vr[m][1];
     }
   } else {
     fence_proxy_async_global();  // the rows are read back by TMA (async proxy)
@@ -1386,6 +1442,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       mbar_init(cx.bar(B_KVEMPTY + b), F8 && (b & 1) ? 128 : 1);
     }
     mbar_init(cx.bar(B_DRAIN), 1);
+    mbar_init(cx.bar(LY::B_OWNRAW), 1);
     *cx.abort_flag = 0u;
     fence_mbar_init();
   }
@@ -1398,20 +1455,25 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   tc_fence_after();
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(smem + LY::SM_TMEM);
   // Work that reads nothing a preceding kernel writes, done while it may still run.
-  float fcs[2][8], fsn[2][8];
+  float fcs[2][8], fsn[2][8], xcs[2][8], xsn[2][8];
   if (warp == 11 && lane == 0) {
     if constexpr (!F8) early_inputs(p, cx);
     early_prefetch<F8>(p, cx);
   }
   if constexpr (!F8) {
-    if (warp < 8) first_angles(p, fcs, fsn);
+    if (warp < 8) {
+      long long t0 = cx.start;
+      Seg s0;
+      const bool own0 = next_seg(t0, cx.end, p.T, s0) && s0.j1 == p.T;
+      first_angles(p, fcs, fsn, xcs, xsn, own0);
+    }
   }
   // Everything below reads what earlier kernels in the stream wrote (layer inputs, caches; e4m3:
   // the prologue's staged Q and own rows).
   pdl_wait_primary();
 
   if (warp < 8) {
-    if constexpr (!F8) first_q_prep(p, cx, fcs, fsn);
+    if constexpr (!F8) first_q_prep(p, cx, fcs, fsn, xcs, xsn);
     softmax_warps<F8>(p, cx);
   } else if (warp == 8) {
     if (lane == 0) producer<F8>(p, cx);
