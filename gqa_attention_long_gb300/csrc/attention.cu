@@ -1363,9 +1363,11 @@ template <bool F8, class PP>
 __device__ __noinline__ void grid_merge(const PP& p, const Ctx cx) {
   EA_LAYOUT_ALIASES;
   volatile uint32_t* go = reinterpret_cast<volatile uint32_t*>(cx.smem + LY::SM_ROLE);
-  __threadfence();  // this thread's partial stores, visible at GPU scope before the count
   __syncthreads();
   if (threadIdx.x == 0) {
+    // the CTA's partial stores (ordered before this thread by the barrier) are visible at GPU
+    // scope before the count: a fence cumulative over them, then the arrival
+    __threadfence();
     atomicAdd(p.grid_sync, 1u);
     const uint64_t t0 = globaltimer_ns();
     bool ok = false;
@@ -1380,7 +1382,8 @@ __device__ __noinline__ void grid_merge(const PP& p, const Ctx cx) {
       __nanosleep(64);
     }
     if (!ok) atomicOr(p.status, kErrMergeWait);
-    __threadfence();
+    // the acquire load that saw the full count orders the partial reads after it (the other
+    // threads are ordered after this one by the barrier below)
     *go = ok ? 1u : 0u;
   }
   __syncthreads();

@@ -68,9 +68,12 @@ __device__ __forceinline__ void norm_rope(const float (&xl)[8], const float (&xh
                                           const float (&gl)[8], const float (&gh)[8],
                                           const float (&cs)[8], const float (&sn)[8],
                                           float (&yl)[8], float (&yh)[8]) {
-  float ss = 0.f;
+  // sum of squares in two independent chains (a single chain of 16 dependent FMAs is the
+  // longest latency of the row)
+  float s2[2] = {0.f, 0.f};
 #pragma unroll
-  for (int e = 0; e < 8; ++e) ss = fmaf(xl[e], xl[e], fmaf(xh[e], xh[e], ss));
+  for (int e = 0; e < 8; ++e) s2[e & 1] = fmaf(xl[e], xl[e], fmaf(xh[e], xh[e], s2[e & 1]));
+  float ss = s2[0] + s2[1];
 #pragma unroll
   for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
   const float rs = rsqrtf(ss * (1.0f / kD) + 1e-6f);
