@@ -227,6 +227,7 @@ void rope_inv_freq(float* hi, float* lo) {
 int n_ctas_for(long long W, int sm_count) {
   int n = g_splits > 0 && g_splits < sm_count ? g_splits : sm_count;
   if (n > kMaxSplitUnits + 1) n = kMaxSplitUnits + 1;  // at most one split unit per boundary
+  if (n > kMaxGridCtas) n = kMaxGridCtas;
   if (static_cast<long long>(n) > W) n = static_cast<int>(W);
   return n < 1 ? 1 : n;
 }
@@ -1033,9 +1034,18 @@ int launch_decode_t(const ea_decode_args* a, int n, int pos, int Smax, int rope_
     attr[cfg.numAttrs].val.clusterDim.y = 1;
     attr[cfg.numAttrs].val.clusterDim.z = 1;
     ++cfg.numAttrs;
+  } else if (n == 1 && dp.T > 8) {
+    // one layer over a longer cache: the same number of CTAs for every kv head (at most one per
+    // key tile, at most kDecodeMaxPerUnit, whose partials fit the drained ring), so that every
+    // CTA holds one segment and the last part of a unit can merge from its own shared memory
+    int per = (sm_count < kMaxGridCtas ? sm_count : kMaxGridCtas) / kHkv;
+    if (per > dp.T) per = dp.T;
+    if (per > kDecodeMaxPerUnit) per = kDecodeMaxPerUnit;
+    dp.per_unit = per;
+    cfg.gridDim = dim3(kHkv * per);
   } else {
     // one CTA per SM (at most 160: the merge stages at most that many parts in shared memory)
-    int n_ctas = sm_count < 160 ? sm_count : 160;
+    int n_ctas = sm_count < kMaxGridCtas ? sm_count : kMaxGridCtas;
     if (static_cast<long long>(n_ctas) > dp.W) n_ctas = static_cast<int>(dp.W);
     cfg.gridDim = dim3(n_ctas);
   }

@@ -70,7 +70,8 @@ constexpr uint32_t SM_BAR = SM_RED + 2 * 4 * kRepText * 4;
 // QFULL and OFREE complete once per segment
 constexpr int B_FULL = 0, B_EMPTY = kStages, B_SDONE = 2 * kStages, B_PFULL = B_SDONE + 2,
               B_ODONE = B_PFULL + 2, B_QFULL = B_ODONE + 2, B_OFREE = B_QFULL + 1,
-              B_TAIL = B_OFREE + 1, B_DRAIN = B_TAIL + 1, kNumBars = B_DRAIN + 1;
+              B_TAIL = B_OFREE + 1, B_DRAIN = B_TAIL + 1, B_MERGE = B_DRAIN + 1,
+              kNumBars = B_MERGE + 1;
 constexpr uint32_t SM_TMEM = SM_BAR + kNumBars * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
 constexpr uint32_t SM_MERGE = SM_ABORT + 4;
@@ -158,6 +159,9 @@ __device__ __noinline__ void producer(const DecodeParams<CAP>& p, uint32_t sbase
       ++n;
     }
   }
+  // every load of this CTA is issued: the next kernel's CTAs may be placed on SMs as they free
+  // up (they wait for this grid to complete before they read anything it writes)
+  pdl_launch_dependents();
   if (!ok) {  // let every copy already issued land before the CTA gives its shared memory back
     for (uint32_t k = 0; k < static_cast<uint32_t>(kStages) && k < n; ++k) {
       const uint32_t q = n - 1 - k;
@@ -480,91 +484,138 @@ __device__ __noinline__ void compute(const DecodeParams<CAP>& p, uint32_t sbase,
       for (int h = 0; h < kRepText; ++h) o[h * kD] = __float2bfloat16_rn(__uint_as_float(ov[h]) / lsum[h]);
     } else {
       // partial: unnormalised output with its (max, sum) per head, then the arrival count; the
-      // part that arrives last merges every part of the unit
-      const int slot = first_seg ? 0 : 1;  // a partial segment is the CTA's first or its last
-      const size_t ps = static_cast<size_t>(blockIdx.x) * 2 + slot;
-      float* po = p.part_o + ps * kRepText * kD + tid;
+      // part that arrives last merges every part of the unit. Part index: 2 c + slot (a partial
+      // segment is the CTA's first or its last), or c in the unit-aligned mode (one segment per
+      // CTA), where the unit's parts are then contiguous. Layout [part][channel][8 heads]: a
+      // thread's 8 values are two 16-byte stores.
+      const int slot = first_seg ? 0 : 1;
+      const size_t ps = p.per_unit ? static_cast<size_t>(blockIdx.x) : static_cast<size_t>(blockIdx.x) * 2 + slot;
+      float4* po = reinterpret_cast<float4*>(p.part_o + ps * kRepText * kD) + 2 * tid;
+      po[0] = make_float4(__uint_as_float(ov[0]), __uint_as_float(ov[1]), __uint_as_float(ov[2]), __uint_as_float(ov[3]));
+      po[1] = make_float4(__uint_as_float(ov[4]), __uint_as_float(ov[5]), __uint_as_float(ov[6]), __uint_as_float(ov[7]));
+      if (tid < kRepText) {  // thread h stores head h's (max, sum): one 8-byte store
+        float mh = m[0], lh = lsum[0];
 #pragma unroll
-      for (int h = 0; h < kRepText; ++h) po[h * kD] = __uint_as_float(ov[h]);
-#pragma unroll
-      for (int h = 0; h < kRepText; ++h)
-        if (tid == h) {
-          p.part_ml[(ps * kRepText + h) * 2] = m[h];
-          p.part_ml[(ps * kRepText + h) * 2 + 1] = lsum[h];
-        }
-      __threadfence();
+        for (int h = 1; h < kRepText; ++h)
+          if (tid == h) {
+            mh = m[h];
+            lh = lsum[h];
+          }
+        *reinterpret_cast<float2*>(p.part_ml + (ps * kRepText + tid) * 2) = make_float2(mh, lh);
+      }
       bar_sync(1, kCompute);
       const long long u0 = static_cast<long long>(s.u) * p.T;
-      const int c0 = cta_of_tile(u0, p.W, gridDim.x), c1 = cta_of_tile(u0 + p.T - 1, p.W, gridDim.x);
+      const int c0 = p.per_unit ? s.u * p.per_unit : cta_of_tile(u0, p.W, gridDim.x);
+      const int c1 = p.per_unit ? c0 + p.per_unit - 1 : cta_of_tile(u0 + p.T - 1, p.W, gridDim.x);
       // the count is an acquire-release atomic: the release publishes this part (every thread's
-      // stores, fenced above and ordered before it by the barrier); for the last part the
+      // stores, ordered before it by the barrier; release is cumulative); for the last part the
       // acquire orders the other parts' partials before its reads (the barrier below extends it
       // to every thread)
       if (tid == 0)
         *merge_flag = atom_add_acq_rel_gpu(p.unit_cnt + s.u, 1u) == static_cast<uint32_t>(c1 - c0) ? 1u : 0u;
       bar_sync(1, kCompute);
       if (*merge_flag) {
-        // One pass over the parts with a running max, kMergeBatch parts per round of independent
-        // 16-byte loads. Thread tid owns heads 2q and 2q + 1 (q = tid / 32) at channels
-        // 4 (tid % 32) .. + 3: per part two float4 of the partial output and one float4 holding
-        // both heads' (max, sum). The first part's partial may sit in its CTA's second slot,
-        // every other part's in its first. Every part has a live key (each tile of a unit holds
-        // a row <= pos), so its max is finite.
         const int np = c1 - c0 + 1;
-        const int slot0 = cta_tile_start(c0, p.W, gridDim.x) >= u0 ? 0 : 1;
-        const int hq = 2 * (tid >> 5), c4 = 4 * (tid & 31);
-        float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f};
-        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        for (int cb = 0; cb < np; cb += kMergeBatch) {
-          float4 v[kMergeBatch][2], ml[kMergeBatch];
+        // part k's index: see above (the first part's partial may sit in its CTA's second slot)
+        const int slot0 = p.per_unit ? 0 : (cta_tile_start(c0, p.W, gridDim.x) >= u0 ? 0 : 1);
+        auto part_index = [&](int k) -> size_t {
+          return p.per_unit ? static_cast<size_t>(c0 + k)
+                            : static_cast<size_t>(c0 + k) * 2 + (k == 0 ? slot0 : 0);
+        };
+        // Unit-aligned mode: this CTA's only segment is done and its ring is free: thread 0
+        // stages the unit's contiguous partials there with one bulk copy (after the acquiring
+        // count: a proxy fence orders the copy's reads after it), while the weights are formed.
+        const uint32_t mb = bar0 + 8 * B_MERGE;
+        if (p.per_unit && tid == 0) {
+          fence_proxy_async_global();
+          const uint32_t bytes = static_cast<uint32_t>(np) * kRepText * kD * 4;
+          mbar_expect_tx(mb, bytes);
+          bulk_load(sbase + SM_RING, p.part_o + static_cast<size_t>(c0) * kRepText * kD, bytes, mb,
+                    l2_policy_evict_first());
+        }
+        // Weights w[k][h] = 2^(m_kh - M_h) / L_h (M_h = max_k m_kh, L_h = sum_k l_kh 2^(m_kh - M_h))
+        // into shared memory: 16 threads per head, each over parts j, j + 16, ... (up to
+        // kMaxParts / 16 = 10), reduced by shuffles within the 16. Every part has a live key, so
+        // every m is finite.
+        float* sw = reinterpret_cast<float*>(smem + SM_PARTML);  // [part][head]
+        {
+          constexpr int kPer = kMaxParts / 16;
+          const int h = tid >> 4, j = tid & 15;
+          float2 ml[kPer];
 #pragma unroll
-          for (int b = 0; b < kMergeBatch; ++b) {
-            const int c = cb + b < np ? cb + b : np - 1;  // past the last part: a repeat, unused
-            const size_t cs = static_cast<size_t>(c0 + c) * 2 + (c == 0 ? slot0 : 0);
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-              v[b][e] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (cs * kRepText + hq + e) * kD + c4));
-            ml[b] = __ldcg(reinterpret_cast<const float4*>(p.part_ml + (cs * kRepText + hq) * 2));
+          for (int e = 0; e < kPer; ++e) {
+            const int k = j + 16 * e;
+            ml[e] = k < np ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + (part_index(k) * kRepText + h) * 2))
+                           : make_float2(-INFINITY, 0.f);
           }
-          const int nb = np - cb < kMergeBatch ? np - cb : kMergeBatch;
-          float Mn[2] = {M[0], M[1]};
+          float M = -INFINITY;
 #pragma unroll
-          for (int b = 0; b < kMergeBatch; ++b)
-            if (b < nb) {
-              Mn[0] = fmaxf(Mn[0], ml[b].x);
-              Mn[1] = fmaxf(Mn[1], ml[b].z);
+          for (int e = 0; e < kPer; ++e) M = fmaxf(M, ml[e].x);
+#pragma unroll
+          for (int m = 8; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+          float L = 0.f;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) {
+            ml[e].x = j + 16 * e < np ? ex2_approx(ml[e].x - M) : 0.f;
+            L = fmaf(ml[e].y, ml[e].x, L);
+          }
+#pragma unroll
+          for (int m = 8; m >= 1; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
+          const float inv = 1.0f / L;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e)
+            if (j + 16 * e < np) sw[(j + 16 * e) * kRepText + h] = ml[e].x * inv;
+        }
+        bar_sync(1, kCompute);
+        // thread = channel: the 8 heads as independent sums over the parts
+        float acc[kRepText];
+#pragma unroll
+        for (int h = 0; h < kRepText; ++h) acc[h] = 0.f;
+        const float4* sw4 = reinterpret_cast<const float4*>(sw);
+        auto add_part = [&](int k, float4 o0, float4 o1) {
+          const float4 w0 = sw4[2 * k], w1 = sw4[2 * k + 1];
+          acc[0] = fmaf(w0.x, o0.x, acc[0]);
+          acc[1] = fmaf(w0.y, o0.y, acc[1]);
+          acc[2] = fmaf(w0.z, o0.z, acc[2]);
+          acc[3] = fmaf(w0.w, o0.w, acc[3]);
+          acc[4] = fmaf(w1.x, o1.x, acc[4]);
+          acc[5] = fmaf(w1.y, o1.y, acc[5]);
+          acc[6] = fmaf(w1.z, o1.z, acc[6]);
+          acc[7] = fmaf(w1.w, o1.w, acc[7]);
+        };
+        bool okm = true;
+        if (p.per_unit) {
+          okm = bar_sync_and(1, kCompute, bounded_wait(mb, 0, abort_flag, p.status, kErrDecodeWait));
+          if (okm) {
+            const float4* so4 = reinterpret_cast<const float4*>(smem + SM_RING) + 2 * tid;
+#pragma unroll 4
+            for (int k = 0; k < np; ++k) add_part(k, so4[k * 2 * kD], so4[k * 2 * kD + 1]);
+          } else if (tid == 0 && !drain_wait(mb, 0)) {  // the copy lands before the CTA exits
+            atomicOr(p.status, kErrDrain);
+          }
+        } else {
+          // from L2, kMergeBatch parts per round of independent 16-byte loads
+          for (int cb = 0; cb < np; cb += kMergeBatch) {
+            float4 v[kMergeBatch][2];
+#pragma unroll
+            for (int b = 0; b < kMergeBatch; ++b) {
+              const int k = cb + b < np ? cb + b : np - 1;  // past the last part: a repeat, unused
+              const float4* src = reinterpret_cast<const float4*>(p.part_o + part_index(k) * kRepText * kD) + 2 * tid;
+              v[b][0] = __ldcg(src);
+              v[b][1] = __ldcg(src + 1);
             }
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {  // earlier parts to the new running max (0 on the first round)
-            const float sc = ex2_approx(M[e] - Mn[e]);
-            L[e] *= sc;
-            acc[e].x *= sc;
-            acc[e].y *= sc;
-            acc[e].z *= sc;
-            acc[e].w *= sc;
-            M[e] = Mn[e];
+            for (int b = 0; b < kMergeBatch; ++b)
+              if (cb + b < np) add_part(cb + b, v[b][0], v[b][1]);
           }
-#pragma unroll
-          for (int b = 0; b < kMergeBatch; ++b)
-            if (b < nb) {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float wgt = ex2_approx((e ? ml[b].z : ml[b].x) - M[e]);
-                L[e] = fmaf(e ? ml[b].w : ml[b].y, wgt, L[e]);
-                acc[e].x = fmaf(v[b][e].x, wgt, acc[e].x);
-                acc[e].y = fmaf(v[b][e].y, wgt, acc[e].y);
-                acc[e].z = fmaf(v[b][e].z, wgt, acc[e].z);
-                acc[e].w = fmaf(v[b][e].w, wgt, acc[e].w);
-              }
-            }
+        }
+        if (!okm) {
+          ok = false;
+          break;
         }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float inv = 1.0f / L[e];
-          __nv_bfloat16* o = p.out[l] + static_cast<size_t>(kRepText * g + hq + e) * kD + c4;
-          *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[e].x * inv, acc[e].y * inv),
-                                                    pack_bf16x2(acc[e].z * inv, acc[e].w * inv));
-        }
+        for (int h = 0; h < kRepText; ++h)
+          p.out[l][static_cast<size_t>(kRepText * g + h) * kD + tid] = __float2bfloat16_rn(acc[h]);
         if (tid == 0) p.unit_cnt[s.u] = 0u;  // every part has arrived: ready for the next call
       }
       bar_sync(1, kCompute);  // the merge flag is read before the next segment overwrites it
@@ -589,6 +640,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
     const long long u = blockIdx.x / p.cluster, r = blockIdx.x % p.cluster;
     start = u * p.T + r * p.T / p.cluster;
     end = u * p.T + (r + 1) * p.T / p.cluster;
+  } else if (p.per_unit) {  // unit u = blockIdx.x / per_unit, part r: its share of the unit's tiles
+    const long long u = blockIdx.x / p.per_unit, r = blockIdx.x % p.per_unit;
+    start = u * p.T + r * p.T / p.per_unit;
+    end = u * p.T + (r + 1) * p.T / p.per_unit;
   } else {
     start = cta_tile_start(blockIdx.x, p.W, gridDim.x);
     end = cta_tile_start(blockIdx.x + 1, p.W, gridDim.x);
@@ -608,6 +663,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
     mbar_init(bar0 + 8 * B_OFREE, 1);
     mbar_init(bar0 + 8 * B_TAIL, 1);
     mbar_init(bar0 + 8 * B_DRAIN, 1);
+    mbar_init(bar0 + 8 * B_MERGE, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -626,9 +682,24 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM);
-  if (warp == 4 && (threadIdx.x & 31) == 0) {
-    // the first tiles of this CTA's range into L2 while the preceding kernel finishes (a hint:
-    // the TMA loads below run after the wait and read whatever that kernel wrote)
+  if (warp == 5 && (threadIdx.x & 31) == 0) {
+    // While the preceding kernel finishes, the MMA thread (idle until the first Q) asks for the
+    // tensor maps and has L2 fetch the first segment's q row block, gains and (for the unit's
+    // last tile) new k and v rows, then the CTA's first tiles (hints only: the loads after the
+    // wait read whatever that kernel wrote). Not the producer: it would reach its first load
+    // only once these requests are accepted.
+    if (start < end) {
+      const int u = static_cast<int>(start / p.T), l = u / kHkv, g = u % kHkv;
+      prefetch_tensormap(&p.kmap[l]);
+      prefetch_tensormap(&p.vmap[l]);
+      prefetch_l2_bulk(p.q_raw[l] + static_cast<size_t>(kRepText * g) * kD, kRepText * kD * 2u);
+      prefetch_l2_bulk(p.q_gamma[l], kD * 2u);
+      if (end - static_cast<long long>(u) * p.T >= p.T) {  // the segment holds the unit's last tile
+        prefetch_l2_bulk(p.k_raw[l] + static_cast<size_t>(g) * kD, kD * 2u);
+        prefetch_l2_bulk(p.v_raw[l] + static_cast<size_t>(g) * kD, kD * 2u);
+        prefetch_l2_bulk(p.k_gamma[l], kD * 2u);
+      }
+    }
     for (long long x = start; x < end && x < start + kStages; ++x) {
       const int u = static_cast<int>(x / p.T), j = static_cast<int>(x - static_cast<long long>(u) * p.T);
       const int l = u / kHkv, g = u % kHkv;
@@ -643,12 +714,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
   if (warp < 4) {
     compute(p, sbase, smem, tmem, start, end, abort_flag);
   } else if (warp == 4 && (threadIdx.x & 31) == 0) {
-    prefetch_tensormap(&p.kmap[0]);
     producer(p, sbase, start, end, abort_flag);
   } else if (warp == 5 && (threadIdx.x & 31) == 0) {
     mma_issuer(p, sbase, tmem, start, end, abort_flag);
   }
-  pdl_launch_dependents();
+  pdl_launch_dependents();  // (a CTA whose producer gave up early has not triggered yet)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

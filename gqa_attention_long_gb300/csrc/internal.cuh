@@ -178,6 +178,7 @@ struct AttnParams {
 constexpr int kHqText = 64;
 constexpr int kRepText = kHqText / kHkv;  // query heads per KV head
 constexpr int kDecodeMaxLayers = 64;
+constexpr int kDecodeMaxPerUnit = 32;  // CTAs per unit in the decode kernel's unit-aligned mode
 
 template <int CAP>
 struct DecodeParams {
@@ -206,6 +207,9 @@ struct DecodeParams {
   int cluster;           // 0: tiles of all units over all CTAs, split units merged through global
                          // memory; else the cluster size: one cluster per unit, merged through
                          // distributed shared memory
+  int per_unit;          // > 0 (no cluster): that many CTAs per unit, each with one segment of
+                         // its unit (ranges aligned to units); the unit's last part to arrive
+                         // stages every part in its drained ring by bulk copy and merges there
   float scale_log2;      // log2(e) / sqrt(128)
 };
 
@@ -257,14 +261,22 @@ struct LinearParams {
 
 
 // The key tiles of all (layer, kv head) units, in unit-major order, are cut into n_ctas
-// contiguous ranges; CTA c owns tiles [c*W/n, (c+1)*W/n).
+// contiguous ranges; CTA c owns tiles [c*W/n, (c+1)*W/n). A launch has at most kMaxGridCtas CTAs
+// and W <= 64 layers x 8 units x (2^22 / 128 + 1) tiles, so c * W and x * n stay below 2^32 and
+// both are taken in 32-bit unsigned arithmetic (a 64-bit division is a long software routine on
+// the GPU, on the path of every partial segment).
+constexpr int kMaxGridCtas = 160;
+static_assert(64ull * kHkv * ((1ull << 22) / kKeyTile + 1) * kMaxGridCtas < (1ull << 32),
+              "tile-range products must fit 32 bits");
 __host__ __device__ inline long long cta_tile_start(int c, long long W, int n_ctas) {
-  return static_cast<long long>(c) * W / n_ctas;
+  return static_cast<long long>(static_cast<uint32_t>(c) * static_cast<uint32_t>(W) /
+                                static_cast<uint32_t>(n_ctas));
 }
 
 // The CTA whose range holds tile x.
 __host__ __device__ inline int cta_of_tile(long long x, long long W, int n_ctas) {
-  int c = static_cast<int>((x * n_ctas) / W);
+  int c = static_cast<int>(static_cast<uint32_t>(x) * static_cast<uint32_t>(n_ctas) /
+                           static_cast<uint32_t>(W));
   while (c + 1 < n_ctas && cta_tile_start(c + 1, W, n_ctas) <= x) ++c;
   while (c > 0 && cta_tile_start(c, W, n_ctas) > x) --c;
   return c;

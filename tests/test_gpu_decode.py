@@ -181,9 +181,10 @@ def test_decode_and_expert_share_one_cache():
 
 def _parts_per_unit(n_layers: int, pos: int, n_sm: int):
     """Parts of each unit under the grid-wide split (the host's plan: T tiles of 128 keys per
-    unit, units laid out layer-major, tile c W / G .. of CTA c), or None in cluster mode."""
+    unit, units laid out layer-major, tile c W / G .. of CTA c), or None when one layer is
+    planned otherwise (cluster mode, or the unit-aligned mode with its staged merge)."""
     T = (pos + 1 + 127) // 128
-    if n_layers == 1 and 2 <= T <= 8:
+    if n_layers == 1:
         return None
     W = n_layers * 8 * T
     G = min(n_sm, 160, W)
@@ -201,12 +202,12 @@ def _parts_per_unit(n_layers: int, pos: int, n_sm: int):
 
 @pytest.mark.parametrize("want", [9, 10, 11, 19])
 def test_decode_merge_batch_boundaries(want):
-    # The last arriver of a split unit reads ten parts per round of loads: a unit of exactly
-    # 9, 10, 11 or 19 parts (19 = the most on 152 SMs: 8 units over 152 CTAs) ends its first
-    # round early, on its last part, with one part left over, or two rounds in.
+    # The last arriver of a split unit (several layers per call) reads ten parts per round of
+    # loads: a unit of exactly 9, 10, 11 or 19 parts ends its first round early, on its last
+    # part, with one part left over, or two rounds in.
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     found = None
-    for n_layers in (1, 2, 3, 4):
+    for n_layers in (2, 3, 4, 5, 6, 7, 8):
         for pos in range(1024, 8192, 37):
             parts = _parts_per_unit(n_layers, pos, n_sm)
             if parts is not None and want in parts:
@@ -215,10 +216,23 @@ def test_decode_merge_batch_boundaries(want):
         if found:
             break
     if found is None:
-        pytest.skip(f"no layer count <= 4 and pos < 8192 gives a {want}-part unit on {n_sm} SMs")
+        pytest.skip(f"no layer count 2..8 and pos < 8192 gives a {want}-part unit on {n_sm} SMs")
     n_layers, pos = found
     xs = [decode_inputs(900 + 10 * want + l, pos, 8192) for l in range(n_layers)]
     Ls, _ = run(xs, rope_delta=5)
     for l, (x, L) in enumerate(zip(xs, Ls)):
         assert_close(f64(L.out), oracle_step(x, rope_delta=5)["out"],
                      f"{want}-part unit: n={n_layers}, pos={pos}, layer {l}")
+
+
+@pytest.mark.parametrize("pos", [1024, 1100, 2431, 2432, 4700, 8191])
+def test_decode_one_layer_unit_aligned_staged_merge(pos):
+    # One layer over more than 8 key tiles: every kv head gets the same number of CTAs
+    # (min(SMs / 8, tiles)), one segment each, and the unit's last part merges all of them from
+    # its own shared memory. pos 1024..1100: 9 tiles (a part per tile); 2431/2432: 19 and 20
+    # tiles around 19 CTAs per unit on 152 SMs; 4700 and 8191: one- and two-tile parts.
+    x = decode_inputs(950 + pos % 97, pos, 8192)
+    (L,), ws = run([x], rope_delta=-3)
+    assert_close(f64(L.out), oracle_step(x, rope_delta=-3)["out"], f"pos={pos}")
+    # the merging parts leave every unit count at zero for the next call
+    assert int(ws[1024:1024 + 8 * 4].count_nonzero()) == 0
