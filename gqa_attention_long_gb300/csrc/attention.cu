@@ -1320,19 +1320,32 @@ __device__ __noinline__ void softmax_warps(const PP& p, const Ctx cx) {
       const float sc = __uint_as_float(static_cast<uint32_t>(es) << 23);
       const float isc = __uint_as_float(static_cast<uint32_t>(254 - es) << 23);
       const size_t mslot = static_cast<size_t>(blockIdx.x) * 2 + slot;
-      uint4* po = p.part_o + mslot * kPartChunks * kRows + static_cast<size_t>(8 * k) * kRows + r;
+      // The chunks go into this segment's Q buffer (its last QK is done) in the global layout,
+      // and the leader stores the whole 32 KB partial with one bulk copy: a handful of global
+      // store instructions per thread cost more, on this path, than the copy's round trip.
+      const uint32_t qst = cx.sbase + SM_Q + (seg & 1) * kQB + static_cast<uint32_t>(8 * k * kRows + r) * 16u;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float* x = &o[ch][8 * q];
-          po[static_cast<size_t>(4 * ch + q) * kRows] =
-              make_uint4(pack_f16x2(x[0] * sc, x[1] * sc), pack_f16x2(x[2] * sc, x[3] * sc),
-                         pack_f16x2(x[4] * sc, x[5] * sc), pack_f16x2(x[6] * sc, x[7] * sc));
+          st_shared_v4(qst + static_cast<uint32_t>((4 * ch + q) * kRows) * 16u,
+                       pack_f16x2(x[0] * sc, x[1] * sc), pack_f16x2(x[2] * sc, x[3] * sc),
+                       pack_f16x2(x[4] * sc, x[5] * sc), pack_f16x2(x[6] * sc, x[7] * sc));
         }
       p.part_lse[(mslot * 3 + 1 + k) * kRows + r] = isc;
       if (k == 0) p.part_lse[mslot * 3 * kRows + r] = lse_row;
-      if (fused) __threadfence();  // the partial is visible before the flag
+      fence_proxy_async_smem();  // the chunks are read by the bulk copy (async proxy)
+      bar_sync(2, kSoftmaxThreads);
+      if (leader) {
+        bulk_store(p.part_o + mslot * kPartChunks * kRows, cx.sbase + SM_Q + (seg & 1) * kQB, kQTileBytes);
+        bulk_commit();
+        bulk_wait_all0();           // written (and its source read: the buffer may be refilled)
+        fence_proxy_async_global();  // ordered before this thread's release of the partial
+      }
+      // The other threads' lse and scale stores reach the leader's release through the CTA
+      // barrier that follows (the flag's STAGED wait, or the grid merge's __syncthreads):
+      // release is cumulative.
     }
     if (leader) sflag[seg & 1] = staged ? 1u : 0u;
     mbar_arrive(cx.bar(B_STAGED + (seg & 1)));
