@@ -269,3 +269,24 @@ def test_running_max_moves_inside_and_across_tiles(splits):
     finally:
         ea.expert_attn_set_splits(prev)
     assert_close(f64(L.out), oracle_on_bf16_q(x), f"running max moves, splits={splits}")
+
+
+@pytest.mark.parametrize("scale", [3.0e5, 1.0e-6])
+@pytest.mark.parametrize("splits", [0, 37])
+def test_split_partials_keep_precision_at_any_magnitude(scale, splits):
+    # The split partials travel as f16 with a power-of-two scale per half row. V rows (cache and
+    # own) far above the f16 range (3e5) or far below its normal range (1e-6) must come out as
+    # accurately as unit-size ones: one layer over every SM (units of ~19 parts, merged by the
+    # grid) and 37 CTAs (two- and three-part units).
+    import dataclasses
+    x = layer_inputs(14, 2000, 2112)
+    x = dataclasses.replace(x, v_raw=(x.v_raw.float() * scale).to(torch.bfloat16),
+                            v_cache=(x.v_cache.float() * scale).to(torch.bfloat16))
+    ea.expert_attn_set_splits(splits)
+    try:
+        L = run_layer(x)
+    finally:
+        ea.expert_attn_set_splits(0)
+    got, ref = f64(L.out), oracle_layer(x)["out"]
+    mx, rel = errors(got, ref)
+    assert mx <= 1e-2 * scale and rel <= 5e-3, f"scale={scale}, splits={splits}: max-abs {mx:.3e}, rel-L2 {rel:.3e}"
