@@ -37,13 +37,24 @@ static_assert(kTok * 128 * 4 <= kStages * kStage, "the fp32 tile fits in the dra
 }  // namespace lin
 
 // Sum over the cluster's S CTAs (in rank order) of the float4 at shared address `addr` of each,
-// four 16-byte remote loads in flight at a time.
-__device__ __forceinline__ float4 cluster_sum4(uint32_t addr, uint32_t S) {
+// up to four loads in flight at a time. The CTA's own partial (rank q) is read with a local
+// shared-memory load: a load through the cluster window costs the same distributed-shared-memory
+// bandwidth whichever CTA it names.
+__device__ __forceinline__ float4 cluster_sum4(uint32_t addr, uint32_t S, uint32_t q) {
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
   for (uint32_t p0 = 0; p0 < S; p0 += 4) {
     float4 v[4];
 #pragma unroll
-    for (uint32_t e = 0; e < 4; ++e) v[e] = ld_shared_cluster_v4(mapa_shared(addr, min(p0 + e, S - 1)));
+    for (uint32_t e = 0; e < 4; ++e) {
+      const uint32_t pe = p0 + e;  // the same for every thread of the CTA
+      if (pe == q) {
+        const uint4 u = ld_shared_v4(addr);
+        v[e] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                           __uint_as_float(u.w));
+      } else if (pe < S) {
+        v[e] = ld_shared_cluster_v4(mapa_shared(addr, pe));
+      }
+    }
 #pragma unroll
     for (uint32_t e = 0; e < 4; ++e) {
       if (p0 + e < S) {
@@ -212,9 +223,9 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
     const int n_items = kTok * per_t;
     for (int item = static_cast<int>(q) * 128 + i; item < n_items; item += static_cast<int>(S) * 128) {
       const int t = item / per_t, c = 4 * (item % per_t);  // token, first row of the float4
-      const float4 a = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + c) * 4u, S);
+      const float4 a = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + c) * 4u, S, q);
       if (p.mode == kLinSwiglu) {
-        const float4 u = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + 64 + c) * 4u, S);
+        const float4 u = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + 64 + c) * 4u, S, q);
         *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(t) * p.N + tile * 64 + c) =
             pack_bf16x4(silu_mul(a.x, u.x), silu_mul(a.y, u.y), silu_mul(a.z, u.z), silu_mul(a.w, u.w));
       } else if (p.mode == kLinQkvHeads) {
