@@ -639,7 +639,7 @@ def main():
                   "us_per_layer": msl * 1e3 / NL, "bytes_per_layer": lb,
                   "hbm_gbs": lb * NL / (msl * 1e-3) / 1e9,
                   "roofline_frac": lb * NL / (msl * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                  "launches_per_layer": 8 if launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count) > 1 else 7}
+                  "launches_per_layer": 4 + launches_per_call(1, S, torch.cuda.get_device_properties(dev).multi_processor_count)}
         del Wl, wsl
 
     # ---- the text model's single-token decode attention over the same caches:

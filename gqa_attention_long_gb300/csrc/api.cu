@@ -646,8 +646,6 @@ extern "C" int expert_attn_noalloc_read_status(ea_stream_t stream, int* status_o
 namespace ea {
 cudaError_t linear_set_attributes();
 cudaError_t launch_linear(const LinearParams& lp, int tiles, int splits, cudaLaunchConfig_t cfg);
-cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, int width, const __nv_bfloat16* gamma,
-                                 __nv_bfloat16* h_out, cudaLaunchConfig_t cfg);
 }  // namespace ea
 
 namespace {
@@ -737,11 +735,13 @@ bool heads_map(const void* a, CUtensorMap* out) {
 // least two k-steps per CTA where the k-steps allow it, at most 16 (the largest cluster), and no
 // empty split.
 constexpr int kMaxLinearCluster = 16;
-void plan_splits(int tiles, int ksteps, int sm_count, int* splits, int* kps) {
+void plan_splits(int tiles, int ksteps, int sm_count, bool norm, int* splits, int* kps) {
   int s = (2 * sm_count) / tiles;
   if (s > ksteps / 2) s = ksteps / 2;
   if (s > kMaxLinearCluster) s = kMaxLinearCluster;
   if (s < 1) s = 1;
+  // a fused RMSNorm stages at most kNormMaxSteps k-steps of gains per CTA
+  if (norm && s < (ksteps + kNormMaxSteps - 1) / kNormMaxSteps) s = (ksteps + kNormMaxSteps - 1) / kNormMaxSteps;
   *kps = (ksteps + s - 1) / s;
   *splits = (ksteps + *kps - 1) / *kps;
 }
@@ -749,7 +749,7 @@ void plan_splits(int tiles, int ksteps, int sm_count, int* splits, int* kps) {
 size_t align_kb(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 struct LayerWs {
-  size_t attn_ws, h, q, k, v, attn, x1, h2, gu, total;
+  size_t attn_ws, q, k, v, attn, x1, gu, total;
 };
 
 // Layer workspace: the attention's own workspace first (its status word, at offset 0, is
@@ -764,13 +764,11 @@ LayerWs layer_ws_layout(int hidden, int inter, int sm_count) {
     off += align_kb(bytes);
     return o;
   };
-  w.h = take(static_cast<size_t>(kTok) * hidden * 2);
   w.q = take(static_cast<size_t>(kHq) * kTok * kD * 2);
   w.k = take(static_cast<size_t>(kHkv) * kTok * kD * 2);
   w.v = take(static_cast<size_t>(kHkv) * kTok * kD * 2);
   w.attn = take(static_cast<size_t>(kHq) * kTok * kD * 2);
   w.x1 = take(static_cast<size_t>(kTok) * hidden * 2);
-  w.h2 = take(static_cast<size_t>(kTok) * hidden * 2);
   w.gu = take(static_cast<size_t>(kTok) * inter * 2);
   w.total = off;
   return w;
@@ -782,10 +780,12 @@ bool layer_dims_ok(int hidden, int inter) {
 }
 
 // One projection with its epilogue (LinearParams). w1 != nullptr: the gate/up pair of SwiGLU
-// (tiles of 64 features of both), else tiles of 128 output features.
+// (tiles of 64 features of both), else tiles of 128 output features. norm_gamma != nullptr: the
+// input rows are RMS-normalised over their K channels and scaled by norm_gamma first.
 int run_linear(const CUtensorMap& xmap, int c1, const void* w0, const void* w1, int N, int K, int mode,
                const __nv_bfloat16* res, __nv_bfloat16* y, __nv_bfloat16* q, __nv_bfloat16* k,
-               __nv_bfloat16* v, uint32_t* status, int sm_count, cudaStream_t st) {
+               __nv_bfloat16* v, uint32_t* status, int sm_count, cudaStream_t st,
+               const void* norm_gamma = nullptr) {
   static_assert(sizeof(LinearParams) < 4096, "linear parameter block");
   LinearParams lp;
   std::memset(&lp, 0, sizeof(lp));
@@ -803,9 +803,10 @@ int run_linear(const CUtensorMap& xmap, int c1, const void* w0, const void* w1, 
   lp.ksteps = K / 64;
   lp.c1 = c1;
   lp.mode = mode;
+  lp.norm_gamma = static_cast<const __nv_bfloat16*>(norm_gamma);
   const int tiles = pair ? N / 64 : N / 128;
   int splits, kps;
-  plan_splits(tiles, lp.ksteps, sm_count, &splits, &kps);
+  plan_splits(tiles, lp.ksteps, sm_count, norm_gamma != nullptr, &splits, &kps);
   lp.kps = kps;
   cudaLaunchAttribute attr[2];  // PDL, and the cluster shape added by the launcher
   if (launch_linear(lp, tiles, splits, launch_config(st, attr, true)) != cudaSuccess) {
@@ -860,7 +861,6 @@ int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int ro
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + wl.attn_ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a->x);
-  cudaLaunchAttribute attr[1];
 
   // the attention step's arguments (validated like any expert_attn_layer call)
   ea_layer_args la;
@@ -877,19 +877,13 @@ int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int ro
   int rc = validate(&la, 1, S, Smax, rope_delta, EA_KV_BF16, ws + wl.attn_ws, true);
   if (rc != EA_OK) return rc;
 
-  CUtensorMap xm_h, xm_attn, xm_h2, xm_gu;
-  if (!rows_map(bf(wl.h), H, &xm_h) || !heads_map(bf(wl.attn), &xm_attn) ||
-      !rows_map(bf(wl.h2), H, &xm_h2) || !rows_map(bf(wl.gu), I, &xm_gu))
+  CUtensorMap xm_x, xm_attn, xm_x1, xm_gu;
+  if (!rows_map(x, H, &xm_x) || !heads_map(bf(wl.attn), &xm_attn) || !rows_map(bf(wl.x1), H, &xm_x1) ||
+      !rows_map(bf(wl.gu), I, &xm_gu))
     return EA_ERR_CUDA;
-  // h = rms_norm(x, ln1)
-  if (launch_rms_norm_rows(x, H, static_cast<const __nv_bfloat16*>(a->ln1), bf(wl.h),
-                           launch_config(st, attr, true)) != cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
-  // q, k, v = heads of h wqkv^T
-  rc = run_linear(xm_h, H / 64, a->wqkv, nullptr, (kHq + 2 * kHkv) * kD, H, kLinQkvHeads, nullptr,
-                  nullptr, bf(wl.q), bf(wl.k), bf(wl.v), status, di.sm_count, st);
+  // q, k, v = heads of h wqkv^T, h = rms_norm(x, ln1) (the norm fused into the projection)
+  rc = run_linear(xm_x, H / 64, a->wqkv, nullptr, (kHq + 2 * kHkv) * kD, H, kLinQkvHeads, nullptr,
+                  nullptr, bf(wl.q), bf(wl.k), bf(wl.v), status, di.sm_count, st, a->ln1);
   if (rc != EA_OK) return rc;
   // attention (q/k norm, RoPE, own rows into the cache tail, split-KV attention, merge)
   rc = launch_chunk(&la, 1, S, Smax, rope_delta, false, ws + wl.attn_ws, ws_layout(1, di.sm_count, false),
@@ -899,15 +893,9 @@ int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int ro
   rc = run_linear(xm_attn, 2, a->wo, nullptr, H, kHq * kD, kLinResidual, x, bf(wl.x1), nullptr, nullptr,
                   nullptr, status, di.sm_count, st);
   if (rc != EA_OK) return rc;
-  // h2 = rms_norm(x1, ln2)
-  if (launch_rms_norm_rows(bf(wl.x1), H, static_cast<const __nv_bfloat16*>(a->ln2), bf(wl.h2),
-                           launch_config(st, attr, true)) != cudaSuccess) {
-    cudaGetLastError();
-    return EA_ERR_CUDA;
-  }
-  // gu = silu(h2 w1^T) * (h2 w3^T)
-  rc = run_linear(xm_h2, H / 64, a->w1, a->w3, I, H, kLinSwiglu, nullptr, bf(wl.gu), nullptr, nullptr,
-                  nullptr, status, di.sm_count, st);
+  // gu = silu(h2 w1^T) * (h2 w3^T), h2 = rms_norm(x1, ln2) (fused)
+  rc = run_linear(xm_x1, H / 64, a->w1, a->w3, I, H, kLinSwiglu, nullptr, bf(wl.gu), nullptr, nullptr,
+                  nullptr, status, di.sm_count, st, a->ln2);
   if (rc != EA_OK) return rc;
   // x_out = x1 + gu w2^T
   return run_linear(xm_gu, I / 64, a->w2, nullptr, H, I, kLinResidual, bf(wl.x1),

@@ -242,6 +242,9 @@ constexpr int kMaxInter = 32768;
 // coordinates (0, kk % c1, 0, kk / c1) (row-major X: c1 = K / 64, c3 = 1; the attention output
 // [16][64][128]: c1 = 2 halves of a head, c3 = 16 heads).
 enum : int { kLinPlain = 0, kLinResidual = 1, kLinQkvHeads = 2, kLinSwiglu = 3 };
+// A projection with a fused RMSNorm stages the gains of its CTA's channels in shared memory: at
+// most this many 64-channel k-steps per CTA (the split planner takes enough splits).
+constexpr int kNormMaxSteps = 64;
 
 struct LinearParams {
   CUtensorMap wmap[2];
@@ -257,6 +260,7 @@ struct LinearParams {
   int kps;                   // k-steps per split (the splits of a tile form one cluster)
   int c1;
   int mode;
+  const __nv_bfloat16* norm_gamma;  // non-null: X is replaced by rms_norm(X) * norm_gamma (over K)
 };
 
 

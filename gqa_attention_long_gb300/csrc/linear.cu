@@ -1,6 +1,6 @@
 // linear.cu — the projections of the expert's decoder layer for its 64 tokens (Y = X W^T with
-// weights stored [out_features, in_features]) on the sm_103a tensor cores, and the small
-// RMSNorm of the layer's residual stream.
+// weights stored [out_features, in_features]) on the sm_103a tensor cores, with the layer's
+// RMSNorms of the residual stream fused into the projections that consume them.
 //
 // alpamayo_tt/expert.py, TTExpert.layer: rms_norm(x, ln1); the fused wqkv projection and
 // nlp_create_qkv_heads; after the attention, nlp_concat_heads, wo and the residual add;
@@ -27,10 +27,17 @@ constexpr int kStages = 4;
 constexpr uint32_t kWTile = 128 * 64 * 2;  // 128 weight rows x 64 channels, bf16, 128-byte rows
 constexpr uint32_t kXTile = 64 * 64 * 2;   // 64 tokens x 64 channels
 constexpr uint32_t kStage = kWTile + kXTile;
-constexpr uint32_t SM_BAR = kStages * kStage;          // full[kStages], empty[kStages], done
-constexpr uint32_t SM_TMEM = SM_BAR + (2 * kStages + 1) * 8;
+// barriers: full[kStages], empty[kStages], done, and (fused RMSNorm) xrdy[kStages], gains
+constexpr uint32_t SM_BAR = kStages * kStage;
+constexpr uint32_t SM_TMEM = SM_BAR + (3 * kStages + 2) * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM + 4;
-constexpr uint32_t kSmemBytes = SM_ABORT + 4 + 1024;   // + slack to align the base to 1 KB
+// fused RMSNorm: per-token sums of squares of this CTA's channels, then 1 / rms; the gains of
+// this CTA's channels (at most kNormMaxSteps k-steps, a split-planning constraint)
+constexpr uint32_t SM_SSQ = (SM_ABORT + 4 + 15) & ~15u;
+constexpr uint32_t SM_INV = SM_SSQ + kTok * 4;
+constexpr uint32_t SM_GAMMA = SM_INV + kTok * 4;
+constexpr uint32_t kSmemBytes = SM_GAMMA + kNormMaxSteps * 128 + 1024;  // + slack to align the base
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 64;
 constexpr int kMaxCluster = 16;                         // K splits of one tile = one cluster
 static_assert(kTok * 128 * 4 <= kStages * kStage, "the fp32 tile fits in the drained ring");
@@ -98,10 +105,13 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
   const uint32_t done = bar0 + 8u * (2 * kStages);
+  auto xrdy = [&](int s) { return bar0 + 8u * (2 * kStages + 1 + s); };
+  const uint32_t gbar = bar0 + 8u * (3 * kStages + 1);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + SM_ABORT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
   const bool pair = p.mode == kLinSwiglu;
+  const bool norm = p.norm_gamma != nullptr;  // the X operand is rms_norm(X) * norm_gamma
   const int k0 = split * p.kps;
   const int nk = min(p.kps, p.ksteps - k0);  // >= 1 by the host's choice of the split count
 
@@ -111,6 +121,8 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       mbar_init(empty(s), 1);
     }
     mbar_init(done, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(xrdy(s), 128);
+    mbar_init(gbar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -143,6 +155,11 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       // weight slice prefetched into L2, while that kernel may still run. The activations
       // are its output: they are loaded only after griddepcontrol.wait.
       const int pre = nk < kStages ? nk : kStages;
+      if (norm) {  // the gains of this CTA's channels, one contiguous bulk copy
+        mbar_expect_tx(gbar, static_cast<uint32_t>(nk) * 128u);
+        bulk_load(sbase + SM_GAMMA, p.norm_gamma + static_cast<size_t>(k0) * 64, static_cast<uint32_t>(nk) * 128u,
+                  gbar, pol_x);
+      }
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(full(i), kStage);
         load_w(i, k0 + i);
@@ -172,6 +189,8 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
         for (int j = (i > kStages ? i - kStages : 0); j < i; ++j)
           if (!drain_wait(full(j % kStages), (j / kStages) & 1)) atomicOr(p.status, kErrDrain);
       }
+      // the gains' copy has landed before the CTA can leave (normally long since)
+      if (norm && !drain_wait(gbar, 0)) atomicOr(p.status, kErrDrain);
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -180,6 +199,7 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       for (int i = 0; i < nk && ok; ++i) {
         const int s = i % kStages;
         ok = bounded_wait(full(s), (i / kStages) & 1, abort_flag, p.status, kErrLinearWait);
+        if (ok && norm) ok = bounded_wait(xrdy(s), (i / kStages) & 1, abort_flag, p.status, kErrLinearWait);
         if (!ok) break;
         tc_fence_after();
         const uint32_t wa = sbase + s * kStage, xa = wa + kWTile;
@@ -194,6 +214,49 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
       if (!drain_wait(done, 0)) atomicOr(p.status, kErrDrain);
     }
   } else {
+    if (norm) {
+      // Fused RMSNorm of the X operand. Y = rms_norm(X) diag(g) W^T is computed as
+      // diag(1 / rms) ((X diag(g)) W^T): while the MMAs run, warps 0-3 scale each landed X tile
+      // by the gains of its 64 channels in place (token t = thread / 2, one half of the row
+      // each) and sum the squares of X over this CTA's channels; the cluster's CTAs cover all K
+      // channels, so after the first cluster barrier every CTA sums those per-token partials in
+      // rank order and applies 1 / rms to the reduced tile.
+      const int t = threadIdx.x >> 1, half = threadIdx.x & 1;
+      float2 ss2 = make_float2(0.f, 0.f);
+      const bool gok = bounded_wait(gbar, 0, abort_flag, p.status, kErrLinearWait);
+      for (int i = 0; i < nk && gok; ++i) {
+        const int s = i % kStages;
+        if (!bounded_wait(full(s), (i / kStages) & 1, abort_flag, p.status, kErrLinearWait)) break;
+        uint4 gc[4];  // gains of channels 64 (k0 + i) + 32 half .. + 31
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) gc[jj] = ld_shared_v4(sbase + SM_GAMMA + i * 128 + 16 * (4 * half + jj));
+        // row t of the tile: 128 bytes, 16-byte chunk j stored at position j ^ (t % 8)
+        const uint32_t row = sbase + s * kStage + kWTile + t * 128;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * half + jj;
+          const uint32_t a = row + 16 * (j ^ (t & 7));
+          const uint4 xv = ld_shared_v4(a);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          const uint32_t gw[4] = {gc[jj].x, gc[jj].y, gc[jj].z, gc[jj].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 xf = make_float2(__uint_as_float(xw[e] << 16), __uint_as_float(xw[e] & 0xFFFF0000u));
+            ss2 = __ffma2_rn(xf, xf, ss2);
+            // g * x of two bf16 values is exact in fp32, so one bf16x2 multiply (round to
+            // nearest) gives the same bits as the fp32 product rounded to bf16
+            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[e]) : "r"(xw[e]), "r"(gw[e]));
+          }
+          st_shared_v4(a, o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();  // the scaled tile is read by the tensor core
+        mbar_arrive(xrdy(s));
+      }
+      float ss = ss2.x + ss2.y;
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (half == 0) st_shared_f32(sbase + SM_SSQ + 4u * t, ss);
+    }
     // thread r of warps 0-3 owns TMEM lane r (tile row r); its 64 columns are the 64 tokens.
     // The split's partial goes to shared memory as [token][row] (conflict-free stores).
     const bool ok = bounded_wait(done, 0, abort_flag, p.status, kErrLinearWait);
@@ -219,13 +282,35 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
     pdl_wait_primary();
     const uint32_t S = gridDim.y, q = cluster_ctarank();
     const int i = threadIdx.x;
+    if (norm) {
+      if (i < kTok) {  // 1 / rms of token i: its sums of squares over the cluster, in rank order
+        const uint32_t a = sbase + SM_SSQ + 4u * i;
+        float v[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          v[r] = 0.f;
+          if (r < static_cast<int>(S))
+            v[r] = r == static_cast<int>(q) ? reinterpret_cast<const float*>(smem + SM_SSQ)[i]
+                                            : ld_shared_cluster_f32(mapa_shared(a, r));
+        }
+        float ssq = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < static_cast<int>(S)) ssq += v[r];
+        st_shared_f32(sbase + SM_INV + 4u * i, rsqrtf(ssq / static_cast<float>(p.ksteps * 64) + 1e-6f));
+      }
+      bar_sync(1, 128);
+    }
     const int per_t = pair ? 16 : 32;  // float4 items per token: (gate) rows of the tile / 4
     const int n_items = kTok * per_t;
     for (int item = static_cast<int>(q) * 128 + i; item < n_items; item += static_cast<int>(S) * 128) {
       const int t = item / per_t, c = 4 * (item % per_t);  // token, first row of the float4
-      const float4 a = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + c) * 4u, S, q);
+      float4 a = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + c) * 4u, S, q);
+      const float inv = norm ? reinterpret_cast<const float*>(smem + SM_INV)[t] : 1.f;
+      if (norm) a = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
       if (p.mode == kLinSwiglu) {
-        const float4 u = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + 64 + c) * 4u, S, q);
+        float4 u = cluster_sum4(sbase + static_cast<uint32_t>(t * 128 + 64 + c) * 4u, S, q);
+        if (norm) u = make_float4(u.x * inv, u.y * inv, u.z * inv, u.w * inv);
         *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(t) * p.N + tile * 64 + c) =
             pack_bf16x4(silu_mul(a.x, u.x), silu_mul(a.y, u.y), silu_mul(a.z, u.z), silu_mul(a.w, u.w));
       } else if (p.mode == kLinQkvHeads) {
@@ -255,44 +340,6 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ----------------------------------------------------------------------------- RMSNorm rows
-// One CTA per token row: h = gamma * x / sqrt(mean(x^2) + eps) over the row's `width` channels,
-// rounded to bf16 (the layer's two RMSNorms; x is the bf16 residual stream).
-__global__ void __launch_bounds__(384) rms_norm_rows_kernel(const __nv_bfloat16* x, int width,
-                                                           const __nv_bfloat16* gamma,
-                                                           __nv_bfloat16* h_out) {
-  pdl_launch_dependents();
-  pdl_wait_primary();
-  __shared__ float red[32];
-  const int t = blockIdx.x;
-  const __nv_bfloat16* row = x + static_cast<size_t>(t) * width;
-  float ss = 0.f;
-  for (int n = 4 * threadIdx.x; n < width; n += 4 * blockDim.x) {
-    const uint2 xv = *reinterpret_cast<const uint2*>(row + n);
-    const float y[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
-                        __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ss = fmaf(y[e], y[e], ss);
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += red[w];
-  const float rs = rsqrtf(tot / static_cast<float>(width) + 1e-6f);
-  for (int n = 4 * threadIdx.x; n < width; n += 4 * blockDim.x) {
-    const uint2 xv = *reinterpret_cast<const uint2*>(row + n);
-    const uint2 gv = *reinterpret_cast<const uint2*>(gamma + n);
-    const float y[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
-                        __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
-    const float g[4] = {__uint_as_float(gv.x << 16), __uint_as_float(gv.x & 0xFFFF0000u),
-                        __uint_as_float(gv.y << 16), __uint_as_float(gv.y & 0xFFFF0000u)};
-    *reinterpret_cast<uint2*>(h_out + static_cast<size_t>(t) * width + n) =
-        pack_bf16x4(g[0] * (y[0] * rs), g[1] * (y[1] * rs), g[2] * (y[2] * rs), g[3] * (y[3] * rs));
-  }
-}
-
 // ------------------------------------------------------------------------------ launchers
 cudaError_t linear_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -314,14 +361,6 @@ cudaError_t launch_linear(const LinearParams& lp, int tiles, int splits, cudaLau
   attr[cfg.numAttrs].val.clusterDim.z = 1;
   cfg.numAttrs += 1;
   return cudaLaunchKernelEx(&cfg, linear_kernel, lp);
-}
-
-cudaError_t launch_rms_norm_rows(const __nv_bfloat16* x, int width, const __nv_bfloat16* gamma,
-                                 __nv_bfloat16* h_out, cudaLaunchConfig_t cfg) {
-  cfg.gridDim = dim3(kTok);
-  cfg.blockDim = dim3(384);  // one float4 of a 1536-wide row per thread
-  cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, rms_norm_rows_kernel, x, width, gamma, h_out);
 }
 
 }  // namespace ea

@@ -209,7 +209,8 @@ int expert_attn_noalloc_read_status(ea_stream_t stream, int* status_out, uint32_
  *   x1 = x + concat_heads(a) wo^T                (token row = the 16 heads side by side)
  *   x_out = x1 + (silu(h2 w1^T) * (h2 w3^T)) w2^T,  h2 = rms_norm(x1, ln2)
  * Every weight is bf16 row-major [out_features][in_features] (y = x W^T); activations between
- * the steps are kept in bf16 and products accumulate in fp32. Widths: hidden and inter are
+ * the steps are kept in bf16 (h and h2 as bf16(gain * x), their 1 / rms applied in fp32) and
+ * products accumulate in fp32. Widths: hidden and inter are
  * multiples of 128 with hidden <= 8192 and inter <= 32768 (the expert: 1536 and 6144). The
  * cache is bf16 [8][Smax][128] with the same rules as expert_attn_layer (rows [Smax-64, Smax)
  * are written). All pointers are device pointers, 16-byte aligned. The projections start
@@ -239,9 +240,11 @@ typedef struct {
  * expert_attn_workspace_init; expert_attn_read_status reads its status word. */
 size_t expert_decoder_layer_workspace_size(int hidden, int inter);
 
-/* One decoder layer (see above): the two RMSNorm kernels, four projections on the tensor cores
- * (each also applies its epilogue: head split, residual add or SwiGLU), and the attention
- * kernel. */
+/* One decoder layer (see above): four projections on the tensor cores and the attention kernel,
+ * five launches. Each projection applies its epilogue (head split, residual add or SwiGLU); the
+ * two RMSNorms are fused into the projections that consume them (wqkv and w1|w3): the input
+ * rows, scaled by the gains, are rounded to bf16 for the tensor cores, and 1 / rms, from the
+ * rows' sums of squares over all channels, scales the fp32 sums before the epilogue. */
 int expert_decoder_layer(const ea_decoder_layer_args* a, int S, int Smax, int rope_delta,
                          void* workspace, size_t ws_bytes, ea_stream_t stream);
 
