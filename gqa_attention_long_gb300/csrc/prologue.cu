@@ -30,7 +30,9 @@ __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* src, float (&x)
   unpack_bf16x8(*reinterpret_cast<const uint4*>(src), x);
 }
 
-__device__ __forceinline__ float block_max_256(float v, float* red) {
+// Maximum over the CTA's NW warps (two CTA barriers).
+template <int NW>
+__device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
   __syncthreads();
@@ -38,7 +40,7 @@ __device__ __forceinline__ float block_max_256(float v, float* red) {
   __syncthreads();
   float r = red[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
+  for (int w = 1; w < NW; ++w) r = fmaxf(r, red[w]);
   return r;
 }
 
@@ -94,16 +96,20 @@ constexpr uint32_t kPUnitBytes = 65536;
 constexpr uint32_t kPBarOff = kPRing * kPUnitBytes;
 constexpr uint32_t kPSmemBytes = kPBarOff + 8 * kPRing + 16;
 
-// TPO = 2 (tokens per octet): grid min(number of SMs, units), block 256 = 32 octets, each owning
-// tokens oc and oc + 32 of every unit in the CTA's range. TPO = 1 (few units, bf16 only): two
-// CTAs per unit, each owning 32 tokens, one per octet; the per-thread work halves.
+// bf16: TPO = 2 (tokens per octet): grid min(number of SMs, units), block 256 = 32 octets, each
+// owning tokens oc and oc + 32 of every unit in the CTA's range. TPO = 1 (few units): two CTAs
+// per unit, each owning 32 tokens, one per octet; the per-thread work halves.
 // F8: the e4m3 cache variant (Q as high and low codes with a per-row scale; the own K and V rows
-// quantised with one scale per head over all 64 tokens: CTA-wide maxima).
+// quantised with one scale per head over all 64 tokens: CTA-wide maxima). Its CTAs have 512
+// threads, 64 octets, one token each, over a range of units (TPO = 2 in the range sense): twice
+// the warps of the bf16 block to hide the latencies of its longer per-token chain.
 template <bool F8, int CAP, int TPO>
-__global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_constant__ PrologueParams<CAP> p) {
+__global__ void __launch_bounds__(F8 ? 512 : 256, 1) prologue_ring_kernel(const __grid_constant__ PrologueParams<CAP> p) {
   static_assert(TPO == 2 || !F8, "the e4m3 own-row scale needs all 64 tokens in one CTA");
-  constexpr int kTpc = 32 * TPO;  // tokens per CTA and unit
-  __shared__ float red[8];
+  constexpr int kNT = F8 ? 512 : 256;     // threads
+  constexpr int kTpt = F8 ? 1 : TPO;      // tokens per octet and unit
+  constexpr int kTpc = F8 ? 64 : 32 * TPO;  // tokens per CTA and unit
+  __shared__ float red[kNT / 32];
   extern __shared__ __align__(128) uint8_t psm[];
   const uint32_t sbase = smem_u32(psm);
   const uint32_t bar0 = sbase + kPBarOff;
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
   const int u1 = TPO == 2 ? static_cast<int>(static_cast<long long>(blockIdx.x + 1) * n_units / gridDim.x)
                           : u0 + 1;
   const int t0 = TPO == 2 ? 0 : 32 * static_cast<int>(blockIdx.x & 1);  // first token of the CTA
-  const int oc = threadIdx.x >> 3;  // octet: tokens oc and oc + 32
+  const int oc = threadIdx.x >> 3;  // octet: tokens oc (and oc + 32 if kTpt = 2)
   const int i = threadIdx.x & 7;    // channels [8i, 8i+8) and [64+8i, 64+8i+8)
   const int dl = 8 * i, dh = 64 + 8 * i;
   const int Smax = p.Smax;
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
   pdl_wait_primary();
   pdl_launch_dependents();
   if (t0 == 0)
-    for (int x = threadIdx.x; x < 2 * (u1 - u0); x += 256) p.unit_sync[2 * u0 + x] = 0u;
+    for (int x = threadIdx.x; x < 2 * (u1 - u0); x += kNT) p.unit_sync[2 * u0 + x] = 0u;
 
   const uint64_t pol = l2_policy_evict_first();  // raw rows are read once
   // slot layout: q head 2g rows, q head 2g+1 rows, k rows, v rows (kTpc rows of 256 B each)
@@ -154,11 +160,11 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
     for (; issued < kPRing && u0 + issued < u1; ++issued) issue(issued);
 
   // cos/sin of this thread's tokens at its eight frequencies (the same in every unit)
-  float cs[TPO][8], sn[TPO][8];
+  float cs[kTpt][8], sn[kTpt][8];
   float ih[8], il[8];
   load_inv8(p.inv_hi, p.inv_lo, dl, ih, il);
 #pragma unroll
-  for (int tt = 0; tt < TPO; ++tt) {
+  for (int tt = 0; tt < kTpt; ++tt) {
     const int pos = t0 + oc + 32 * tt + p.rope_delta + p.S;
 #pragma unroll
     for (int e = 0; e < 8; ++e) rope_cos_sin(pos, ih[e], il[e], cs[tt][e], sn[tt][e]);
@@ -181,23 +187,64 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
       load_bf16x8(L.k_gamma + dh, gkh);
       cur_l = l;
     }
-    const uint8_t* src = psm + (k % kPRing) * kPUnitBytes;
-    uint8_t* qdst = F8 ? p.q_ws + static_cast<size_t>(u) * kQTileBytes : nullptr;
-    float krl[TPO][8], krh[TPO][8], vrl[TPO][8], vrh[TPO][8];  // FP8: kept for the heads' scales
-    float kmax = 0.f, vmax = 0.f;
+    uint8_t* const slot = psm + (k % kPRing) * kPUnitBytes;
+    const uint8_t* src = slot;
+    if constexpr (F8) {
+      // e4m3 cache. The unit's outputs are staged in its own ring slot, over raw rows every
+      // thread has already read, and leave by three bulk stores: the Q codes (high then low,
+      // 32 KB in the attention kernel's shared-memory layout) over the raw q rows, the own K
+      // and V rows' codes (8 KB each, cache-row layout) over the raw k rows.
+      const int ncol = Smax / kScaleBlock + 1;
+      const int n_main = (p.S + kKeyTile - 1) / kKeyTile;
+      // the unit's cache-block V scales, requested now and used after the own rows' maximum
+      float vpre = 0.f;
+      for (int b = threadIdx.x; b < n_main; b += kNT) vpre = fmaxf(vpre, L.v_scale[g * ncol + b]);
+      uint4 rq[kTpt][2][2];  // raw q: token oc + 32 tt, head 2g + hh, channels [8i..), [64+8i..)
 #pragma unroll
-    for (int tt = 0; tt < TPO; ++tt) {
-      const int tl = oc + 32 * tt, t = t0 + tl;  // token within the CTA's block, within the unit
+      for (int tt = 0; tt < kTpt; ++tt)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint8_t* row = src + (hh * kTpc + tl) * (kD * 2);
-        float xl[8], xh[8], yl[8], yh[8];
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dl * 2), xl);
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dh * 2), xh);
-        norm_rope(xl, xh, gql, gqh, cs[tt], sn[tt], yl, yh);
-        const int r = hh * kTok + t;
-        const uint4 ql = pack8(yl, false), qh = pack8(yh, false);
-        if constexpr (F8) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint8_t* row = src + (hh * kTok + oc + 32 * tt) * (kD * 2);
+          rq[tt][hh][0] = *reinterpret_cast<const uint4*>(row + dl * 2);
+          rq[tt][hh][1] = *reinterpret_cast<const uint4*>(row + dh * 2);
+        }
+      float krl[kTpt][8], krh[kTpt][8];  // roped k, kept for the head's scale
+      uint4 rv[kTpt][2];                 // raw v (bf16), likewise
+      float kmax = 0.f, vmax = 0.f;
+#pragma unroll
+      for (int tt = 0; tt < kTpt; ++tt) {
+        const int t = oc + 32 * tt;
+        const uint8_t* krow = src + 2 * kRowsB + t * (kD * 2);
+        const uint8_t* vrow = src + 3 * kRowsB + t * (kD * 2);
+        float xl[8], xh[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl * 2), xl);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh * 2), xh);
+        norm_rope(xl, xh, gkl, gkh, cs[tt], sn[tt], krl[tt], krh[tt]);
+        rv[tt][0] = *reinterpret_cast<const uint4*>(vrow + dl * 2);
+        rv[tt][1] = *reinterpret_cast<const uint4*>(vrow + dh * 2);
+        float vl[8], vh[8];
+        unpack_bf16x8(rv[tt][0], vl);
+        unpack_bf16x8(rv[tt][1], vh);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kmax = fmaxf(kmax, fmaxf(fabsf(krl[tt][e]), fabsf(krh[tt][e])));
+          vmax = fmaxf(vmax, fmaxf(fabsf(vl[e]), fabsf(vh[e])));
+        }
+      }
+      // every raw row of the slot is in registers once the CTA-wide maxima are formed (each
+      // block_max passes two CTA barriers)
+      kmax = block_max<kNT / 32>(kmax, red);
+      vmax = block_max<kNT / 32>(vmax, red);
+#pragma unroll
+      for (int tt = 0; tt < kTpt; ++tt) {
+        const int t = oc + 32 * tt;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float xl[8], xh[8], yl[8], yh[8];
+          unpack_bf16x8(rq[tt][hh][0], xl);
+          unpack_bf16x8(rq[tt][hh][1], xh);
+          norm_rope(xl, xh, gql, gqh, cs[tt], sn[tt], yl, yh);
+          const int r = hh * kTok + t;
           // the row as two sets of e4m3 codes (high, low) with one scale amax / 448
           float am = 0.f;
 #pragma unroll
@@ -206,38 +253,91 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
           for (int m = 4; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
           const float sq = am > 0.f ? am * (1.0f / 448.0f) : 1.0f;
           const float isq = am > 0.f ? 448.0f / am : 1.0f;
-          uint2 hi, lo;  // high codes in the first 16 KB of the unit's slot, low codes in the second
+          uint2 hi, lo;  // high codes in the first 16 KB of the staged tile, low codes in the second
           quant8_hilo(yl, isq, hi, lo);
-          *reinterpret_cast<uint2*>(qdst + swz8_off(r, i)) = hi;
-          *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i)) = lo;
+          *reinterpret_cast<uint2*>(slot + swz8_off(r, i)) = hi;
+          *reinterpret_cast<uint2*>(slot + kQTileBytesF8 + swz8_off(r, i)) = lo;
           quant8_hilo(yh, isq, hi, lo);
-          *reinterpret_cast<uint2*>(qdst + swz8_off(r, i + 8)) = hi;
-          *reinterpret_cast<uint2*>(qdst + kQTileBytesF8 + swz8_off(r, i + 8)) = lo;
+          *reinterpret_cast<uint2*>(slot + swz8_off(r, i + 8)) = hi;
+          *reinterpret_cast<uint2*>(slot + kQTileBytesF8 + swz8_off(r, i + 8)) = lo;
           if (i == 0) p.q_scale[static_cast<size_t>(u) * kRows + r] = sq;
-        }
-        if (L.q_rope != nullptr) {
-          __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
-          *reinterpret_cast<uint4*>(qr + dl) = ql;
-          *reinterpret_cast<uint4*>(qr + dh) = qh;
+          if (L.q_rope != nullptr) {
+            __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
+            *reinterpret_cast<uint4*>(qr + dl) = pack8(yl, false);
+            *reinterpret_cast<uint4*>(qr + dh) = pack8(yh, false);
+          }
         }
       }
-      const uint8_t* krow = src + 2 * kRowsB + tl * (kD * 2);
-      const uint8_t* vrow = src + 3 * kRowsB + tl * (kD * 2);
-      float xl[8], xh[8];
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl * 2), xl);
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh * 2), xh);
-      norm_rope(xl, xh, gkl, gkh, cs[tt], sn[tt], krl[tt], krh[tt]);
-      const uint4 vpl = *reinterpret_cast<const uint4*>(vrow + dl * 2);
-      const uint4 vph = *reinterpret_cast<const uint4*>(vrow + dh * 2);
-      if constexpr (F8) {
-        unpack_bf16x8(vpl, vrl[tt]);
-        unpack_bf16x8(vph, vrh[tt]);
+      // the 64 own rows of this head share one scale slot, column Smax/128; the unit's
+      // reference V scale is the largest over the cache blocks it reads and its own rows
+      const float ksc = kmax > 0.f ? __fdiv_rn(kmax, 448.0f) : 1.0f;
+      const float vsc = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
+      const float vr = block_max<kNT / 32>(fmaxf(vsc, vpre), red);
+      if (threadIdx.x == 0) {
+        L.k_scale[g * ncol + ncol - 1] = ksc;
+        L.v_scale[g * ncol + ncol - 1] = vsc;
+        p.sv_ref[u] = vr;
+      }
+      uint8_t* kst = slot + 2 * kRowsB;  // own K codes, then own V codes: row t at t * 128
+      uint8_t* vst = kst + kTok * kD;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kmax = fmaxf(kmax, fmaxf(fabsf(krl[tt][e]), fabsf(krh[tt][e])));
-          vmax = fmaxf(vmax, fmaxf(fabsf(vrl[tt][e]), fabsf(vrh[tt][e])));
+      for (int tt = 0; tt < kTpt; ++tt) {
+        const int t = oc + 32 * tt;
+        uint2 c;
+        uint4 w;
+        quant8(krl[tt], ksc, c, w);
+        *reinterpret_cast<uint2*>(kst + t * kD + dl) = c;
+        quant8(krh[tt], ksc, c, w);
+        *reinterpret_cast<uint2*>(kst + t * kD + dh) = c;
+        float vv[8];
+        unpack_bf16x8(rv[tt][0], vv);
+        quant8(vv, vsc, c, w);
+        *reinterpret_cast<uint2*>(vst + t * kD + dl) = c;
+        unpack_bf16x8(rv[tt][1], vv);
+        quant8(vv, vsc, c, w);
+        *reinterpret_cast<uint2*>(vst + t * kD + dh) = c;
+      }
+      fence_proxy_async_smem();  // the staged codes are read by the bulk stores (async proxy)
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok);
+        bulk_store(p.q_ws + static_cast<size_t>(u) * kQTileBytes, smem_u32(slot), kQTileBytes);
+        bulk_store(static_cast<uint8_t*>(L.k_cache) + crow * kD, smem_u32(kst), kTok * kD);
+        bulk_store(static_cast<uint8_t*>(L.v_cache) + crow * kD, smem_u32(vst), kTok * kD);
+        bulk_commit();
+        if (u0 + issued < u1) {
+          bulk_wait_read0();  // the stores have read the slot before it is refilled
+          issue(issued);
+          ++issued;
         }
-      } else {
+      }
+    } else {
+      float krl[TPO][8], krh[TPO][8];
+#pragma unroll
+      for (int tt = 0; tt < TPO; ++tt) {
+        const int tl = oc + 32 * tt, t = t0 + tl;  // token within the CTA's block, within the unit
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint8_t* row = src + (hh * kTpc + tl) * (kD * 2);
+          float xl[8], xh[8], yl[8], yh[8];
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dl * 2), xl);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(row + dh * 2), xh);
+          norm_rope(xl, xh, gql, gqh, cs[tt], sn[tt], yl, yh);
+          const uint4 ql = pack8(yl, false), qh = pack8(yh, false);
+          if (L.q_rope != nullptr) {
+            __nv_bfloat16* qr = L.q_rope + (static_cast<size_t>(2 * g + hh) * kTok + t) * kD;
+            *reinterpret_cast<uint4*>(qr + dl) = ql;
+            *reinterpret_cast<uint4*>(qr + dh) = qh;
+          }
+        }
+        const uint8_t* krow = src + 2 * kRowsB + tl * (kD * 2);
+        const uint8_t* vrow = src + 3 * kRowsB + tl * (kD * 2);
+        float xl[8], xh[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dl * 2), xl);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + dh * 2), xh);
+        norm_rope(xl, xh, gkl, gkh, cs[tt], sn[tt], krl[tt], krh[tt]);
+        const uint4 vpl = *reinterpret_cast<const uint4*>(vrow + dl * 2);
+        const uint4 vph = *reinterpret_cast<const uint4*>(vrow + dh * 2);
         const uint4 kpl = pack8(krl[tt], false), kph = pack8(krh[tt], false);
         const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
         __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(L.k_cache) + crow * kD;
@@ -247,49 +347,16 @@ __global__ void __launch_bounds__(256, 1) prologue_ring_kernel(const __grid_cons
         *reinterpret_cast<uint4*>(vc + dl) = vpl;
         *reinterpret_cast<uint4*>(vc + dh) = vph;
       }
-    }
-    if constexpr (F8) {
-      // e4m3 cache: the 64 own rows of this head share one scale slot, column Smax/128; the
-      // unit's reference V scale is the largest over the cache blocks it reads and its own rows
-      kmax = block_max_256(kmax, red);
-      vmax = block_max_256(vmax, red);
-      const float ksc = kmax > 0.f ? __fdiv_rn(kmax, 448.0f) : 1.0f;
-      const float vsc = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
-      const int ncol = Smax / kScaleBlock + 1;
-      const int n_main = (p.S + kKeyTile - 1) / kKeyTile;
-      float vr = vsc;
-      for (int b = threadIdx.x; b < n_main; b += 256) vr = fmaxf(vr, L.v_scale[g * ncol + b]);
-      vr = block_max_256(vr, red);
-      if (threadIdx.x == 0) {
-        L.k_scale[g * ncol + ncol - 1] = ksc;
-        L.v_scale[g * ncol + ncol - 1] = vsc;
-        p.sv_ref[u] = vr;
+      __syncthreads();  // every thread is done with the slot
+      if (threadIdx.x == 0 && u0 + issued < u1) {
+        fence_proxy_async_smem();  // generic-proxy reads of the slot before the async-proxy refill
+        issue(issued);
+        ++issued;
       }
-#pragma unroll
-      for (int tt = 0; tt < TPO; ++tt) {
-        const int t = oc + 32 * tt;
-        const size_t crow = static_cast<size_t>(g) * Smax + (Smax - kTok) + t;
-        uint8_t* kc = static_cast<uint8_t*>(L.k_cache) + crow * kD;
-        uint8_t* vc = static_cast<uint8_t*>(L.v_cache) + crow * kD;
-        uint2 c;
-        uint4 w;
-        quant8(krl[tt], ksc, c, w);
-        *reinterpret_cast<uint2*>(kc + dl) = c;
-        quant8(krh[tt], ksc, c, w);
-        *reinterpret_cast<uint2*>(kc + dh) = c;
-        quant8(vrl[tt], vsc, c, w);
-        *reinterpret_cast<uint2*>(vc + dl) = c;
-        quant8(vrh[tt], vsc, c, w);
-        *reinterpret_cast<uint2*>(vc + dh) = c;
-      }
-    }
-    __syncthreads();  // every thread is done with the slot
-    if (threadIdx.x == 0 && u0 + issued < u1) {
-      fence_proxy_async_smem();  // generic-proxy reads of the slot before the async-proxy refill
-      issue(issued);
-      ++issued;
     }
   }
+  if constexpr (F8)
+    if (threadIdx.x == 0) bulk_wait_all0();  // the staged outputs have left shared memory
   if (!ok && threadIdx.x == 0) {
     // let the copies already issued land before the CTA gives its shared memory back
     for (int kk = k; kk < issued; ++kk)
@@ -301,7 +368,7 @@ template <int CAP>
 cudaError_t launch_prologue_kernel(const PrologueParams<CAP>& pp, bool fp8, int sm_count,
                                    cudaLaunchConfig_t cfg) {
   const int n_units = pp.n_layers * kHkv;
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(fp8 ? 512 : 256);
   cfg.dynamicSmemBytes = kPSmemBytes;
   if (fp8) {
     cfg.gridDim = dim3(n_units < sm_count ? n_units : sm_count);
