@@ -91,6 +91,13 @@ def test_decoder_layer_small_widths_and_rope_delta():
     assert rel(f64(kc[:, 1152 - 64:]), r["k_store"]) < 1e-2
 
 
+def test_decoder_layer_widest_residual_stream():
+    """hidden = 8192, the widest accepted: the fused RMSNorms then stage the gains of 64 k-steps
+    per CTA (the split planner's bound) and sum the squares over 128 k-steps per cluster."""
+    out, r, _, _, _ = run_layer(15, 300, 512, hidden=8192, inter=256)
+    assert_layer_close(f64(out), r["x2"], "hidden=8192")
+
+
 def test_decoder_layer_repeatable_bitwise():
     out, _, _, _, (x, wd, kc, vc, ws) = run_layer(13, 700, 1024, hidden=512, inter=1024)
     again = torch.full_like(out, float("nan"))
