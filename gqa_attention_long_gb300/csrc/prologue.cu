@@ -11,11 +11,11 @@
 // An octet (8 lanes) owns one token at a time; lane i holds channels [8i, 8i+8) and their RoPE
 // partners [64+8i, 64+8i+8), so the rotation is in-thread and the norm needs three shuffles.
 // Every global access is a 16-byte vector access.
-// Persistent CTAs (one per SM) of 256 threads walk a range of (layer, g) units (q heads 2g,
-// 2g+1, k head g, v head g; all 64 tokens, two per octet), computing the tokens' cos/sin once
-// (positions are the same in every layer and head); the raw rows arrive by bulk copy into a
-// shared-memory ring several units ahead. With an e4m3 cache the own K and V rows of a head
-// share one scale over all 64 tokens, a CTA-wide maximum.
+// Persistent CTAs (one per SM) walk a range of (layer, g) units (q heads 2g, 2g+1, k head g,
+// v head g; all 64 tokens: bf16, 256 threads, two tokens per octet; e4m3, 512 threads, one),
+// computing the tokens' cos/sin once (positions are the same in every layer and head); the raw
+// rows arrive by bulk copy into a shared-memory ring several units ahead. With an e4m3 cache the
+// own K and V rows of a head share one scale over all 64 tokens, a CTA-wide maximum.
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
@@ -87,7 +87,7 @@ __device__ __forceinline__ void quant8(const float (&y)[8], float scale, uint2& 
 
 }  // namespace
 
-// bf16 kernel: persistent CTAs of 256 threads walk a contiguous range of (layer, g) units. The
+// Persistent CTAs walk a contiguous range of (layer, g) units. The
 // raw rows of a unit (q heads 2g and 2g+1: 32 KB, k head g: 16 KB, v head g: 16 KB, each one
 // contiguous block) arrive by bulk copy in a three-slot shared-memory ring, so that up to
 // 192 KB of loads per SM are in flight while the threads work on an earlier unit.
