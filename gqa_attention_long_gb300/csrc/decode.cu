@@ -46,6 +46,7 @@
 // score buffer: it runs while the softmax of tile n-1 does, and the compute warps go from one
 // tile's softmax to the next without waiting for the tensor core.
 #include "internal.cuh"
+#include "cluster_exit.cuh"
 #include "ptx.cuh"
 #include "rope.cuh"
 
@@ -762,7 +763,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_attention_kernel(cons
       *reinterpret_cast<uint2*>(p.out[l] + static_cast<size_t>(kRepText * g) * kD + 4 * chunk) =
           make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     }
-    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    cluster_sync_exit();  // no CTA leaves while another still reads its shared memory
   }
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }

@@ -17,6 +17,7 @@
 // partial sum travels through global memory. Two CTAs fit on an SM (96 KB ring, 64 TMEM
 // columns each).
 #include "internal.cuh"
+#include "cluster_exit.cuh"
 #include "ptx.cuh"
 
 namespace ea {
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(lin::kThreads, 2) linear_kernel(const __grid_c
     }
   }
   // no CTA leaves (or reuses its shared memory) while a peer may still read it
-  cluster_sync();
+  cluster_sync_exit();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
